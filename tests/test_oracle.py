@@ -1,0 +1,349 @@
+"""Pins for the CPU oracle (no GPU).
+
+The oracle is checked against things other than itself:
+
+* its binary16 / bfloat16 decoders against numpy's conversions, for every one
+  of the 65536 bit patterns of each type;
+* the sequential scan against an independent closed form, exhaustively over
+  every row of length 1..5 on the special-value alphabet of the randomized
+  fuzz in onnxruntime PR #32092 (Testing);
+* numpy.argmax / numpy.argmin (documented to return the first occurrence) on
+  NaN-free rows, including heavy ties;
+* invariants planted by construction (unique and duplicated extremes);
+* golden rows built to the pages' own test descriptions (tests/golden/);
+* a mutation check: plausible mistakes planted into the oracle's C source
+  must each be caught by at least one of these pins.
+"""
+import json
+import os
+import shutil
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------------------
+# Independent decoding (numpy) and the closed form.
+# ---------------------------------------------------------------------------
+def np_decode(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Decode raw elements to float64 with numpy's own conversions."""
+    if dtype == "f32":
+        return x.astype(np.float64)
+    if dtype == "f64":
+        return x.astype(np.float64)
+    if dtype == "f16":
+        return x.view(np.float16).astype(np.float64)
+    if dtype == "bf16":
+        with np.errstate(invalid="ignore"):  # signalling NaN patterns stay NaN
+            return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    raise ValueError(dtype)
+
+
+def closed_form(x: np.ndarray, dtype: str, op: str) -> np.ndarray:
+    """Second formulation of the result: 0 when element 0 is NaN, otherwise the
+    smallest j whose value is not NaN and equals the max (min) over the
+    non-NaN values of the row."""
+    v = np_decode(x, dtype)
+    rows, cols = v.shape
+    out = np.zeros(rows, dtype=np.int64)
+    nan = np.isnan(v)
+    lead_nan = nan[:, 0]
+    fill = -np.inf if op == "max" else np.inf
+    w = np.where(nan, fill, v)
+    m = w.max(axis=1) if op == "max" else w.min(axis=1)
+    hit = (~nan) & (v == m[:, None])
+    first = np.argmax(hit, axis=1)
+    out[:] = np.where(lead_nan, 0, first)
+    return out
+
+
+def raw_equal(a: np.ndarray, b: np.ndarray) -> bool:
+    """Bitwise equality of raw element arrays (NaN payloads included)."""
+    ua = a.view(np.uint8)
+    ub = b.view(np.uint8)
+    return ua.shape == ub.shape and bool((ua == ub).all())
+
+
+def take_rows(x: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    return x[np.arange(x.shape[0]), idx]
+
+
+# ---------------------------------------------------------------------------
+# Decoders.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_decoder_exhaustive(dtype):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = np_decode(bits.reshape(1, -1), dtype)[0]
+    dec = oracle.decode_f16 if dtype == "f16" else oracle.decode_bf16
+    got = np.array([dec(int(b)) for b in bits], dtype=np.float64)
+    nan = np.isnan(ref)
+    assert (np.isnan(got) == nan).all()
+    assert (got[~nan] == ref[~nan]).all()
+    # signs of zeros and infinities survive decoding
+    assert (np.signbit(got[~nan]) == np.signbit(ref[~nan])).all()
+
+
+# ---------------------------------------------------------------------------
+# Exhaustive brute force over the special-value alphabet.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", W.DTYPES)
+@pytest.mark.parametrize("op", W.OPS)
+def test_exhaustive_alphabet(dtype, op):
+    for length in range(1, 6):
+        x = W.exhaustive_rows(dtype, length)
+        idx, val, _ = oracle.argreduce(x, dtype, op)
+        exp = closed_form(x, dtype, op)
+        bad = np.nonzero(idx != exp)[0]
+        assert bad.size == 0, (length, x[bad[:5]], idx[bad[:5]], exp[bad[:5]])
+        assert raw_equal(val, take_rows(x, idx))
+
+
+def test_brute_force_python_loop():
+    """A third formulation on a small random sample: pure Python, pairwise
+    'is any earlier element at least as good / any element strictly better'."""
+    for dtype in W.DTYPES:
+        x = W.fuzz_rows(dtype, 400, 9, seed=77, p_special=0.4)
+        v = np_decode(x, dtype)
+        for op in W.OPS:
+            idx, _, _ = oracle.argreduce(x, dtype, op)
+            for r in range(x.shape[0]):
+                row = v[r]
+                if np.isnan(row[0]):
+                    exp = 0
+                else:
+                    exp = None
+                    for j in range(len(row)):
+                        if np.isnan(row[j]):
+                            continue
+                        beats_all = all(
+                            np.isnan(row[k]) or (row[j] >= row[k] if op == "max" else row[j] <= row[k])
+                            for k in range(len(row)))
+                        if beats_all:
+                            exp = j
+                            break
+                assert idx[r] == exp, (dtype, op, r, row)
+
+
+# ---------------------------------------------------------------------------
+# numpy special case: NaN-free rows.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", W.DTYPES)
+def test_numpy_nan_free(dtype):
+    rng = np.random.Generator(np.random.PCG64(123))
+    g = W.encode(rng.standard_normal((64, 3001)) * 3.0, dtype)
+    t = W.encode(rng.integers(0, 8, size=(64, 1000)).astype(np.float64), dtype)
+    for x in (g, t):
+        v = np_decode(x, dtype)
+        assert not np.isnan(v).any()
+        for op in W.OPS:
+            idx, val, _ = oracle.argreduce(x, dtype, op)
+            exp = np.argmax(v, axis=1) if op == "max" else np.argmin(v, axis=1)
+            assert (idx == exp).all()
+            assert raw_equal(val, take_rows(x, idx))
+
+
+def test_mt_wrapper_matches_single():
+    x = W.fuzz_rows("f32", 1000, 77, seed=5)
+    for op in W.OPS:
+        a, va, _ = oracle.argreduce(x, "f32", op, threads=1)
+        b, vb, used = oracle.argreduce(x, "f32", op, threads=7)
+        assert used == 7
+        assert (a == b).all() and raw_equal(va, vb)
+
+
+def test_invalid_arguments():
+    x = np.zeros((2, 0), dtype=np.float32)
+    with pytest.raises(ValueError):
+        oracle.argreduce(x, "f32", "max")
+
+
+# ---------------------------------------------------------------------------
+# Invariants by construction on the workload recipes (reduced sizes).
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("op", W.OPS)
+def test_planted_extreme(dtype, op):
+    for variant in ("unique", "dup"):
+        c = W.Case("t", 3, 20011, dtype, op, "planted", 99, variant)
+        x = W.make(c)
+        v = np_decode(x, dtype)
+        target = 64.0 if op == "max" else -64.0
+        idx, _, _ = oracle.argreduce(x, dtype, op)
+        for r in range(c.rows):
+            pos = np.nonzero(v[r] == target)[0]
+            assert len(pos) == (1 if variant == "unique" else 2)
+            assert idx[r] == pos[0]
+
+
+def test_small_ints_first_seven():
+    c = W.Case("t", 512, 64, "f32", "max", "small_ints", 5001)
+    x = W.make(c)
+    idx, _, _ = oracle.argreduce(x, "f32", "max")
+    for r in range(c.rows):
+        row = list(x[r])
+        assert idx[r] == row.index(max(row))
+    idx, _, _ = oracle.argreduce(x, "f32", "min")
+    for r in range(c.rows):
+        row = list(x[r])
+        assert idx[r] == row.index(min(row))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f64"])
+@pytest.mark.parametrize("op", W.OPS)
+def test_uniform_special_classes(dtype, op):
+    c = W.Case("t", 200, 301, dtype, op, "uniform_special", 4001)
+    x = W.make(c)
+    v = np_decode(x, dtype)
+    idx, val, _ = oracle.argreduce(x, dtype, op)
+    cls = np.arange(c.rows) % W.N_ROW_CLASSES
+    for r in range(c.rows):
+        k = cls[r]
+        row = v[r]
+        if k in (0, 4, 6):  # all-equal, leading NaN, all -inf
+            assert idx[r] == 0
+        elif k == 7:  # -0.0 then +0.0, everything else worse than zero
+            z = np.nonzero(row == 0.0)[0]
+            assert len(z) == 2 and np.signbit(row[z[0]]) and not np.signbit(row[z[1]])
+            assert idx[r] == z[0]
+        elif k == 5:  # a NaN mid-row is never chosen
+            assert not np.isnan(row[idx[r]])
+        if k == 1 and op == "max":
+            assert np.isposinf(row[idx[r]])
+        if k == 2 and op == "min":
+            assert np.isneginf(row[idx[r]])
+    assert raw_equal(val, take_rows(x, idx))
+
+
+# ---------------------------------------------------------------------------
+# Golden rows built to the pages' test descriptions.
+# ---------------------------------------------------------------------------
+def _token(tok, dtype):
+    sv = W.special_values(dtype)
+    if isinstance(tok, (int, float)):
+        return W.encode(np.array([float(tok)]), dtype)[0]
+    m = {"nan": "nan", "inf": "pinf", "-inf": "ninf", "-0": "nzero", "denorm": "denorm"}
+    if tok in m:
+        return sv[m[tok]]
+    if tok in ("lowest", "highest"):
+        if dtype == "f16":
+            return np.uint16(0xFBFF if tok == "lowest" else 0x7BFF)
+        if dtype == "bf16":
+            return np.uint16(0xFF7F if tok == "lowest" else 0x7F7F)
+        ft = np.float32 if dtype == "f32" else np.float64
+        return np.finfo(ft).min if tok == "lowest" else np.finfo(ft).max
+    raise ValueError(tok)
+
+
+@pytest.mark.parametrize("dtype", W.DTYPES)
+def test_golden_semantics(dtype):
+    with open(os.path.join(GOLDEN, "onnxruntime_32092_semantics.json")) as f:
+        fx = json.load(f)
+    raw_t = oracle.RAW_NP[dtype]
+    for case in fx["cases"]:
+        x = np.array([[_token(t, dtype) for t in case["row"]]], dtype=raw_t)
+        for op in W.OPS:
+            idx, val, _ = oracle.argreduce(x, dtype, op)
+            assert idx[0] == case[op], (case["what"], op)
+            assert raw_equal(val, x[0, idx])
+
+
+@pytest.mark.parametrize("dtype", W.DTYPES)
+def test_golden_long_axis(dtype):
+    with open(os.path.join(GOLDEN, "onnxruntime_31694_long_axis_300x4.json")) as f:
+        fx = json.load(f)
+    x = W.encode(np.array(fx["rows"], dtype=np.float64), dtype)
+    for op in W.OPS:
+        idx, _, _ = oracle.argreduce(x, dtype, op)
+        assert list(idx) == fx["expected"][op]
+
+
+def test_golden_first_index_65536():
+    with open(os.path.join(GOLDEN, "onnxruntime_31694_first_index_65536.json")) as f:
+        fx = json.load(f)
+    rng = np.random.Generator(np.random.PCG64(fx["seed"]))
+    row = rng.standard_normal(fx["cols"]).astype(np.float32)
+    row[fx["inf_positions"]] = np.inf
+    idx, _, _ = oracle.argreduce(row.reshape(1, -1), "f32", "max")
+    assert idx[0] == fx["expected_max"]
+
+
+# ---------------------------------------------------------------------------
+# Mutation check: each planted mistake must fail a pin.
+# ---------------------------------------------------------------------------
+MUTANTS = [
+    ("last-index ties", "return op == ORACLE_MAX ? (a > b) : (a < b);",
+     "return op == ORACLE_MAX ? (a >= b) : (a <= b);"),
+    ("ops swapped", "return op == ORACLE_MAX ? (a > b) : (a < b);",
+     "return op == ORACLE_MIN ? (a > b) : (a < b);"),
+    ("NaN wins", "return op == ORACLE_MAX ? (a > b) : (a < b);",
+     "return op == ORACLE_MAX ? !(a <= b) : !(a >= b);"),
+    ("element 1 skipped", "for (int64_t j = 1; j < cols; ++j)", "for (int64_t j = 2; j < cols; ++j)"),
+    ("last element skipped", "for (int64_t j = 1; j < cols; ++j)", "for (int64_t j = 1; j + 1 < cols; ++j)"),
+    ("value from wrong index", "row + (size_t)best_j * es, es);", "row, es);"),
+    ("f16 subnormal scale", "v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
+    ("f16 implicit bit", "ldexp((double)(1024 + f), e - 25)", "ldexp((double)(f), e - 15)"),
+    ("bf16 fraction width", "ldexp((double)(128 + f), e - 134)", "ldexp((double)(256 + f), e - 135)"),
+    ("bf16 sign dropped", "    return sign ? -v : v;\n}\n\nstatic size_t", "    return v;\n}\n\nstatic size_t"),
+    ("row stride", "(size_t)r * (size_t)cols * es", "(size_t)r * (size_t)cols"),
+]
+
+
+def _pin_suite_passes(lib_path: str) -> bool:
+    """Run a compact version of the pins above against another build."""
+    import ctypes
+    saved = oracle._lib
+    try:
+        oracle._lib = None
+        lib = ctypes.CDLL(lib_path)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        lib.oracle_argreduce.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_int, i64p, ctypes.c_void_p]
+        lib.oracle_argreduce_mt.argtypes = lib.oracle_argreduce.argtypes + [ctypes.c_int]
+        for name in ("oracle_decode_f16", "oracle_decode_bf16"):
+            getattr(lib, name).argtypes = [ctypes.c_uint16]
+            getattr(lib, name).restype = ctypes.c_double
+        oracle._lib = lib
+        try:
+            for dtype in ("f16", "bf16"):
+                test_decoder_exhaustive(dtype)
+            for dtype in W.DTYPES:
+                for op in W.OPS:
+                    test_exhaustive_alphabet(dtype, op)
+                test_numpy_nan_free(dtype)
+                test_golden_semantics(dtype)
+                test_golden_long_axis(dtype)
+        except AssertionError:
+            return False
+        return True
+    finally:
+        oracle._lib = saved
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, old, new):
+    if shutil.which("gcc") is None:
+        pytest.skip("no host C compiler")
+    with open(oracle._SRC) as f:
+        src = f.read()
+    assert src.count(old) >= 1, f"mutation site not found: {old!r}"
+    mutated = src.replace(old, new, 1)
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "m.c")
+        so = os.path.join(d, "libm_oracle.so")
+        with open(c, "w") as f:
+            f.write(mutated)
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", c, "-o", so, "-lm"],
+                       check=True)
+        assert not _pin_suite_passes(so), f"mutant '{name}' survived the pins"
+
+
+def test_unmutated_passes_pin_suite():
+    assert _pin_suite_passes(oracle.build())
