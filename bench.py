@@ -1,0 +1,474 @@
+#!/usr/bin/env python3
+"""Benchmark of row-wise ArgMax/ArgMin on one GB300 (or N replicas).
+
+Workload (the default line): the wide-row sampler-logit group, i.e. ArgMax and
+ArgMin over [1, 202048] and [1, 262144] rows, fp32 and bf16, each with a unique
+planted extreme and with a duplicated one: 16 calls. One *step* is those 16
+calls, each on its own input already resident in HBM. Inputs are rotated over
+enough copies that the bytes touched between two reuses of a copy exceed the
+L2 cache, so every call reads from HBM. The steps are replayed as CUDA graphs
+(one per input copy) so that the device time is not host-bound.
+
+Metric: microseconds per call (lower is better) and achieved HBM GB/s of the
+algorithmic bytes (rows*cols*elem read + rows*8 written), against the measured
+copy bandwidth of this GPU.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--no-configs] [--no-cpu-baseline] [--workload NAME]
+
+One JSON line on stdout (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+L2_BYTES = 129 * 2**20
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "ArgMax/ArgMin µs/call and achieved HBM GB/s (% of GB300 peak) per [rows,cols]"
+WORKLOADS = {
+    # name -> (workload group, description)
+    "wide_rows": (2, "ArgMax+ArgMin fp32+bf16 [1,202048]+[1,262144], unique and duplicated planted extreme"),
+    "logits_32000": (1, "ArgMax fp32 [1,32000]"),
+    "batches": (3, "ArgMax fp16/bf16/fp32 [8,202048]+[32,202048]"),
+    "uniform_special": (4, "ArgMin/ArgMax fp32/f64 [4096,4096]+[65536,1024] with special rows"),
+    "narrow": (5, "ArgMax fp32 [65536,64]+[4096,8]+[4096,128]"),
+}
+DTYPE_LABEL = {"f32": "f32", "f16": "f16", "bf16": "bf16", "f64": "f64"}
+
+
+def algo_bytes(c: W.Case, with_values: bool = False) -> int:
+    """Algorithmic bytes of one call: the input read once, int64 indices written."""
+    es = W.ELEM_SIZE[c.dtype]
+    return c.rows * c.cols * es + c.rows * 8 + (c.rows * es if with_values else 0)
+
+
+def load_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "row_wise_arg_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        if n.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(csrc, n), "rb") as f:
+                h.update(n.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    src = kernel_source_hash()
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == workload and not line.startswith("#"):
+            if parts[2] != src:
+                return None
+            return float(parts[1])
+    return None
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region.
+# ---------------------------------------------------------------------------
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) >= 9:
+                    rows.append(f)
+        except Exception:
+            return None
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (replicas: every rank runs the same workload).
+# ---------------------------------------------------------------------------
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world <= 1:
+        return 0, 1, 0, None
+    import torch
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if backend == "nccl":
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend=backend)
+    return rank, world, local, dist
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None:
+            dist.barrier(device_ids=[device])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, v: float) -> float:
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline.
+# ---------------------------------------------------------------------------
+def oracle_time(cases, inputs, budget_s: float, max_calls: int = None):
+    """Time the oracle (as it stands) on host cores over a bounded sample of
+    calls, cycling through the cases. Returns (us_per_call, calls, cores)."""
+    import oracle
+    calls = 0
+    cores = 1
+    t0 = time.perf_counter()
+    while True:
+        c = cases[calls % len(cases)]
+        threads = min(os.cpu_count() or 1, c.rows) if c.rows > 1 else 1
+        _, _, used = oracle.argreduce(inputs[calls % len(cases)], c.dtype, c.op, threads=threads, want_val=False)
+        cores = max(cores, used)
+        calls += 1
+        el = time.perf_counter() - t0
+        if (max_calls is not None and calls >= max_calls) or (max_calls is None and el >= budget_s
+                                                                and calls >= len(cases)):
+            break
+    return el * 1e6 / calls, calls, cores, el
+
+
+# ---------------------------------------------------------------------------
+# GPU timing.
+# ---------------------------------------------------------------------------
+def to_dev(torch, x: np.ndarray, dtype: str):
+    view = {"f32": np.float32, "f16": np.int16, "bf16": np.int16, "f64": np.float64}[dtype]
+    return torch.from_numpy(np.ascontiguousarray(x).view(view)).cuda()
+
+
+class GraphSet:
+    """Calls captured as CUDA graphs over rotating input copies. Graph g runs
+    every case once on each of the copies g*per_graph .. (g+1)*per_graph-1,
+    so one replay is `per_graph` steps and consecutive uses of a copy are
+    separated by all the other copies' bytes."""
+
+    def __init__(self, torch, A, cases, dev_inputs, copies, per_graph, stream):
+        self.torch = torch
+        self.stream = stream
+        self.per_graph = per_graph
+        self.scratch = A.Scratch()
+        need = max([A.argreduce_scratch_bytes(c.rows, c.cols, c.dtype, c.op) for c in cases] + [0])
+        self.scratch.ensure(max(need, 4096), stream.cuda_stream)
+        self.copies = [[x] + [x.clone() for _ in range(copies - 1)] for x in dev_inputs]
+        self.outs = [torch.empty(max(c.rows, 1), dtype=torch.int64, device="cuda") for c in cases]
+        self.graphs = []
+
+        def calls(k):
+            for i, c in enumerate(cases):
+                A.argreduce(self.copies[i][k].view(c.rows, c.cols), c.op, dtype=c.dtype,
+                            out_idx=self.outs[i], scratch=self.scratch, stream=stream)
+
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for k in range(copies):  # eager warm-up of every call
+                calls(k)
+            stream.synchronize()
+            for g0 in range(0, copies, per_graph):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for k in range(g0, g0 + per_graph):
+                        calls(k)
+                self.graphs.append(g)
+        torch.cuda.synchronize()
+
+    def run(self, replays: int, start: int = 0):
+        for s in range(replays):
+            self.graphs[(start + s) % len(self.graphs)].replay()
+
+    def timed(self, replays: int, warmup: int, dist=None, device=None, clocks=None):
+        torch = self.torch
+        self.run(warmup)
+        torch.cuda.synchronize()
+        barrier(dist, device)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        if clocks:
+            clocks.start()
+        with torch.cuda.stream(self.stream):
+            e0.record(self.stream)
+            self.run(replays, start=warmup)
+            e1.record(self.stream)
+        e1.synchronize()
+        torch.cuda.synchronize()
+        clk = clocks.stop() if clocks else None
+        barrier(dist, device)
+        return e0.elapsed_time(e1) / 1e3, clk
+
+
+def copies_for(cases, cap: int = 4096) -> int:
+    """Input copies whose total exceeds twice the L2 cache."""
+    step_bytes = sum(c.nbytes for c in cases)
+    return max(1, min(cap, math.ceil(2 * L2_BYTES / max(step_bytes, 1))))
+
+
+def time_group(torch, A, cases, inputs, steps, warmup, stream, dist=None, device=None, clocks=None,
+               exact: bool = True):
+    """Time `steps` steps (each: every case once). With exact=True every graph
+    is one step (at most 64 copies); otherwise graphs hold several steps and
+    the step count is rounded up to whole replays. Returns (seconds, steps
+    timed, copies, clocks)."""
+    copies = copies_for(cases, cap=64 if exact else 4096)
+    per_graph = 1 if exact else max(1, math.ceil(copies / 16))
+    copies = per_graph * math.ceil(copies / per_graph)
+    dev = [to_dev(torch, x, c.dtype).reshape(-1) for c, x in zip(cases, inputs)]
+    gs = GraphSet(torch, A, cases, dev, copies, per_graph, stream)
+    replays = math.ceil(steps / per_graph)
+    secs, clk = gs.timed(replays, max(3, math.ceil(warmup / per_graph)), dist, device, clocks)
+    del gs, dev
+    return secs, replays * per_graph, copies, clk
+
+
+def e2e_time(torch, A, cases, inputs, steps, stream):
+    """The public call path with host buffers: every step copies the inputs
+    from pinned host memory, runs the calls and reads the indices back."""
+    hosts = [torch.from_numpy(np.ascontiguousarray(x).view(
+        {"f32": np.float32, "f16": np.int16, "bf16": np.int16, "f64": np.float64}[c.dtype])).pin_memory()
+        for c, x in zip(cases, inputs)]
+    devs = [torch.empty_like(h, device="cuda") for h in hosts]
+    outs = [torch.empty(c.rows, dtype=torch.int64, device="cuda") for c in cases]
+    host_out = torch.empty(sum(c.rows for c in cases), dtype=torch.int64).pin_memory()
+    scratch = A.Scratch()
+    h2d = sum(h.numel() * h.element_size() for h in hosts)
+    d2h = host_out.numel() * 8
+
+    def step():
+        off = 0
+        for c, h, d, o in zip(cases, hosts, devs, outs):
+            d.copy_(h, non_blocking=True)
+            A.argreduce(d, c.op, dtype=c.dtype, out_idx=o, scratch=scratch, stream=stream)
+            host_out[off:off + c.rows].copy_(o, non_blocking=True)
+            off += c.rows
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        e1.synchronize()
+        wall = time.perf_counter() - t0
+    return e0.elapsed_time(e1) / 1e3, wall, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+def reference_arm(args, rank, world, dist):
+    """The oracle on host cores, on the same workload and metric."""
+    if rank != 0:
+        return 0
+    group, desc = WORKLOADS[args.workload]
+    cases = W.config_cases(group)
+    inputs = [W.make(c) for c in cases]
+    oracle_time(cases, inputs, 0.0, max_calls=min(len(cases), max(1, args.warmup)))
+    us, calls, cores, el = oracle_time(cases, inputs, 0.0, max_calls=max(1, args.steps))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": "us/call", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": us * len(cases) / 1e3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32+bf16"
+        if group == 2 else "mixed", "data": "synthetic",
+        "config": {"workload": args.workload, "description": desc, "cases": len(cases),
+                   "step": "one oracle call per step, cycling through the cases (bounded sample)"},
+        "cpu_baseline": {"value": us, "unit": "us/call", "cores": cores, "kind": "oracle",
+                         "sample": f"{calls} calls cycling over {len(cases)} cases, {el:.2f} s"},
+        "e2e": {"value": us, "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="wide_rows", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload table")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--e2e-steps", type=int, default=300)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    rank, world, local, dist = dist_setup(args.gpus)
+    if args.impl == "reference":
+        return reference_arm(args, rank, world, dist)
+
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    from row_wise_arg_gb300.build import build
+    if rank == 0 or world == 1:
+        build()
+    barrier(dist, local if world > 1 else None)
+    import row_wise_arg_gb300 as A
+
+    torch.cuda.set_device(local)
+    stream = torch.cuda.Stream()
+    group, desc = WORKLOADS[args.workload]
+    cases = W.config_cases(group)
+    inputs = [W.make(c) for c in cases]
+    step_bytes = sum(algo_bytes(c) for c in cases)
+    peak, peak_src = load_peak()
+
+    clocks = Clocks(local)
+    secs, _, copies, clk = time_group(torch, A, cases, inputs, args.steps, args.warmup, stream,
+                                      dist, local if world > 1 else None, clocks)
+    secs = max_over_ranks(dist, secs)
+    calls = args.steps * len(cases)
+    us_per_call = secs * 1e6 / (calls * world)
+    achieved = step_bytes * args.steps / secs / 1e9  # per GPU (every rank runs the same steps)
+    plans = {}
+    for c in cases:
+        p = A.argreduce_plan(c.rows, c.cols, c.dtype, c.op).as_dict()
+        plans[f"{c.rows}x{c.cols}_{c.dtype}"] = {k: p[k] for k in ("path_name", "blocks_per_row", "block",
+                                                                    "unroll", "group")}
+
+    result = {
+        "metric": METRIC, "value": round(us_per_call, 4), "unit": "us/call", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3 / args.steps, 5),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "+".join(sorted({DTYPE_LABEL[c.dtype] for c in cases})), "data": "synthetic",
+        "config": {"workload": args.workload, "description": desc, "calls_per_step": len(cases),
+                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                   "l2": f"inputs larger than L2: {copies} rotating copies of the step's inputs "
+                         f"({copies * sum(c.nbytes for c in cases) / 2**20:.0f} MiB)",
+                   "launch": "CUDA graph per input copy, 16 argreduce calls per graph",
+                   "plans": plans},
+        "hbm_gbs": round(achieved, 2),
+        "gpu_launches": calls,
+    }
+    result["clocks"] = clk
+    traffic = read_traffic(args.workload)
+    result["roofline"] = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                          "frac": round(achieved / peak, 5), "traffic": traffic,
+                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                          else "fallback", "kernel": "split_kernel (all calls of this workload)",
+                          "bytes_per_launch_avg": step_bytes / len(cases)}
+
+    if world == 1 or rank == 0:
+        dev_s, wall, h2d, d2h = e2e_time(torch, A, cases, inputs, args.e2e_steps, stream)
+        result["e2e"] = {"value": round(dev_s * 1e6 / (args.e2e_steps * len(cases)), 4), "unit": "us/call",
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                         "host_wall_us_per_call": round(wall * 1e6 / (args.e2e_steps * len(cases)), 4),
+                         "steps": args.e2e_steps}
+
+    if not args.no_configs and (world == 1 or rank == 0):
+        table = []
+        for name, (g, _) in sorted(WORKLOADS.items(), key=lambda kv: kv[1][0]):
+            gcases = W.config_cases(g)
+            ginputs = [W.make(c) for c in gcases]
+            for c, x in zip(gcases, ginputs):
+                if c.variant == "dup":
+                    continue
+                n = max(20, min(4000, int(2e9 / max(c.nbytes, 1) / 50)))
+                s, n, cp, _ = time_group(torch, A, [c], [x], n, 5, stream, exact=False)
+                us = s * 1e6 / n
+                gbs = algo_bytes(c) / (s / n) / 1e9
+                table.append({"case": c.name, "us_per_call": round(us, 3), "gbs": round(gbs, 1),
+                              "frac": round(gbs / peak, 4),
+                              "path": A.argreduce_plan(c.rows, c.cols, c.dtype, c.op).as_dict()["path_name"]})
+            del ginputs
+        result["configs"] = table
+
+    if not args.no_cpu_baseline and (world == 1 or rank == 0):
+        us, ncalls, cores, el = oracle_time(cases, inputs, args.cpu_budget)
+        result["cpu_baseline"] = {"value": round(us, 3), "unit": "us/call", "cores": cores, "kind": "oracle",
+                                  "sample": f"{ncalls} oracle calls cycling over the {len(cases)} cases of the "
+                                            f"step on host cores ({el:.1f} s)"}
+
+    if world == 1 or rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,186 @@
+/*
+ * argreduce.h - row-wise ArgMax / ArgMin over the last axis on a GB300 GPU.
+ *
+ * C ABI of libargreduce.so. Every argument is a plain pointer or integer; no
+ * C++ or framework type crosses this boundary. Device pointers are CUDA
+ * device addresses in the caller's current context. The library never
+ * allocates, frees or synchronises memory inside argreduce(); all work is
+ * queued on the caller's stream.
+ *
+ * The operation is defined by two onnxruntime pull requests:
+ *   - "[CUDA] Parallelize ArgMax/ArgMin over wide last axes" (#32092),
+ *     sections Approach and Semantics: a [rows, cols] row-major tensor is
+ *     reduced over its last axis to one int64 index per row; ties resolve to
+ *     the lowest index; a leading NaN yields index 0; rows that are entirely
+ *     -inf, +inf or NaN yield index 0; the result equals the sequential
+ *     one-thread-per-row scan bit for bit for every input.
+ *   - "[CUDA] Parallelize ArgMax/ArgMin over the reduction axis" (#31694),
+ *     section Semantics: the sequential scan seeds with element 0 and a later
+ *     element replaces the candidate only when strictly better.
+ *
+ * "Strictly better" is an IEEE comparison: greater (ArgMax) or less (ArgMin),
+ * false when either operand is NaN. So a NaN after element 0 never wins, +0.0
+ * and -0.0 tie (lowest index wins), and subnormals are compared exactly
+ * (no flush to zero). binary16 and bfloat16 values are compared after an
+ * exact widening to binary32.
+ */
+#ifndef ARGREDUCE_H
+#define ARGREDUCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t. NULL is the legacy default stream. */
+typedef struct CUstream_st* argr_stream;
+
+/* Element type of x (and of out_val). */
+typedef enum {
+    ARGR_F32 = 0,  /* IEEE binary32 */
+    ARGR_F16 = 1,  /* IEEE binary16 */
+    ARGR_BF16 = 2, /* bfloat16 (upper half of binary32) */
+    ARGR_F64 = 3   /* IEEE binary64 */
+} argr_dtype;
+
+typedef enum { ARGR_MAX = 0, ARGR_MIN = 1 } argr_op;
+
+typedef enum {
+    ARGR_OK = 0,
+    ARGR_EINVAL = 1,      /* bad pointer, size, enum or plan; nothing was launched */
+    ARGR_ESCRATCH = 2,    /* scratch missing, too small or not 16-byte aligned; nothing launched */
+    ARGR_EUNSUPPORTED = 3,/* valid request this build or device cannot run; nothing launched */
+    ARGR_ECUDA = 4,       /* a CUDA runtime call failed (launch or device query) */
+    ARGR_ETIMEOUT = 5     /* a bounded device-side wait expired (reported by argreduce_read_error) */
+} argr_status;
+
+/* Kernel paths the planner chooses between (#32092 Approach: thread per row
+ * for narrow rows; a row spread over warps and blocks otherwise). */
+typedef enum {
+    ARGR_PATH_NONE = 0,    /* rows == 0: nothing to launch */
+    ARGR_PATH_ROWS = 1,    /* `group` lanes per row (1 = thread per row, 32 = warp per row) */
+    ARGR_PATH_SPLIT = 2,   /* `blocks_per_row` CTAs per row; >1 merges through scratch,
+                              the last CTA to arrive for a row reduces the partials */
+    ARGR_PATH_CLUSTER = 3  /* one thread-block cluster of `cluster` CTAs per row, merged
+                              through distributed shared memory; no scratch */
+} argr_path;
+
+/* Device properties the planner uses. */
+typedef struct {
+    int32_t sm_count;           /* streaming multiprocessors */
+    int32_t max_threads_per_sm; /* resident threads per SM */
+    int32_t max_cluster;        /* largest cluster size this device launches (1 = none) */
+    int32_t cc_major, cc_minor; /* compute capability */
+} argr_caps;
+
+/* A launch plan. Produced by argreduce_plan(); tests may edit it to force a
+ * path and pass it to argreduce_with_plan(), which re-validates it. */
+typedef struct {
+    int32_t path;           /* argr_path */
+    int32_t block;          /* threads per CTA: multiple of 32, 32..1024 */
+    int32_t group;          /* ROWS: lanes per row, power of two 1..32 */
+    int32_t vec;            /* 1: 16-byte vector loads (ROWS needs every row 16-byte aligned) */
+    int32_t unroll;         /* vector (or scalar) loads in flight per thread per step: 1,2,4,8 */
+    int32_t cluster;        /* CLUSTER: CTAs per cluster, 2..16 */
+    int64_t blocks_per_row; /* SPLIT / CLUSTER: CTAs that share one row */
+    int64_t grid_rows;      /* SPLIT / CLUSTER: row slots in the grid (rows loop over them);
+                               ROWS: number of CTAs */
+    uint64_t scratch_bytes; /* bytes of scratch this plan needs (0 = none) */
+} argr_plan;
+
+/*
+ * Scratch bytes argreduce() needs for this problem on the current device
+ * (0 when the chosen path needs none). The bound is small: a multi-CTA row
+ * needs one 16-byte partial per CTA plus a 4-byte counter per row, and such
+ * plans are only chosen while the whole grid fits one wave of the device
+ * (#32092 Approach: scratch bounded by the device's thread capacity).
+ * Returns 0 also when the device cannot be queried; argreduce() then reports
+ * the error.
+ */
+size_t argreduce_scratch_bytes(int64_t rows, int64_t cols, argr_dtype dtype, argr_op op);
+
+/*
+ * Prepare a scratch buffer once after allocating it: zeroes the per-row
+ * arrival counters and the error word (an asynchronous memset on `stream`).
+ * After that the counters reset themselves at the end of every call, so no
+ * per-call memset is needed and argreduce() can be captured in a CUDA graph
+ * and replayed. The partial-result region may hold any bytes between calls.
+ * `scratch` must be a device pointer, 16-byte aligned.
+ */
+argr_status argreduce_scratch_init(void* scratch, size_t scratch_bytes, argr_stream stream);
+
+/*
+ * Row-wise ArgMax (op = ARGR_MAX) or ArgMin (ARGR_MIN) of x[rows, cols].
+ *
+ *   x         device pointer to rows*cols elements of `dtype`, row-major and
+ *             contiguous (row r starts at element r*cols). Any address that is
+ *             a multiple of the element size; unaligned row starts are handled.
+ *   rows      >= 0. rows == 0 returns ARGR_OK and launches nothing.
+ *   cols      1 .. INT32_MAX (the index is computed in 32 bits within a row).
+ *   out_idx   device pointer to rows int64 values (written).
+ *   out_val   NULL, or a device pointer to rows elements of `dtype`, aligned to
+ *             the element size; receives the raw bits of x[r, out_idx[r]]
+ *             (NaN payloads and the sign of zero preserved).
+ *   scratch   device pointer prepared by argreduce_scratch_init(), 16-byte
+ *             aligned, at least argreduce_scratch_bytes() bytes; may be NULL
+ *             when that is 0. Owned by the caller. Two calls that may run at
+ *             the same time on the GPU must not share a scratch buffer.
+ *   stream    CUDA stream the kernel is queued on.
+ *
+ * All validation happens before any launch: on an error status nothing was
+ * queued. The call does not synchronise; kernel faults surface on the stream.
+ * No per-call allocation, memset or host synchronisation, so the call can be
+ * captured into a CUDA graph (as long as the same scratch stays alive).
+ */
+argr_status argreduce(const void* x, argr_dtype dtype, int64_t rows, int64_t cols, argr_op op,
+                      int64_t* out_idx, void* out_val, void* scratch, size_t scratch_bytes,
+                      argr_stream stream);
+
+/*
+ * Query the planner. caps == NULL uses the current device (one query per
+ * device, cached); a non-NULL caps plans for those properties instead, which
+ * lets tests force geometries of other device sizes (#32092 Testing: fuzz
+ * repeated with several simulated device capacities). Pure host code when
+ * caps is given: needs no GPU.
+ */
+argr_status argreduce_plan(int64_t rows, int64_t cols, argr_dtype dtype, argr_op op,
+                           const argr_caps* caps, argr_plan* out);
+
+/*
+ * argreduce() with an explicit plan (tests and benchmarks force each path
+ * with it). The plan is checked against the problem and the device: an
+ * impossible plan returns ARGR_EINVAL (or ARGR_EUNSUPPORTED for a cluster the
+ * device cannot launch) before anything is queued. Scratch must be at least
+ * plan->scratch_bytes as recomputed for the problem.
+ */
+argr_status argreduce_with_plan(const argr_plan* plan, const void* x, argr_dtype dtype, int64_t rows,
+                                int64_t cols, argr_op op, int64_t* out_idx, void* out_val, void* scratch,
+                                size_t scratch_bytes, argr_stream stream);
+
+/* Scratch bytes a given plan needs for `rows` rows. */
+size_t argreduce_plan_scratch_bytes(const argr_plan* plan, int64_t rows);
+
+/*
+ * Synchronise `stream` and read the device error word in `scratch` (written
+ * by a kernel whose bounded wait expired). Returns ARGR_ETIMEOUT if set (and
+ * clears it), ARGR_OK otherwise, ARGR_ECUDA if the stream reports a fault.
+ * For tests and benchmarks; it blocks the host.
+ */
+argr_status argreduce_read_error(void* scratch, argr_stream stream);
+
+/* Properties of `device` as the planner sees them (queried once, cached). */
+argr_status argreduce_device_caps(int device, argr_caps* out);
+
+/* Static, human-readable name of a status code. */
+const char* argreduce_status_string(argr_status status);
+
+/* Build identification: "argreduce <version> sm_103a". */
+const char* argreduce_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ARGREDUCE_H */

@@ -1,0 +1,164 @@
+"""Row-wise ArgMax / ArgMin over the last axis on a GB300 (sm_103a).
+
+The reduction runs in hand-written CUDA kernels behind the C ABI of
+``libargreduce.so`` (``include/argreduce.h``). This package is the thin Python
+binding: it takes torch tensors for device memory and streams and passes raw
+pointers to the library. It has no CPU fallback.
+
+Semantics (onnxruntime #32092 and #31694, Semantics sections): one int64 index
+per row; ties resolve to the lowest index; a leading NaN gives index 0; later
+NaNs never win; rows entirely -inf, +inf or NaN give index 0.
+"""
+from __future__ import annotations
+
+import threading
+from typing import Dict, Optional, Tuple
+
+from . import _lib
+from ._lib import (ARGR_BF16, ARGR_F16, ARGR_F32, ARGR_F64, ARGR_MAX, ARGR_MIN,  # noqa: F401
+                   ARGR_OK, ArgreduceError, DTYPE_CODES, OP_CODES, argr_caps, argr_plan, argreduce_device_caps,
+                   argreduce_plan, argreduce_plan_scratch_bytes, argreduce_read_error, argreduce_scratch_bytes,
+                   argreduce_scratch_init, argreduce_status_string, argreduce_version, load, make_caps)
+
+__all__ = [
+    "argreduce", "argmax", "argmin", "argreduce_with_plan", "argreduce_plan", "argreduce_scratch_bytes",
+    "argreduce_scratch_init", "argreduce_read_error", "argreduce_device_caps", "argreduce_status_string",
+    "argreduce_version", "argreduce_plan_scratch_bytes", "ArgreduceError", "Scratch", "make_caps",
+]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def dtype_code(t, dtype: Optional[str]) -> int:
+    """Element type code for a tensor; raw 16-bit tensors need ``dtype``."""
+    torch = _torch()
+    if dtype is not None:
+        code = DTYPE_CODES[dtype]
+        if t.element_size() != {0: 4, 1: 2, 2: 2, 3: 8}[code]:
+            raise TypeError(f"dtype {dtype} does not match element size {t.element_size()}")
+        return code
+    m = {torch.float32: ARGR_F32, torch.float16: ARGR_F16, torch.bfloat16: ARGR_BF16, torch.float64: ARGR_F64}
+    if t.dtype not in m:
+        raise TypeError(f"unsupported tensor dtype {t.dtype}; pass dtype= for raw 16-bit storage")
+    return m[t.dtype]
+
+
+class Scratch:
+    """Device scratch for one stream, grown on demand and prepared with
+    argreduce_scratch_init() whenever it is (re)allocated. Two calls that can
+    run concurrently on the GPU must use different Scratch objects."""
+
+    def __init__(self, device=None, nbytes: int = 0):
+        torch = _torch()
+        self.device = torch.device("cuda", torch.cuda.current_device() if device is None else
+                                   torch.device(device).index or 0)
+        self.buf = None
+        self.nbytes = 0
+        if nbytes:
+            self.ensure(nbytes, torch.cuda.current_stream(self.device).cuda_stream)
+
+    def ensure(self, nbytes: int, stream_ptr: int):
+        if nbytes <= self.nbytes:
+            return
+        torch = _torch()
+        n = max(nbytes, 4096)
+        self.buf = torch.empty(n, dtype=torch.uint8, device=self.device)
+        st = argreduce_scratch_init(self.buf.data_ptr(), n, stream_ptr)
+        if st != ARGR_OK:
+            raise ArgreduceError(st, "argreduce_scratch_init")
+        self.nbytes = n
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr() if self.buf is not None else 0
+
+
+_scratch_lock = threading.Lock()
+_scratch: Dict[Tuple[int, int], Scratch] = {}
+
+
+def _default_scratch(device_index: int, stream_ptr: int) -> Scratch:
+    key = (device_index, stream_ptr)
+    with _scratch_lock:
+        s = _scratch.get(key)
+        if s is None:
+            s = _scratch[key] = Scratch(device_index)
+        return s
+
+
+def _prepare(x, op, dtype, with_values, out_idx, out_val):
+    torch = _torch()
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor (the library has no CPU path)")
+    if x.dim() == 0:
+        raise ValueError("x must have at least one dimension")
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous (row-major, reduced over its last axis)")
+    cols = x.shape[-1]
+    rows = x.numel() // cols if cols else 0
+    code = dtype_code(x, dtype)
+    lead = tuple(x.shape[:-1])
+    if out_idx is None:
+        out_idx = torch.empty(lead, dtype=torch.int64, device=x.device)
+    if with_values and out_val is None:
+        out_val = torch.empty(lead, dtype=x.dtype, device=x.device)
+    return rows, cols, code, _lib._code(OP_CODES, op), out_idx, out_val
+
+
+def argreduce(x, op="max", *, dtype: Optional[str] = None, with_values: bool = False, out_idx=None, out_val=None,
+              scratch: Optional[Scratch] = None, stream=None):
+    """Reduce the last axis of a contiguous CUDA tensor.
+
+    Returns ``(indices, values)``: int64 indices of shape ``x.shape[:-1]`` and,
+    if ``with_values`` (or ``out_val``) is given, the raw elements
+    ``x[..., index]`` (else ``None``). Runs on ``stream`` (default: torch's
+    current stream) without synchronising.
+    """
+    torch = _torch()
+    rows, cols, code, opc, out_idx, out_val = _prepare(x, op, dtype, with_values, out_idx, out_val)
+    st_ptr = (stream if isinstance(stream, int) else stream.cuda_stream) if stream is not None else \
+        torch.cuda.current_stream(x.device).cuda_stream
+    need = argreduce_scratch_bytes(rows, cols, code, opc) if rows else 0
+    if scratch is None and need:
+        scratch = _default_scratch(x.device.index, st_ptr)
+    if need:
+        scratch.ensure(need, st_ptr)
+    st = _lib.argreduce_raw(x.data_ptr(), code, rows, cols, opc, out_idx.data_ptr(),
+                            out_val.data_ptr() if out_val is not None else 0,
+                            scratch.ptr if scratch is not None else 0,
+                            scratch.nbytes if scratch is not None else 0, st_ptr)
+    if st != ARGR_OK:
+        raise ArgreduceError(st, "argreduce")
+    return out_idx, out_val
+
+
+def argreduce_with_plan(plan: argr_plan, x, op="max", *, dtype: Optional[str] = None, with_values: bool = False,
+                        out_idx=None, out_val=None, scratch: Optional[Scratch] = None, stream=None):
+    """argreduce() with an explicit (possibly forced) plan."""
+    torch = _torch()
+    rows, cols, code, opc, out_idx, out_val = _prepare(x, op, dtype, with_values, out_idx, out_val)
+    st_ptr = (stream if isinstance(stream, int) else stream.cuda_stream) if stream is not None else \
+        torch.cuda.current_stream(x.device).cuda_stream
+    need = argreduce_plan_scratch_bytes(plan, rows)
+    if scratch is None and need:
+        scratch = _default_scratch(x.device.index, st_ptr)
+    if need:
+        scratch.ensure(need, st_ptr)
+    st = _lib.argreduce_with_plan_raw(plan, x.data_ptr(), code, rows, cols, opc, out_idx.data_ptr(),
+                                      out_val.data_ptr() if out_val is not None else 0,
+                                      scratch.ptr if scratch is not None else 0,
+                                      scratch.nbytes if scratch is not None else 0, st_ptr)
+    if st != ARGR_OK:
+        raise ArgreduceError(st, "argreduce_with_plan")
+    return out_idx, out_val
+
+
+def argmax(x, **kw):
+    return argreduce(x, "max", **kw)[0]
+
+
+def argmin(x, **kw):
+    return argreduce(x, "min", **kw)[0]

@@ -1,0 +1,69 @@
+// Host-side declarations shared by the planner, the API layer and the kernel
+// launchers. Not part of the public interface (include/argreduce.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "argreduce.h"
+
+#ifdef __CUDACC__
+#define ARGR_HD __host__ __device__
+#else
+#define ARGR_HD
+#endif
+
+namespace argr {
+
+// Scratch layout (the buffer is 16-byte aligned):
+//   [0, 4)                 device error word (set by an expired bounded wait)
+//   [kCounterOffset, ...)  one uint32 arrival counter per row slot
+//   [partials_offset, ...) row_slots * blocks_per_row partials of 16 bytes
+//                          (raw value bits in the low bytes of 8, index in 4)
+constexpr size_t kCounterOffset = 256;
+constexpr size_t kPartialBytes = 16;
+
+ARGR_HD inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+ARGR_HD inline size_t partials_offset(int64_t row_slots) {
+    return align_up(kCounterOffset + 4 * static_cast<size_t>(row_slots), 256);
+}
+
+struct Problem {
+    const void* x;
+    int dtype;     // argr_dtype
+    int op;        // argr_op
+    int64_t rows;
+    int cols;      // 1 .. INT32_MAX
+    int64_t* out_idx;
+    void* out_val;
+    void* scratch;
+    cudaStream_t stream;
+};
+
+int elem_size(int dtype);
+
+// Planner (plan.cpp): pure host code. `base_aligned`: x is 16-byte aligned.
+argr_status make_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_caps& caps, bool base_aligned,
+                      argr_plan* out);
+// Validates a (possibly hand-edited) plan for this problem and device.
+// `row_aligned`: every row start is 16-byte aligned (base aligned and
+// cols * elem_size a multiple of 16).
+argr_status check_plan(const argr_plan& p, int64_t rows, int64_t cols, int dtype, const argr_caps& caps,
+                       bool row_aligned);
+size_t plan_scratch(const argr_plan& p, int64_t rows);
+
+// Kernel launchers (one translation unit per element type). They assume a
+// checked plan and return the launch's CUDA error.
+#define ARGR_DECLARE_LAUNCHERS(sfx)                                              \
+    cudaError_t launch_rows_##sfx(const argr_plan& p, const Problem& pr);    \
+    cudaError_t launch_split_##sfx(const argr_plan& p, const Problem& pr);   \
+    cudaError_t launch_cluster_##sfx(const argr_plan& p, const Problem& pr);
+ARGR_DECLARE_LAUNCHERS(f32)
+ARGR_DECLARE_LAUNCHERS(f16)
+ARGR_DECLARE_LAUNCHERS(bf16)
+ARGR_DECLARE_LAUNCHERS(f64)
+#undef ARGR_DECLARE_LAUNCHERS
+
+}  // namespace argr

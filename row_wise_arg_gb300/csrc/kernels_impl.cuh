@@ -1,0 +1,394 @@
+// argreduce kernels, templated on element tag, op and geometry. Each
+// kernels_<dtype>.cu instantiates them for one element type.
+//
+// Three paths (onnxruntime #32092 Approach, #31694 Description):
+//  * rows_kernel    - G lanes per row (G = 1: one thread per row, G = 32: one
+//                     warp per row), many rows per CTA, rows 16-byte aligned
+//                     (VEC) or not (scalar loads). For narrow and medium rows.
+//  * split_kernel   - one or more CTAs per row. A row spread over several CTAs
+//                     is merged through a small global scratch: each CTA
+//                     writes a partial, fences, and bumps the row's arrival
+//                     counter; the CTA that arrives last merges the partials.
+//                     The counter is bumped with a wrapping increment, so it
+//                     is back at zero after every row and needs no memset.
+//  * cluster_kernel - one thread-block cluster per row: CTAs push their
+//                     candidates into CTA 0's shared memory (distributed shared
+//                     memory) and meet at a cluster barrier. No scratch.
+//
+// Index arithmetic: within a row every position is an int in [0, cols) with
+// cols <= INT32_MAX. Loops are written with differences (remaining = end -
+// position, and a step is only taken when it is smaller than what remains), so
+// no sum can leave [0, cols) (#32092 review follow-up on the overflowing scan).
+// Row offsets are 64-bit.
+#pragma once
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace argr {
+
+// ---------------------------------------------------------------------------
+// G lanes per row.
+// ---------------------------------------------------------------------------
+template <class Tag, int OP, int G, bool VEC, int U>
+__global__ void __launch_bounds__(1024)
+rows_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int64_t* __restrict__ out_idx,
+            typename Tag::raw* __restrict__ out_val) {
+    using R = typename Tag::raw;
+    constexpr int E = 16 / sizeof(R);
+    const int lg = threadIdx.x & (G - 1);
+    const int lane = threadIdx.x & 31;
+    const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
+    const int groups_per_block = blockDim.x / G;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * groups_per_block;
+
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * groups_per_block + threadIdx.x / G; r < rows;
+         r += stride) {
+        const R* row = x + r * static_cast<int64_t>(cols);
+        Cand<Tag> c;
+        if constexpr (VEC) {
+            // Every row starts on a 16-byte boundary and cols % E == 0.
+            const uint4* rv = reinterpret_cast<const uint4*>(row);
+            const int nvec = cols / E;
+            int v0 = lg;
+            int rem = nvec - v0;
+            uint4 buf[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) buf[u] = (u * G < rem) ? ld_stream16(rv + v0 + u * G) : make_uint4(0, 0, 0, 0);
+            // Lane 0 of the group always holds vector 0, whose first element is x[0].
+            c.v = shfl_raw(gmask, vec_elem<R>(buf[0], 0), 0, G);
+            c.i = 0;
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (u * G < rem) visit_vec<Tag, OP>(c, buf[u], (v0 + u * G) * E);
+            while (rem > G * U) {
+                v0 += G * U;
+                rem = nvec - v0;
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (u * G < rem) buf[u] = ld_stream16(rv + v0 + u * G);
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (u * G < rem) visit_vec<Tag, OP>(c, buf[u], (v0 + u * G) * E);
+            }
+        } else {
+            int j0 = lg;
+            int rem = cols - j0;
+            R buf[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) buf[u] = (u * G < rem) ? ld_scalar(row + j0 + u * G) : R(0);
+            c.v = shfl_raw(gmask, buf[0], 0, G);  // lane 0 loaded x[0]
+            c.i = 0;
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (u * G < rem) visit<Tag, OP>(c, buf[u], j0 + u * G);
+            while (rem > G * U) {
+                j0 += G * U;
+                rem = cols - j0;
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (u * G < rem) buf[u] = ld_scalar(row + j0 + u * G);
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (u * G < rem) visit<Tag, OP>(c, buf[u], j0 + u * G);
+            }
+        }
+        c = group_merge<Tag, OP, G>(c, gmask);
+        if (lg == 0) {
+            out_idx[r] = c.i;
+            if (out_val) out_val[r] = c.v;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Scan of this CTA's share of one row (shared by the split and cluster paths).
+// The row is cut into a scalar head up to the first 16-byte boundary, a body
+// of 16-byte vectors and a scalar tail. CTA b of nb owns a contiguous chunk of
+// the body; CTA 0 also owns the head and CTA nb-1 the tail. Each thread visits
+// its elements in increasing index order (head, body, tail).
+// ---------------------------------------------------------------------------
+template <class Tag, int OP, int U>
+__device__ __forceinline__ Cand<Tag> scan_share(const typename Tag::raw* __restrict__ row, int cols, int b, int nb,
+                                                typename Tag::raw x0) {
+    using R = typename Tag::raw;
+    constexpr int E = 16 / sizeof(R);
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
+    int head = static_cast<int>(((16u - (addr & 15u)) & 15u) / sizeof(R));
+    if (head > cols) head = cols;
+    const int nvec = (cols - head) / E;
+    const int tail0 = head + nvec * E;
+    const uint4* rv = reinterpret_cast<const uint4*>(row + head);
+    const int chunk = nvec / nb + (nvec % nb != 0);
+    const int vb = b * chunk < nvec ? b * chunk : nvec;
+    const int ve = nvec - vb > chunk ? vb + chunk : nvec;
+
+    Cand<Tag> c{x0, 0};
+    const int t = threadIdx.x;
+    const int nt = blockDim.x;
+    if (b == 0 && t < head) visit<Tag, OP>(c, ld_scalar(row + t), t);
+
+    int v0 = vb + t;
+    if (v0 < ve) {
+        for (;;) {
+            const int rem = ve - v0;
+            uint4 buf[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (u * nt < rem) buf[u] = ld_stream16(rv + v0 + u * nt);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (u * nt < rem) visit_vec<Tag, OP>(c, buf[u], head + (v0 + u * nt) * E);
+            if (rem <= U * nt) break;
+            v0 += U * nt;
+        }
+    }
+    if (b == nb - 1 && t < cols - tail0) visit<Tag, OP>(c, ld_scalar(row + tail0 + t), tail0 + t);
+    return c;
+}
+
+template <class Tag>
+__device__ __forceinline__ uint4 pack_cand(const Cand<Tag>& c) {
+    using R = typename Tag::raw;
+    uint64_t bits = 0;
+    if constexpr (sizeof(R) == 8)
+        bits = static_cast<uint64_t>(__double_as_longlong(c.v));
+    else if constexpr (sizeof(R) == 4)
+        bits = __float_as_uint(c.v);
+    else
+        bits = c.v;
+    return make_uint4(static_cast<uint32_t>(bits), static_cast<uint32_t>(bits >> 32), static_cast<uint32_t>(c.i), 0u);
+}
+
+template <class Tag>
+__device__ __forceinline__ Cand<Tag> unpack_cand(const uint4& p) {
+    using R = typename Tag::raw;
+    Cand<Tag> c;
+    if constexpr (sizeof(R) == 8)
+        c.v = __hiloint2double(static_cast<int>(p.y), static_cast<int>(p.x));
+    else if constexpr (sizeof(R) == 4)
+        c.v = __uint_as_float(p.x);
+    else
+        c.v = static_cast<uint16_t>(p.x);
+    c.i = static_cast<int>(p.z);
+    return c;
+}
+
+// ---------------------------------------------------------------------------
+// One or more CTAs per row; grid = (blocks_per_row, row_slots).
+// With blocks_per_row > 1 every row has its own slot (row_slots >= rows).
+// ---------------------------------------------------------------------------
+template <class Tag, int OP, int U>
+__global__ void __launch_bounds__(1024)
+split_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int64_t* __restrict__ out_idx,
+             typename Tag::raw* __restrict__ out_val, unsigned char* __restrict__ scratch) {
+    using R = typename Tag::raw;
+    __shared__ Cand<Tag> smem[32];
+    __shared__ int s_last;
+    const int nb = gridDim.x;
+    const int b = blockIdx.x;
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+        const R* row = x + r * static_cast<int64_t>(cols);
+        const R x0 = ld_scalar(row);
+        const Cand<Tag> seed{x0, 0};
+        Cand<Tag> c = scan_share<Tag, OP, U>(row, cols, b, nb, x0);
+        c = block_merge<Tag, OP>(c, smem, seed);
+        if (nb == 1) {
+            if (threadIdx.x == 0) {
+                out_idx[r] = c.i;
+                if (out_val) out_val[r] = c.v;
+            }
+        } else {
+            unsigned int* counter = reinterpret_cast<unsigned int*>(scratch + kCounterOffset) + blockIdx.y;
+            uint4* parts = reinterpret_cast<uint4*>(scratch + partials_offset(gridDim.y)) +
+                           static_cast<size_t>(blockIdx.y) * nb;
+            if (threadIdx.x == 0) {
+                __stcg(parts + b, pack_cand<Tag>(c));
+                __threadfence();  // the partial is visible device-wide before the arrival
+                // Wrapping increment: the nb-th arrival returns nb-1 and leaves 0.
+                const unsigned old = atomicInc(counter, static_cast<unsigned>(nb - 1));
+                s_last = old == static_cast<unsigned>(nb - 1);
+            }
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+                Cand<Tag> m = seed;
+                for (int k = threadIdx.x; k < nb; k += blockDim.x)
+                    m = merge<Tag, OP>(m, unpack_cand<Tag>(__ldcg(parts + k)));
+                m = block_merge<Tag, OP>(m, smem, seed);
+                if (threadIdx.x == 0) {
+                    out_idx[r] = m.i;
+                    if (out_val) out_val[r] = m.v;
+                }
+            }
+        }
+        __syncthreads();  // shared memory is reused by the next row
+    }
+}
+
+// ---------------------------------------------------------------------------
+// One cluster of gridDim.x CTAs per row; grid = (cluster, row_slots).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned smem_addr(const void* p) {
+    return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <class Tag, int OP, int U>
+__global__ void __launch_bounds__(1024)
+cluster_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int64_t* __restrict__ out_idx,
+               typename Tag::raw* __restrict__ out_val) {
+    using R = typename Tag::raw;
+    __shared__ Cand<Tag> smem[32];
+    __shared__ __align__(16) uint4 slots[2][16];  // written by every CTA of the cluster into CTA 0
+    const int nb = gridDim.x;   // the cluster spans the grid's x dimension
+    const int b = blockIdx.x;   // == rank in the cluster
+    int parity = 0;
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y, parity ^= 1) {
+        const R* row = x + r * static_cast<int64_t>(cols);
+        const R x0 = ld_scalar(row);
+        const Cand<Tag> seed{x0, 0};
+        Cand<Tag> c = scan_share<Tag, OP, U>(row, cols, b, nb, x0);
+        c = block_merge<Tag, OP>(c, smem, seed);
+        if (threadIdx.x == 0) {
+            const uint4 p = pack_cand<Tag>(c);
+            unsigned remote;
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                         : "=r"(remote)
+                         : "r"(smem_addr(&slots[parity][b])), "r"(0));
+            asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "r"(p.x), "r"(p.y),
+                         "r"(p.z), "r"(p.w)
+                         : "memory");
+        }
+        // Release the pushes, acquire everyone else's. Reuse of a slot two rows
+        // later is ordered by the barrier of the row in between.
+        cluster_barrier();
+        if (b == 0 && threadIdx.x < 32) {
+            Cand<Tag> m = threadIdx.x < nb ? unpack_cand<Tag>(slots[parity][threadIdx.x]) : seed;
+            m = group_merge<Tag, OP, 32>(m, 0xffffffffu);
+            if (threadIdx.x == 0) {
+                out_idx[r] = m.i;
+                if (out_val) out_val[r] = m.v;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Launchers.
+// ---------------------------------------------------------------------------
+template <class Tag, int OP, int G>
+cudaError_t launch_rows_g(const argr_plan& p, const Problem& pr) {
+    using R = typename Tag::raw;
+    const dim3 grid(static_cast<unsigned>(p.grid_rows));
+    const dim3 block(p.block);
+    const R* x = static_cast<const R*>(pr.x);
+    R* ov = static_cast<R*>(pr.out_val);
+    if (p.vec)
+        rows_kernel<Tag, OP, G, true, 4><<<grid, block, 0, pr.stream>>>(x, pr.rows, pr.cols, pr.out_idx, ov);
+    else
+        rows_kernel<Tag, OP, G, false, 4><<<grid, block, 0, pr.stream>>>(x, pr.rows, pr.cols, pr.out_idx, ov);
+    return cudaGetLastError();
+}
+
+template <class Tag, int OP>
+cudaError_t launch_rows_op(const argr_plan& p, const Problem& pr) {
+    switch (p.group) {
+        case 1: return launch_rows_g<Tag, OP, 1>(p, pr);
+        case 2: return launch_rows_g<Tag, OP, 2>(p, pr);
+        case 4: return launch_rows_g<Tag, OP, 4>(p, pr);
+        case 8: return launch_rows_g<Tag, OP, 8>(p, pr);
+        case 16: return launch_rows_g<Tag, OP, 16>(p, pr);
+        case 32: return launch_rows_g<Tag, OP, 32>(p, pr);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <class Tag>
+cudaError_t launch_rows_t(const argr_plan& p, const Problem& pr) {
+    return pr.op == kOpMax ? launch_rows_op<Tag, kOpMax>(p, pr) : launch_rows_op<Tag, kOpMin>(p, pr);
+}
+
+template <class Tag, int OP, int U>
+cudaError_t launch_split_u(const argr_plan& p, const Problem& pr) {
+    using R = typename Tag::raw;
+    const dim3 grid(static_cast<unsigned>(p.blocks_per_row), static_cast<unsigned>(p.grid_rows));
+    split_kernel<Tag, OP, U><<<grid, p.block, 0, pr.stream>>>(static_cast<const R*>(pr.x), pr.rows, pr.cols,
+                                                              pr.out_idx, static_cast<R*>(pr.out_val),
+                                                              static_cast<unsigned char*>(pr.scratch));
+    return cudaGetLastError();
+}
+
+template <class Tag, int OP>
+cudaError_t launch_split_op(const argr_plan& p, const Problem& pr) {
+    switch (p.unroll) {
+        case 1: return launch_split_u<Tag, OP, 1>(p, pr);
+        case 2: return launch_split_u<Tag, OP, 2>(p, pr);
+        case 4: return launch_split_u<Tag, OP, 4>(p, pr);
+        case 8: return launch_split_u<Tag, OP, 8>(p, pr);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <class Tag>
+cudaError_t launch_split_t(const argr_plan& p, const Problem& pr) {
+    return pr.op == kOpMax ? launch_split_op<Tag, kOpMax>(p, pr) : launch_split_op<Tag, kOpMin>(p, pr);
+}
+
+template <class Tag, int OP, int U>
+cudaError_t launch_cluster_u(const argr_plan& p, const Problem& pr) {
+    using R = typename Tag::raw;
+    auto kern = cluster_kernel<Tag, OP, U>;
+    if (p.cluster > 8) {
+        // Cluster sizes above the portable 8 must be enabled per kernel.
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.cluster), static_cast<unsigned>(p.grid_rows));
+    cfg.blockDim = dim3(p.block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = pr.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<const R*>(pr.x), pr.rows, pr.cols, pr.out_idx,
+                              static_cast<R*>(pr.out_val));
+}
+
+template <class Tag, int OP>
+cudaError_t launch_cluster_op(const argr_plan& p, const Problem& pr) {
+    switch (p.unroll) {
+        case 1: return launch_cluster_u<Tag, OP, 1>(p, pr);
+        case 2: return launch_cluster_u<Tag, OP, 2>(p, pr);
+        case 4: return launch_cluster_u<Tag, OP, 4>(p, pr);
+        case 8: return launch_cluster_u<Tag, OP, 8>(p, pr);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <class Tag>
+cudaError_t launch_cluster_t(const argr_plan& p, const Problem& pr) {
+    return pr.op == kOpMax ? launch_cluster_op<Tag, kOpMax>(p, pr) : launch_cluster_op<Tag, kOpMin>(p, pr);
+}
+
+}  // namespace argr
+
+#define ARGR_DEFINE_LAUNCHERS(sfx, Tag)                                                                       \
+    namespace argr {                                                                                          \
+    cudaError_t launch_rows_##sfx(const argr_plan& p, const Problem& pr) { return launch_rows_t<Tag>(p, pr); } \
+    cudaError_t launch_split_##sfx(const argr_plan& p, const Problem& pr) {                                  \
+        return launch_split_t<Tag>(p, pr);                                                                    \
+    }                                                                                                         \
+    cudaError_t launch_cluster_##sfx(const argr_plan& p, const Problem& pr) {                                \
+        return launch_cluster_t<Tag>(p, pr);                                                                  \
+    }                                                                                                         \
+    }

@@ -1,0 +1,173 @@
+// Launch-geometry planner: a pure function of the problem and the device's
+// properties (no CUDA call), so it can be tested on a machine without a GPU.
+//
+// Geometry rules (onnxruntime #32092 Approach and Kernel profile; #31694
+// Description), re-derived for a GB300:
+//  * narrow rows (at most kNarrowRowBytes) use G lanes per row, with G the
+//    smallest power of two that covers the row in one batch of U loads per
+//    lane (G = 1 is one thread per row);
+//  * when there are enough rows to fill the device with one warp each, rows of
+//    medium width use one warp per row and wider rows one CTA per row;
+//  * otherwise a row is split over several CTAs so that the grid is about one
+//    wave of the device (more CTAs than one wave was measured slower on the
+//    pages' H200, and the merge cost grows with the CTA count), while every
+//    thread keeps at least kMinBytesPerThread of the row.
+#include <algorithm>
+#include <climits>
+
+#include "internal.h"
+
+namespace argr {
+
+namespace {
+
+constexpr int64_t kNarrowRowBytes = 1024;  // rows up to this width: G lanes per row
+constexpr int64_t kWarpRowBytes = 16384;   // many rows up to this width: one warp per row
+constexpr int kBlock = 256;                // threads per CTA on every path
+constexpr int kRowsUnroll = 4;             // loads in flight per lane on the rows path
+constexpr int kSplitUnroll = 4;            // vector loads in flight per thread on the split path
+constexpr int64_t kMinBytesPerThread = 16; // one 16-byte vector per thread at least
+constexpr int64_t kRowsWaves = 8;          // rows path: grid of at most this many waves (grid-stride beyond)
+constexpr int64_t kMaxGridY = 65535;       // hardware limit of gridDim.y
+constexpr int64_t kMaxBlocksPerRow = 65535;
+
+int64_t ceil_div(int64_t a, int64_t b) { return a / b + (a % b != 0); }
+
+int pow2_ceil(int64_t v) {
+    int p = 1;
+    while (p < v && p < 32) p <<= 1;
+    return p;
+}
+
+bool valid_dtype(int d) { return d == ARGR_F32 || d == ARGR_F16 || d == ARGR_BF16 || d == ARGR_F64; }
+bool valid_op(int o) { return o == ARGR_MAX || o == ARGR_MIN; }
+
+int64_t ctas_per_wave(const argr_caps& caps, int block) {
+    const int64_t per_sm = std::max<int64_t>(1, caps.max_threads_per_sm / block);
+    return std::max<int64_t>(1, caps.sm_count) * per_sm;
+}
+
+}  // namespace
+
+int elem_size(int dtype) {
+    switch (dtype) {
+        case ARGR_F32: return 4;
+        case ARGR_F16: return 2;
+        case ARGR_BF16: return 2;
+        case ARGR_F64: return 8;
+        default: return 0;
+    }
+}
+
+size_t plan_scratch(const argr_plan& p, int64_t rows) {
+    (void)rows;
+    if (p.path == ARGR_PATH_SPLIT && p.blocks_per_row > 1)
+        return partials_offset(p.grid_rows) +
+               static_cast<size_t>(p.grid_rows) * static_cast<size_t>(p.blocks_per_row) * kPartialBytes;
+    return 0;
+}
+
+static bool caps_ok(const argr_caps& c) { return c.sm_count > 0 && c.max_threads_per_sm >= 32; }
+
+argr_status make_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_caps& caps, bool base_aligned,
+                      argr_plan* out) {
+    if (!out) return ARGR_EINVAL;
+    *out = argr_plan{};
+    if (!valid_dtype(dtype) || !valid_op(op) || rows < 0 || cols < 1 || cols > INT_MAX) return ARGR_EINVAL;
+    if (!caps_ok(caps)) return ARGR_EINVAL;
+    if (rows == 0) {
+        out->path = ARGR_PATH_NONE;
+        return ARGR_OK;
+    }
+    const int64_t es = elem_size(dtype);
+    const int64_t E = 16 / es;
+    const int64_t row_bytes = cols * es;
+    const bool aligned = base_aligned && row_bytes % 16 == 0;  // every row starts 16-byte aligned
+
+    out->block = kBlock;
+    out->cluster = 0;
+
+    if (row_bytes <= kNarrowRowBytes) {
+        // One batch of kRowsUnroll loads per lane covers the row.
+        const int64_t units = aligned ? cols / E : cols;
+        const int g = pow2_ceil(ceil_div(units, kRowsUnroll));
+        out->path = ARGR_PATH_ROWS;
+        out->group = g;
+        out->vec = aligned ? 1 : 0;
+        out->unroll = kRowsUnroll;
+        const int64_t rows_per_cta = kBlock / g;
+        out->grid_rows = std::min(ceil_div(rows, rows_per_cta), kRowsWaves * ctas_per_wave(caps, kBlock));
+        out->blocks_per_row = 1;
+        out->scratch_bytes = 0;
+        return ARGR_OK;
+    }
+
+    const int64_t wave = ctas_per_wave(caps, kBlock);
+    if (rows >= wave) {
+        // Enough rows: no row is split.
+        if (row_bytes <= kWarpRowBytes) {
+            out->path = ARGR_PATH_ROWS;
+            out->group = 32;
+            out->vec = aligned ? 1 : 0;
+            out->unroll = kRowsUnroll;
+            out->grid_rows = std::min(ceil_div(rows, kBlock / 32), kRowsWaves * wave);
+            out->blocks_per_row = 1;
+        } else {
+            out->path = ARGR_PATH_SPLIT;
+            out->unroll = kSplitUnroll;
+            out->blocks_per_row = 1;
+            out->grid_rows = std::min(rows, kMaxGridY);
+        }
+        out->scratch_bytes = plan_scratch(*out, rows);
+        return ARGR_OK;
+    }
+
+    // Few rows: split each row over CTAs, about one wave in total.
+    const int64_t by_wave = std::max<int64_t>(1, wave / rows);
+    const int64_t by_work = std::max<int64_t>(1, row_bytes / (kBlock * kMinBytesPerThread));
+    const int64_t bpr = std::min({by_wave, by_work, kMaxBlocksPerRow});
+    out->path = ARGR_PATH_SPLIT;
+    out->unroll = kSplitUnroll;
+    out->blocks_per_row = bpr;
+    out->grid_rows = rows;  // rows < one wave <= kMaxGridY here
+    if (bpr == 1) out->grid_rows = std::min(rows, kMaxGridY);
+    out->scratch_bytes = plan_scratch(*out, rows);
+    (void)E;
+    return ARGR_OK;
+}
+
+argr_status check_plan(const argr_plan& p, int64_t rows, int64_t cols, int dtype, const argr_caps& caps,
+                       bool row_aligned) {
+    if (!valid_dtype(dtype) || rows < 0 || cols < 1 || cols > INT_MAX) return ARGR_EINVAL;
+    if (rows == 0) return ARGR_OK;
+    if (p.block < 32 || p.block > 1024 || p.block % 32 != 0) return ARGR_EINVAL;
+    switch (p.path) {
+        case ARGR_PATH_ROWS: {
+            const int g = p.group;
+            if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16 && g != 32) return ARGR_EINVAL;
+            if (p.unroll != kRowsUnroll) return ARGR_EINVAL;
+            if (p.vec && !row_aligned) return ARGR_EINVAL;
+            if (p.vec != 0 && p.vec != 1) return ARGR_EINVAL;
+            if (p.grid_rows < 1 || p.grid_rows > INT_MAX) return ARGR_EINVAL;
+            return ARGR_OK;
+        }
+        case ARGR_PATH_SPLIT: {
+            if (p.unroll != 1 && p.unroll != 2 && p.unroll != 4 && p.unroll != 8) return ARGR_EINVAL;
+            if (p.blocks_per_row < 1 || p.blocks_per_row > kMaxBlocksPerRow) return ARGR_EINVAL;
+            if (p.grid_rows < 1 || p.grid_rows > kMaxGridY) return ARGR_EINVAL;
+            // A split row owns its partial slots and counter: no row loop.
+            if (p.blocks_per_row > 1 && p.grid_rows < rows) return ARGR_EINVAL;
+            return ARGR_OK;
+        }
+        case ARGR_PATH_CLUSTER: {
+            if (p.unroll != 1 && p.unroll != 2 && p.unroll != 4 && p.unroll != 8) return ARGR_EINVAL;
+            if (p.cluster < 2 || p.cluster > 16 || p.blocks_per_row != p.cluster) return ARGR_EINVAL;
+            if (p.grid_rows < 1 || p.grid_rows > kMaxGridY) return ARGR_EINVAL;
+            if (caps.max_cluster < p.cluster) return ARGR_EUNSUPPORTED;
+            return ARGR_OK;
+        }
+        default: return ARGR_EINVAL;
+    }
+}
+
+}  // namespace argr

@@ -1,0 +1,189 @@
+"""GPU checks of the boundary's contract: scratch validation, self-resetting
+counters, a dirtied partials region, CUDA graph capture and replay, streams,
+empty and maximal inputs (onnxruntime #32092 Testing: undersized and unaligned
+buffers, a dirtied intermediate buffer, graph capture with repeated replay,
+and a [1, INT_MAX] fp16 row)."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+import row_wise_arg_gb300 as A  # noqa: E402
+from row_wise_arg_gb300 import _lib  # noqa: E402
+
+from gpu_util import forced_plan, raw_equal, run, to_device  # noqa: E402
+
+INT_MAX = 2**31 - 1
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from row_wise_arg_gb300.build import build
+    build()
+
+
+def test_rows_zero_and_one_col():
+    x = torch.empty((0, 17), dtype=torch.float32, device="cuda")
+    idx, _ = A.argreduce(x, "max")
+    assert idx.shape == (0,)
+    x = W.fuzz_rows("f32", 1000, 1, seed=1)
+    i, v = run(x, "f32", "max")
+    assert (i == 0).all() and raw_equal(v, x[:, 0])
+
+
+def test_scratch_errors():
+    rows, cols = 4, 100000
+    x = torch.randn(rows, cols, device="cuda")
+    out = torch.empty(rows, dtype=torch.int64, device="cuda")
+    need = A.argreduce_scratch_bytes(rows, cols, "f32", "max")
+    assert need > 0
+    buf = torch.zeros(need + 64, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    f = _lib.argreduce_raw
+    assert f(x.data_ptr(), "f32", rows, cols, "max", out.data_ptr(), 0, 0, 0, s) == _lib.ARGR_ESCRATCH
+    assert f(x.data_ptr(), "f32", rows, cols, "max", out.data_ptr(), 0, buf.data_ptr(), need - 1, s) == \
+        _lib.ARGR_ESCRATCH
+    assert f(x.data_ptr(), "f32", rows, cols, "max", out.data_ptr(), 0, buf.data_ptr() + 8, need, s) == \
+        _lib.ARGR_ESCRATCH
+    assert A.argreduce_scratch_init(buf.data_ptr(), need, s) == _lib.ARGR_OK
+    assert f(x.data_ptr(), "f32", rows, cols, "max", out.data_ptr(), 0, buf.data_ptr(), need, s) == _lib.ARGR_OK
+    torch.cuda.synchronize()
+    assert (out.cpu().numpy() == oracle.argreduce(x.cpu().numpy(), "f32", "max")[0]).all()
+    assert A.argreduce_read_error(buf.data_ptr(), s) == _lib.ARGR_OK
+
+
+def test_forced_plan_validation():
+    x = torch.randn(4, 1000, device="cuda")
+    bad = [
+        forced_plan("rows", group=3),                       # not a power of two
+        forced_plan("rows", group=4, vec=1),                # unroll 5 (set below) is not offered
+        forced_plan("split", bpr=4, grid_rows=2),           # split rows may not loop
+        forced_plan("split", bpr=0, grid_rows=4),
+        forced_plan("split", bpr=2, grid_rows=4, block=48),  # not a multiple of 32
+        forced_plan("split", bpr=2, grid_rows=4, unroll=3),
+        forced_plan("cluster", cluster=17, grid_rows=4),
+        forced_plan("cluster", cluster=1, grid_rows=4),
+    ]
+    bad[1].unroll = 5
+    for p in bad:
+        with pytest.raises(A.ArgreduceError) as e:
+            A.argreduce_with_plan(p, x, "max")
+        assert e.value.status in (_lib.ARGR_EINVAL, _lib.ARGR_EUNSUPPORTED)
+    # vector loads on rows that are not 16-byte aligned are refused
+    x2 = torch.randn(4, 1001, device="cuda")
+    with pytest.raises(A.ArgreduceError):
+        A.argreduce_with_plan(forced_plan("rows", group=4, vec=1), x2, "max")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f64"])
+def test_dirtied_partials_and_repeat(dtype):
+    """Counters reset themselves; garbage in the partials region is harmless."""
+    rows, cols = 8, 202048
+    c = W.Case("t", rows, cols, dtype, "max", "batch_logits", 3001)
+    x = W.make(c)
+    eidx, _, _ = oracle.argreduce(x, dtype, "max")
+    xd, _k = to_device(x, dtype)
+    plan = A.argreduce_plan(rows, cols, dtype, "max")
+    assert plan.blocks_per_row > 1
+    scratch = A.Scratch(nbytes=plan.scratch_bytes)
+    from row_wise_arg_gb300._lib import argreduce_plan_scratch_bytes
+    # partials start after the 256-byte header and the counters, 256-aligned
+    off = ((256 + 4 * plan.grid_rows + 255) // 256) * 256
+    assert argreduce_plan_scratch_bytes(plan, rows) <= scratch.nbytes
+    for it in range(5):
+        scratch.buf[off:].fill_(0xFF if it % 2 else 0xA5)  # dirty the partials only
+        idx, _ = A.argreduce(xd, "max", dtype=dtype, scratch=scratch)
+        torch.cuda.synchronize()
+        assert (idx.cpu().numpy() == eidx).all()
+    # the counters are back at zero after every call
+    counters = scratch.buf[256:256 + 4 * plan.grid_rows].cpu()
+    assert (counters == 0).all()
+
+
+@pytest.mark.parametrize("path", ["planner", "split", "cluster", "rows"])
+def test_graph_capture_replay(path):
+    """Capture one call into a CUDA graph and replay it 100 times with new
+    input contents each time; every replay matches the oracle."""
+    rows, cols = 6, 150001
+    dtype = "f32"
+    if path == "planner":
+        plan = A.argreduce_plan(rows, cols, dtype, "max")
+    elif path == "split":
+        plan = forced_plan("split", bpr=40, grid_rows=rows)
+    elif path == "cluster":
+        plan = forced_plan("cluster", cluster=8, grid_rows=rows)
+    else:
+        plan = forced_plan("rows", group=32, vec=0, grid=2)
+    xs = [W.fuzz_rows(dtype, rows, cols, seed=900 + k, p_special=0.001) for k in range(4)]
+    exp = [oracle.argreduce(x, dtype, "max")[0] for x in xs]
+    xd = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
+    out = torch.empty(rows, dtype=torch.int64, device="cuda")
+    scratch = A.Scratch(nbytes=max(4096, plan.scratch_bytes))
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        A.argreduce_with_plan(plan, xd, "max", out_idx=out, scratch=scratch, stream=stream)  # warm-up
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            A.argreduce_with_plan(plan, xd, "max", out_idx=out, scratch=scratch, stream=stream)
+    host = [torch.from_numpy(x) for x in xs]
+    for k in range(100):
+        xd.copy_(host[k % 4])
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert (out.cpu().numpy() == exp[k % 4]).all(), f"replay {k}"
+
+
+def test_streams_independent():
+    """Two streams with their own scratch run concurrently and both match."""
+    a = W.fuzz_rows("f32", 16, 300000, seed=3, p_special=0.001)
+    b = W.fuzz_rows("f32", 16, 300000, seed=4, p_special=0.001)
+    da, _ka = to_device(a, "f32")
+    db, _kb = to_device(b, "f32")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    sa, sb = A.Scratch(), A.Scratch()
+    torch.cuda.synchronize()
+    for _ in range(20):
+        ia, _ = A.argreduce(da, "max", scratch=sa, stream=s1)
+        ib, _ = A.argreduce(db, "max", scratch=sb, stream=s2)
+    torch.cuda.synchronize()
+    assert (ia.cpu().numpy() == oracle.argreduce(a, "f32", "max")[0]).all()
+    assert (ib.cpu().numpy() == oracle.argreduce(b, "f32", "max")[0]).all()
+
+
+def test_int_max_row_f16():
+    """[1, INT_MAX] fp16 (4 GiB): a property check at the widest admitted row.
+    Zeros with planted values near both ends; the expected indices follow
+    from the construction."""
+    free, _ = torch.cuda.mem_get_info()
+    if free < 6 * 2**30:
+        pytest.skip("needs ~5 GiB of device memory")
+    n = INT_MAX
+    x = torch.zeros((1, n), dtype=torch.float16, device="cuda")
+    x[0, n - 3] = 1.0
+    x[0, n - 1] = 1.0
+    x[0, 5] = -1.0
+    x[0, n - 2] = -1.0
+    plans = [None, forced_plan("split", bpr=3, grid_rows=1, block=1024, unroll=8),
+             forced_plan("split", bpr=1, grid_rows=1)]
+    for p in plans:
+        for op, want in (("max", n - 3), ("min", 5)):
+            if p is None:
+                idx, val = A.argreduce(x, op, with_values=True)
+            else:
+                idx, val = A.argreduce_with_plan(p, x, op, with_values=True)
+            torch.cuda.synchronize()
+            assert int(idx[0]) == want, (p, op)
+    x[0, 0] = float("nan")
+    idx, _ = A.argreduce(x, "max")
+    torch.cuda.synchronize()
+    assert int(idx[0]) == 0
+    del x
+    torch.cuda.empty_cache()

@@ -1,0 +1,174 @@
+"""GPU parity: the CUDA path against the CPU oracle, bit for bit (index and
+raw value bits, tolerance 0), through the C ABI.
+
+* every workload case at full size, in the planner's launch configuration
+  (the one the benchmark times);
+* every kernel path forced (thread/group/warp per row, vector and scalar
+  loads, one or many CTAs per row with the global merge, clusters of 2..16)
+  on special-value fuzz rows whose widths span several tiles and ragged tails,
+  with unaligned base pointers;
+* the test shapes described by onnxruntime #31694 and #32092 (Testing).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+import row_wise_arg_gb300 as A  # noqa: E402
+from row_wise_arg_gb300 import _lib  # noqa: E402
+
+from gpu_util import forced_plan, raw_equal, run  # noqa: E402
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from row_wise_arg_gb300.build import build
+    build()
+
+
+def check(x, dtype, op, **kw):
+    idx, val = run(x, dtype, op, **kw)
+    eidx, evalue, _ = oracle.argreduce(x, dtype, op)
+    bad = np.nonzero(idx != eidx)[0]
+    assert bad.size == 0, f"{bad.size} rows differ, first rows {bad[:5]}: got {idx[bad[:5]]} want {eidx[bad[:5]]}"
+    assert raw_equal(val, evalue), "value bits differ"
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads in the benchmark's launch configuration.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("case", [c for _, c in W.all_cases()], ids=lambda c: c.name)
+def test_workload_full_size(case):
+    x = W.make(case)
+    check(x, case.dtype, case.op)
+
+
+def test_narrow_matches_thread_per_row():
+    """Narrow rows: the planner's path and a forced one-thread-per-row scan
+    give the same bits (and both equal the oracle)."""
+    for c in W.config_cases(5):
+        x = W.make(c)
+        check(x, c.dtype, c.op)
+        check(x, c.dtype, c.op, plan=forced_plan("rows", group=1, vec=0, grid=1024))
+
+
+# ---------------------------------------------------------------------------
+# Every path forced, on fuzz rows.
+# ---------------------------------------------------------------------------
+WIDTHS = [1, 2, 3, 7, 8, 9, 31, 32, 33, 127, 128, 129, 255, 256, 257, 1000, 4099, 20011]
+
+
+@pytest.mark.parametrize("dtype", W.DTYPES)
+@pytest.mark.parametrize("group", [1, 2, 4, 8, 16, 32])
+def test_rows_path(dtype, group):
+    es = W.ELEM_SIZE[dtype]
+    for cols in WIDTHS[:-1]:
+        rows = 37 if cols < 2000 else 5
+        x = W.fuzz_rows(dtype, rows, cols, seed=cols * 31 + group)
+        for op in W.OPS:
+            check(x, dtype, op, plan=forced_plan("rows", group=group, vec=0, grid=3))
+            check(x, dtype, op, plan=forced_plan("rows", group=group, vec=0, grid=64), offset=1)
+            if (cols * es) % 16 == 0:
+                check(x, dtype, op, plan=forced_plan("rows", group=group, vec=1, grid=5))
+
+
+@pytest.mark.parametrize("dtype", W.DTYPES)
+@pytest.mark.parametrize("bpr", [1, 2, 5, 64])
+def test_split_path(dtype, bpr):
+    for cols in WIDTHS:
+        rows = 3 if cols > 4000 else 9
+        x = W.fuzz_rows(dtype, rows, cols, seed=cols * 7 + bpr)
+        for op in W.OPS:
+            for block, unroll in ((256, 4), (32, 1), (1024, 8), (64, 2)):
+                check(x, dtype, op, plan=forced_plan("split", bpr=bpr, grid_rows=rows, block=block,
+                                                     unroll=unroll))
+            for off in (1, 3):
+                check(x, dtype, op, plan=forced_plan("split", bpr=bpr, grid_rows=rows), offset=off)
+            if bpr == 1:  # row loop: fewer row slots than rows
+                check(x, dtype, op, plan=forced_plan("split", bpr=1, grid_rows=2))
+
+
+@pytest.mark.parametrize("dtype", W.DTYPES)
+@pytest.mark.parametrize("cluster", [2, 4, 8, 16])
+def test_cluster_path(dtype, cluster):
+    caps = A.argreduce_device_caps(torch.cuda.current_device())
+    if caps.max_cluster < cluster:
+        pytest.skip("cluster size not supported")
+    for cols in WIDTHS:
+        rows = 3 if cols > 4000 else 7
+        x = W.fuzz_rows(dtype, rows, cols, seed=cols * 13 + cluster)
+        for op in W.OPS:
+            check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=rows))
+            check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=2, unroll=1), offset=1)
+
+
+@pytest.mark.parametrize("dtype", W.DTYPES)
+def test_exhaustive_alphabet_rows(dtype):
+    """All 8**4 rows of length 4 over the special alphabet, on every path."""
+    x = W.exhaustive_rows(dtype, 4)
+    rows = x.shape[0]
+    for op in W.OPS:
+        check(x, dtype, op)
+        check(x, dtype, op, plan=forced_plan("rows", group=4, vec=0, grid=100))
+        check(x, dtype, op, plan=forced_plan("split", bpr=1, grid_rows=min(rows, 1000), block=32))
+        check(x, dtype, op, plan=forced_plan("split", bpr=3, grid_rows=rows, block=32))
+
+
+@pytest.mark.parametrize("dtype", W.DTYPES)
+def test_planner_default_on_fuzz(dtype):
+    for rows, cols in [(1, 1), (1, 5), (3, 100000), (2000, 33), (500, 3000), (64, 70000), (1, 300001)]:
+        x = W.fuzz_rows(dtype, rows, cols, seed=rows + cols)
+        for op in W.OPS:
+            check(x, dtype, op)
+            check(x, dtype, op, offset=1)
+
+
+# ---------------------------------------------------------------------------
+# The pages' test shapes.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", W.DTYPES)
+def test_golden_long_axis_300x4(dtype):
+    with open(os.path.join(GOLDEN, "onnxruntime_31694_long_axis_300x4.json")) as f:
+        fx = json.load(f)
+    x = W.encode(np.array(fx["rows"], dtype=np.float64), dtype)
+    for op in W.OPS:
+        idx, _ = run(x, dtype, op)
+        assert list(idx) == fx["expected"][op]
+        for bpr in (1, 2):
+            idx, _ = run(x, dtype, op, plan=forced_plan("split", bpr=bpr, grid_rows=4))
+            assert list(idx) == fx["expected"][op]
+
+
+def test_golden_first_index_65536():
+    with open(os.path.join(GOLDEN, "onnxruntime_31694_first_index_65536.json")) as f:
+        fx = json.load(f)
+    rng = np.random.Generator(np.random.PCG64(fx["seed"]))
+    row = rng.standard_normal(fx["cols"]).astype(np.float32)
+    row[fx["inf_positions"]] = np.inf
+    idx, _ = run(row.reshape(1, -1), "f32", "max")
+    assert idx[0] == fx["expected_max"]
+
+
+@pytest.mark.parametrize("dtype", W.DTYPES)
+def test_operator_shapes(dtype):
+    """#32092 Testing: {3, 40000} and {2, 202048}; #31694 Testing: lengths on
+    both sides of a 256-wide block and rows 1..300."""
+    for rows, cols in [(3, 40000), (2, 202048)]:
+        for op in W.OPS:
+            check(W.fuzz_rows(dtype, rows, cols, seed=rows, p_special=0.001), dtype, op)
+    for cols in (1, 2, 255, 256, 257, 1000, 129280):
+        for rows in (1, 300):
+            if rows * cols > 4_000_000:
+                continue
+            for op in W.OPS:
+                check(W.fuzz_rows(dtype, rows, cols, seed=cols, p_special=0.01), dtype, op)

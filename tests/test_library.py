@@ -1,0 +1,245 @@
+"""CPU-only checks of the C-ABI library: it builds, loads, exports every
+symbol include/argreduce.h declares, validates arguments before touching the
+device, and its planner (pure host code) produces sound geometry."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import row_wise_arg_gb300 as A
+from row_wise_arg_gb300 import _lib
+from row_wise_arg_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "argreduce.h")
+INT_MAX = 2**31 - 1
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    build()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*[A-Za-z_][\w \*]*?\b(argreduce\w*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_expected_entry_points():
+    names = header_functions()
+    assert set(_lib.EXPORTS) <= set(names), names
+    assert "argreduce" in names and "argreduce_scratch_bytes" in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(_lib.LIB_PATH)
+    for name in header_functions():
+        assert hasattr(lib, name), f"{name} declared in argreduce.h but not exported"
+
+
+def test_version_and_status_strings():
+    assert "sm_103a" in A.argreduce_version()
+    for s in range(6):
+        assert A.argreduce_status_string(s).startswith("ARGR_")
+    assert "unknown" in A.argreduce_status_string(99)
+
+
+def test_validation_before_any_device_work():
+    """Bad arguments are rejected before the library asks for a device (this
+    machine has none, so anything reaching the device would be ECUDA)."""
+    f = _lib.argreduce_raw
+    X = 0x10000  # a fake, never dereferenced address
+    assert f(X, "f32", 0, 5, "max", X, 0, 0, 0, 0) == _lib.ARGR_OK  # rows == 0: nothing to do
+    assert f(0, "f32", 3, 5, "max", X, 0, 0, 0, 0) == _lib.ARGR_EINVAL  # null x
+    assert f(X, "f32", 3, 5, "max", 0, 0, 0, 0, 0) == _lib.ARGR_EINVAL  # null out_idx
+    assert f(X, "f32", 3, 0, "max", X, 0, 0, 0, 0) == _lib.ARGR_EINVAL  # cols == 0
+    assert f(X, "f32", 3, INT_MAX + 1, "max", X, 0, 0, 0, 0) == _lib.ARGR_EINVAL  # cols > INT_MAX
+    assert f(X, "f32", -1, 5, "max", X, 0, 0, 0, 0) == _lib.ARGR_EINVAL  # rows < 0
+    assert f(X, 7, 3, 5, "max", X, 0, 0, 0, 0) == _lib.ARGR_EINVAL  # bad dtype
+    assert f(X, "f32", 3, 5, 9, X, 0, 0, 0, 0) == _lib.ARGR_EINVAL  # bad op
+    assert f(X + 2, "f32", 3, 5, "max", X, 0, 0, 0, 0) == _lib.ARGR_EINVAL  # x not element aligned
+    assert f(X, "f32", 3, 5, "max", X + 4, 0, 0, 0, 0) == _lib.ARGR_EINVAL  # out_idx not 8-aligned
+    assert f(X, "f64", 3, 5, "max", X, X + 4, 0, 0, 0) == _lib.ARGR_EINVAL  # out_val not aligned
+    assert f(X, "f32", 2**62, 2**20, "max", X, 0, 0, 0, 0) == _lib.ARGR_EINVAL  # byte size overflows
+    assert A.argreduce_scratch_init(X + 8, 64, 0) == _lib.ARGR_ESCRATCH
+    assert A.argreduce_scratch_init(0, 64, 0) == _lib.ARGR_EINVAL
+    assert A.argreduce_scratch_init(0, 0, 0) == _lib.ARGR_OK
+
+
+GB300 = A.make_caps(152)
+H200_LIKE = A.make_caps(132)
+TINY = A.make_caps(2, 2048)
+
+CONFIG_SHAPES = [(1, 32000), (1, 202048), (1, 262144), (8, 202048), (32, 202048), (4096, 4096),
+                 (65536, 1024), (65536, 64), (4096, 8), (4096, 128)]
+
+
+@pytest.mark.parametrize("caps", [GB300, H200_LIKE, TINY], ids=["152sm", "132sm", "2sm"])
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16", "f64"])
+def test_plan_geometry(caps, dtype):
+    es = {"f32": 4, "f16": 2, "bf16": 2, "f64": 8}[dtype]
+    wave = caps.sm_count * (caps.max_threads_per_sm // 256)
+    for rows, cols in CONFIG_SHAPES + [(1, 1), (3, 7), (1, INT_MAX), (70000, 3), (2, 5000)]:
+        p = A.argreduce_plan(rows, cols, dtype, "max", caps)
+        d = p.as_dict()
+        assert d["block"] % 32 == 0 and 32 <= d["block"] <= 1024
+        if d["path_name"] == "rows":
+            assert d["group"] in (1, 2, 4, 8, 16, 32)
+            if d["vec"]:
+                assert (cols * es) % 16 == 0
+            assert d["scratch_bytes"] == 0
+        elif d["path_name"] == "split":
+            bpr = d["blocks_per_row"]
+            assert 1 <= bpr <= 65535 and 1 <= d["grid_rows"] <= 65535
+            if bpr > 1:
+                assert d["grid_rows"] >= rows
+                # about one wave, and the scratch stays in the kilobytes
+                assert rows * bpr <= max(wave, rows)
+                assert d["scratch_bytes"] <= 512 + 20 * wave
+            else:
+                assert d["scratch_bytes"] == 0
+        else:
+            pytest.fail(f"unexpected path {d}")
+
+
+def test_plan_paths_for_configs():
+    """The planner's choices for the five workload groups on a 152-SM part."""
+    def path(rows, cols, dt="f32"):
+        return A.argreduce_plan(rows, cols, dt, "max", GB300).as_dict()
+
+    assert path(1, 32000)["path_name"] == "split" and path(1, 32000)["blocks_per_row"] > 1
+    assert path(1, 202048)["blocks_per_row"] > 100
+    assert path(32, 202048)["blocks_per_row"] > 1
+    assert path(4096, 4096)["path_name"] == "rows" and path(4096, 4096)["group"] == 32
+    for cols in (8, 64, 128):
+        d = path(65536 if cols == 64 else 4096, cols)
+        assert d["path_name"] == "rows" and d["vec"] == 1 and d["group"] <= 8
+
+
+def test_plan_rejects_bad_input():
+    with pytest.raises(A.ArgreduceError):
+        A.argreduce_plan(1, 0, "f32", "max", GB300)
+    with pytest.raises(A.ArgreduceError):
+        A.argreduce_plan(1, 10, "f32", "max", A.make_caps(0))
+    assert A.argreduce_plan(0, 10, "f32", "max", GB300).as_dict()["path_name"] == "none"
+
+
+# ---------------------------------------------------------------------------
+# Host simulation of the kernels' index arithmetic.
+# ---------------------------------------------------------------------------
+class Overflow(Exception):
+    pass
+
+
+def i32(v):
+    if not (-2**31 <= v < 2**31):
+        raise Overflow(v)
+    return v
+
+
+def sim_split_thread(cols, es, misalign, b, nb, t, nt, U, count_only=False):
+    """Positions one thread of scan_share() visits, computed with the same
+    int operations (each checked for int32 overflow)."""
+    E = 16 // es
+    head = ((16 - misalign) & 15) // es
+    head = min(head, cols)
+    nvec = i32(i32(cols - head) // E)
+    tail0 = i32(head + i32(nvec * E))
+    chunk = i32(nvec // nb + (1 if nvec % nb else 0))
+    bc = i32(b * chunk)
+    vb = bc if bc < nvec else nvec
+    ve = i32(vb + chunk) if i32(nvec - vb) > chunk else nvec
+    out = []
+    n = 0
+    if b == 0 and t < head:
+        out.append(t)
+    v0 = i32(vb + t)
+    if v0 < ve:
+        while True:
+            rem = i32(ve - v0)
+            for u in range(U):
+                if i32(u * nt) < rem:
+                    j0 = i32(head + i32(i32(v0 + u * nt) * E))
+                    n += E
+                    if not count_only:
+                        out.extend(range(j0, j0 + E))
+                    else:
+                        assert 0 <= j0 and j0 + E <= cols
+            if rem <= i32(U * nt):
+                break
+            if count_only:
+                # jump to the last iteration without changing the arithmetic
+                steps = (rem - 1) // (U * nt)
+                v0 = i32(v0 + steps * U * nt)
+                n += (steps - 1) * U * E if steps > 1 else 0
+                continue
+            v0 = i32(v0 + U * nt)
+    if b == nb - 1 and t < cols - tail0:
+        out.append(i32(tail0 + t))
+    return out, n
+
+
+@pytest.mark.parametrize("es", [2, 4, 8])
+def test_split_partition_exact_small(es):
+    """Every element of the row is visited exactly once, in increasing order
+    per thread, for many widths, misalignments and CTA counts."""
+    for cols in list(range(1, 70)) + [127, 128, 129, 255, 256, 257, 1000, 4099]:
+        for misalign in range(0, 16, es):
+            for nb in (1, 2, 3, 7):
+                for nt, U in ((32, 1), (64, 2), (32, 4)):
+                    seen = []
+                    for b in range(nb):
+                        for t in range(nt):
+                            pos, _ = sim_split_thread(cols, es, misalign, b, nb, t, nt, U)
+                            assert pos == sorted(pos)
+                            seen.extend(pos)
+                    assert sorted(seen) == list(range(cols)), (cols, misalign, nb, nt, U)
+
+
+@pytest.mark.parametrize("cols", [INT_MAX, INT_MAX - 1, INT_MAX - 262143, 2**30 + 5])
+@pytest.mark.parametrize("es", [2, 4, 8])
+def test_split_index_arithmetic_at_int_max(cols, es):
+    """The widest rows: no int32 intermediate overflows and every position
+    stays inside [0, cols), for the first, last and boundary threads."""
+    for nb in (1, 197, 1184):
+        for nt, U in ((256, 4), (1024, 8)):
+            for b in (0, 1, nb // 2, nb - 1):
+                for t in (0, 1, nt - 1):
+                    for misalign in (0, es, 16 - es):
+                        sim_split_thread(cols, es, misalign, b, nb, t, nt, U, count_only=True)
+
+
+def sim_rows_lane(cols, es, vec, G, U, lg):
+    E = 16 // es if vec else 1
+    n = i32(cols // E) if vec else cols
+    v0 = lg
+    rem = i32(n - v0)
+    out = []
+    while True:
+        for u in range(U):
+            if i32(u * G) < rem:
+                idx = i32(v0 + u * G)
+                out.extend(range(i32(idx * E), i32(idx * E) + E))
+        if not rem > i32(G * U):
+            break
+        v0 = i32(v0 + G * U)
+        rem = i32(n - v0)
+    return out
+
+
+def test_rows_partition_exact():
+    for es in (2, 4, 8):
+        for G in (1, 2, 4, 8, 16, 32):
+            for cols in range(1, 300):
+                for vec in (False, True):
+                    if vec and (cols * es) % 16:
+                        continue
+                    seen = []
+                    for lg in range(G):
+                        pos = sim_rows_lane(cols, es, vec, G, 4, lg)
+                        assert pos == sorted(pos)
+                        seen.extend(pos)
+                    assert sorted(seen) == list(range(cols))
