@@ -75,6 +75,11 @@ typedef struct {
     int32_t cc_major, cc_minor; /* compute capability */
 } argr_caps;
 
+/* Plan flag: launch as a programmatic dependent of the previous grid in the
+ * stream. The kernel still waits for that grid to complete before it touches
+ * memory, so results are the same; only the launch latency overlaps. */
+#define ARGR_PLAN_PDL 1
+
 /* A launch plan. Produced by argreduce_plan(); tests may edit it to force a
  * path and pass it to argreduce_with_plan(), which re-validates it. */
 typedef struct {
@@ -82,8 +87,10 @@ typedef struct {
     int32_t block;          /* threads per CTA: multiple of 32, 32..1024 */
     int32_t group;          /* ROWS: lanes per row, power of two 1..32 */
     int32_t vec;            /* 1: 16-byte vector loads (ROWS needs every row 16-byte aligned) */
-    int32_t unroll;         /* vector (or scalar) loads in flight per thread per step: 1,2,4,8 */
+    int32_t unroll;         /* loads in flight per thread per step: ROWS 4 or 8; SPLIT/CLUSTER 1,2,4,8 */
     int32_t cluster;        /* CLUSTER: CTAs per cluster, 2..16 */
+    int32_t flags;          /* ARGR_PLAN_* bits */
+    int32_t reserved;       /* 0 */
     int64_t blocks_per_row; /* SPLIT / CLUSTER: CTAs that share one row */
     int64_t grid_rows;      /* SPLIT / CLUSTER: row slots in the grid (rows loop over them);
                                ROWS: number of CTAs */

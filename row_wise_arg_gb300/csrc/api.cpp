@@ -96,7 +96,7 @@ argr_status run(const argr_plan& p, const Problem& pr, size_t scratch_bytes) {
 #undef ARGR_DISPATCH
     if (e != cudaSuccess) {
         cudaGetLastError();  // clear a non-sticky launch error
-        return ARGR_ECUDA;
+        return e == cudaErrorInvalidClusterSize ? ARGR_EUNSUPPORTED : ARGR_ECUDA;
     }
     return ARGR_OK;
 }

@@ -14,6 +14,8 @@
 //    is (x[0], 0) and so is the merge. Otherwise no candidate holds a NaN,
 //    and the merge is the maximum of a total order (value, then lower index),
 //    so any merge tree gives the sequential result.
+// Comparisons go through per-type keys (below) that decide exactly as the
+// IEEE comparison of the element type.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -26,65 +28,133 @@ constexpr int kOpMax = 0;
 constexpr int kOpMin = 1;
 
 // ---------------------------------------------------------------------------
-// Element tags: raw storage type, comparison type and the exact widening.
-// binary16 and bfloat16 widen exactly to binary32; comparisons there decide
-// exactly as in the narrow type.
+// Element tags: raw storage type and a comparison key.
+//
+// elem_key(x) is the key of an element the scan visits; seed_key(x) the key
+// of a candidate value. better(a, b) says key a is strictly better than key b.
+// For binary32, binary16 and bfloat16 the key is the exactly widened binary32
+// value and better() is the IEEE comparison, false when either side is NaN.
+//
+// binary64 is compared through order-preserving 64-bit integer keys instead
+// (this GPU's FP64 pipe is far too slow to compare at memory speed): for
+// non-NaN values the key is monotone in the value (reversed for ArgMin) and
+// +0.0 and -0.0 share one key. A NaN element gets key 0, which nothing is
+// worse than, so it never wins; a NaN candidate (only ever x[0]) gets the
+// all-ones key, so nothing displaces it. Neither sentinel is the key of a
+// number, so "strictly better" decides exactly as the IEEE comparison does.
 // ---------------------------------------------------------------------------
 struct TagF32 {
     using raw = float;
-    using cmp = float;
-    static __device__ __forceinline__ float to_cmp(float v) { return v; }
-};
-struct TagF64 {
-    using raw = double;
-    using cmp = double;
-    static __device__ __forceinline__ double to_cmp(double v) { return v; }
+    using key = float;
+    template <int OP> static __device__ __forceinline__ float elem_key(float v) { return v; }
+    template <int OP> static __device__ __forceinline__ float seed_key(float v) { return v; }
+    template <int OP> static __device__ __forceinline__ bool better(float a, float b) {
+        if constexpr (OP == kOpMax) return a > b; else return a < b;
+    }
 };
 struct TagF16 {
     using raw = uint16_t;
-    using cmp = float;
-    static __device__ __forceinline__ float to_cmp(uint16_t v) {
-        return __half2float(__ushort_as_half(v));
+    using key = float;
+    static __device__ __forceinline__ float widen(uint16_t v) { return __half2float(__ushort_as_half(v)); }
+    template <int OP> static __device__ __forceinline__ float elem_key(uint16_t v) { return widen(v); }
+    template <int OP> static __device__ __forceinline__ float seed_key(uint16_t v) { return widen(v); }
+    template <int OP> static __device__ __forceinline__ bool better(float a, float b) {
+        if constexpr (OP == kOpMax) return a > b; else return a < b;
     }
 };
 struct TagBF16 {
     using raw = uint16_t;
-    using cmp = float;
-    static __device__ __forceinline__ float to_cmp(uint16_t v) {
+    using key = float;
+    static __device__ __forceinline__ float widen(uint16_t v) {
         return __uint_as_float(static_cast<uint32_t>(v) << 16);
+    }
+    template <int OP> static __device__ __forceinline__ float elem_key(uint16_t v) { return widen(v); }
+    template <int OP> static __device__ __forceinline__ float seed_key(uint16_t v) { return widen(v); }
+    template <int OP> static __device__ __forceinline__ bool better(float a, float b) {
+        if constexpr (OP == kOpMax) return a > b; else return a < b;
+    }
+};
+struct TagF64 {
+    // Raw binary64 elements are carried as their 64-bit patterns: no value
+    // of type double exists in the kernels, so nothing runs on the FP64 pipe.
+    using raw = unsigned long long;
+    using key = unsigned long long;
+    static constexpr unsigned long long kSign = 0x8000000000000000ull;
+    static constexpr unsigned long long kInfBits = 0x7FF0000000000000ull;
+    // Monotone key of a non-NaN value (larger key = better for OP).
+    template <int OP> static __device__ __forceinline__ unsigned long long ordered(unsigned long long b) {
+        const unsigned long long mag = b & ~kSign;
+        unsigned long long u = mag == 0 ? kSign : ((b & kSign) ? ~b : (b | kSign));
+        if constexpr (OP == kOpMin) u = ~u;
+        return u;
+    }
+    template <int OP> static __device__ __forceinline__ unsigned long long elem_key(unsigned long long b) {
+        return (b & ~kSign) > kInfBits ? 0ull : ordered<OP>(b);
+    }
+    template <int OP> static __device__ __forceinline__ unsigned long long seed_key(unsigned long long b) {
+        return (b & ~kSign) > kInfBits ? ~0ull : ordered<OP>(b);
+    }
+    template <int OP> static __device__ __forceinline__ bool better(unsigned long long a, unsigned long long b) {
+        return a > b;
     }
 };
 
-template <int OP, typename C>
-__device__ __forceinline__ bool better(C a, C b) {
-    // IEEE comparison: false when either side is NaN.
-    if constexpr (OP == kOpMax)
-        return a > b;
-    else
-        return a < b;
-}
-
+// A candidate: raw value (its bits are what out_val receives), its key, and
+// its index in the row.
 template <class Tag>
 struct Cand {
     typename Tag::raw v;
+    typename Tag::key k;
     int i;
 };
+
+template <class Tag, int OP>
+__device__ __forceinline__ Cand<Tag> make_cand(typename Tag::raw v, int i) {
+    return Cand<Tag>{v, Tag::template seed_key<OP>(v), i};
+}
 
 // Strict update for elements visited in increasing index order.
 template <class Tag, int OP>
 __device__ __forceinline__ void visit(Cand<Tag>& c, typename Tag::raw x, int j) {
-    if (better<OP>(Tag::to_cmp(x), Tag::to_cmp(c.v))) {
-        c.v = x;
-        c.i = j;
+    if constexpr (sizeof(typename Tag::raw) == 8) {
+        // binary64: a 32-bit pre-test on the high word first. filter(x) is the
+        // high half of x's key (one above it for -0.0, and at least as large
+        // for NaNs), so an element that fails "filter(x) >= high half of the
+        // candidate's key" cannot be strictly better and is skipped with two
+        // integer operations. The full 64-bit key is only formed for the rare
+        // elements that pass.
+        const unsigned hi = static_cast<unsigned>(x >> 32);
+        unsigned f = hi ^ (static_cast<unsigned>(static_cast<int>(hi) >> 31) | 0x80000000u);
+        if constexpr (OP == kOpMin) f = ~f;
+        if (f >= static_cast<unsigned>(c.k >> 32)) {
+            const typename Tag::key k = Tag::template elem_key<OP>(x);
+            if (Tag::template better<OP>(k, c.k)) {
+                c.v = x;
+                c.k = k;
+                c.i = j;
+            }
+        }
+    } else {
+        const typename Tag::key k = Tag::template elem_key<OP>(x);
+        if (Tag::template better<OP>(k, c.k)) {
+            c.v = x;
+            c.k = k;
+            c.i = j;
+        }
     }
 }
 
-// Merge of two candidates: better value wins; equal values keep the lower index.
+// Programmatic dependent launch. Every kernel waits for the grid before it in
+// the stream to complete (and its memory to be visible) before touching global
+// memory, and lets the next grid start launching early; when a kernel was not
+// launched as a dependent, the wait returns at once.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Merge of two candidates: better key wins; equal keys keep the lower index.
 template <class Tag, int OP>
 __device__ __forceinline__ Cand<Tag> merge(Cand<Tag> a, Cand<Tag> b) {
-    const auto av = Tag::to_cmp(a.v);
-    const auto bv = Tag::to_cmp(b.v);
-    const bool take_b = better<OP>(bv, av) || (bv == av && b.i < a.i);
+    const bool take_b = Tag::template better<OP>(b.k, a.k) || (b.k == a.k && b.i < a.i);
     return take_b ? b : a;
 }
 
@@ -94,7 +164,7 @@ __device__ __forceinline__ Cand<Tag> merge(Cand<Tag> a, Cand<Tag> b) {
 __device__ __forceinline__ float shfl_xor_raw(unsigned m, float v, int o, int w) {
     return __shfl_xor_sync(m, v, o, w);
 }
-__device__ __forceinline__ double shfl_xor_raw(unsigned m, double v, int o, int w) {
+__device__ __forceinline__ unsigned long long shfl_xor_raw(unsigned m, unsigned long long v, int o, int w) {
     return __shfl_xor_sync(m, v, o, w);
 }
 __device__ __forceinline__ uint16_t shfl_xor_raw(unsigned m, uint16_t v, int o, int w) {
@@ -103,7 +173,7 @@ __device__ __forceinline__ uint16_t shfl_xor_raw(unsigned m, uint16_t v, int o, 
 __device__ __forceinline__ float shfl_raw(unsigned m, float v, int src, int w) {
     return __shfl_sync(m, v, src, w);
 }
-__device__ __forceinline__ double shfl_raw(unsigned m, double v, int src, int w) {
+__device__ __forceinline__ unsigned long long shfl_raw(unsigned m, unsigned long long v, int src, int w) {
     return __shfl_sync(m, v, src, w);
 }
 __device__ __forceinline__ uint16_t shfl_raw(unsigned m, uint16_t v, int src, int w) {
@@ -116,9 +186,7 @@ template <class Tag, int OP, int G>
 __device__ __forceinline__ Cand<Tag> group_merge(Cand<Tag> c, unsigned mask) {
 #pragma unroll
     for (int off = G / 2; off >= 1; off >>= 1) {
-        Cand<Tag> o;
-        o.v = shfl_xor_raw(mask, c.v, off, G);
-        o.i = __shfl_xor_sync(mask, c.i, off, G);
+        const Cand<Tag> o = make_cand<Tag, OP>(shfl_xor_raw(mask, c.v, off, G), __shfl_xor_sync(mask, c.i, off, G));
         c = merge<Tag, OP>(c, o);
     }
     return c;
@@ -173,9 +241,9 @@ __device__ __forceinline__ float vec_elem<float>(const uint4& v, int k) {
     return __uint_as_float(w);
 }
 template <>
-__device__ __forceinline__ double vec_elem<double>(const uint4& v, int k) {
-    return k == 0 ? __hiloint2double(static_cast<int>(v.y), static_cast<int>(v.x))
-                  : __hiloint2double(static_cast<int>(v.w), static_cast<int>(v.z));
+__device__ __forceinline__ unsigned long long vec_elem<unsigned long long>(const uint4& v, int k) {
+    return k == 0 ? (static_cast<unsigned long long>(v.y) << 32 | v.x)
+                  : (static_cast<unsigned long long>(v.w) << 32 | v.z);
 }
 template <>
 __device__ __forceinline__ uint16_t vec_elem<uint16_t>(const uint4& v, int k) {

@@ -16,19 +16,20 @@
 
 namespace argr {
 
-// Scratch layout (the buffer is 16-byte aligned):
-//   [0, 4)                 device error word (set by an expired bounded wait)
-//   [kCounterOffset, ...)  one uint32 arrival counter per row slot
-//   [partials_offset, ...) row_slots * blocks_per_row partials of 16 bytes
-//                          (raw value bits in the low bytes of 8, index in 4)
+// Scratch layout (the buffer is 16-byte aligned). The layout does not depend
+// on the plan, so calls with different plans can share one buffer: no call's
+// partials ever overlap another call's counters.
+//   [0, 4)                     device error word (set by an expired bounded wait)
+//   [kCounterOffset, +4*kMaxSplitRows)
+//                              one uint32 arrival counter per row slot
+//   [kPartialsOffset, ...)     row_slots * blocks_per_row partials of 16 bytes
+//                              (raw value bits in the low 8 bytes, index in 4)
 constexpr size_t kCounterOffset = 256;
+constexpr int64_t kMaxSplitRows = 2048;  // row slots a multi-CTA split may use
+constexpr size_t kPartialsOffset = kCounterOffset + 4 * kMaxSplitRows;
 constexpr size_t kPartialBytes = 16;
 
 ARGR_HD inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-
-ARGR_HD inline size_t partials_offset(int64_t row_slots) {
-    return align_up(kCounterOffset + 4 * static_cast<size_t>(row_slots), 256);
-}
 
 struct Problem {
     const void* x;

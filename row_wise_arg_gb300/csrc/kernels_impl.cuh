@@ -36,6 +36,8 @@ rows_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int
             typename Tag::raw* __restrict__ out_val) {
     using R = typename Tag::raw;
     constexpr int E = 16 / sizeof(R);
+    grid_dependency_wait();
+    allow_dependents();
     const int lg = threadIdx.x & (G - 1);
     const int lane = threadIdx.x & 31;
     const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
@@ -56,8 +58,7 @@ rows_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int
 #pragma unroll
             for (int u = 0; u < U; ++u) buf[u] = (u * G < rem) ? ld_stream16(rv + v0 + u * G) : make_uint4(0, 0, 0, 0);
             // Lane 0 of the group always holds vector 0, whose first element is x[0].
-            c.v = shfl_raw(gmask, vec_elem<R>(buf[0], 0), 0, G);
-            c.i = 0;
+            c = make_cand<Tag, OP>(shfl_raw(gmask, vec_elem<R>(buf[0], 0), 0, G), 0);
 #pragma unroll
             for (int u = 0; u < U; ++u)
                 if (u * G < rem) visit_vec<Tag, OP>(c, buf[u], (v0 + u * G) * E);
@@ -77,8 +78,7 @@ rows_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int
             R buf[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) buf[u] = (u * G < rem) ? ld_scalar(row + j0 + u * G) : R(0);
-            c.v = shfl_raw(gmask, buf[0], 0, G);  // lane 0 loaded x[0]
-            c.i = 0;
+            c = make_cand<Tag, OP>(shfl_raw(gmask, buf[0], 0, G), 0);  // lane 0 loaded x[0]
 #pragma unroll
             for (int u = 0; u < U; ++u)
                 if (u * G < rem) visit<Tag, OP>(c, buf[u], j0 + u * G);
@@ -123,7 +123,7 @@ __device__ __forceinline__ Cand<Tag> scan_share(const typename Tag::raw* __restr
     const int vb = b * chunk < nvec ? b * chunk : nvec;
     const int ve = nvec - vb > chunk ? vb + chunk : nvec;
 
-    Cand<Tag> c{x0, 0};
+    Cand<Tag> c = make_cand<Tag, OP>(x0, 0);
     const int t = threadIdx.x;
     const int nt = blockDim.x;
     if (b == 0 && t < head) visit<Tag, OP>(c, ld_scalar(row + t), t);
@@ -152,7 +152,7 @@ __device__ __forceinline__ uint4 pack_cand(const Cand<Tag>& c) {
     using R = typename Tag::raw;
     uint64_t bits = 0;
     if constexpr (sizeof(R) == 8)
-        bits = static_cast<uint64_t>(__double_as_longlong(c.v));
+        bits = c.v;
     else if constexpr (sizeof(R) == 4)
         bits = __float_as_uint(c.v);
     else
@@ -160,18 +160,35 @@ __device__ __forceinline__ uint4 pack_cand(const Cand<Tag>& c) {
     return make_uint4(static_cast<uint32_t>(bits), static_cast<uint32_t>(bits >> 32), static_cast<uint32_t>(c.i), 0u);
 }
 
-template <class Tag>
+template <class Tag, int OP>
 __device__ __forceinline__ Cand<Tag> unpack_cand(const uint4& p) {
     using R = typename Tag::raw;
-    Cand<Tag> c;
+    R v;
     if constexpr (sizeof(R) == 8)
-        c.v = __hiloint2double(static_cast<int>(p.y), static_cast<int>(p.x));
+        v = static_cast<unsigned long long>(p.y) << 32 | p.x;
     else if constexpr (sizeof(R) == 4)
-        c.v = __uint_as_float(p.x);
+        v = __uint_as_float(p.x);
     else
-        c.v = static_cast<uint16_t>(p.x);
-    c.i = static_cast<int>(p.z);
-    return c;
+        v = static_cast<uint16_t>(p.x);
+    return make_cand<Tag, OP>(v, static_cast<int>(p.z));
+}
+
+// Arrival at a row's counter: a wrapping increment with acquire-release
+// semantics at GPU scope. Release publishes this CTA's partial (stored before
+// by the same thread); acquire lets the last arrival read every partial.
+__device__ __forceinline__ unsigned arrive_acq_rel(unsigned* counter, unsigned wrap) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(counter), "r"(wrap) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ uint4 ld_relaxed_gpu(const uint4* p) {
+    uint4 r;
+    asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p)
+                 : "memory");
+    return r;
 }
 
 // ---------------------------------------------------------------------------
@@ -184,41 +201,45 @@ split_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, in
              typename Tag::raw* __restrict__ out_val, unsigned char* __restrict__ scratch) {
     using R = typename Tag::raw;
     __shared__ Cand<Tag> smem[32];
-    __shared__ int s_last;
     const int nb = gridDim.x;
     const int b = blockIdx.x;
+    const int lane = threadIdx.x & 31;
+    grid_dependency_wait();
+    allow_dependents();
     for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
         const R* row = x + r * static_cast<int64_t>(cols);
         const R x0 = ld_scalar(row);
-        const Cand<Tag> seed{x0, 0};
+        const Cand<Tag> seed = make_cand<Tag, OP>(x0, 0);
         Cand<Tag> c = scan_share<Tag, OP, U>(row, cols, b, nb, x0);
-        c = block_merge<Tag, OP>(c, smem, seed);
-        if (nb == 1) {
-            if (threadIdx.x == 0) {
-                out_idx[r] = c.i;
-                if (out_val) out_val[r] = c.v;
-            }
-        } else {
-            unsigned int* counter = reinterpret_cast<unsigned int*>(scratch + kCounterOffset) + blockIdx.y;
-            uint4* parts = reinterpret_cast<uint4*>(scratch + partials_offset(gridDim.y)) +
-                           static_cast<size_t>(blockIdx.y) * nb;
-            if (threadIdx.x == 0) {
-                __stcg(parts + b, pack_cand<Tag>(c));
-                __threadfence();  // the partial is visible device-wide before the arrival
-                // Wrapping increment: the nb-th arrival returns nb-1 and leaves 0.
-                const unsigned old = atomicInc(counter, static_cast<unsigned>(nb - 1));
-                s_last = old == static_cast<unsigned>(nb - 1);
-            }
-            __syncthreads();
-            if (s_last) {
-                __threadfence();
-                Cand<Tag> m = seed;
-                for (int k = threadIdx.x; k < nb; k += blockDim.x)
-                    m = merge<Tag, OP>(m, unpack_cand<Tag>(__ldcg(parts + k)));
-                m = block_merge<Tag, OP>(m, smem, seed);
-                if (threadIdx.x == 0) {
-                    out_idx[r] = m.i;
-                    if (out_val) out_val[r] = m.v;
+        c = block_merge<Tag, OP>(c, smem, seed);  // merged candidate in warp 0
+        if (threadIdx.x < 32) {
+            if (nb == 1) {
+                if (lane == 0) {
+                    out_idx[r] = c.i;
+                    if (out_val) out_val[r] = c.v;
+                }
+            } else {
+                // Multi-CTA row: publish the partial, then arrive. The arrival
+                // that returns nb-1 is the last one; the wrapping increment has
+                // left the counter at zero for the next call.
+                unsigned* counter = reinterpret_cast<unsigned*>(scratch + kCounterOffset) + blockIdx.y;
+                uint4* parts = reinterpret_cast<uint4*>(scratch + kPartialsOffset) +
+                               static_cast<size_t>(blockIdx.y) * nb;
+                unsigned old = 0;
+                if (lane == 0) {
+                    parts[b] = pack_cand<Tag>(c);
+                    old = arrive_acq_rel(counter, static_cast<unsigned>(nb - 1));
+                }
+                old = __shfl_sync(0xffffffffu, old, 0);
+                __syncwarp();
+                if (old == static_cast<unsigned>(nb - 1)) {
+                    Cand<Tag> m = seed;
+                    for (int k = lane; k < nb; k += 32) m = merge<Tag, OP>(m, unpack_cand<Tag, OP>(ld_relaxed_gpu(parts + k)));
+                    m = group_merge<Tag, OP, 32>(m, 0xffffffffu);
+                    if (lane == 0) {
+                        out_idx[r] = m.i;
+                        if (out_val) out_val[r] = m.v;
+                    }
                 }
             }
         }
@@ -247,10 +268,12 @@ cluster_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, 
     const int nb = gridDim.x;   // the cluster spans the grid's x dimension
     const int b = blockIdx.x;   // == rank in the cluster
     int parity = 0;
+    grid_dependency_wait();
+    allow_dependents();
     for (int64_t r = blockIdx.y; r < rows; r += gridDim.y, parity ^= 1) {
         const R* row = x + r * static_cast<int64_t>(cols);
         const R x0 = ld_scalar(row);
-        const Cand<Tag> seed{x0, 0};
+        const Cand<Tag> seed = make_cand<Tag, OP>(x0, 0);
         Cand<Tag> c = scan_share<Tag, OP, U>(row, cols, b, nb, x0);
         c = block_merge<Tag, OP>(c, smem, seed);
         if (threadIdx.x == 0) {
@@ -267,7 +290,7 @@ cluster_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, 
         // later is ordered by the barrier of the row in between.
         cluster_barrier();
         if (b == 0 && threadIdx.x < 32) {
-            Cand<Tag> m = threadIdx.x < nb ? unpack_cand<Tag>(slots[parity][threadIdx.x]) : seed;
+            Cand<Tag> m = threadIdx.x < nb ? unpack_cand<Tag, OP>(slots[parity][threadIdx.x]) : seed;
             m = group_merge<Tag, OP, 32>(m, 0xffffffffu);
             if (threadIdx.x == 0) {
                 out_idx[r] = m.i;
@@ -279,20 +302,53 @@ cluster_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, 
 }
 
 // ---------------------------------------------------------------------------
-// Launchers.
+// Launchers. Every launch goes through cudaLaunchKernelEx so that it can carry
+// the programmatic-dependent-launch attribute (plan flag ARGR_PLAN_PDL) and,
+// on the cluster path, the cluster shape.
 // ---------------------------------------------------------------------------
-template <class Tag, int OP, int G>
-cudaError_t launch_rows_g(const argr_plan& p, const Problem& pr) {
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, int cluster, const argr_plan& p,
+                      cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (p.flags & ARGR_PLAN_PDL) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <class Tag, int OP, int G, int U>
+cudaError_t launch_rows_gu(const argr_plan& p, const Problem& pr) {
     using R = typename Tag::raw;
     const dim3 grid(static_cast<unsigned>(p.grid_rows));
-    const dim3 block(p.block);
     const R* x = static_cast<const R*>(pr.x);
     R* ov = static_cast<R*>(pr.out_val);
     if (p.vec)
-        rows_kernel<Tag, OP, G, true, 4><<<grid, block, 0, pr.stream>>>(x, pr.rows, pr.cols, pr.out_idx, ov);
-    else
-        rows_kernel<Tag, OP, G, false, 4><<<grid, block, 0, pr.stream>>>(x, pr.rows, pr.cols, pr.out_idx, ov);
-    return cudaGetLastError();
+        return launch_ex(rows_kernel<Tag, OP, G, true, U>, grid, dim3(p.block), 1, p, pr.stream, x, pr.rows, pr.cols,
+                         pr.out_idx, ov);
+    return launch_ex(rows_kernel<Tag, OP, G, false, U>, grid, dim3(p.block), 1, p, pr.stream, x, pr.rows, pr.cols,
+                     pr.out_idx, ov);
+}
+
+template <class Tag, int OP, int G>
+cudaError_t launch_rows_g(const argr_plan& p, const Problem& pr) {
+    return p.unroll == 8 ? launch_rows_gu<Tag, OP, G, 8>(p, pr) : launch_rows_gu<Tag, OP, G, 4>(p, pr);
 }
 
 template <class Tag, int OP>
@@ -317,10 +373,9 @@ template <class Tag, int OP, int U>
 cudaError_t launch_split_u(const argr_plan& p, const Problem& pr) {
     using R = typename Tag::raw;
     const dim3 grid(static_cast<unsigned>(p.blocks_per_row), static_cast<unsigned>(p.grid_rows));
-    split_kernel<Tag, OP, U><<<grid, p.block, 0, pr.stream>>>(static_cast<const R*>(pr.x), pr.rows, pr.cols,
-                                                              pr.out_idx, static_cast<R*>(pr.out_val),
-                                                              static_cast<unsigned char*>(pr.scratch));
-    return cudaGetLastError();
+    return launch_ex(split_kernel<Tag, OP, U>, grid, dim3(p.block), 1, p, pr.stream, static_cast<const R*>(pr.x),
+                     pr.rows, pr.cols, pr.out_idx, static_cast<R*>(pr.out_val),
+                     static_cast<unsigned char*>(pr.scratch));
 }
 
 template <class Tag, int OP>
@@ -348,20 +403,31 @@ cudaError_t launch_cluster_u(const argr_plan& p, const Problem& pr) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.cluster), static_cast<unsigned>(p.grid_rows));
-    cfg.blockDim = dim3(p.block);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = pr.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, static_cast<const R*>(pr.x), pr.rows, pr.cols, pr.out_idx,
-                              static_cast<R*>(pr.out_val));
+    const dim3 grid(static_cast<unsigned>(p.cluster), static_cast<unsigned>(p.grid_rows));
+    // Refuse a cluster shape the device cannot co-schedule (checked once per
+    // kernel, block size and cluster size).
+    static thread_local int checked_block = 0, checked_cluster = 0, checked_ok = 0;
+    if (checked_block != p.block || checked_cluster != p.cluster) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(p.block);
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = static_cast<unsigned>(p.cluster);
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        checked_block = p.block;
+        checked_cluster = p.cluster;
+        checked_ok = n > 0;
+    }
+    if (!checked_ok) return cudaErrorInvalidClusterSize;  // reported as ARGR_EUNSUPPORTED
+    return launch_ex(kern, grid, dim3(p.block), p.cluster, p, pr.stream, static_cast<const R*>(pr.x), pr.rows,
+                     pr.cols, pr.out_idx, static_cast<R*>(pr.out_val));
 }
 
 template <class Tag, int OP>

@@ -8,10 +8,16 @@
 //    lane (G = 1 is one thread per row);
 //  * when there are enough rows to fill the device with one warp each, rows of
 //    medium width use one warp per row and wider rows one CTA per row;
-//  * otherwise a row is split over several CTAs so that the grid is about one
-//    wave of the device (more CTAs than one wave was measured slower on the
-//    pages' H200, and the merge cost grows with the CTA count), while every
-//    thread keeps at least kMinBytesPerThread of the row.
+//  * a few wide rows get one thread-block cluster each (up to 16 CTAs, at most
+//    about two CTAs per SM in total), merged through distributed shared memory
+//    with no global round trip, as long as a CTA's share stays small enough
+//    (kClusterMaxCtaBytes) for the cluster's SMs to stream it quickly;
+//  * otherwise (very wide rows) a row is split over several CTAs of the whole
+//    device, about one wave in total (more CTAs than one wave was measured
+//    slower on the pages' H200, and the merge cost grows with the CTA count),
+//    while every thread keeps at least kMinBytesPerThread of the row.
+// Every default plan launches as a programmatic dependent of the previous grid
+// in the stream, which hides launch latency between back-to-back calls.
 #include <algorithm>
 #include <climits>
 
@@ -22,7 +28,9 @@ namespace argr {
 namespace {
 
 constexpr int64_t kNarrowRowBytes = 1024;  // rows up to this width: G lanes per row
-constexpr int64_t kWarpRowBytes = 16384;   // many rows up to this width: one warp per row
+constexpr int64_t kWarpRowBytes = 32768;   // many rows up to this width: a warp (or half) per row
+constexpr int kManyRowsBlock = 128;        // CTA size on the many-rows path
+constexpr int kManyRowsUnroll = 8;         // 16-byte loads in flight per lane on the many-rows path
 constexpr int kBlock = 256;                // threads per CTA on every path
 constexpr int kRowsUnroll = 4;             // loads in flight per lane on the rows path
 constexpr int kSplitUnroll = 4;            // vector loads in flight per thread on the split path
@@ -30,6 +38,7 @@ constexpr int64_t kMinBytesPerThread = 16; // one 16-byte vector per thread at l
 constexpr int64_t kRowsWaves = 8;          // rows path: grid of at most this many waves (grid-stride beyond)
 constexpr int64_t kMaxGridY = 65535;       // hardware limit of gridDim.y
 constexpr int64_t kMaxBlocksPerRow = 65535;
+constexpr int64_t kClusterMaxCtaBytes = 128 * 1024;  // largest share of a row per cluster CTA
 
 int64_t ceil_div(int64_t a, int64_t b) { return a / b + (a % b != 0); }
 
@@ -62,7 +71,7 @@ int elem_size(int dtype) {
 size_t plan_scratch(const argr_plan& p, int64_t rows) {
     (void)rows;
     if (p.path == ARGR_PATH_SPLIT && p.blocks_per_row > 1)
-        return partials_offset(p.grid_rows) +
+        return kPartialsOffset +
                static_cast<size_t>(p.grid_rows) * static_cast<size_t>(p.blocks_per_row) * kPartialBytes;
     return 0;
 }
@@ -86,6 +95,7 @@ argr_status make_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_
 
     out->block = kBlock;
     out->cluster = 0;
+    out->flags = ARGR_PLAN_PDL;
 
     if (row_bytes <= kNarrowRowBytes) {
         // One batch of kRowsUnroll loads per lane covers the row.
@@ -103,14 +113,19 @@ argr_status make_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_
     }
 
     const int64_t wave = ctas_per_wave(caps, kBlock);
-    if (rows >= wave) {
+    if (rows >= wave || rows > kMaxSplitRows) {
         // Enough rows: no row is split.
         if (row_bytes <= kWarpRowBytes) {
+            // Measured on GB300: 128-thread CTAs with 8 loads in flight per
+            // lane, a whole warp for rows of 16 KB and more, half a warp below.
+            const int g = row_bytes >= 16384 ? 32 : 16;
             out->path = ARGR_PATH_ROWS;
-            out->group = 32;
+            out->group = g;
+            out->block = kManyRowsBlock;
             out->vec = aligned ? 1 : 0;
-            out->unroll = kRowsUnroll;
-            out->grid_rows = std::min(ceil_div(rows, kBlock / 32), kRowsWaves * wave);
+            out->unroll = kManyRowsUnroll;
+            out->grid_rows = std::min(ceil_div(rows, kManyRowsBlock / g),
+                                      kRowsWaves * ctas_per_wave(caps, kManyRowsBlock));
             out->blocks_per_row = 1;
         } else {
             out->path = ARGR_PATH_SPLIT;
@@ -122,7 +137,28 @@ argr_status make_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_
         return ARGR_OK;
     }
 
-    // Few rows: split each row over CTAs, about one wave in total.
+    // Few rows: one cluster per row while a CTA's share stays small.
+    if (caps.max_cluster >= 2 && rows <= caps.sm_count) {
+        int c = 16;
+        while (c > 2 && (c > caps.max_cluster || rows * c > 2 * static_cast<int64_t>(caps.sm_count))) c /= 2;
+        const int64_t per_cta = row_bytes / c;
+        if (c <= caps.max_cluster && rows * c <= 2 * static_cast<int64_t>(caps.sm_count) &&
+            per_cta <= kClusterMaxCtaBytes) {
+            const int block = per_cta >= 16384 ? 512 : (per_cta >= 4096 ? 256 : 128);
+            int unroll = 1;
+            while (unroll < 8 && static_cast<int64_t>(unroll) * block * 16 < per_cta) unroll <<= 1;
+            out->path = ARGR_PATH_CLUSTER;
+            out->cluster = c;
+            out->block = block;
+            out->unroll = unroll;
+            out->blocks_per_row = c;
+            out->grid_rows = std::min(rows, kMaxGridY);
+            out->scratch_bytes = 0;
+            return ARGR_OK;
+        }
+    }
+
+    // Very wide rows: split each row over CTAs, about one wave in total.
     const int64_t by_wave = std::max<int64_t>(1, wave / rows);
     const int64_t by_work = std::max<int64_t>(1, row_bytes / (kBlock * kMinBytesPerThread));
     const int64_t bpr = std::min({by_wave, by_work, kMaxBlocksPerRow});
@@ -141,11 +177,12 @@ argr_status check_plan(const argr_plan& p, int64_t rows, int64_t cols, int dtype
     if (!valid_dtype(dtype) || rows < 0 || cols < 1 || cols > INT_MAX) return ARGR_EINVAL;
     if (rows == 0) return ARGR_OK;
     if (p.block < 32 || p.block > 1024 || p.block % 32 != 0) return ARGR_EINVAL;
+    if (p.flags & ~ARGR_PLAN_PDL) return ARGR_EINVAL;
     switch (p.path) {
         case ARGR_PATH_ROWS: {
             const int g = p.group;
             if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16 && g != 32) return ARGR_EINVAL;
-            if (p.unroll != kRowsUnroll) return ARGR_EINVAL;
+            if (p.unroll != 4 && p.unroll != 8) return ARGR_EINVAL;
             if (p.vec && !row_aligned) return ARGR_EINVAL;
             if (p.vec != 0 && p.vec != 1) return ARGR_EINVAL;
             if (p.grid_rows < 1 || p.grid_rows > INT_MAX) return ARGR_EINVAL;
@@ -155,8 +192,9 @@ argr_status check_plan(const argr_plan& p, int64_t rows, int64_t cols, int dtype
             if (p.unroll != 1 && p.unroll != 2 && p.unroll != 4 && p.unroll != 8) return ARGR_EINVAL;
             if (p.blocks_per_row < 1 || p.blocks_per_row > kMaxBlocksPerRow) return ARGR_EINVAL;
             if (p.grid_rows < 1 || p.grid_rows > kMaxGridY) return ARGR_EINVAL;
-            // A split row owns its partial slots and counter: no row loop.
-            if (p.blocks_per_row > 1 && p.grid_rows < rows) return ARGR_EINVAL;
+            // A split row owns its partial slots and counter: no row loop, and
+            // at most kMaxSplitRows counters exist.
+            if (p.blocks_per_row > 1 && (p.grid_rows < rows || p.grid_rows > kMaxSplitRows)) return ARGR_EINVAL;
             return ARGR_OK;
         }
         case ARGR_PATH_CLUSTER: {

@@ -73,11 +73,12 @@ def forced_plan(path: str, **kw):
     p = _lib.argr_plan()
     p.block = kw.get("block", 256)
     p.unroll = kw.get("unroll", 4)
+    p.flags = _lib.ARGR_PLAN_PDL if kw.get("pdl", True) else 0
     if path == "rows":
         p.path = _lib.ARGR_PATH_ROWS
         p.group = kw["group"]
         p.vec = kw.get("vec", 0)
-        p.unroll = 4
+        p.unroll = kw.get("unroll", 4)
         p.grid_rows = kw.get("grid", 64)
         p.blocks_per_row = 1
     elif path == "split":

@@ -37,7 +37,7 @@ def test_rows_zero_and_one_col():
 
 
 def test_scratch_errors():
-    rows, cols = 4, 100000
+    rows, cols = 2, 3_000_000  # too wide for one cluster: split over the device, with scratch
     x = torch.randn(rows, cols, device="cuda")
     out = torch.empty(rows, dtype=torch.int64, device="cuda")
     need = A.argreduce_scratch_bytes(rows, cols, "f32", "max")
@@ -83,7 +83,7 @@ def test_forced_plan_validation():
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f64"])
 def test_dirtied_partials_and_repeat(dtype):
     """Counters reset themselves; garbage in the partials region is harmless."""
-    rows, cols = 8, 202048
+    rows, cols = 4, 2_500_000  # split over the device: partials and counters in scratch
     c = W.Case("t", rows, cols, dtype, "max", "batch_logits", 3001)
     x = W.make(c)
     eidx, _, _ = oracle.argreduce(x, dtype, "max")
@@ -92,8 +92,8 @@ def test_dirtied_partials_and_repeat(dtype):
     assert plan.blocks_per_row > 1
     scratch = A.Scratch(nbytes=plan.scratch_bytes)
     from row_wise_arg_gb300._lib import argreduce_plan_scratch_bytes
-    # partials start after the 256-byte header and the counters, 256-aligned
-    off = ((256 + 4 * plan.grid_rows + 255) // 256) * 256
+    # partials start after the 256-byte header and 2048 row-slot counters
+    off = 256 + 4 * 2048
     assert argreduce_plan_scratch_bytes(plan, rows) <= scratch.nbytes
     for it in range(5):
         scratch.buf[off:].fill_(0xFF if it % 2 else 0xA5)  # dirty the partials only
@@ -103,6 +103,21 @@ def test_dirtied_partials_and_repeat(dtype):
     # the counters are back at zero after every call
     counters = scratch.buf[256:256 + 4 * plan.grid_rows].cpu()
     assert (counters == 0).all()
+
+
+def test_shared_scratch_across_plans():
+    """Calls with different split plans share one scratch buffer; a call's
+    partials never disturb another call's arrival counters."""
+    shapes = [(1, 300000), (500, 3000), (7, 90001), (1200, 5000), (1, 33), (300, 20000)]
+    data = [W.fuzz_rows("f32", r, c, seed=r * 7 + c, p_special=0.01) for r, c in shapes]
+    exp = [oracle.argreduce(x, "f32", "max")[0] for x in data]
+    dev = [to_device(x, "f32")[0] for x in data]
+    scratch = A.Scratch()
+    for rep in range(3):
+        for k in (list(range(len(shapes))) if rep % 2 == 0 else list(reversed(range(len(shapes))))):
+            idx, _ = A.argreduce(dev[k], "max", scratch=scratch)
+            torch.cuda.synchronize()
+            assert (idx.cpu().numpy() == exp[k]).all(), (rep, shapes[k])
 
 
 @pytest.mark.parametrize("path", ["planner", "split", "cluster", "rows"])

@@ -76,10 +76,11 @@ def test_rows_path(dtype, group):
         rows = 37 if cols < 2000 else 5
         x = W.fuzz_rows(dtype, rows, cols, seed=cols * 31 + group)
         for op in W.OPS:
-            check(x, dtype, op, plan=forced_plan("rows", group=group, vec=0, grid=3))
-            check(x, dtype, op, plan=forced_plan("rows", group=group, vec=0, grid=64), offset=1)
+            check(x, dtype, op, plan=forced_plan("rows", group=group, vec=0, grid=3, pdl=False))
+            check(x, dtype, op, plan=forced_plan("rows", group=group, vec=0, grid=64, unroll=8), offset=1)
             if (cols * es) % 16 == 0:
                 check(x, dtype, op, plan=forced_plan("rows", group=group, vec=1, grid=5))
+                check(x, dtype, op, plan=forced_plan("rows", group=group, vec=1, grid=7, unroll=8, pdl=False))
 
 
 @pytest.mark.parametrize("dtype", W.DTYPES)
@@ -91,7 +92,7 @@ def test_split_path(dtype, bpr):
         for op in W.OPS:
             for block, unroll in ((256, 4), (32, 1), (1024, 8), (64, 2)):
                 check(x, dtype, op, plan=forced_plan("split", bpr=bpr, grid_rows=rows, block=block,
-                                                     unroll=unroll))
+                                                     unroll=unroll, pdl=block != 32))
             for off in (1, 3):
                 check(x, dtype, op, plan=forced_plan("split", bpr=bpr, grid_rows=rows), offset=off)
             if bpr == 1:  # row loop: fewer row slots than rows
@@ -109,7 +110,9 @@ def test_cluster_path(dtype, cluster):
         x = W.fuzz_rows(dtype, rows, cols, seed=cols * 13 + cluster)
         for op in W.OPS:
             check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=rows))
-            check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=2, unroll=1), offset=1)
+            check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=2, unroll=1, pdl=False),
+                  offset=1)
+            check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=rows, block=512, unroll=8))
 
 
 @pytest.mark.parametrize("dtype", W.DTYPES)
@@ -121,7 +124,9 @@ def test_exhaustive_alphabet_rows(dtype):
         check(x, dtype, op)
         check(x, dtype, op, plan=forced_plan("rows", group=4, vec=0, grid=100))
         check(x, dtype, op, plan=forced_plan("split", bpr=1, grid_rows=min(rows, 1000), block=32))
-        check(x, dtype, op, plan=forced_plan("split", bpr=3, grid_rows=rows, block=32))
+        for r0 in range(0, rows, 2048):  # a multi-CTA split has at most 2048 row slots
+            xs = np.ascontiguousarray(x[r0:r0 + 2048])
+            check(xs, dtype, op, plan=forced_plan("split", bpr=3, grid_rows=xs.shape[0], block=32))
 
 
 @pytest.mark.parametrize("dtype", W.DTYPES)

@@ -91,6 +91,9 @@ def test_plan_geometry(caps, dtype):
             if d["vec"]:
                 assert (cols * es) % 16 == 0
             assert d["scratch_bytes"] == 0
+        elif d["path_name"] == "cluster":
+            assert 2 <= d["cluster"] <= 16 and d["blocks_per_row"] == d["cluster"]
+            assert rows * d["cluster"] <= 2 * caps.sm_count and d["scratch_bytes"] == 0
         elif d["path_name"] == "split":
             bpr = d["blocks_per_row"]
             assert 1 <= bpr <= 65535 and 1 <= d["grid_rows"] <= 65535
@@ -98,7 +101,8 @@ def test_plan_geometry(caps, dtype):
                 assert d["grid_rows"] >= rows
                 # about one wave, and the scratch stays in the kilobytes
                 assert rows * bpr <= max(wave, rows)
-                assert d["scratch_bytes"] <= 512 + 20 * wave
+                assert d["scratch_bytes"] <= 256 + 4 * 2048 + 16 * max(wave, rows)
+                assert d["grid_rows"] <= 2048
             else:
                 assert d["scratch_bytes"] == 0
         else:
@@ -110,13 +114,27 @@ def test_plan_paths_for_configs():
     def path(rows, cols, dt="f32"):
         return A.argreduce_plan(rows, cols, dt, "max", GB300).as_dict()
 
-    assert path(1, 32000)["path_name"] == "split" and path(1, 32000)["blocks_per_row"] > 1
-    assert path(1, 202048)["blocks_per_row"] > 100
-    assert path(32, 202048)["blocks_per_row"] > 1
+    for rows, cols in ((1, 32000), (1, 202048), (1, 262144), (8, 202048), (32, 202048)):
+        d = path(rows, cols)
+        assert d["path_name"] == "cluster" and d["cluster"] >= 8, d
+        assert rows * d["cluster"] <= 2 * 152 and d["scratch_bytes"] == 0
+        assert d["flags"] & _lib.ARGR_PLAN_PDL
+    d = path(1, 10_000_000)  # too wide for one cluster: split over the device
+    assert d["path_name"] == "split" and d["blocks_per_row"] > 152
     assert path(4096, 4096)["path_name"] == "rows" and path(4096, 4096)["group"] == 32
     for cols in (8, 64, 128):
         d = path(65536 if cols == 64 else 4096, cols)
         assert d["path_name"] == "rows" and d["vec"] == 1 and d["group"] <= 8
+
+
+def test_split_rows_capped():
+    """A multi-CTA split never uses more row slots than the scratch has
+    counters (2048), even on a device whose wave holds more rows."""
+    big = A.make_caps(2000)
+    for rows in (2047, 2048, 2049, 5000):
+        d = A.argreduce_plan(rows, 100000, "f32", "max", big).as_dict()
+        if d["blocks_per_row"] > 1:
+            assert d["grid_rows"] == rows <= 2048
 
 
 def test_plan_rejects_bad_input():
