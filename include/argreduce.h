@@ -177,6 +177,35 @@ size_t argreduce_plan_scratch_bytes(const argr_plan* plan, int64_t rows);
  */
 argr_status argreduce_read_error(void* scratch, argr_stream stream);
 
+/*
+ * argreduce() for callers that cannot allocate device memory. The paper has
+ * no counterpart to this entry point: it exists for code that runs where
+ * cudaMalloc is not available to it, for example a plugin inside an inference
+ * engine that owns every device allocation and hands it no allocator, a
+ * real-time path that may not make a call that can synchronise the device or
+ * block for an unbounded time, or code that must not grow its memory use
+ * after start-up.
+ *
+ * It runs the split-row kernel (a row spread over CTAs of the whole device,
+ * merged by the CTA that arrives last) with its scratch in a 32 KiB array
+ * inside this library instead of caller memory. That array exists once per
+ * GPU, on every GPU that loads the library, until the process exits. The
+ * caller still passes x, out_idx and out_val exactly as for argreduce();
+ * there is no scratch argument. The call allocates and frees nothing.
+ *
+ *   - The first call on each device (with that device current) finds the
+ *     array's device address and zeroes it, synchronously. Make that first
+ *     call before capturing any stream on the device.
+ *   - Every call reuses the same array: two calls that can overlap on the GPU
+ *     (other streams, other host threads) race on it and give wrong results;
+ *     serialise them. Each call clears the counters it uses before its kernel.
+ *   - A problem whose plan needs more than the array holds returns
+ *     ARGR_ESCRATCH before anything is queued (on a GB300 every shape fits).
+ *   - Other errors as for argreduce().
+ */
+argr_status argreduce_noalloc(const void* x, argr_dtype dtype, int64_t rows, int64_t cols, argr_op op,
+                              int64_t* out_idx, void* out_val, argr_stream stream);
+
 /* Properties of `device` as the planner sees them (queried once, cached). */
 argr_status argreduce_device_caps(int device, argr_caps* out);
 

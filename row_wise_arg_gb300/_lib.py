@@ -29,7 +29,7 @@ PATH_NAMES = {ARGR_PATH_NONE: "none", ARGR_PATH_ROWS: "rows", ARGR_PATH_SPLIT: "
 EXPORTS = (
     "argreduce_scratch_bytes", "argreduce_scratch_init", "argreduce", "argreduce_plan",
     "argreduce_with_plan", "argreduce_plan_scratch_bytes", "argreduce_read_error",
-    "argreduce_device_caps", "argreduce_status_string", "argreduce_version",
+    "argreduce_device_caps", "argreduce_status_string", "argreduce_version", "argreduce_noalloc",
 )
 
 
@@ -94,6 +94,8 @@ def load() -> ctypes.CDLL:
         lib.argreduce_device_caps.restype = i32
         lib.argreduce_status_string.argtypes = [i32]
         lib.argreduce_status_string.restype = ctypes.c_char_p
+        lib.argreduce_noalloc.argtypes = [vp, i32, i64, i64, i32, vp, vp, vp]
+        lib.argreduce_noalloc.restype = i32
         lib.argreduce_version.argtypes = []
         lib.argreduce_version.restype = ctypes.c_char_p
         del i64p
@@ -134,6 +136,14 @@ def argreduce_raw(x_ptr: int, dtype, rows: int, cols: int, op, out_idx_ptr: int,
     return load().argreduce(x_ptr or None, _code(DTYPE_CODES, dtype), rows, cols, _code(OP_CODES, op),
                             out_idx_ptr or None, out_val_ptr or None, scratch_ptr or None, scratch_bytes,
                             stream_ptr or None)
+
+
+def argreduce_noalloc_raw(x_ptr: int, dtype, rows: int, cols: int, op, out_idx_ptr: int, out_val_ptr: int,
+                         stream_ptr: int) -> int:
+    """The C call argreduce_noalloc(): no scratch argument, allocates nothing;
+    its scratch is an array inside the library shared by every call."""
+    return load().argreduce_noalloc(x_ptr or None, _code(DTYPE_CODES, dtype), rows, cols, _code(OP_CODES, op),
+                                    out_idx_ptr or None, out_val_ptr or None, stream_ptr or None)
 
 
 def argreduce_with_plan_raw(plan: argr_plan, x_ptr: int, dtype, rows: int, cols: int, op, out_idx_ptr: int,

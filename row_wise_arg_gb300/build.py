@@ -29,7 +29,8 @@ NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-
                      "-ftz=false", "-prec-div=true", "-prec-sqrt=true",
                      "-I" + INCLUDE, "-I" + CSRC]
 
-SOURCES = ["api.cpp", "plan.cpp", "kernels_f32.cu", "kernels_f16.cu", "kernels_bf16.cu", "kernels_f64.cu"]
+SOURCES = ["api.cpp", "plan.cpp", "kernels_f32.cu", "kernels_f16.cu", "kernels_bf16.cu", "kernels_f64.cu",
+           "noalloc.cu"]
 HEADERS = ["device_common.cuh", "kernels_impl.cuh", "internal.h"]
 
 
