@@ -50,6 +50,7 @@ WORKLOADS = {
     "narrow": (5, "ArgMax fp32 [65536,64]+[4096,8]+[4096,128]"),
 }
 DTYPE_LABEL = {"f32": "f32", "f16": "f16", "bf16": "bf16", "f64": "f64"}
+KERNEL_OF_PATH = {"rows": "rows_kernel", "split": "split_kernel", "cluster": "cluster_kernel", "none": "none"}
 
 
 def algo_bytes(c: W.Case, with_values: bool = False) -> int:
@@ -87,10 +88,9 @@ def read_traffic(workload: str):
     src = kernel_source_hash()
     for line in open(p):
         parts = line.split()
-        if len(parts) >= 3 and parts[0] == workload and not line.startswith("#"):
-            if parts[2] != src:
-                return None
-            return float(parts[1])
+        if line.startswith("#") or len(parts) < 3 or parts[0] != workload:
+            continue
+        return float(parts[1]) if parts[2] == src else None
     return None
 
 
@@ -378,7 +378,10 @@ def main():
 
     rank, world, local, dist = dist_setup(args.gpus)
     if args.impl == "reference":
-        return reference_arm(args, rank, world, dist)
+        rc = reference_arm(args, rank, world, dist)
+        if dist is not None:
+            dist.destroy_process_group()
+        return rc
 
     import torch
     if not torch.cuda.is_available():
@@ -405,10 +408,12 @@ def main():
     us_per_call = secs * 1e6 / (calls * world)
     achieved = step_bytes * args.steps / secs / 1e9  # per GPU (every rank runs the same steps)
     plans = {}
+    kernels = set()
     for c in cases:
         p = A.argreduce_plan(c.rows, c.cols, c.dtype, c.op).as_dict()
-        plans[f"{c.rows}x{c.cols}_{c.dtype}"] = {k: p[k] for k in ("path_name", "blocks_per_row", "block",
-                                                                    "unroll", "group")}
+        plans[f"{c.rows}x{c.cols}_{c.dtype}"] = {k: p[k] for k in ("path_name", "blocks_per_row", "cluster",
+                                                                    "block", "unroll", "group", "flags")}
+        kernels.add(KERNEL_OF_PATH[p["path_name"]])
 
     result = {
         "metric": METRIC, "value": round(us_per_call, 4), "unit": "us/call", "n_gpus": world,
@@ -429,7 +434,9 @@ def main():
     result["roofline"] = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                           "frac": round(achieved / peak, 5), "traffic": traffic,
                           "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
-                          else "fallback", "kernel": "split_kernel (all calls of this workload)",
+                          else "fallback", "kernel": " + ".join(sorted(kernels)) + " (every call of the step)",
+                          "traffic_source": "profiles/traffic.txt (ncu dram__bytes_read.sum + dram__bytes_write.sum "
+                                            "per launch, averaged over the step's calls)",
                           "bytes_per_launch_avg": step_bytes / len(cases)}
 
     if world == 1 or rank == 0:
