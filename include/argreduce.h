@@ -63,8 +63,12 @@ typedef enum {
     ARGR_PATH_ROWS = 1,    /* `group` lanes per row (1 = thread per row, 32 = warp per row) */
     ARGR_PATH_SPLIT = 2,   /* `blocks_per_row` CTAs per row; >1 merges through scratch,
                               the last CTA to arrive for a row reduces the partials */
-    ARGR_PATH_CLUSTER = 3  /* one thread-block cluster of `cluster` CTAs per row, merged
+    ARGR_PATH_CLUSTER = 3, /* one thread-block cluster of `cluster` CTAs per row, merged
                               through distributed shared memory; no scratch */
+    ARGR_PATH_STREAM = 4   /* every warp streams a contiguous range of rows through its own
+                              `stages` shared-memory buffers of `stage_bytes`, filled by bulk
+                              (TMA) copies; `group` lanes per row for rows that fit a buffer,
+                              the whole warp otherwise. Needs 16-byte aligned rows. */
 } argr_path;
 
 /* Device properties the planner uses. */
@@ -79,21 +83,33 @@ typedef struct {
  * stream. The kernel still waits for that grid to complete before it touches
  * memory, so results are the same; only the launch latency overlaps. */
 #define ARGR_PLAN_PDL 1
+/* Plan flag (CLUSTER path): each CTA's share of the row is fetched into shared
+ * memory by bulk (TMA) copies issued all at once, instead of by loads from
+ * every thread. The share must be at most 128 KiB. */
+#define ARGR_PLAN_BULK 2
+/* Plan flag for tests of failure handling (STREAM path only): one bulk copy's
+ * barrier is made to expect more bytes than arrive, so the kernel's bounded
+ * wait (2 ms under this flag) expires; the kernel records the expiry, skips its
+ * work and returns, and argreduce_read_error() reports ARGR_ETIMEOUT. Outputs
+ * are undefined. Never set in the planner's plans. */
+#define ARGR_PLAN_TEST_EXPIRE 4
 
 /* A launch plan. Produced by argreduce_plan(); tests may edit it to force a
  * path and pass it to argreduce_with_plan(), which re-validates it. */
 typedef struct {
     int32_t path;           /* argr_path */
     int32_t block;          /* threads per CTA: multiple of 32, 32..1024 */
-    int32_t group;          /* ROWS: lanes per row, power of two 1..32 */
+    int32_t group;          /* ROWS / STREAM: lanes per row, power of two 1..32 */
     int32_t vec;            /* 1: 16-byte vector loads (ROWS needs every row 16-byte aligned) */
     int32_t unroll;         /* loads in flight per thread per step: ROWS 4 or 8; SPLIT/CLUSTER 1,2,4,8 */
     int32_t cluster;        /* CLUSTER: CTAs per cluster, 2..16 */
     int32_t flags;          /* ARGR_PLAN_* bits */
+    int32_t stages;         /* STREAM: buffers per warp, 1..4 */
+    int32_t stage_bytes;    /* STREAM: bytes per buffer, multiple of 16, 1 KiB..64 KiB */
     int32_t reserved;       /* 0 */
     int64_t blocks_per_row; /* SPLIT / CLUSTER: CTAs that share one row */
     int64_t grid_rows;      /* SPLIT / CLUSTER: row slots in the grid (rows loop over them);
-                               ROWS: number of CTAs */
+                               ROWS / STREAM: number of CTAs */
     uint64_t scratch_bytes; /* bytes of scratch this plan needs (0 = none) */
 } argr_plan;
 
@@ -170,10 +186,12 @@ argr_status argreduce_with_plan(const argr_plan* plan, const void* x, argr_dtype
 size_t argreduce_plan_scratch_bytes(const argr_plan* plan, int64_t rows);
 
 /*
- * Synchronise `stream` and read the device error word in `scratch` (written
- * by a kernel whose bounded wait expired). Returns ARGR_ETIMEOUT if set (and
- * clears it), ARGR_OK otherwise, ARGR_ECUDA if the stream reports a fault.
- * For tests and benchmarks; it blocks the host.
+ * Synchronise `stream` and read the library's device error words (set by a
+ * kernel whose bounded wait for a bulk copy expired; such a kernel skips the
+ * rest of its work and returns) and the one in `scratch` (may be NULL).
+ * Returns ARGR_ETIMEOUT if any was set (and clears them), ARGR_OK otherwise,
+ * ARGR_ECUDA if the stream reports a fault. For tests and benchmarks; it
+ * blocks the host.
  */
 argr_status argreduce_read_error(void* scratch, argr_stream stream);
 

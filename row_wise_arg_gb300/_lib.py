@@ -17,13 +17,15 @@ LIB_PATH = os.path.join(PKG, "libargreduce.so")
 ARGR_F32, ARGR_F16, ARGR_BF16, ARGR_F64 = 0, 1, 2, 3
 ARGR_MAX, ARGR_MIN = 0, 1
 (ARGR_OK, ARGR_EINVAL, ARGR_ESCRATCH, ARGR_EUNSUPPORTED, ARGR_ECUDA, ARGR_ETIMEOUT) = range(6)
-ARGR_PATH_NONE, ARGR_PATH_ROWS, ARGR_PATH_SPLIT, ARGR_PATH_CLUSTER = range(4)
+ARGR_PATH_NONE, ARGR_PATH_ROWS, ARGR_PATH_SPLIT, ARGR_PATH_CLUSTER, ARGR_PATH_STREAM = range(5)
 ARGR_PLAN_PDL = 1
+ARGR_PLAN_BULK = 2
+ARGR_PLAN_TEST_EXPIRE = 4
 
 DTYPE_CODES = {"f32": ARGR_F32, "f16": ARGR_F16, "bf16": ARGR_BF16, "f64": ARGR_F64}
 OP_CODES = {"max": ARGR_MAX, "min": ARGR_MIN}
 PATH_NAMES = {ARGR_PATH_NONE: "none", ARGR_PATH_ROWS: "rows", ARGR_PATH_SPLIT: "split",
-              ARGR_PATH_CLUSTER: "cluster"}
+              ARGR_PATH_CLUSTER: "cluster", ARGR_PATH_STREAM: "stream"}
 
 # Every function the header declares (checked by the tests).
 EXPORTS = (
@@ -41,7 +43,8 @@ class argr_caps(ctypes.Structure):
 class argr_plan(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("block", ctypes.c_int32), ("group", ctypes.c_int32),
                 ("vec", ctypes.c_int32), ("unroll", ctypes.c_int32), ("cluster", ctypes.c_int32),
-                ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("flags", ctypes.c_int32), ("stages", ctypes.c_int32), ("stage_bytes", ctypes.c_int32),
+                ("reserved", ctypes.c_int32),
                 ("blocks_per_row", ctypes.c_int64), ("grid_rows", ctypes.c_int64),
                 ("scratch_bytes", ctypes.c_uint64)]
 

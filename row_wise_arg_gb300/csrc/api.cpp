@@ -84,6 +84,7 @@ argr_status run(const argr_plan& p, const Problem& pr, size_t scratch_bytes) {
         case ARGR_PATH_ROWS: e = launch_rows_##sfx(p, pr); break;          \
         case ARGR_PATH_SPLIT: e = launch_split_##sfx(p, pr); break;        \
         case ARGR_PATH_CLUSTER: e = launch_cluster_##sfx(p, pr); break;    \
+        case ARGR_PATH_STREAM: e = launch_stream_##sfx(p, pr); break;      \
         default: return ARGR_EINVAL;                                       \
     }
     switch (pr.dtype) {
@@ -191,20 +192,36 @@ argr_status argreduce_read_error(void* scratch, argr_stream stream) {
         cudaGetLastError();
         return ARGR_ECUDA;
     }
-    if (!scratch) return ARGR_OK;
-    if (reinterpret_cast<uintptr_t>(scratch) % 16 != 0) return ARGR_ESCRATCH;
-    unsigned int word = 0;
-    if (cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
-        cudaGetLastError();
-        return ARGR_ECUDA;
+    if (scratch && reinterpret_cast<uintptr_t>(scratch) % 16 != 0) return ARGR_ESCRATCH;
+    // Error words of the kernels of every element type (bounded waits that
+    // expired), and the one in the caller's scratch.
+    unsigned any = 0;
+    cudaError_t (*readers[])(unsigned*) = {read_and_clear_error_f32, read_and_clear_error_f16,
+                                           read_and_clear_error_bf16, read_and_clear_error_f64};
+    for (auto rd : readers) {
+        unsigned v = 0;
+        if (rd(&v) != cudaSuccess) {
+            cudaGetLastError();
+            return ARGR_ECUDA;
+        }
+        any |= v;
     }
-    if (word == 0) return ARGR_OK;
-    const unsigned int zero = 0;
-    if (cudaMemcpy(scratch, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
-        cudaGetLastError();
-        return ARGR_ECUDA;
+    if (scratch) {
+        unsigned int word = 0;
+        if (cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+            cudaGetLastError();
+            return ARGR_ECUDA;
+        }
+        if (word) {
+            const unsigned int zero = 0;
+            if (cudaMemcpy(scratch, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
+                cudaGetLastError();
+                return ARGR_ECUDA;
+            }
+        }
+        any |= word;
     }
-    return ARGR_ETIMEOUT;
+    return any ? ARGR_ETIMEOUT : ARGR_OK;
 }
 
 argr_status argreduce_device_caps(int device, argr_caps* out) {

@@ -60,7 +60,9 @@ size_t plan_scratch(const argr_plan& p, int64_t rows);
 #define ARGR_DECLARE_LAUNCHERS(sfx)                                              \
     cudaError_t launch_rows_##sfx(const argr_plan& p, const Problem& pr);    \
     cudaError_t launch_split_##sfx(const argr_plan& p, const Problem& pr);   \
-    cudaError_t launch_cluster_##sfx(const argr_plan& p, const Problem& pr);
+    cudaError_t launch_cluster_##sfx(const argr_plan& p, const Problem& pr); \
+    cudaError_t launch_stream_##sfx(const argr_plan& p, const Problem& pr);  \
+    cudaError_t read_and_clear_error_##sfx(unsigned* out);
 ARGR_DECLARE_LAUNCHERS(f32)
 ARGR_DECLARE_LAUNCHERS(f16)
 ARGR_DECLARE_LAUNCHERS(bf16)

@@ -14,6 +14,11 @@
 //  * cluster_kernel - one thread-block cluster per row: CTAs push their
 //                     candidates into CTA 0's shared memory (distributed shared
 //                     memory) and meet at a cluster barrier. No scratch.
+//  * stream_kernel  - every warp owns a contiguous range of rows and streams
+//                     them through its own shared-memory stages with bulk
+//                     (TMA) copies, several in flight; rows that fit a stage
+//                     are scanned G lanes per row, wider rows piece by piece
+//                     by the whole warp. Rows must start on 16-byte boundaries.
 //
 // Index arithmetic: within a row every position is an int in [0, cols) with
 // cols <= INT32_MAX. Loops are written with differences (remaining = end -
@@ -24,6 +29,7 @@
 
 #include "device_common.cuh"
 #include "internal.h"
+#include "tma.cuh"
 
 namespace argr {
 
@@ -302,17 +308,288 @@ cluster_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, 
 }
 
 // ---------------------------------------------------------------------------
+// One cluster per row, with every CTA's share fetched by bulk copies.
+//
+// Same decomposition and merge as cluster_kernel, but CTA b's part of the
+// row's 16-byte-aligned body (at most kBulkMaxPieces * kBulkPieceBytes bytes)
+// is copied into shared memory by up to eight bulk copies issued at once, each
+// completing on its own mbarrier, so the whole share is in flight at the start
+// instead of a few loads per thread. Threads scan piece p as soon as it lands.
+// The scalar head and tail are read directly as in scan_share().
+// If a bounded wait expires the CTA records the error and skips its scans but
+// keeps the control flow (merges, cluster barriers) of the other CTAs.
+// ---------------------------------------------------------------------------
+constexpr int kBulkPieceBytes = 16384;
+constexpr int kBulkMaxPieces = 8;
+
+template <class Tag, int OP>
+__global__ void __launch_bounds__(1024)
+cluster_bulk_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int64_t* __restrict__ out_idx,
+                    typename Tag::raw* __restrict__ out_val) {
+    using R = typename Tag::raw;
+    constexpr int E = 16 / sizeof(R);
+    extern __shared__ __align__(128) unsigned char bulk_smem[];
+    __shared__ Cand<Tag> smem[32];
+    __shared__ __align__(16) uint4 slots[2][16];
+    __shared__ __align__(8) unsigned long long bars[kBulkMaxPieces];
+    grid_dependency_wait();
+    allow_dependents();
+    const int nb = gridDim.x;  // the cluster spans the grid's x dimension
+    const int b = blockIdx.x;  // == rank in the cluster
+    const int t = threadIdx.x;
+    const int nt = blockDim.x;
+    const unsigned buf = smem_u32(bulk_smem);
+    const unsigned bar0 = smem_u32(bars);
+    if (t == 0) {
+        for (int p = 0; p < kBulkMaxPieces; ++p) mbar_init(bar0 + 8 * p, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    bool abort = false;         // CTA-uniform from one row to the next
+    unsigned phase_bits = 0;    // bit p: parity of barrier p's next phase
+    unsigned pending = 0;       // bit p: a copy on barrier p not yet waited for (thread 0)
+    int parity = 0;
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y, parity ^= 1) {
+        const R* row = x + r * static_cast<int64_t>(cols);
+        const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
+        int head = static_cast<int>(((16u - (addr & 15u)) & 15u) / sizeof(R));
+        if (head > cols) head = cols;
+        const int nvec = (cols - head) / E;
+        const int tail0 = head + nvec * E;
+        const uint4* rv = reinterpret_cast<const uint4*>(row + head);
+        const int chunk = nvec / nb + (nvec % nb != 0);
+        const int vb = b * chunk < nvec ? b * chunk : nvec;
+        const int ve = nvec - vb > chunk ? vb + chunk : nvec;
+        const int nbytes = (ve - vb) * 16;
+        const int npieces = (nbytes + kBulkPieceBytes - 1) / kBulkPieceBytes;
+        if (t == 0 && !abort) {
+            fence_proxy_async_smem();  // earlier reads of the buffer come before the copies that overwrite it
+            for (int p = 0; p < npieces; ++p) {
+                const int off = p * kBulkPieceBytes;
+                const int bytes = nbytes - off < kBulkPieceBytes ? nbytes - off : kBulkPieceBytes;
+                mbar_arrive_expect_tx(bar0 + 8 * p, static_cast<unsigned>(bytes));
+                bulk_copy_g2s(buf + off, reinterpret_cast<const unsigned char*>(rv + vb) + off,
+                              static_cast<unsigned>(bytes), bar0 + 8 * p);
+                pending |= 1u << p;
+            }
+        }
+        const R x0 = ld_scalar(row);
+        const Cand<Tag> seed = make_cand<Tag, OP>(x0, 0);
+        Cand<Tag> c = seed;
+        if (b == 0 && t < head) visit<Tag, OP>(c, ld_scalar(row + t), t);
+        for (int p = 0; p < npieces; ++p) {
+            const unsigned par = (phase_bits >> p) & 1u;
+            if (!abort) {
+                if (mbar_wait_bounded(bar0 + 8 * p, par)) {
+                    const int off = p * kBulkPieceBytes;
+                    const int nvp = (nbytes - off < kBulkPieceBytes ? nbytes - off : kBulkPieceBytes) >> 4;
+                    const int v0 = vb + (off >> 4);
+                    for (int v = t; v < nvp; v += nt)
+                        visit_vec<Tag, OP>(c, ld_shared16(buf + off + 16u * v), head + (v0 + v) * E);
+                } else {
+                    record_device_error(kErrWaitExpired);
+                    abort = true;
+                }
+            }
+        }
+        if (b == nb - 1 && t < cols - tail0) visit<Tag, OP>(c, ld_scalar(row + tail0 + t), tail0 + t);
+        c = block_merge<Tag, OP>(c, smem, seed);
+        if (t == 0) {
+            const uint4 pk = pack_cand<Tag>(c);
+            unsigned remote;
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(&slots[parity][b])), "r"(0));
+            asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "r"(pk.x), "r"(pk.y),
+                         "r"(pk.z), "r"(pk.w)
+                         : "memory");
+        }
+        cluster_barrier();
+        if (b == 0 && t < 32) {
+            Cand<Tag> m = t < nb ? unpack_cand<Tag, OP>(slots[parity][t]) : seed;
+            m = group_merge<Tag, OP, 32>(m, 0xffffffffu);
+            if (t == 0) {
+                out_idx[r] = m.i;
+                if (out_val) out_val[r] = m.v;
+            }
+        }
+        const bool was_aborted = abort;
+        abort = __syncthreads_or(abort) != 0;  // also: the buffer is free for the next row
+        if (!was_aborted && !abort) {
+            // every piece of this row was waited for: its barrier moved one phase
+            phase_bits ^= (npieces >= 32 ? ~0u : ((1u << npieces) - 1u));
+            if (t == 0) pending = 0;
+        }
+    }
+    if (abort && t == 0) {
+        // Copies still in flight into this CTA's buffer: wait for them, bounded.
+        for (int p = 0; p < kBulkMaxPieces; ++p)
+            if (pending & (1u << p)) mbar_wait_bounded(bar0 + 8 * p, (phase_bits >> p) & 1u);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Per-warp streaming through shared memory with bulk copies.
+// ---------------------------------------------------------------------------
+constexpr int kMaxStreamWarps = 32;
+constexpr int kMaxStreamStages = 4;
+
+// Where piece q of a warp's row range [r0, r1) comes from.
+struct Piece {
+    int64_t row;      // first row of the piece
+    int64_t off;      // byte offset of the piece inside that row (wide rows)
+    int bytes;        // bytes in the piece
+    int nrows;        // whole rows in the piece (rows that fit a stage)
+    bool row_end;     // the piece ends its row (wide rows)
+};
+
+__device__ __forceinline__ Piece stream_piece(int64_t q, int64_t r0, int64_t r1, int64_t row_bytes, int stage_bytes,
+                                              int rows_per_piece, int pieces_per_row) {
+    Piece p;
+    if (rows_per_piece > 0) {
+        p.row = r0 + q * rows_per_piece;
+        const int64_t left = r1 - p.row;
+        p.nrows = static_cast<int>(left < rows_per_piece ? left : rows_per_piece);
+        p.off = 0;
+        p.bytes = static_cast<int>(p.nrows * row_bytes);
+        p.row_end = true;
+    } else {
+        const int64_t k = q / pieces_per_row;
+        const int64_t j = q - k * pieces_per_row;
+        p.row = r0 + k;
+        p.off = j * stage_bytes;
+        const int64_t left = row_bytes - p.off;
+        p.bytes = static_cast<int>(left < stage_bytes ? left : stage_bytes);
+        p.nrows = 1;
+        p.row_end = j == pieces_per_row - 1;
+    }
+    return p;
+}
+
+template <class Tag, int OP, int G>
+__global__ void __launch_bounds__(1024)
+stream_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int64_t* __restrict__ out_idx,
+              typename Tag::raw* __restrict__ out_val, int stages, int stage_bytes, int flags) {
+    using R = typename Tag::raw;
+    constexpr int E = 16 / sizeof(R);
+    extern __shared__ __align__(128) unsigned char stream_smem[];
+    __shared__ __align__(8) unsigned long long bars[kMaxStreamWarps * kMaxStreamStages];
+    grid_dependency_wait();
+    allow_dependents();
+
+    const int lane = threadIdx.x & 31;
+    const int w = threadIdx.x >> 5;
+    const int W = blockDim.x >> 5;
+    const int64_t nw = static_cast<int64_t>(gridDim.x) * W;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * W + w;
+    const int64_t r0 = rows * gw / nw;
+    const int64_t r1 = rows * (gw + 1) / nw;
+    const int64_t row_bytes = static_cast<int64_t>(cols) * static_cast<int64_t>(sizeof(R));
+    // Rows that fit a stage travel whole (rows_per_piece > 0); wider rows in pieces.
+    const int rows_per_piece = row_bytes <= stage_bytes ? static_cast<int>(stage_bytes / row_bytes) : 0;
+    const int pieces_per_row = rows_per_piece > 0 ? 1 : static_cast<int>((row_bytes + stage_bytes - 1) / stage_bytes);
+    const int64_t nrows = r1 - r0;
+    const int64_t total = rows_per_piece > 0 ? (nrows + rows_per_piece - 1) / rows_per_piece : nrows * pieces_per_row;
+
+    const unsigned my_smem = smem_u32(stream_smem) + static_cast<unsigned>(w * stages * stage_bytes);
+    const unsigned my_bar = smem_u32(bars) + static_cast<unsigned>(w * kMaxStreamStages * 8);
+    const unsigned char* xb = reinterpret_cast<const unsigned char*>(x);
+
+    if (lane == 0) {
+        for (int s = 0; s < stages; ++s) mbar_init(my_bar + 8 * s, 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+    // Test hook (ARGR_PLAN_TEST_EXPIRE): the first piece's barrier expects 16
+    // bytes more than are copied, so its phase never completes and the bounded
+    // wait (shortened to 2 ms) runs out. The copy itself lands.
+    const bool expire = (flags & ARGR_PLAN_TEST_EXPIRE) != 0;
+    const unsigned long long limit_ns = expire ? 2ull * 1000 * 1000 : kWaitLimitNs;
+    auto issue = [&](int64_t q) {
+        const Piece p = stream_piece(q, r0, r1, row_bytes, stage_bytes, rows_per_piece, pieces_per_row);
+        const int s = static_cast<int>(q % stages);
+        const unsigned bar = my_bar + 8 * s;
+        mbar_arrive_expect_tx(bar, static_cast<unsigned>(p.bytes) + (expire && q == 0 ? 16u : 0u));
+        bulk_copy_g2s(my_smem + static_cast<unsigned>(s * stage_bytes), xb + p.row * row_bytes + p.off,
+                      static_cast<unsigned>(p.bytes), bar);
+    };
+    if (lane == 0)
+        for (int64_t q = 0; q < total && q < stages; ++q) issue(q);
+
+    const int lg = lane & (G - 1);
+    const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
+    bool abort = false;
+    int64_t waited = 0;  // pieces whose barrier this warp has passed
+    Cand<Tag> c = make_cand<Tag, OP>(R(0), 0);
+    for (int64_t q = 0; q < total; ++q) {
+        const int s = static_cast<int>(q % stages);
+        const unsigned parity = static_cast<unsigned>((q / stages) & 1);
+        if (!abort) {
+            const bool ok = mbar_wait_bounded(my_bar + 8 * s, parity, limit_ns);
+            abort = __any_sync(0xffffffffu, !ok);
+            if (abort) {
+                if (lane == 0) record_device_error(kErrWaitExpired);
+            } else {
+                waited = q + 1;
+            }
+        }
+        if (!abort) {
+            const Piece p = stream_piece(q, r0, r1, row_bytes, stage_bytes, rows_per_piece, pieces_per_row);
+            const unsigned base = my_smem + static_cast<unsigned>(s * stage_bytes);
+            if (rows_per_piece > 0) {
+                // Whole rows: G lanes per row, 32 / G rows at a time.
+                const int nv = static_cast<int>(row_bytes >> 4);
+                for (int rr = lane / G; rr < p.nrows; rr += 32 / G) {
+                    const unsigned rbase = base + static_cast<unsigned>(rr * row_bytes);
+                    Cand<Tag> rc = make_cand<Tag, OP>(vec_elem<R>(ld_shared16(rbase), 0), 0);
+                    for (int v = lg; v < nv; v += G) visit_vec<Tag, OP>(rc, ld_shared16(rbase + 16u * v), v * E);
+                    rc = group_merge<Tag, OP, G>(rc, gmask);
+                    if (lg == 0) {
+                        out_idx[p.row + rr] = rc.i;
+                        if (out_val) out_val[p.row + rr] = rc.v;
+                    }
+                }
+            } else {
+                // A piece of a wide row: the whole warp, a running candidate.
+                const int v0 = static_cast<int>(p.off >> 4);
+                if (p.off == 0) c = make_cand<Tag, OP>(vec_elem<R>(ld_shared16(base), 0), 0);
+                const int nvp = p.bytes >> 4;
+                for (int v = lane; v < nvp; v += 32) visit_vec<Tag, OP>(c, ld_shared16(base + 16u * v), (v0 + v) * E);
+                if (p.row_end) {
+                    c = group_merge<Tag, OP, 32>(c, 0xffffffffu);
+                    if (lane == 0) {
+                        out_idx[p.row] = c.i;
+                        if (out_val) out_val[p.row] = c.v;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && !abort && q + stages < total) {
+            fence_proxy_async_smem();  // this stage's reads come before the copy that overwrites it
+            issue(q + stages);
+        }
+    }
+    if (abort && lane == 0) {
+        // Copies issued but not waited for: wait for them (bounded) before leaving.
+        const int64_t issued = total < waited + stages ? total : waited + stages;
+        for (int64_t q = waited; q < issued; ++q)
+            mbar_wait_bounded(my_bar + 8 * static_cast<int>(q % stages), static_cast<unsigned>((q / stages) & 1),
+                              limit_ns);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Launchers. Every launch goes through cudaLaunchKernelEx so that it can carry
 // the programmatic-dependent-launch attribute (plan flag ARGR_PLAN_PDL) and,
 // on the cluster path, the cluster shape.
 // ---------------------------------------------------------------------------
 template <typename... KArgs, typename... Args>
-cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, int cluster, const argr_plan& p,
-                      cudaStream_t stream, Args... args) {
+cudaError_t launch_ex_smem(void (*kern)(KArgs...), dim3 grid, dim3 block, int cluster, size_t smem,
+                           const argr_plan& p, cudaStream_t stream, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     int n = 0;
@@ -333,6 +610,11 @@ cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, int cluster
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, int cluster, const argr_plan& p,
+                      cudaStream_t stream, Args... args) {
+    return launch_ex_smem(kern, grid, block, cluster, 0, p, stream, args...);
+}
 template <class Tag, int OP, int G, int U>
 cudaError_t launch_rows_gu(const argr_plan& p, const Problem& pr) {
     using R = typename Tag::raw;
@@ -430,8 +712,59 @@ cudaError_t launch_cluster_u(const argr_plan& p, const Problem& pr) {
                      pr.cols, pr.out_idx, static_cast<R*>(pr.out_val));
 }
 
+// Dynamic shared memory the bulk cluster kernel needs: the largest share of a
+// row's 16-byte-aligned body one CTA can own.
+inline size_t cluster_bulk_smem(const argr_plan& p, int cols, int es) {
+    const int64_t nvec = static_cast<int64_t>(cols) * es / 16;
+    return static_cast<size_t>((nvec + p.cluster - 1) / p.cluster) * 16;
+}
+
+template <class Tag, int OP>
+cudaError_t launch_cluster_bulk(const argr_plan& p, const Problem& pr) {
+    using R = typename Tag::raw;
+    auto kern = cluster_bulk_kernel<Tag, OP>;
+    const size_t smem = cluster_bulk_smem(p, pr.cols, sizeof(R));
+    static thread_local size_t smem_set = 0;
+    if (smem > 48 * 1024 && smem > smem_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        smem_set = smem;
+    }
+    if (p.cluster > 8) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    const dim3 grid(static_cast<unsigned>(p.cluster), static_cast<unsigned>(p.grid_rows));
+    static thread_local int checked_block = 0, checked_cluster = 0, checked_ok = 0;
+    static thread_local size_t checked_smem = 0;
+    if (checked_block != p.block || checked_cluster != p.cluster || checked_smem != smem) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(p.block);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = static_cast<unsigned>(p.cluster);
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        checked_block = p.block;
+        checked_cluster = p.cluster;
+        checked_smem = smem;
+        checked_ok = n > 0;
+    }
+    if (!checked_ok) return cudaErrorInvalidClusterSize;  // reported as ARGR_EUNSUPPORTED
+    return launch_ex_smem(kern, grid, dim3(p.block), p.cluster, smem, p, pr.stream, static_cast<const R*>(pr.x),
+                          pr.rows, pr.cols, pr.out_idx, static_cast<R*>(pr.out_val));
+}
+
 template <class Tag, int OP>
 cudaError_t launch_cluster_op(const argr_plan& p, const Problem& pr) {
+    if (p.flags & ARGR_PLAN_BULK) return launch_cluster_bulk<Tag, OP>(p, pr);
     switch (p.unroll) {
         case 1: return launch_cluster_u<Tag, OP, 1>(p, pr);
         case 2: return launch_cluster_u<Tag, OP, 2>(p, pr);
@@ -446,6 +779,53 @@ cudaError_t launch_cluster_t(const argr_plan& p, const Problem& pr) {
     return pr.op == kOpMax ? launch_cluster_op<Tag, kOpMax>(p, pr) : launch_cluster_op<Tag, kOpMin>(p, pr);
 }
 
+template <class Tag, int OP, int G>
+cudaError_t launch_stream_g(const argr_plan& p, const Problem& pr) {
+    using R = typename Tag::raw;
+    auto kern = stream_kernel<Tag, OP, G>;
+    const size_t smem = static_cast<size_t>(p.block / 32) * p.stages * p.stage_bytes;
+    static thread_local size_t smem_set = 0;
+    if (smem > 48 * 1024 && smem > smem_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        smem_set = smem;
+    }
+    return launch_ex_smem(kern, dim3(static_cast<unsigned>(p.grid_rows)), dim3(p.block), 1, smem, p, pr.stream,
+                          static_cast<const R*>(pr.x), pr.rows, pr.cols, pr.out_idx, static_cast<R*>(pr.out_val),
+                          p.stages, p.stage_bytes, p.flags);
+}
+
+template <class Tag, int OP>
+cudaError_t launch_stream_op(const argr_plan& p, const Problem& pr) {
+    switch (p.group) {
+        case 1: return launch_stream_g<Tag, OP, 1>(p, pr);
+        case 2: return launch_stream_g<Tag, OP, 2>(p, pr);
+        case 4: return launch_stream_g<Tag, OP, 4>(p, pr);
+        case 8: return launch_stream_g<Tag, OP, 8>(p, pr);
+        case 16: return launch_stream_g<Tag, OP, 16>(p, pr);
+        case 32: return launch_stream_g<Tag, OP, 32>(p, pr);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <class Tag>
+cudaError_t launch_stream_t(const argr_plan& p, const Problem& pr) {
+    return pr.op == kOpMax ? launch_stream_op<Tag, kOpMax>(p, pr) : launch_stream_op<Tag, kOpMin>(p, pr);
+}
+
+// The device error word of this translation unit: read it, then clear it.
+static inline cudaError_t read_and_clear_error_t(unsigned* out) {
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v));
+    if (e != cudaSuccess) return e;
+    *out = v;
+    if (v) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
+    }
+    return e;
+}
+
 }  // namespace argr
 
 #define ARGR_DEFINE_LAUNCHERS(sfx, Tag)                                                                       \
@@ -457,4 +837,8 @@ cudaError_t launch_cluster_t(const argr_plan& p, const Problem& pr) {
     cudaError_t launch_cluster_##sfx(const argr_plan& p, const Problem& pr) {                                \
         return launch_cluster_t<Tag>(p, pr);                                                                  \
     }                                                                                                         \
+    cudaError_t launch_stream_##sfx(const argr_plan& p, const Problem& pr) {                                 \
+        return launch_stream_t<Tag>(p, pr);                                                                   \
+    }                                                                                                         \
+    cudaError_t read_and_clear_error_##sfx(unsigned* out) { return read_and_clear_error_t(out); }           \
     }

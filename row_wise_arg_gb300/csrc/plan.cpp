@@ -39,6 +39,7 @@ constexpr int64_t kRowsWaves = 8;          // rows path: grid of at most this ma
 constexpr int64_t kMaxGridY = 65535;       // hardware limit of gridDim.y
 constexpr int64_t kMaxBlocksPerRow = 65535;
 constexpr int64_t kClusterMaxCtaBytes = 128 * 1024;  // largest share of a row per cluster CTA
+constexpr int64_t kMaxDynamicSmem = 227 * 1024;        // dynamic shared memory one CTA may use
 
 int64_t ceil_div(int64_t a, int64_t b) { return a / b + (a % b != 0); }
 
@@ -177,7 +178,9 @@ argr_status check_plan(const argr_plan& p, int64_t rows, int64_t cols, int dtype
     if (!valid_dtype(dtype) || rows < 0 || cols < 1 || cols > INT_MAX) return ARGR_EINVAL;
     if (rows == 0) return ARGR_OK;
     if (p.block < 32 || p.block > 1024 || p.block % 32 != 0) return ARGR_EINVAL;
-    if (p.flags & ~ARGR_PLAN_PDL) return ARGR_EINVAL;
+    if (p.flags & ~(ARGR_PLAN_PDL | ARGR_PLAN_BULK | ARGR_PLAN_TEST_EXPIRE)) return ARGR_EINVAL;
+    if ((p.flags & ARGR_PLAN_BULK) && p.path != ARGR_PATH_CLUSTER) return ARGR_EINVAL;
+    if ((p.flags & ARGR_PLAN_TEST_EXPIRE) && p.path != ARGR_PATH_STREAM) return ARGR_EINVAL;
     switch (p.path) {
         case ARGR_PATH_ROWS: {
             const int g = p.group;
@@ -197,11 +200,29 @@ argr_status check_plan(const argr_plan& p, int64_t rows, int64_t cols, int dtype
             if (p.blocks_per_row > 1 && (p.grid_rows < rows || p.grid_rows > kMaxSplitRows)) return ARGR_EINVAL;
             return ARGR_OK;
         }
+        case ARGR_PATH_STREAM: {
+            const int g = p.group;
+            if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16 && g != 32) return ARGR_EINVAL;
+            if (!row_aligned) return ARGR_EINVAL;  // bulk copies need 16-byte aligned rows
+            if (p.stages < 1 || p.stages > 4) return ARGR_EINVAL;
+            if (p.stage_bytes < 1024 || p.stage_bytes > 65536 || p.stage_bytes % 16 != 0) return ARGR_EINVAL;
+            if (p.block > 1024) return ARGR_EINVAL;
+            if (static_cast<int64_t>(p.block / 32) * p.stages * p.stage_bytes > kMaxDynamicSmem) return ARGR_EINVAL;
+            const int64_t row_bytes = cols * elem_size(dtype);
+            if (row_bytes > p.stage_bytes && g != 32) return ARGR_EINVAL;  // pieces of a row need the whole warp
+            if (p.grid_rows < 1 || p.grid_rows > INT_MAX) return ARGR_EINVAL;
+            return ARGR_OK;
+        }
         case ARGR_PATH_CLUSTER: {
             if (p.unroll != 1 && p.unroll != 2 && p.unroll != 4 && p.unroll != 8) return ARGR_EINVAL;
             if (p.cluster < 2 || p.cluster > 16 || p.blocks_per_row != p.cluster) return ARGR_EINVAL;
             if (p.grid_rows < 1 || p.grid_rows > kMaxGridY) return ARGR_EINVAL;
             if (caps.max_cluster < p.cluster) return ARGR_EUNSUPPORTED;
+            if (p.flags & ARGR_PLAN_BULK) {
+                // one CTA's share of the aligned body must fit the bulk buffer
+                const int64_t nvec = cols * elem_size(dtype) / 16;
+                if ((nvec + p.cluster - 1) / p.cluster * 16 > kClusterMaxCtaBytes) return ARGR_EINVAL;
+            }
             return ARGR_OK;
         }
         default: return ARGR_EINVAL;

@@ -85,8 +85,20 @@ def forced_plan(path: str, **kw):
         p.path = _lib.ARGR_PATH_SPLIT
         p.blocks_per_row = kw["bpr"]
         p.grid_rows = kw["grid_rows"]
+    elif path == "stream":
+        p.path = _lib.ARGR_PATH_STREAM
+        p.group = kw["group"]
+        p.stages = kw.get("stages", 2)
+        p.stage_bytes = kw.get("stage_bytes", 8192)
+        p.grid_rows = kw.get("grid", 8)
+        p.blocks_per_row = 1
+        p.vec = 1
+        if kw.get("expire"):
+            p.flags |= _lib.ARGR_PLAN_TEST_EXPIRE
     elif path == "cluster":
         p.path = _lib.ARGR_PATH_CLUSTER
+        if kw.get("bulk"):
+            p.flags |= _lib.ARGR_PLAN_BULK
         p.cluster = kw["cluster"]
         p.blocks_per_row = kw["cluster"]
         p.grid_rows = kw["grid_rows"]

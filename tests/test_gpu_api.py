@@ -27,6 +27,41 @@ def built():
     build()
 
 
+def test_bounded_wait_expires_and_is_reported():
+    """A bulk copy whose barrier never completes (test flag): the kernel's
+    bounded wait runs out, the kernel returns, the host reads ARGR_ETIMEOUT,
+    and the next call is unaffected."""
+    x = torch.randn(64, 4096, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert A.argreduce_read_error(0, s) == _lib.ARGR_OK
+    plan = forced_plan("stream", group=32, stages=2, stage_bytes=16384, block=128, grid=4, expire=True)
+    A.argreduce_with_plan(plan, x, "max")
+    assert A.argreduce_read_error(0, s) == _lib.ARGR_ETIMEOUT
+    assert A.argreduce_read_error(0, s) == _lib.ARGR_OK  # cleared
+    idx, _ = A.argreduce_with_plan(forced_plan("stream", group=32, stages=2, stage_bytes=16384, block=128, grid=4),
+                                   x, "max")
+    torch.cuda.synchronize()
+    assert (idx.cpu().numpy() == oracle.argreduce(x.cpu().numpy(), "f32", "max")[0]).all()
+    assert A.argreduce_read_error(0, s) == _lib.ARGR_OK
+
+
+def test_stream_plan_validation():
+    x = torch.randn(4, 1001, device="cuda")  # rows not 16-byte aligned
+    with pytest.raises(A.ArgreduceError):
+        A.argreduce_with_plan(forced_plan("stream", group=32), x, "max")
+    y = torch.randn(4, 8192, device="cuda")
+    for bad in (dict(group=4, stage_bytes=8192),        # a row wider than a stage needs the whole warp
+                dict(group=32, stages=5),
+                dict(group=32, stage_bytes=1000),
+                dict(group=32, stage_bytes=65536, stages=4, block=512)):  # too much shared memory
+        with pytest.raises(A.ArgreduceError):
+            A.argreduce_with_plan(forced_plan("stream", **bad), y, "max")
+    split = forced_plan("split", bpr=1, grid_rows=4)
+    split.flags |= _lib.ARGR_PLAN_TEST_EXPIRE
+    with pytest.raises(A.ArgreduceError):  # the test flag only exists on the stream path
+        A.argreduce_with_plan(split, y, "max")
+
+
 def test_rows_zero_and_one_col():
     x = torch.empty((0, 17), dtype=torch.float32, device="cuda")
     idx, _ = A.argreduce(x, "max")

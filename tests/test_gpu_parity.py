@@ -113,6 +113,32 @@ def test_cluster_path(dtype, cluster):
             check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=2, unroll=1, pdl=False),
                   offset=1)
             check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=rows, block=512, unroll=8))
+            if cols * W.ELEM_SIZE[dtype] // 16 <= cluster * 8192:  # share fits the 128 KiB bulk buffer
+                check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=rows, bulk=True))
+                check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=2, bulk=True, block=128),
+                      offset=1)
+
+
+@pytest.mark.parametrize("dtype", W.DTYPES)
+@pytest.mark.parametrize("group", [1, 4, 32])
+def test_stream_path(dtype, group):
+    """Per-warp bulk-copy streaming: rows that fit a stage (whole rows, G
+    lanes per row) and rows cut into pieces (whole warp); warps with many rows,
+    one row and none."""
+    es = W.ELEM_SIZE[dtype]
+    for cols in [16 // es, 32 // es, 64, 256, 1000 - 1000 % (16 // es), 2048, 4096, 20008, 100000]:
+        for rows in (1, 7, 300):
+            if rows * cols > 3_000_000:
+                continue
+            x = W.fuzz_rows(dtype, rows, cols, seed=rows * 7 + cols + group)
+            row_bytes = cols * es
+            for stages, stage_bytes, block, grid in ((2, 8192, 256, 3), (4, 4096, 128, 40), (1, 1024, 1024, 1),
+                                                     (3, 65536, 32, 2)):
+                if row_bytes > stage_bytes and group != 32:
+                    continue
+                for op in W.OPS:
+                    check(x, dtype, op, plan=forced_plan("stream", group=group, stages=stages,
+                                                         stage_bytes=stage_bytes, block=block, grid=grid))
 
 
 @pytest.mark.parametrize("dtype", W.DTYPES)
@@ -124,6 +150,8 @@ def test_exhaustive_alphabet_rows(dtype):
         check(x, dtype, op)
         check(x, dtype, op, plan=forced_plan("rows", group=4, vec=0, grid=100))
         check(x, dtype, op, plan=forced_plan("split", bpr=1, grid_rows=min(rows, 1000), block=32))
+        if W.ELEM_SIZE[dtype] * 4 % 16 == 0:
+            check(x, dtype, op, plan=forced_plan("stream", group=1, stages=2, stage_bytes=4096, grid=50))
         for r0 in range(0, rows, 2048):  # a multi-CTA split has at most 2048 row slots
             xs = np.ascontiguousarray(x[r0:r0 + 2048])
             check(xs, dtype, op, plan=forced_plan("split", bpr=3, grid_rows=xs.shape[0], block=32))

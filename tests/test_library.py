@@ -261,3 +261,38 @@ def test_rows_partition_exact():
                         assert pos == sorted(pos)
                         seen.extend(pos)
                     assert sorted(seen) == list(range(cols))
+
+
+def sim_stream_pieces(rows, row_bytes, stage_bytes, n_warps):
+    """Byte ranges the stream kernel's warps copy (same arithmetic as
+    stream_piece()): every 16-byte unit of the matrix exactly once, every copy
+    16-byte aligned, a multiple of 16 bytes, at most one stage, in bounds."""
+    covered = bytearray(rows * row_bytes // 16)
+    for gw in range(n_warps):
+        r0, r1 = rows * gw // n_warps, rows * (gw + 1) // n_warps
+        rpp = stage_bytes // row_bytes if row_bytes <= stage_bytes else 0
+        ppr = 1 if rpp else -(-row_bytes // stage_bytes)
+        total = -(-(r1 - r0) // rpp) if rpp else (r1 - r0) * ppr
+        for q in range(total):
+            if rpp:
+                row = r0 + q * rpp
+                off, nbytes = 0, min(rpp, r1 - row) * row_bytes
+            else:
+                row, j = r0 + q // ppr, q % ppr
+                off = j * stage_bytes
+                nbytes = min(stage_bytes, row_bytes - off)
+            start = row * row_bytes + off
+            assert 0 < nbytes <= stage_bytes and nbytes % 16 == 0 and start % 16 == 0
+            assert start + nbytes <= rows * row_bytes
+            for u in range(start // 16, (start + nbytes) // 16):
+                assert covered[u] == 0
+                covered[u] = 1
+    assert all(covered)
+
+
+def test_stream_piece_mapping():
+    for rows in (1, 2, 7, 33, 300):
+        for row_bytes in (16, 32, 64, 256, 1008, 4000, 8192, 16384, 80000):
+            for stage_bytes in (1024, 4096, 8192):
+                for n_warps in (1, 3, 40, 64):
+                    sim_stream_pieces(rows, row_bytes, stage_bytes, n_warps)
