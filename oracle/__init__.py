@@ -6,7 +6,9 @@ the two share no code.
 
 The arithmetic lives in ``argreduce_oracle.c``: a plain sequential scan per
 row that seeds the candidate with element 0 and replaces it only on a strictly
-better value (onnxruntime PRs #32092 "Semantics" and #31694 "Semantics").
+better value (onnxruntime PRs #32092 "Semantics" and #31694 "Semantics"); the
+"max_last" / "min_last" ops replace it on a value that is not worse, which
+makes ties go to the last index (ONNX select_last_index = 1).
 This module compiles that file with the host C compiler and calls it through
 ctypes.
 """
@@ -25,7 +27,7 @@ _SRC = os.path.join(_HERE, "argreduce_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
 DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2, "f64": 3}
-OP_CODE = {"max": 0, "min": 1}
+OP_CODE = {"max": 0, "min": 1, "max_last": 2, "min_last": 3}
 RAW_NP = {"f32": np.float32, "f16": np.uint16, "bf16": np.uint16, "f64": np.float64}
 
 _lock = threading.Lock()

@@ -23,6 +23,13 @@
  * comparison that is false when either side is NaN) then best = (x[j], j).
  * The output is the int64 index and, optionally, the raw bits of x[r, index].
  *
+ * Last-index variants (ONNX ArgMax/ArgMin attribute select_last_index = 1,
+ * which #32092's Semantics section notes the CUDA provider sends to the CPU):
+ * the same scan with a non-strict test, x[j] >= best (ArgMax) or x[j] <= best
+ * (ArgMin), so among equal values the last one wins. The test is still false
+ * when either side is NaN, so NaN handling is unchanged: a leading NaN keeps
+ * index 0 and a later NaN is never chosen.
+ *
  * Precision: every element is decoded exactly to binary64 and compared there.
  * Decoding binary16, bfloat16 and binary32 into binary64 is exact (including
  * subnormals, signed zeros and infinities), so each comparison decides the
@@ -34,7 +41,7 @@
 #include <string.h>
 
 enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2, ORACLE_F64 = 3 };
-enum { ORACLE_MAX = 0, ORACLE_MIN = 1 };
+enum { ORACLE_MAX = 0, ORACLE_MIN = 1, ORACLE_MAX_LAST = 2, ORACLE_MIN_LAST = 3 };
 
 /* IEEE 754 binary16: sign (1 bit), exponent (5 bits, bias 15), fraction
  * (10 bits). exponent 0 -> subnormal fraction * 2^-24; exponent 31 -> inf
@@ -105,11 +112,19 @@ static double decode(const unsigned char* p, int dtype) {
     }
 }
 
-/* "Strictly better": greater for ArgMax, less for ArgMin; false if either
- * operand is NaN (a C relational operator on a NaN is false). */
+/* "Strictly better": greater for ArgMax, less for ArgMin; "not worse" for
+ * the last-index variants: greater or equal / less or equal. Every test is
+ * false if either operand is NaN (a C relational operator on a NaN is false). */
 static int better(double a, double b, int op) {
-    return op == ORACLE_MAX ? (a > b) : (a < b);
+    switch (op) {
+        case ORACLE_MAX: return a > b;
+        case ORACLE_MIN: return a < b;
+        case ORACLE_MAX_LAST: return a >= b;
+        default: return a <= b;
+    }
 }
+
+static int valid_op(int op) { return op >= ORACLE_MAX && op <= ORACLE_MIN_LAST; }
 
 static void scan_rows(const unsigned char* x, int dtype, int64_t row_begin, int64_t row_end,
                       int64_t cols, int op, int64_t* out_idx, unsigned char* out_val) {
@@ -133,7 +148,7 @@ static void scan_rows(const unsigned char* x, int dtype, int64_t row_begin, int6
 /* Returns 0 on success, -1 on invalid arguments. out_val may be NULL. */
 int oracle_argreduce(const void* x, int dtype, int64_t rows, int64_t cols, int op,
                      int64_t* out_idx, void* out_val) {
-    if (elem_size(dtype) == 0 || (op != ORACLE_MAX && op != ORACLE_MIN)) return -1;
+    if (elem_size(dtype) == 0 || !valid_op(op)) return -1;
     if (rows < 0 || cols < 1 || (rows > 0 && (!x || !out_idx))) return -1;
     scan_rows((const unsigned char*)x, dtype, 0, rows, cols, op, out_idx, (unsigned char*)out_val);
     return 0;
@@ -158,7 +173,7 @@ static void* run_job(void* arg) {
 
 int oracle_argreduce_mt(const void* x, int dtype, int64_t rows, int64_t cols, int op,
                         int64_t* out_idx, void* out_val, int nthreads) {
-    if (elem_size(dtype) == 0 || (op != ORACLE_MAX && op != ORACLE_MIN)) return -1;
+    if (elem_size(dtype) == 0 || !valid_op(op)) return -1;
     if (rows < 0 || cols < 1 || (rows > 0 && (!x || !out_idx))) return -1;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;

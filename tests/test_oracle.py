@@ -48,19 +48,23 @@ def np_decode(x: np.ndarray, dtype: str) -> np.ndarray:
 
 def closed_form(x: np.ndarray, dtype: str, op: str) -> np.ndarray:
     """Second formulation of the result: 0 when element 0 is NaN, otherwise the
-    smallest j whose value is not NaN and equals the max (min) over the
-    non-NaN values of the row."""
+    smallest j (largest j for the last-index ops) whose value is not NaN and
+    equals the max (min) over the non-NaN values of the row."""
     v = np_decode(x, dtype)
     rows, cols = v.shape
     out = np.zeros(rows, dtype=np.int64)
     nan = np.isnan(v)
     lead_nan = nan[:, 0]
-    fill = -np.inf if op == "max" else np.inf
+    is_max = op.startswith("max")
+    fill = -np.inf if is_max else np.inf
     w = np.where(nan, fill, v)
-    m = w.max(axis=1) if op == "max" else w.min(axis=1)
+    m = w.max(axis=1) if is_max else w.min(axis=1)
     hit = (~nan) & (v == m[:, None])
-    first = np.argmax(hit, axis=1)
-    out[:] = np.where(lead_nan, 0, first)
+    if op.endswith("_last"):
+        pick = cols - 1 - np.argmax(hit[:, ::-1], axis=1)
+    else:
+        pick = np.argmax(hit, axis=1)
+    out[:] = np.where(lead_nan, 0, pick)
     return out
 
 
@@ -95,7 +99,7 @@ def test_decoder_exhaustive(dtype):
 # Exhaustive brute force over the special-value alphabet.
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("dtype", W.DTYPES)
-@pytest.mark.parametrize("op", W.OPS)
+@pytest.mark.parametrize("op", W.ALL_OPS)
 def test_exhaustive_alphabet(dtype, op):
     for length in range(1, 6):
         x = W.exhaustive_rows(dtype, length)
@@ -112,19 +116,21 @@ def test_brute_force_python_loop():
     for dtype in W.DTYPES:
         x = W.fuzz_rows(dtype, 400, 9, seed=77, p_special=0.4)
         v = np_decode(x, dtype)
-        for op in W.OPS:
+        for op in W.ALL_OPS:
             idx, _, _ = oracle.argreduce(x, dtype, op)
+            is_max = op.startswith("max")
+            order = range(x.shape[1] - 1, -1, -1) if op.endswith("_last") else range(x.shape[1])
             for r in range(x.shape[0]):
                 row = v[r]
                 if np.isnan(row[0]):
                     exp = 0
                 else:
                     exp = None
-                    for j in range(len(row)):
+                    for j in order:
                         if np.isnan(row[j]):
                             continue
                         beats_all = all(
-                            np.isnan(row[k]) or (row[j] >= row[k] if op == "max" else row[j] <= row[k])
+                            np.isnan(row[k]) or (row[j] >= row[k] if is_max else row[j] <= row[k])
                             for k in range(len(row)))
                         if beats_all:
                             exp = j
@@ -147,6 +153,14 @@ def test_numpy_nan_free(dtype):
             idx, val, _ = oracle.argreduce(x, dtype, op)
             exp = np.argmax(v, axis=1) if op == "max" else np.argmin(v, axis=1)
             assert (idx == exp).all()
+            assert raw_equal(val, take_rows(x, idx))
+        # last occurrence: numpy's first occurrence on the reversed row
+        cols = v.shape[1]
+        for op in W.LAST_OPS:
+            idx, val, _ = oracle.argreduce(x, dtype, op)
+            rv = v[:, ::-1]
+            first_rev = np.argmax(rv, axis=1) if op == "max_last" else np.argmin(rv, axis=1)
+            assert (idx == cols - 1 - first_rev).all()
             assert raw_equal(val, take_rows(x, idx))
 
 
@@ -256,6 +270,19 @@ def test_golden_semantics(dtype):
 
 
 @pytest.mark.parametrize("dtype", W.DTYPES)
+def test_golden_semantics_last_index(dtype):
+    with open(os.path.join(GOLDEN, "onnx_select_last_index.json")) as f:
+        fx = json.load(f)
+    raw_t = oracle.RAW_NP[dtype]
+    for case in fx["cases"]:
+        x = np.array([[_token(t, dtype) for t in case["row"]]], dtype=raw_t)
+        for op in W.LAST_OPS:
+            idx, val, _ = oracle.argreduce(x, dtype, op)
+            assert idx[0] == case[op], (case["what"], op)
+            assert raw_equal(val, x[0, idx])
+
+
+@pytest.mark.parametrize("dtype", W.DTYPES)
 def test_golden_long_axis(dtype):
     with open(os.path.join(GOLDEN, "onnxruntime_31694_long_axis_300x4.json")) as f:
         fx = json.load(f)
@@ -279,12 +306,10 @@ def test_golden_first_index_65536():
 # Mutation check: each planted mistake must fail a pin.
 # ---------------------------------------------------------------------------
 MUTANTS = [
-    ("last-index ties", "return op == ORACLE_MAX ? (a > b) : (a < b);",
-     "return op == ORACLE_MAX ? (a >= b) : (a <= b);"),
-    ("ops swapped", "return op == ORACLE_MAX ? (a > b) : (a < b);",
-     "return op == ORACLE_MIN ? (a > b) : (a < b);"),
-    ("NaN wins", "return op == ORACLE_MAX ? (a > b) : (a < b);",
-     "return op == ORACLE_MAX ? !(a <= b) : !(a >= b);"),
+    ("first-index ties become last", "case ORACLE_MAX: return a > b;", "case ORACLE_MAX: return a >= b;"),
+    ("min ties become last", "case ORACLE_MIN: return a < b;", "case ORACLE_MIN: return a <= b;"),
+    ("ops swapped", "case ORACLE_MAX: return a > b;", "case ORACLE_MAX: return a < b;"),
+    ("NaN wins", "case ORACLE_MAX: return a > b;", "case ORACLE_MAX: return !(a <= b);"),
     ("element 1 skipped", "for (int64_t j = 1; j < cols; ++j)", "for (int64_t j = 2; j < cols; ++j)"),
     ("last element skipped", "for (int64_t j = 1; j < cols; ++j)", "for (int64_t j = 1; j + 1 < cols; ++j)"),
     ("value from wrong index", "row + (size_t)best_j * es, es);", "row, es);"),
@@ -293,6 +318,8 @@ MUTANTS = [
     ("bf16 fraction width", "ldexp((double)(128 + f), e - 134)", "ldexp((double)(256 + f), e - 135)"),
     ("bf16 sign dropped", "    return sign ? -v : v;\n}\n\nstatic size_t", "    return v;\n}\n\nstatic size_t"),
     ("row stride", "(size_t)r * (size_t)cols * es", "(size_t)r * (size_t)cols"),
+    ("last-index ties dropped", "case ORACLE_MAX_LAST: return a >= b;", "case ORACLE_MAX_LAST: return a > b;"),
+    ("last-index lets NaN in", "default: return a <= b;", "default: return !(a > b);"),
 ]
 
 
@@ -315,10 +342,11 @@ def _pin_suite_passes(lib_path: str) -> bool:
             for dtype in ("f16", "bf16"):
                 test_decoder_exhaustive(dtype)
             for dtype in W.DTYPES:
-                for op in W.OPS:
+                for op in W.ALL_OPS:
                     test_exhaustive_alphabet(dtype, op)
                 test_numpy_nan_free(dtype)
                 test_golden_semantics(dtype)
+                test_golden_semantics_last_index(dtype)
                 test_golden_long_axis(dtype)
         except AssertionError:
             return False

@@ -31,6 +31,9 @@ import numpy as np
 
 DTYPES = ("f32", "f16", "bf16", "f64")
 OPS = ("max", "min")
+# Last-index variants (ties resolve to the highest index; ONNX select_last_index = 1).
+LAST_OPS = ("max_last", "min_last")
+ALL_OPS = OPS + LAST_OPS
 
 ELEM_SIZE = {"f32": 4, "f16": 2, "bf16": 2, "f64": 8}
 
@@ -201,7 +204,7 @@ def make_planted(c: Case) -> np.ndarray:
     """
     vals = _gauss(c.rows, c.cols, 3.0, c.seed)
     rng = np.random.Generator(np.random.PCG64(c.seed + 7919))
-    extreme = np.float32(64.0 if c.op == "max" else -64.0)
+    extreme = np.float32(64.0 if c.op.startswith("max") else -64.0)
     for r in range(c.rows):
         p1 = int(rng.integers(0, c.cols))
         vals[r, p1] = extreme
@@ -260,7 +263,7 @@ def make_uniform_special(c: Case) -> np.ndarray:
     rr = rows_of(7)
     if len(rr):
         sub = np.abs(vals[rr]) + wide(0.25)  # strictly positive, away from zero
-        vals[rr] = -sub if c.op == "max" else sub
+        vals[rr] = -sub if c.op.startswith("max") else sub
         if cols >= 2:
             p = pos[rr, 0] % (cols - 1)
             q = p + 1 + (pos[rr, 1] % (cols - 1 - p)) if cols > 2 else p + 1
