@@ -21,6 +21,7 @@ One JSON line on stdout (rank 0).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -48,9 +49,17 @@ WORKLOADS = {
     "batches": (3, "ArgMax fp16/bf16/fp32 [8,202048]+[32,202048]"),
     "uniform_special": (4, "ArgMin/ArgMax fp32/f64 [4096,4096]+[65536,1024] with special rows"),
     "narrow": (5, "ArgMax fp32 [65536,64]+[4096,8]+[4096,128]"),
+    "wide_rows_last": (-2, "the wide_rows cases with ties to the last index (ONNX select_last_index = 1)"),
 }
 DTYPE_LABEL = {"f32": "f32", "f16": "f16", "bf16": "bf16", "f64": "f64"}
 KERNEL_OF_PATH = {"rows": "rows_kernel", "split": "split_kernel", "cluster": "cluster_kernel", "none": "none"}
+
+
+def workload_cases(group: int):
+    """Cases of a workload group; a negative group is the last-index variant."""
+    if group > 0:
+        return W.config_cases(group)
+    return [dataclasses.replace(c, op=c.op + "_last", name=c.name + "_last") for c in W.config_cases(-group)]
 
 
 def algo_bytes(c: W.Case, with_values: bool = False) -> int:
@@ -342,15 +351,15 @@ def reference_arm(args, rank, world, dist):
     if rank != 0:
         return 0
     group, desc = WORKLOADS[args.workload]
-    cases = W.config_cases(group)
+    cases = workload_cases(group)
     inputs = [W.make(c) for c in cases]
     oracle_time(cases, inputs, 0.0, max_calls=min(len(cases), max(1, args.warmup)))
     us, calls, cores, el = oracle_time(cases, inputs, 0.0, max_calls=max(1, args.steps))
     line = {
         "impl": "reference", "metric": METRIC, "value": us, "unit": "us/call", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": us * len(cases) / 1e3,
-        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32+bf16"
-        if group == 2 else "mixed", "data": "synthetic",
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "+".join(sorted({c.dtype for c in cases})), "data": "synthetic",
         "config": {"workload": args.workload, "description": desc, "cases": len(cases),
                    "step": "one oracle call per step, cycling through the cases (bounded sample)"},
         "cpu_baseline": {"value": us, "unit": "us/call", "cores": cores, "kind": "oracle",
@@ -395,7 +404,7 @@ def main():
     torch.cuda.set_device(local)
     stream = torch.cuda.Stream()
     group, desc = WORKLOADS[args.workload]
-    cases = W.config_cases(group)
+    cases = workload_cases(group)
     inputs = [W.make(c) for c in cases]
     step_bytes = sum(algo_bytes(c) for c in cases)
     peak, peak_src = load_peak()
@@ -449,18 +458,22 @@ def main():
     if not args.no_configs and (world == 1 or rank == 0):
         table = []
         for name, (g, _) in sorted(WORKLOADS.items(), key=lambda kv: kv[1][0]):
+            if g < 0:
+                continue
             gcases = W.config_cases(g)
             ginputs = [W.make(c) for c in gcases]
-            for c, x in zip(gcases, ginputs):
-                if c.variant == "dup":
+            for c0, x in zip(gcases, ginputs):
+                if c0.variant == "dup":
                     continue
-                n = max(20, min(4000, int(2e9 / max(c.nbytes, 1) / 50)))
-                s, n, cp, _ = time_group(torch, A, [c], [x], n, 5, stream, exact=False)
-                us = s * 1e6 / n
-                gbs = algo_bytes(c) / (s / n) / 1e9
-                table.append({"case": c.name, "us_per_call": round(us, 3), "gbs": round(gbs, 1),
-                              "frac": round(gbs / peak, 4),
-                              "path": A.argreduce_plan(c.rows, c.cols, c.dtype, c.op).as_dict()["path_name"]})
+                # each case as written, and the same rows with ties to the last index
+                for c in (c0, dataclasses.replace(c0, op=c0.op + "_last", name=c0.name + "_last")):
+                    n = max(20, min(4000, int(2e9 / max(c.nbytes, 1) / 50)))
+                    s, n, cp, _ = time_group(torch, A, [c], [x], n, 5, stream, exact=False)
+                    us = s * 1e6 / n
+                    gbs = algo_bytes(c) / (s / n) / 1e9
+                    table.append({"case": c.name, "us_per_call": round(us, 3), "gbs": round(gbs, 1),
+                                  "frac": round(gbs / peak, 4),
+                                  "path": A.argreduce_plan(c.rows, c.cols, c.dtype, c.op).as_dict()["path_name"]})
             del ginputs
         result["configs"] = table
 

@@ -45,7 +45,10 @@ typedef enum {
     ARGR_F64 = 3   /* IEEE binary64 */
 } argr_dtype;
 
-typedef enum { ARGR_MAX = 0, ARGR_MIN = 1 } argr_op;
+/* ArgMax / ArgMin; ties resolve to the first index, or to the last index for
+ * the *_LAST ops (ONNX select_last_index = 1: the same scan with a non-strict
+ * comparison, still false on NaN, so NaN handling is unchanged). */
+typedef enum { ARGR_MAX = 0, ARGR_MIN = 1, ARGR_MAX_LAST = 2, ARGR_MIN_LAST = 3 } argr_op;
 
 typedef enum {
     ARGR_OK = 0,

@@ -51,7 +51,7 @@ argr_status current_caps(argr_caps* out) {
 }
 
 bool valid_dtype(int d) { return d == ARGR_F32 || d == ARGR_F16 || d == ARGR_BF16 || d == ARGR_F64; }
-bool valid_op(int o) { return o == ARGR_MAX || o == ARGR_MIN; }
+bool valid_op(int o) { return o == ARGR_MAX || o == ARGR_MIN || o == ARGR_MAX_LAST || o == ARGR_MIN_LAST; }
 
 // Checks shared by argreduce() and argreduce_with_plan().
 argr_status check_args(const void* x, int dtype, int64_t rows, int64_t cols, int op, const int64_t* out_idx,

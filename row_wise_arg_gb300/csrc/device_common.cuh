@@ -14,6 +14,9 @@
 //    is (x[0], 0) and so is the merge. Otherwise no candidate holds a NaN,
 //    and the merge is the maximum of a total order (value, then lower index),
 //    so any merge tree gives the sequential result.
+//  * the last-occurrence ops use the non-strict test ("not worse", still
+//    false on NaN) and merge equal values toward the higher index; the same
+//    argument applies with the index order reversed.
 // Comparisons go through per-type keys (below) that decide exactly as the
 // IEEE comparison of the element type.
 #pragma once
@@ -24,8 +27,14 @@
 
 namespace argr {
 
+// Ops: ArgMax and ArgMin, first occurrence (0, 1) and last occurrence (2, 3:
+// ONNX select_last_index = 1). Bit 0 selects min, bit 1 selects last.
 constexpr int kOpMax = 0;
 constexpr int kOpMin = 1;
+constexpr int kOpMaxLast = 2;
+constexpr int kOpMinLast = 3;
+template <int OP> constexpr bool kIsMin = (OP & 1) != 0;
+template <int OP> constexpr bool kIsLast = (OP & 2) != 0;
 
 // ---------------------------------------------------------------------------
 // Element tags: raw storage type and a comparison key.
@@ -49,7 +58,7 @@ struct TagF32 {
     template <int OP> static __device__ __forceinline__ float elem_key(float v) { return v; }
     template <int OP> static __device__ __forceinline__ float seed_key(float v) { return v; }
     template <int OP> static __device__ __forceinline__ bool better(float a, float b) {
-        if constexpr (OP == kOpMax) return a > b; else return a < b;
+        if constexpr (kIsMin<OP>) return a < b; else return a > b;
     }
 };
 struct TagF16 {
@@ -59,7 +68,7 @@ struct TagF16 {
     template <int OP> static __device__ __forceinline__ float elem_key(uint16_t v) { return widen(v); }
     template <int OP> static __device__ __forceinline__ float seed_key(uint16_t v) { return widen(v); }
     template <int OP> static __device__ __forceinline__ bool better(float a, float b) {
-        if constexpr (OP == kOpMax) return a > b; else return a < b;
+        if constexpr (kIsMin<OP>) return a < b; else return a > b;
     }
 };
 struct TagBF16 {
@@ -71,7 +80,7 @@ struct TagBF16 {
     template <int OP> static __device__ __forceinline__ float elem_key(uint16_t v) { return widen(v); }
     template <int OP> static __device__ __forceinline__ float seed_key(uint16_t v) { return widen(v); }
     template <int OP> static __device__ __forceinline__ bool better(float a, float b) {
-        if constexpr (OP == kOpMax) return a > b; else return a < b;
+        if constexpr (kIsMin<OP>) return a < b; else return a > b;
     }
 };
 struct TagF64 {
@@ -85,7 +94,7 @@ struct TagF64 {
     template <int OP> static __device__ __forceinline__ unsigned long long ordered(unsigned long long b) {
         const unsigned long long mag = b & ~kSign;
         unsigned long long u = mag == 0 ? kSign : ((b & kSign) ? ~b : (b | kSign));
-        if constexpr (OP == kOpMin) u = ~u;
+        if constexpr (kIsMin<OP>) u = ~u;
         return u;
     }
     template <int OP> static __device__ __forceinline__ unsigned long long elem_key(unsigned long long b) {
@@ -113,22 +122,25 @@ __device__ __forceinline__ Cand<Tag> make_cand(typename Tag::raw v, int i) {
     return Cand<Tag>{v, Tag::template seed_key<OP>(v), i};
 }
 
-// Strict update for elements visited in increasing index order.
+// Update for elements visited in increasing index order: strictly better for
+// the first-occurrence ops, not worse for the last-occurrence ops.
 template <class Tag, int OP>
 __device__ __forceinline__ void visit(Cand<Tag>& c, typename Tag::raw x, int j) {
     if constexpr (sizeof(typename Tag::raw) == 8) {
-        // binary64: a 32-bit pre-test on the high word first. filter(x) is the
-        // high half of x's key (one above it for -0.0, and at least as large
-        // for NaNs), so an element that fails "filter(x) >= high half of the
-        // candidate's key" cannot be strictly better and is skipped with two
-        // integer operations. The full 64-bit key is only formed for the rare
-        // elements that pass.
+        // binary64: a 32-bit pre-test on the high word first. f(x) equals the
+        // high half of x's key, except for -0.0 under ArgMax, where it is one
+        // below (the key of -0.0 is that of +0.0), and it is at least that
+        // high half for NaNs. An element with f(x) + 1 < high half of the
+        // candidate's key can be neither better nor equal and is skipped with
+        // a few integer operations; the full 64-bit key is only formed for the
+        // rare elements that pass.
         const unsigned hi = static_cast<unsigned>(x >> 32);
         unsigned f = hi ^ (static_cast<unsigned>(static_cast<int>(hi) >> 31) | 0x80000000u);
-        if constexpr (OP == kOpMin) f = ~f;
-        if (f >= static_cast<unsigned>(c.k >> 32)) {
+        if constexpr (kIsMin<OP>) f = ~f;
+        const unsigned kh = static_cast<unsigned>(c.k >> 32);
+        if (f >= kh || f + 1u == kh) {
             const typename Tag::key k = Tag::template elem_key<OP>(x);
-            if (Tag::template better<OP>(k, c.k)) {
+            if (Tag::template better<OP>(k, c.k) || (kIsLast<OP> && k == c.k)) {
                 c.v = x;
                 c.k = k;
                 c.i = j;
@@ -136,7 +148,7 @@ __device__ __forceinline__ void visit(Cand<Tag>& c, typename Tag::raw x, int j) 
         }
     } else {
         const typename Tag::key k = Tag::template elem_key<OP>(x);
-        if (Tag::template better<OP>(k, c.k)) {
+        if (Tag::template better<OP>(k, c.k) || (kIsLast<OP> && k == c.k)) {
             c.v = x;
             c.k = k;
             c.i = j;
@@ -151,10 +163,12 @@ __device__ __forceinline__ void visit(Cand<Tag>& c, typename Tag::raw x, int j) 
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// Merge of two candidates: better key wins; equal keys keep the lower index.
+// Merge of two candidates: better key wins; equal keys keep the lower index
+// (the higher index for the last-occurrence ops).
 template <class Tag, int OP>
 __device__ __forceinline__ Cand<Tag> merge(Cand<Tag> a, Cand<Tag> b) {
-    const bool take_b = Tag::template better<OP>(b.k, a.k) || (b.k == a.k && b.i < a.i);
+    const bool tie_to_b = kIsLast<OP> ? b.i > a.i : b.i < a.i;
+    const bool take_b = Tag::template better<OP>(b.k, a.k) || (b.k == a.k && tie_to_b);
     return take_b ? b : a;
 }
 

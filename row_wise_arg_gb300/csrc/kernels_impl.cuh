@@ -648,7 +648,13 @@ cudaError_t launch_rows_op(const argr_plan& p, const Problem& pr) {
 
 template <class Tag>
 cudaError_t launch_rows_t(const argr_plan& p, const Problem& pr) {
-    return pr.op == kOpMax ? launch_rows_op<Tag, kOpMax>(p, pr) : launch_rows_op<Tag, kOpMin>(p, pr);
+    switch (pr.op) {
+        case kOpMax: return launch_rows_op<Tag, kOpMax>(p, pr);
+        case kOpMin: return launch_rows_op<Tag, kOpMin>(p, pr);
+        case kOpMaxLast: return launch_rows_op<Tag, kOpMaxLast>(p, pr);
+        case kOpMinLast: return launch_rows_op<Tag, kOpMinLast>(p, pr);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 template <class Tag, int OP, int U>
@@ -673,7 +679,13 @@ cudaError_t launch_split_op(const argr_plan& p, const Problem& pr) {
 
 template <class Tag>
 cudaError_t launch_split_t(const argr_plan& p, const Problem& pr) {
-    return pr.op == kOpMax ? launch_split_op<Tag, kOpMax>(p, pr) : launch_split_op<Tag, kOpMin>(p, pr);
+    switch (pr.op) {
+        case kOpMax: return launch_split_op<Tag, kOpMax>(p, pr);
+        case kOpMin: return launch_split_op<Tag, kOpMin>(p, pr);
+        case kOpMaxLast: return launch_split_op<Tag, kOpMaxLast>(p, pr);
+        case kOpMinLast: return launch_split_op<Tag, kOpMinLast>(p, pr);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 template <class Tag, int OP, int U>
@@ -776,7 +788,13 @@ cudaError_t launch_cluster_op(const argr_plan& p, const Problem& pr) {
 
 template <class Tag>
 cudaError_t launch_cluster_t(const argr_plan& p, const Problem& pr) {
-    return pr.op == kOpMax ? launch_cluster_op<Tag, kOpMax>(p, pr) : launch_cluster_op<Tag, kOpMin>(p, pr);
+    switch (pr.op) {
+        case kOpMax: return launch_cluster_op<Tag, kOpMax>(p, pr);
+        case kOpMin: return launch_cluster_op<Tag, kOpMin>(p, pr);
+        case kOpMaxLast: return launch_cluster_op<Tag, kOpMaxLast>(p, pr);
+        case kOpMinLast: return launch_cluster_op<Tag, kOpMinLast>(p, pr);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 template <class Tag, int OP, int G>
@@ -810,7 +828,13 @@ cudaError_t launch_stream_op(const argr_plan& p, const Problem& pr) {
 
 template <class Tag>
 cudaError_t launch_stream_t(const argr_plan& p, const Problem& pr) {
-    return pr.op == kOpMax ? launch_stream_op<Tag, kOpMax>(p, pr) : launch_stream_op<Tag, kOpMin>(p, pr);
+    switch (pr.op) {
+        case kOpMax: return launch_stream_op<Tag, kOpMax>(p, pr);
+        case kOpMin: return launch_stream_op<Tag, kOpMin>(p, pr);
+        case kOpMaxLast: return launch_stream_op<Tag, kOpMaxLast>(p, pr);
+        case kOpMinLast: return launch_stream_op<Tag, kOpMinLast>(p, pr);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 // The device error word of this translation unit: read it, then clear it.

@@ -55,7 +55,7 @@ argr_status scratch_for_current_device(void** out) {
 bool valid_args(const void* x, int dtype, int64_t rows, int64_t cols, int op, const int64_t* out_idx,
                 const void* out_val) {
     const int es = elem_size(dtype);
-    if (es == 0 || (op != ARGR_MAX && op != ARGR_MIN)) return false;
+    if (es == 0 || op < ARGR_MAX || op > ARGR_MIN_LAST) return false;
     if (rows < 0 || cols < 1 || cols > INT32_MAX || rows > INT64_MAX / cols / es) return false;
     if (rows == 0) return true;
     if (!x || !out_idx) return false;

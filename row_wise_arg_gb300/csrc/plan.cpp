@@ -50,7 +50,7 @@ int pow2_ceil(int64_t v) {
 }
 
 bool valid_dtype(int d) { return d == ARGR_F32 || d == ARGR_F16 || d == ARGR_BF16 || d == ARGR_F64; }
-bool valid_op(int o) { return o == ARGR_MAX || o == ARGR_MIN; }
+bool valid_op(int o) { return o == ARGR_MAX || o == ARGR_MIN || o == ARGR_MAX_LAST || o == ARGR_MIN_LAST; }
 
 int64_t ctas_per_wave(const argr_caps& caps, int block) {
     const int64_t per_sm = std::max<int64_t>(1, caps.max_threads_per_sm / block);

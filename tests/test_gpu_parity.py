@@ -51,6 +51,7 @@ def check(x, dtype, op, **kw):
 def test_workload_full_size(case):
     x = W.make(case)
     check(x, case.dtype, case.op)
+    check(x, case.dtype, case.op + "_last")  # the same rows with ties to the last index
 
 
 def test_narrow_matches_thread_per_row():
@@ -75,7 +76,7 @@ def test_rows_path(dtype, group):
     for cols in WIDTHS[:-1]:
         rows = 37 if cols < 2000 else 5
         x = W.fuzz_rows(dtype, rows, cols, seed=cols * 31 + group)
-        for op in W.OPS:
+        for op in W.ALL_OPS:
             check(x, dtype, op, plan=forced_plan("rows", group=group, vec=0, grid=3, pdl=False))
             check(x, dtype, op, plan=forced_plan("rows", group=group, vec=0, grid=64, unroll=8), offset=1)
             if (cols * es) % 16 == 0:
@@ -89,7 +90,7 @@ def test_split_path(dtype, bpr):
     for cols in WIDTHS:
         rows = 3 if cols > 4000 else 9
         x = W.fuzz_rows(dtype, rows, cols, seed=cols * 7 + bpr)
-        for op in W.OPS:
+        for op in W.ALL_OPS:
             for block, unroll in ((256, 4), (32, 1), (1024, 8), (64, 2)):
                 check(x, dtype, op, plan=forced_plan("split", bpr=bpr, grid_rows=rows, block=block,
                                                      unroll=unroll, pdl=block != 32))
@@ -108,7 +109,7 @@ def test_cluster_path(dtype, cluster):
     for cols in WIDTHS:
         rows = 3 if cols > 4000 else 7
         x = W.fuzz_rows(dtype, rows, cols, seed=cols * 13 + cluster)
-        for op in W.OPS:
+        for op in W.ALL_OPS:
             check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=rows))
             check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=2, unroll=1, pdl=False),
                   offset=1)
@@ -136,7 +137,7 @@ def test_stream_path(dtype, group):
                                                      (3, 65536, 32, 2)):
                 if row_bytes > stage_bytes and group != 32:
                     continue
-                for op in W.OPS:
+                for op in W.ALL_OPS:
                     check(x, dtype, op, plan=forced_plan("stream", group=group, stages=stages,
                                                          stage_bytes=stage_bytes, block=block, grid=grid))
 
@@ -146,7 +147,7 @@ def test_exhaustive_alphabet_rows(dtype):
     """All 8**4 rows of length 4 over the special alphabet, on every path."""
     x = W.exhaustive_rows(dtype, 4)
     rows = x.shape[0]
-    for op in W.OPS:
+    for op in W.ALL_OPS:
         check(x, dtype, op)
         check(x, dtype, op, plan=forced_plan("rows", group=4, vec=0, grid=100))
         check(x, dtype, op, plan=forced_plan("split", bpr=1, grid_rows=min(rows, 1000), block=32))
@@ -161,7 +162,7 @@ def test_exhaustive_alphabet_rows(dtype):
 def test_planner_default_on_fuzz(dtype):
     for rows, cols in [(1, 1), (1, 5), (3, 100000), (2000, 33), (500, 3000), (64, 70000), (1, 300001)]:
         x = W.fuzz_rows(dtype, rows, cols, seed=rows + cols)
-        for op in W.OPS:
+        for op in W.ALL_OPS:
             check(x, dtype, op)
             check(x, dtype, op, offset=1)
 
@@ -190,6 +191,21 @@ def test_golden_first_index_65536():
     row[fx["inf_positions"]] = np.inf
     idx, _ = run(row.reshape(1, -1), "f32", "max")
     assert idx[0] == fx["expected_max"]
+
+
+@pytest.mark.parametrize("dtype", W.DTYPES)
+def test_golden_last_index(dtype):
+    with open(os.path.join(GOLDEN, "onnx_select_last_index.json")) as f:
+        fx = json.load(f)
+    from test_oracle import _token
+    raw_t = oracle.RAW_NP[dtype]
+    for case in fx["cases"]:
+        x = np.array([[_token(t, dtype) for t in case["row"]]], dtype=raw_t)
+        for op in W.LAST_OPS:
+            for plan in (None, forced_plan("split", bpr=2, grid_rows=1, block=32),
+                         forced_plan("rows", group=4, vec=0, grid=1)):
+                idx, _ = run(x, dtype, op, plan=plan)
+                assert idx[0] == case[op], (case["what"], op, plan)
 
 
 @pytest.mark.parametrize("dtype", W.DTYPES)

@@ -60,6 +60,8 @@ def test_validation_before_any_device_work():
     assert f(X, "f32", -1, 5, "max", X, 0, 0, 0, 0) == _lib.ARGR_EINVAL  # rows < 0
     assert f(X, 7, 3, 5, "max", X, 0, 0, 0, 0) == _lib.ARGR_EINVAL  # bad dtype
     assert f(X, "f32", 3, 5, 9, X, 0, 0, 0, 0) == _lib.ARGR_EINVAL  # bad op
+    assert f(X, "f32", 3, 5, 4, X, 0, 0, 0, 0) == _lib.ARGR_EINVAL  # bad op
+    assert f(X, "f32", 0, 5, "max_last", X, 0, 0, 0, 0) == _lib.ARGR_OK  # last-index ops are valid
     assert f(X + 2, "f32", 3, 5, "max", X, 0, 0, 0, 0) == _lib.ARGR_EINVAL  # x not element aligned
     assert f(X, "f32", 3, 5, "max", X + 4, 0, 0, 0, 0) == _lib.ARGR_EINVAL  # out_idx not 8-aligned
     assert f(X, "f64", 3, 5, "max", X, X + 4, 0, 0, 0) == _lib.ARGR_EINVAL  # out_val not aligned
@@ -296,3 +298,65 @@ def test_stream_piece_mapping():
             for stage_bytes in (1024, 4096, 8192):
                 for n_warps in (1, 3, 40, 64):
                     sim_stream_pieces(rows, row_bytes, stage_bytes, n_warps)
+
+
+# ---------------------------------------------------------------------------
+# Host simulation of the binary64 integer keys and their high-word pre-test.
+# ---------------------------------------------------------------------------
+M64 = (1 << 64) - 1
+SIGN = 1 << 63
+INF_BITS = 0x7FF0000000000000
+
+
+def f64_bits(v):
+    import struct
+    return struct.unpack("<Q", struct.pack("<d", v))[0]
+
+
+def ordered(b, is_min):
+    mag = b & ~SIGN & M64
+    u = SIGN if mag == 0 else ((~b & M64) if b & SIGN else (b | SIGN))
+    return (~u & M64) if is_min else u
+
+
+def elem_key(b, is_min):
+    return 0 if (b & ~SIGN & M64) > INF_BITS else ordered(b, is_min)
+
+
+def seed_key(b, is_min):
+    return M64 if (b & ~SIGN & M64) > INF_BITS else ordered(b, is_min)
+
+
+def prefilter(b, cand_key, is_min):
+    hi = b >> 32
+    s = 0xFFFFFFFF if hi & 0x80000000 else 0
+    f = hi ^ (s | 0x80000000)
+    if is_min:
+        f = ~f & 0xFFFFFFFF
+    kh = cand_key >> 32
+    return f >= kh or ((f + 1) & 0xFFFFFFFF) == kh
+
+
+def test_f64_keys_and_prefilter():
+    import math
+    import random
+    specials = [0.0, -0.0, 5e-324, -5e-324, 2.2250738585072014e-308, -2.2250738585072014e-308, 1.0, -1.0,
+                1.0000000000000002, 0.9999999999999999, -1.0000000000000002, 1.7976931348623157e308,
+                -1.7976931348623157e308, math.inf, -math.inf, 2.0 ** -1022, 3.0, -3.0]
+    rnd = random.Random(7)
+    vals = [f64_bits(v) for v in specials] + [rnd.getrandbits(64) for _ in range(300)]
+    vals += [0x7FF8000000000000, 0xFFF8000000000000, 0x7FF0000000000001, 0x8000000000000001, 0x8000000100000000,
+             0x0000000100000000, 0x7FFFFFFFFFFFFFFF]
+    import struct
+    dv = {b: struct.unpack("<d", struct.pack("<Q", b))[0] for b in vals}
+    for is_min in (False, True):
+        for a in vals:
+            for b in vals:
+                xa, xb = dv[a], dv[b]
+                better = (xa < xb) if is_min else (xa > xb)      # element a strictly better than candidate b
+                equal = xa == xb                                  # IEEE equality (false on NaN)
+                ka, kb = elem_key(a, is_min), seed_key(b, is_min)
+                assert (ka > kb) == better, (hex(a), hex(b), is_min)
+                assert (ka == kb) == equal, (hex(a), hex(b), is_min)
+                if better or equal:  # the pre-test must let every such element through
+                    assert prefilter(a, kb, is_min), (hex(a), hex(b), is_min)
