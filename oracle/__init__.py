@@ -57,6 +57,9 @@ def _load():
             lib.oracle_argreduce.restype = ctypes.c_int
             lib.oracle_argreduce_mt.argtypes = lib.oracle_argreduce.argtypes + [ctypes.c_int]
             lib.oracle_argreduce_mt.restype = ctypes.c_int
+            lib.oracle_argreduce_axis.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                                  ctypes.c_int64, ctypes.c_int, i64p, ctypes.c_void_p]
+            lib.oracle_argreduce_axis.restype = ctypes.c_int
             lib.oracle_decode_f16.argtypes = [ctypes.c_uint16]
             lib.oracle_decode_f16.restype = ctypes.c_double
             lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
@@ -90,6 +93,26 @@ def argreduce(x: np.ndarray, dtype: str, op: str, threads: int = 1,
     if rc < 0:
         raise ValueError(f"oracle rejected arguments: rows={rows} cols={cols} dtype={dtype} op={op}")
     return idx, val, used
+
+
+def argreduce_axis(x: np.ndarray, dtype: str, op: str, want_val: bool = True):
+    """Reduce the middle axis of the 3-D raw array ``x[outer, R, inner]``.
+    Returns ``(idx int64[outer, inner], val raw[outer, inner] or None)``."""
+    lib = _load()
+    x = np.ascontiguousarray(x)
+    if x.ndim != 3:
+        raise ValueError("x must be 3-D [outer, R, inner]")
+    if x.dtype != RAW_NP[dtype]:
+        raise TypeError(f"{dtype} expects raw numpy dtype {RAW_NP[dtype]}, got {x.dtype}")
+    outer, R, inner = x.shape
+    idx = np.empty((outer, inner), dtype=np.int64)
+    val = np.empty((outer, inner), dtype=x.dtype) if want_val else None
+    rc = lib.oracle_argreduce_axis(x.ctypes.data_as(ctypes.c_void_p), DTYPE_CODE[dtype], outer, R, inner,
+                                   OP_CODE[op], idx.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                   val.ctypes.data_as(ctypes.c_void_p) if val is not None else None)
+    if rc < 0:
+        raise ValueError(f"oracle rejected arguments: shape={x.shape} dtype={dtype} op={op}")
+    return idx, val
 
 
 def decode_f16(bits: int) -> float:

@@ -154,6 +154,37 @@ int oracle_argreduce(const void* x, int dtype, int64_t rows, int64_t cols, int o
     return 0;
 }
 
+/* Reduction over the middle axis of x[outer][R][inner] (row-major): for each
+ * (o, i), the same sequential scan over r = 0 .. R-1 of x[o][r][i] (elements
+ * `inner` apart). out_idx[o*inner + i] = the chosen r; out_val the raw bits of
+ * that element. With inner == 1 this is the last-axis reduction above. */
+int oracle_argreduce_axis(const void* x, int dtype, int64_t outer, int64_t R, int64_t inner, int op,
+                          int64_t* out_idx, void* out_val) {
+    if (elem_size(dtype) == 0 || !valid_op(op)) return -1;
+    if (outer < 0 || R < 1 || inner < 1 || (outer > 0 && (!x || !out_idx))) return -1;
+    const size_t es = elem_size(dtype);
+    const unsigned char* base = (const unsigned char*)x;
+    unsigned char* ov = (unsigned char*)out_val;
+    for (int64_t o = 0; o < outer; ++o) {
+        for (int64_t i = 0; i < inner; ++i) {
+            const unsigned char* col = base + ((size_t)o * (size_t)R * (size_t)inner + (size_t)i) * es;
+            const size_t stride = (size_t)inner * es;
+            double best = decode(col, dtype);
+            int64_t best_r = 0;
+            for (int64_t r = 1; r < R; ++r) {
+                double v = decode(col + (size_t)r * stride, dtype);
+                if (better(v, best, op)) {
+                    best = v;
+                    best_r = r;
+                }
+            }
+            out_idx[o * inner + i] = best_r;
+            if (ov) memcpy(ov + (size_t)(o * inner + i) * es, col + (size_t)best_r * stride, es);
+        }
+    }
+    return 0;
+}
+
 /* Row-parallel wrapper for timing on several host cores: rows are cut into
  * contiguous, independent ranges, one per thread, each scanned exactly as
  * above. Returns the number of threads used (>= 1), or -1 on error. */

@@ -375,3 +375,104 @@ def test_mutant_is_caught(name, old, new):
 
 def test_unmutated_passes_pin_suite():
     assert _pin_suite_passes(oracle.build())
+
+
+# ---------------------------------------------------------------------------
+# Reduction over a non-last (strided) axis: x[outer, R, inner] over R.
+# ---------------------------------------------------------------------------
+def closed_form_axis(x3, dtype, op):
+    """The closed form applied to every (o, i) column: move R last, reuse the
+    2-D closed form on the [outer*inner, R] view."""
+    outer, R, inner = x3.shape
+    cols = np.ascontiguousarray(np.transpose(x3, (0, 2, 1))).reshape(outer * inner, R)
+    return closed_form(cols, dtype, op).reshape(outer, inner)
+
+
+@pytest.mark.parametrize("dtype", W.DTYPES)
+@pytest.mark.parametrize("op", W.ALL_OPS)
+def test_axis_exhaustive_alphabet(dtype, op):
+    # every length-4 column over the alphabet, laid out with inner = 8, 64, 512
+    rows = W.exhaustive_rows(dtype, 4)  # [4096, 4]
+    for inner in (8, 64, 512):
+        x3 = np.ascontiguousarray(rows.reshape(-1, inner, 4).transpose(0, 2, 1))  # [outer, R=4, inner]
+        idx, val = oracle.argreduce_axis(x3, dtype, op)
+        assert (idx == closed_form_axis(x3, dtype, op)).all()
+        gathered = np.take_along_axis(x3, idx[:, None, :], axis=1)[:, 0, :]
+        assert raw_equal(val, np.ascontiguousarray(gathered))
+
+
+@pytest.mark.parametrize("dtype", W.DTYPES)
+def test_axis_numpy_nan_free(dtype):
+    rng = np.random.Generator(np.random.PCG64(9))
+    for shape in ((3, 1000, 17), (1, 257, 64), (5, 2, 3), (2, 1, 9), (4, 33, 1)):
+        x3 = W.encode(rng.integers(-4, 5, size=shape).astype(np.float64), dtype)
+        v = np_decode(x3.reshape(-1, 1), dtype).reshape(shape)
+        idx, _ = oracle.argreduce_axis(x3, dtype, "max")
+        assert (idx == np.argmax(v, axis=1)).all()
+        idx, _ = oracle.argreduce_axis(x3, dtype, "min")
+        assert (idx == np.argmin(v, axis=1)).all()
+        idx, _ = oracle.argreduce_axis(x3, dtype, "max_last")
+        assert (idx == shape[1] - 1 - np.argmax(v[:, ::-1, :], axis=1)).all()
+
+
+def test_axis_brute_force_loops():
+    """Pure-Python loops over (o, r, i) on a small special-value tensor."""
+    for dtype in ("f32", "bf16"):
+        x = W.fuzz_rows(dtype, 6, 5 * 7, seed=3, p_special=0.4).reshape(6, 5, 7)
+        v = np_decode(x.reshape(-1, 1), dtype).reshape(x.shape)
+        for op in W.ALL_OPS:
+            idx, _ = oracle.argreduce_axis(x, dtype, op)
+            for o in range(6):
+                for i in range(7):
+                    col = [v[o, r, i] for r in range(5)]
+                    if np.isnan(col[0]):
+                        exp = 0
+                    else:
+                        ok = [r for r in range(5) if not np.isnan(col[r]) and all(
+                            np.isnan(col[k]) or (col[r] >= col[k] if op.startswith("max") else col[r] <= col[k])
+                            for k in range(5))]
+                        exp = ok[-1] if op.endswith("_last") else ok[0]
+                    assert idx[o, i] == exp, (op, o, i, col)
+
+
+AXIS_MUTANTS = [
+    ("column stride", "const size_t stride = (size_t)inner * es;", "const size_t stride = es;"),
+    ("outer offset", "(size_t)o * (size_t)R * (size_t)inner + (size_t)i", "(size_t)o * (size_t)inner + (size_t)i"),
+    ("output position", "out_idx[o * inner + i] = best_r;", "out_idx[i * outer + o] = best_r;"),
+    ("first r skipped", "for (int64_t r = 1; r < R; ++r) {", "for (int64_t r = 2; r < R; ++r) {"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", AXIS_MUTANTS, ids=[m[0] for m in AXIS_MUTANTS])
+def test_axis_mutant_is_caught(name, old, new):
+    import ctypes
+    if shutil.which("gcc") is None:
+        pytest.skip("no host C compiler")
+    src = open(oracle._SRC).read()
+    assert src.count(old) == 1, old
+    with tempfile.TemporaryDirectory() as d:
+        c, so = os.path.join(d, "m.c"), os.path.join(d, "libm.so")
+        open(c, "w").write(src.replace(old, new))
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", c, "-o", so, "-lm"], check=True)
+        lib = ctypes.CDLL(so)
+        lib.oracle_argreduce_axis.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                              ctypes.c_int64, ctypes.c_int, ctypes.POINTER(ctypes.c_int64),
+                                              ctypes.c_void_p]
+        saved = oracle._lib
+        try:
+            class Shim:
+                pass
+            shim = Shim()
+            shim.oracle_argreduce_axis = lib.oracle_argreduce_axis
+            oracle._lib = shim
+            caught = False
+            try:
+                for dtype in ("f32", "f64"):
+                    test_axis_numpy_nan_free(dtype)
+                    for op in W.ALL_OPS:
+                        test_axis_exhaustive_alphabet(dtype, op)
+            except AssertionError:
+                caught = True
+            assert caught, f"axis mutant '{name}' survived"
+        finally:
+            oracle._lib = saved
