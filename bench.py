@@ -50,9 +50,12 @@ WORKLOADS = {
     "uniform_special": (4, "ArgMin/ArgMax fp32/f64 [4096,4096]+[65536,1024] with special rows"),
     "narrow": (5, "ArgMax fp32 [65536,64]+[4096,8]+[4096,128]"),
     "wide_rows_last": (-2, "the wide_rows cases with ties to the last index (ONNX select_last_index = 1)"),
+    "axis": (6, "ArgMax/ArgMin over a non-last axis: [1,100000,1000], [1,1000,100000], [64,512,256] bf16, "
+                "[128,4096,8], [16,2048,384] f64"),
 }
 DTYPE_LABEL = {"f32": "f32", "f16": "f16", "bf16": "bf16", "f64": "f64"}
-KERNEL_OF_PATH = {"rows": "rows_kernel", "split": "split_kernel", "cluster": "cluster_kernel", "none": "none"}
+KERNEL_OF_PATH = {"rows": "rows_kernel", "split": "split_kernel", "cluster": "cluster_kernel", "axis": "axis_kernel",
+                  "stream": "stream_kernel", "none": "none"}
 
 
 def workload_cases(group: int):
@@ -65,7 +68,17 @@ def workload_cases(group: int):
 def algo_bytes(c: W.Case, with_values: bool = False) -> int:
     """Algorithmic bytes of one call: the input read once, int64 indices written."""
     es = W.ELEM_SIZE[c.dtype]
-    return c.rows * c.cols * es + c.rows * 8 + (c.rows * es if with_values else 0)
+    outputs = c.rows * c.inner
+    return c.rows * c.cols * c.inner * es + outputs * 8 + (outputs * es if with_values else 0)
+
+
+def call(A, c: W.Case, x, out_idx, scratch, stream):
+    """One library call for case c on device data x (flat)."""
+    if c.inner > 1:
+        A.argreduce_axis(x.view(c.rows, c.cols, c.inner), 1, c.op, dtype=c.dtype, out_idx=out_idx, scratch=scratch,
+                         stream=stream)
+    else:
+        A.argreduce(x.view(c.rows, c.cols), c.op, dtype=c.dtype, out_idx=out_idx, scratch=scratch, stream=stream)
 
 
 def load_peak():
@@ -206,8 +219,13 @@ def oracle_time(cases, inputs, budget_s: float, max_calls: int = None):
     t0 = time.perf_counter()
     while True:
         c = cases[calls % len(cases)]
-        threads = min(os.cpu_count() or 1, c.rows) if c.rows > 1 else 1
-        _, _, used = oracle.argreduce(inputs[calls % len(cases)], c.dtype, c.op, threads=threads, want_val=False)
+        if c.inner > 1:
+            oracle.argreduce_axis(inputs[calls % len(cases)], c.dtype, c.op, want_val=False)
+            used = 1
+        else:
+            threads = min(os.cpu_count() or 1, c.rows) if c.rows > 1 else 1
+            _, _, used = oracle.argreduce(inputs[calls % len(cases)], c.dtype, c.op, threads=threads,
+                                          want_val=False)
         cores = max(cores, used)
         calls += 1
         el = time.perf_counter() - t0
@@ -239,13 +257,12 @@ class GraphSet:
         need = max([A.argreduce_scratch_bytes(c.rows, c.cols, c.dtype, c.op) for c in cases] + [0])
         self.scratch.ensure(max(need, 4096), stream.cuda_stream)
         self.copies = [[x] + [x.clone() for _ in range(copies - 1)] for x in dev_inputs]
-        self.outs = [torch.empty(max(c.rows, 1), dtype=torch.int64, device="cuda") for c in cases]
+        self.outs = [torch.empty(max(c.rows * c.inner, 1), dtype=torch.int64, device="cuda") for c in cases]
         self.graphs = []
 
         def calls(k):
             for i, c in enumerate(cases):
-                A.argreduce(self.copies[i][k].view(c.rows, c.cols), c.op, dtype=c.dtype,
-                            out_idx=self.outs[i], scratch=self.scratch, stream=stream)
+                call(A, c, self.copies[i][k], self.outs[i], self.scratch, stream)
 
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
@@ -315,8 +332,8 @@ def e2e_time(torch, A, cases, inputs, steps, stream):
         {"f32": np.float32, "f16": np.int16, "bf16": np.int16, "f64": np.float64}[c.dtype])).pin_memory()
         for c, x in zip(cases, inputs)]
     devs = [torch.empty_like(h, device="cuda") for h in hosts]
-    outs = [torch.empty(c.rows, dtype=torch.int64, device="cuda") for c in cases]
-    host_out = torch.empty(sum(c.rows for c in cases), dtype=torch.int64).pin_memory()
+    outs = [torch.empty(c.rows * c.inner, dtype=torch.int64, device="cuda") for c in cases]
+    host_out = torch.empty(sum(c.rows * c.inner for c in cases), dtype=torch.int64).pin_memory()
     scratch = A.Scratch()
     h2d = sum(h.numel() * h.element_size() for h in hosts)
     d2h = host_out.numel() * 8
@@ -325,9 +342,9 @@ def e2e_time(torch, A, cases, inputs, steps, stream):
         off = 0
         for c, h, d, o in zip(cases, hosts, devs, outs):
             d.copy_(h, non_blocking=True)
-            A.argreduce(d, c.op, dtype=c.dtype, out_idx=o, scratch=scratch, stream=stream)
-            host_out[off:off + c.rows].copy_(o, non_blocking=True)
-            off += c.rows
+            call(A, c, d.reshape(-1), o, scratch, stream)
+            host_out[off:off + c.rows * c.inner].copy_(o, non_blocking=True)
+            off += c.rows * c.inner
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -419,8 +436,8 @@ def main():
     plans = {}
     kernels = set()
     for c in cases:
-        p = A.argreduce_plan(c.rows, c.cols, c.dtype, c.op).as_dict()
-        plans[f"{c.rows}x{c.cols}_{c.dtype}"] = {k: p[k] for k in ("path_name", "blocks_per_row", "cluster",
+        p = A.argreduce_axis_plan(c.rows, c.cols, c.inner, c.dtype, c.op).as_dict()
+        plans[f"{c.rows}x{c.cols}" + (f"x{c.inner}" if c.inner > 1 else "") + f"_{c.dtype}"] = {k: p[k] for k in ("path_name", "blocks_per_row", "cluster",
                                                                     "block", "unroll", "group", "flags")}
         kernels.add(KERNEL_OF_PATH[p["path_name"]])
 
@@ -473,7 +490,8 @@ def main():
                     gbs = algo_bytes(c) / (s / n) / 1e9
                     table.append({"case": c.name, "us_per_call": round(us, 3), "gbs": round(gbs, 1),
                                   "frac": round(gbs / peak, 4),
-                                  "path": A.argreduce_plan(c.rows, c.cols, c.dtype, c.op).as_dict()["path_name"]})
+                                  "path": A.argreduce_axis_plan(c.rows, c.cols, c.inner, c.dtype,
+                                                                c.op).as_dict()["path_name"]})
             del ginputs
         result["configs"] = table
 

@@ -68,6 +68,9 @@ typedef enum {
                               the last CTA to arrive for a row reduces the partials */
     ARGR_PATH_CLUSTER = 3, /* one thread-block cluster of `cluster` CTAs per row, merged
                               through distributed shared memory; no scratch */
+    ARGR_PATH_AXIS = 5,    /* non-last axis (argreduce_axis): a warp covers 32 lanes x V consecutive
+                              inner positions (`vec`: V-element vectors), the CTA's block/32 warps
+                              split R, and a cluster of `cluster` CTAs (1 = none) splits it further */
     ARGR_PATH_STREAM = 4   /* every warp streams a contiguous range of rows through its own
                               `stages` shared-memory buffers of `stage_bytes`, filled by bulk
                               (TMA) copies; `group` lanes per row for rows that fit a buffer,
@@ -184,6 +187,32 @@ argr_status argreduce_plan(int64_t rows, int64_t cols, argr_dtype dtype, argr_op
 argr_status argreduce_with_plan(const argr_plan* plan, const void* x, argr_dtype dtype, int64_t rows,
                                 int64_t cols, argr_op op, int64_t* out_idx, void* out_val, void* scratch,
                                 size_t scratch_bytes, argr_stream stream);
+
+/*
+ * ArgMax / ArgMin over a non-last axis: x is row-major [outer, reduce, inner]
+ * and the result is out_idx[outer, inner] (int64, the position along the
+ * reduced axis), out_val[outer, inner] optional. Element (o, r, i) is at
+ * x[(o * reduce + r) * inner + i]; each output applies exactly the rules of
+ * argreduce() to the `reduce` elements x[o, 0..reduce-1, i], which lie
+ * `inner` elements apart. With inner == 1 this is argreduce() on
+ * [outer, reduce]. Needs no scratch unless inner == 1 and the last-axis plan
+ * does (pass scratch as for argreduce(); argreduce_scratch_bytes(outer,
+ * reduce, ...) sizes it). Errors as for argreduce(); ARGR_EUNSUPPORTED if
+ * inner needs more than 65535 column tiles of 32 lanes.
+ */
+argr_status argreduce_axis(const void* x, argr_dtype dtype, int64_t outer, int64_t reduce, int64_t inner,
+                           argr_op op, int64_t* out_idx, void* out_val, void* scratch, size_t scratch_bytes,
+                           argr_stream stream);
+
+/* The planner for argreduce_axis() (a last-axis plan when inner == 1). */
+argr_status argreduce_axis_plan(int64_t outer, int64_t reduce, int64_t inner, argr_dtype dtype, argr_op op,
+                                const argr_caps* caps, argr_plan* out);
+
+/* argreduce_axis() with an explicit plan (re-validated; an ARGR_PATH_AXIS
+ * plan for any inner, a last-axis plan only for inner == 1). */
+argr_status argreduce_axis_with_plan(const argr_plan* plan, const void* x, argr_dtype dtype, int64_t outer,
+                                     int64_t reduce, int64_t inner, argr_op op, int64_t* out_idx, void* out_val,
+                                     void* scratch, size_t scratch_bytes, argr_stream stream);
 
 /* Scratch bytes a given plan needs for `rows` rows. */
 size_t argreduce_plan_scratch_bytes(const argr_plan* plan, int64_t rows);

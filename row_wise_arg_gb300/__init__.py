@@ -16,12 +16,13 @@ from typing import Dict, Optional, Tuple
 
 from . import _lib
 from ._lib import (ARGR_BF16, ARGR_F16, ARGR_F32, ARGR_F64, ARGR_MAX, ARGR_MIN,  # noqa: F401
-                   ARGR_OK, ArgreduceError, DTYPE_CODES, OP_CODES, argr_caps, argr_plan, argreduce_device_caps,
+                   ARGR_OK, ArgreduceError, DTYPE_CODES, OP_CODES, argr_caps, argr_plan, argreduce_axis_plan,
+                   argreduce_device_caps,
                    argreduce_plan, argreduce_plan_scratch_bytes, argreduce_read_error, argreduce_scratch_bytes,
                    argreduce_scratch_init, argreduce_status_string, argreduce_version, load, make_caps)
 
 __all__ = [
-    "argreduce", "argmax", "argmin", "argreduce_with_plan", "argreduce_plan", "argreduce_scratch_bytes",
+    "argreduce", "argreduce_axis", "argreduce_axis_plan", "argmax", "argmin", "argreduce_with_plan", "argreduce_plan", "argreduce_scratch_bytes",
     "argreduce_scratch_init", "argreduce_read_error", "argreduce_device_caps", "argreduce_status_string",
     "argreduce_version", "argreduce_plan_scratch_bytes", "ArgreduceError", "Scratch", "make_caps",
 ]
@@ -153,6 +154,48 @@ def argreduce_with_plan(plan: argr_plan, x, op="max", *, dtype: Optional[str] = 
                                       scratch.nbytes if scratch is not None else 0, st_ptr)
     if st != ARGR_OK:
         raise ArgreduceError(st, "argreduce_with_plan")
+    return out_idx, out_val
+
+
+def argreduce_axis(x, dim: int, op="max", *, dtype: Optional[str] = None, with_values: bool = False,
+                   out_idx=None, out_val=None, scratch: Optional[Scratch] = None, stream=None, plan=None):
+    """Reduce dimension ``dim`` of a contiguous CUDA tensor. The tensor is
+    viewed as [outer, reduce, inner] around ``dim``; results have the shape of
+    ``x`` without ``dim``. Ties and NaNs follow the same rules as argreduce()."""
+    torch = _torch()
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor")
+    dim = dim % x.dim()
+    outer = 1
+    for d in x.shape[:dim]:
+        outer *= d
+    inner = 1
+    for d in x.shape[dim + 1:]:
+        inner *= d
+    reduce = x.shape[dim]
+    code = dtype_code(x, dtype)
+    opc = _lib._code(OP_CODES, op)
+    shape = tuple(x.shape[:dim]) + tuple(x.shape[dim + 1:])
+    if out_idx is None:
+        out_idx = torch.empty(shape, dtype=torch.int64, device=x.device)
+    if with_values and out_val is None:
+        out_val = torch.empty(shape, dtype=x.dtype, device=x.device)
+    st_ptr = (stream if isinstance(stream, int) else stream.cuda_stream) if stream is not None else \
+        torch.cuda.current_stream(x.device).cuda_stream
+    need = 0
+    if inner == 1 and outer > 0 and reduce > 0:
+        need = argreduce_plan_scratch_bytes(plan, outer) if plan is not None else \
+            argreduce_scratch_bytes(outer, reduce, code, opc)
+    if scratch is None and need:
+        scratch = _default_scratch(x.device.index, st_ptr)
+    if need:
+        scratch.ensure(need, st_ptr)
+    st = _lib.argreduce_axis_raw(x.data_ptr(), code, outer, reduce, inner, opc, out_idx.data_ptr(),
+                                 out_val.data_ptr() if out_val is not None else 0,
+                                 scratch.ptr if scratch is not None else 0,
+                                 scratch.nbytes if scratch is not None else 0, st_ptr, plan)
+    if st != ARGR_OK:
+        raise ArgreduceError(st, "argreduce_axis")
     return out_idx, out_val
 
 

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(PKG, "libargreduce.so")
 ARGR_F32, ARGR_F16, ARGR_BF16, ARGR_F64 = 0, 1, 2, 3
 ARGR_MAX, ARGR_MIN, ARGR_MAX_LAST, ARGR_MIN_LAST = 0, 1, 2, 3
 (ARGR_OK, ARGR_EINVAL, ARGR_ESCRATCH, ARGR_EUNSUPPORTED, ARGR_ECUDA, ARGR_ETIMEOUT) = range(6)
-ARGR_PATH_NONE, ARGR_PATH_ROWS, ARGR_PATH_SPLIT, ARGR_PATH_CLUSTER, ARGR_PATH_STREAM = range(5)
+ARGR_PATH_NONE, ARGR_PATH_ROWS, ARGR_PATH_SPLIT, ARGR_PATH_CLUSTER, ARGR_PATH_STREAM, ARGR_PATH_AXIS = range(6)
 ARGR_PLAN_PDL = 1
 ARGR_PLAN_BULK = 2
 ARGR_PLAN_TEST_EXPIRE = 4
@@ -25,13 +25,14 @@ ARGR_PLAN_TEST_EXPIRE = 4
 DTYPE_CODES = {"f32": ARGR_F32, "f16": ARGR_F16, "bf16": ARGR_BF16, "f64": ARGR_F64}
 OP_CODES = {"max": ARGR_MAX, "min": ARGR_MIN, "max_last": ARGR_MAX_LAST, "min_last": ARGR_MIN_LAST}
 PATH_NAMES = {ARGR_PATH_NONE: "none", ARGR_PATH_ROWS: "rows", ARGR_PATH_SPLIT: "split",
-              ARGR_PATH_CLUSTER: "cluster", ARGR_PATH_STREAM: "stream"}
+              ARGR_PATH_CLUSTER: "cluster", ARGR_PATH_STREAM: "stream", ARGR_PATH_AXIS: "axis"}
 
 # Every function the header declares (checked by the tests).
 EXPORTS = (
     "argreduce_scratch_bytes", "argreduce_scratch_init", "argreduce", "argreduce_plan",
     "argreduce_with_plan", "argreduce_plan_scratch_bytes", "argreduce_read_error",
     "argreduce_device_caps", "argreduce_status_string", "argreduce_version", "argreduce_noalloc",
+    "argreduce_axis", "argreduce_axis_plan", "argreduce_axis_with_plan",
 )
 
 
@@ -97,6 +98,14 @@ def load() -> ctypes.CDLL:
         lib.argreduce_device_caps.restype = i32
         lib.argreduce_status_string.argtypes = [i32]
         lib.argreduce_status_string.restype = ctypes.c_char_p
+        lib.argreduce_axis.argtypes = [vp, i32, i64, i64, i64, i32, vp, vp, vp, sz, vp]
+        lib.argreduce_axis.restype = i32
+        lib.argreduce_axis_plan.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(argr_caps),
+                                            ctypes.POINTER(argr_plan)]
+        lib.argreduce_axis_plan.restype = i32
+        lib.argreduce_axis_with_plan.argtypes = [ctypes.POINTER(argr_plan), vp, i32, i64, i64, i64, i32, vp, vp, vp,
+                                                 sz, vp]
+        lib.argreduce_axis_with_plan.restype = i32
         lib.argreduce_noalloc.argtypes = [vp, i32, i64, i64, i32, vp, vp, vp]
         lib.argreduce_noalloc.restype = i32
         lib.argreduce_version.argtypes = []
@@ -162,6 +171,26 @@ def argreduce_plan(rows: int, cols: int, dtype, op, caps: Optional[argr_caps] = 
                                ctypes.byref(caps) if caps is not None else None, ctypes.byref(p))
     if st != ARGR_OK:
         raise ArgreduceError(st, "argreduce_plan")
+    return p
+
+
+def argreduce_axis_raw(x_ptr: int, dtype, outer: int, reduce: int, inner: int, op, out_idx_ptr: int,
+                       out_val_ptr: int, scratch_ptr: int, scratch_bytes: int, stream_ptr: int,
+                       plan: Optional[argr_plan] = None) -> int:
+    """argreduce_axis() (or argreduce_axis_with_plan() when a plan is given)."""
+    args = (x_ptr or None, _code(DTYPE_CODES, dtype), outer, reduce, inner, _code(OP_CODES, op),
+            out_idx_ptr or None, out_val_ptr or None, scratch_ptr or None, scratch_bytes, stream_ptr or None)
+    if plan is None:
+        return load().argreduce_axis(*args)
+    return load().argreduce_axis_with_plan(ctypes.byref(plan), *args)
+
+
+def argreduce_axis_plan(outer: int, reduce: int, inner: int, dtype, op, caps: Optional[argr_caps] = None) -> argr_plan:
+    p = argr_plan()
+    st = load().argreduce_axis_plan(outer, reduce, inner, _code(DTYPE_CODES, dtype), _code(OP_CODES, op),
+                                    ctypes.byref(caps) if caps is not None else None, ctypes.byref(p))
+    if st != ARGR_OK:
+        raise ArgreduceError(st, "argreduce_axis_plan")
     return p
 
 

@@ -85,6 +85,7 @@ argr_status run(const argr_plan& p, const Problem& pr, size_t scratch_bytes) {
         case ARGR_PATH_SPLIT: e = launch_split_##sfx(p, pr); break;        \
         case ARGR_PATH_CLUSTER: e = launch_cluster_##sfx(p, pr); break;    \
         case ARGR_PATH_STREAM: e = launch_stream_##sfx(p, pr); break;      \
+        case ARGR_PATH_AXIS: e = launch_axis_##sfx(p, pr); break;          \
         default: return ARGR_EINVAL;                                       \
     }
     switch (pr.dtype) {
@@ -110,6 +111,7 @@ Problem make_problem(const void* x, int dtype, int64_t rows, int64_t cols, int o
     pr.op = op;
     pr.rows = rows;
     pr.cols = static_cast<int>(cols);
+    pr.inner = 1;
     pr.out_idx = out_idx;
     pr.out_val = out_val;
     pr.scratch = scratch;
@@ -180,6 +182,74 @@ argr_status argreduce_with_plan(const argr_plan* plan, const void* x, argr_dtype
     if ((s = current_caps(&caps)) != ARGR_OK) return s;
     if ((s = check_plan(*plan, rows, cols, dtype, caps, rows_aligned(x, dtype, cols))) != ARGR_OK) return s;
     return run(*plan, make_problem(x, dtype, rows, cols, op, out_idx, out_val, scratch, stream), scratch_bytes);
+}
+
+// ---------------------------------------------------------------------------
+// Reduction over a non-last axis.
+// ---------------------------------------------------------------------------
+static argr_status check_axis_args(const void* x, int dtype, int64_t outer, int64_t reduce, int64_t inner, int op,
+                                   const int64_t* out_idx, const void* out_val) {
+    if (inner < 1 || outer < 0) return ARGR_EINVAL;
+    if (outer > 0 && inner > INT64_MAX / outer) return ARGR_EINVAL;
+    // the same checks as a [outer * inner, reduce] problem (sizes, alignment)
+    return check_args(x, dtype, outer * inner, reduce, op, out_idx, out_val);
+}
+
+argr_status argreduce_axis_plan(int64_t outer, int64_t reduce, int64_t inner, argr_dtype dtype, argr_op op,
+                                const argr_caps* caps, argr_plan* out) {
+    if (!out) return ARGR_EINVAL;
+    argr_caps c;
+    if (caps) {
+        c = *caps;
+    } else {
+        argr_status s = current_caps(&c);
+        if (s != ARGR_OK) return s;
+    }
+    return make_axis_plan(outer, reduce, inner, dtype, op, c, true, out);
+}
+
+static argr_status run_axis(const argr_plan& p, const void* x, int dtype, int64_t outer, int64_t reduce,
+                            int64_t inner, int op, int64_t* out_idx, void* out_val, void* scratch,
+                            size_t scratch_bytes, argr_stream stream) {
+    if (p.path != ARGR_PATH_AXIS) {
+        // inner == 1: the last-axis problem [outer, reduce]
+        return run(p, make_problem(x, dtype, outer, reduce, op, out_idx, out_val, scratch, stream), scratch_bytes);
+    }
+    Problem pr = make_problem(x, dtype, outer, reduce, op, out_idx, out_val, scratch, stream);
+    pr.inner = inner;
+    return run(p, pr, scratch_bytes);
+}
+
+argr_status argreduce_axis(const void* x, argr_dtype dtype, int64_t outer, int64_t reduce, int64_t inner,
+                           argr_op op, int64_t* out_idx, void* out_val, void* scratch, size_t scratch_bytes,
+                           argr_stream stream) {
+    argr_status s = check_axis_args(x, dtype, outer, reduce, inner, op, out_idx, out_val);
+    if (s != ARGR_OK || outer == 0) return s;
+    argr_caps caps;
+    if ((s = current_caps(&caps)) != ARGR_OK) return s;
+    argr_plan p;
+    if ((s = make_axis_plan(outer, reduce, inner, dtype, op, caps, reinterpret_cast<uintptr_t>(x) % 16 == 0, &p)) !=
+        ARGR_OK)
+        return s;
+    return run_axis(p, x, dtype, outer, reduce, inner, op, out_idx, out_val, scratch, scratch_bytes, stream);
+}
+
+argr_status argreduce_axis_with_plan(const argr_plan* plan, const void* x, argr_dtype dtype, int64_t outer,
+                                     int64_t reduce, int64_t inner, argr_op op, int64_t* out_idx, void* out_val,
+                                     void* scratch, size_t scratch_bytes, argr_stream stream) {
+    if (!plan) return ARGR_EINVAL;
+    argr_status s = check_axis_args(x, dtype, outer, reduce, inner, op, out_idx, out_val);
+    if (s != ARGR_OK || outer == 0) return s;
+    argr_caps caps;
+    if ((s = current_caps(&caps)) != ARGR_OK) return s;
+    if (plan->path == ARGR_PATH_AXIS) {
+        if ((s = check_axis_plan(*plan, outer, reduce, inner, dtype, caps, reinterpret_cast<uintptr_t>(x))) != ARGR_OK)
+            return s;
+    } else {
+        if (inner != 1) return ARGR_EINVAL;  // a last-axis plan needs inner == 1
+        if ((s = check_plan(*plan, outer, reduce, dtype, caps, rows_aligned(x, dtype, reduce))) != ARGR_OK) return s;
+    }
+    return run_axis(*plan, x, dtype, outer, reduce, inner, op, out_idx, out_val, scratch, scratch_bytes, stream);
 }
 
 size_t argreduce_plan_scratch_bytes(const argr_plan* plan, int64_t rows) {

@@ -35,8 +35,9 @@ struct Problem {
     const void* x;
     int dtype;     // argr_dtype
     int op;        // argr_op
-    int64_t rows;
-    int cols;      // 1 .. INT32_MAX
+    int64_t rows;  // last axis: rows. Non-last axis: outer
+    int cols;      // 1 .. INT32_MAX. Last axis: columns. Non-last axis: the reduced extent R
+    int64_t inner; // non-last axis: elements after the reduced axis (1 for the last axis)
     int64_t* out_idx;
     void* out_val;
     void* scratch;
@@ -54,6 +55,12 @@ argr_status make_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_
 argr_status check_plan(const argr_plan& p, int64_t rows, int64_t cols, int dtype, const argr_caps& caps,
                        bool row_aligned);
 size_t plan_scratch(const argr_plan& p, int64_t rows);
+// Non-last axis x[outer][reduce][inner]: a last-axis plan when inner == 1,
+// else an ARGR_PATH_AXIS plan. `base_aligned`: x is 16-byte aligned.
+argr_status make_axis_plan(int64_t outer, int64_t reduce, int64_t inner, int dtype, int op, const argr_caps& caps,
+                           bool base_aligned, argr_plan* out);
+argr_status check_axis_plan(const argr_plan& p, int64_t outer, int64_t reduce, int64_t inner, int dtype,
+                            const argr_caps& caps, uintptr_t x_addr);
 
 // Kernel launchers (one translation unit per element type). They assume a
 // checked plan and return the launch's CUDA error.
@@ -62,6 +69,7 @@ size_t plan_scratch(const argr_plan& p, int64_t rows);
     cudaError_t launch_split_##sfx(const argr_plan& p, const Problem& pr);   \
     cudaError_t launch_cluster_##sfx(const argr_plan& p, const Problem& pr); \
     cudaError_t launch_stream_##sfx(const argr_plan& p, const Problem& pr);  \
+    cudaError_t launch_axis_##sfx(const argr_plan& p, const Problem& pr);    \
     cudaError_t read_and_clear_error_##sfx(unsigned* out);
 ARGR_DECLARE_LAUNCHERS(f32)
 ARGR_DECLARE_LAUNCHERS(f16)

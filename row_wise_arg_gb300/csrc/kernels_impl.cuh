@@ -428,6 +428,145 @@ cluster_bulk_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int c
 }
 
 // ---------------------------------------------------------------------------
+// Reduction over a non-last axis: x[outer][R][inner] over R.
+//
+// A warp owns 32 * V consecutive inner positions (V per lane: a 16-byte vector
+// for 4- and 8-byte elements, 8 bytes for 16-bit ones, one element when the
+// columns are not aligned), so every step along R reads one contiguous
+// segment. The Y warps of a CTA take contiguous parts of R and merge per
+// column through shared memory; with a cluster of C CTAs, R is first cut into
+// C parts and the CTAs merge through distributed shared memory into CTA 0.
+// grid = (C, column tiles, outer slots); outer loops over the slots when C == 1.
+// ---------------------------------------------------------------------------
+template <typename R, int V>
+struct AxisVec;
+template <typename R>
+struct AxisVec<R, 1> {
+    static __device__ __forceinline__ void load(const R* p, R (&v)[1]) { v[0] = ld_scalar(p); }
+};
+template <>
+struct AxisVec<float, 4> {
+    static __device__ __forceinline__ void load(const float* p, float (&v)[4]) {
+        const uint4 q = ld_stream16(p);
+        v[0] = __uint_as_float(q.x); v[1] = __uint_as_float(q.y); v[2] = __uint_as_float(q.z); v[3] = __uint_as_float(q.w);
+    }
+};
+template <>
+struct AxisVec<unsigned long long, 2> {
+    static __device__ __forceinline__ void load(const unsigned long long* p, unsigned long long (&v)[2]) {
+        const uint4 q = ld_stream16(p);
+        v[0] = static_cast<unsigned long long>(q.y) << 32 | q.x;
+        v[1] = static_cast<unsigned long long>(q.w) << 32 | q.z;
+    }
+};
+template <>
+struct AxisVec<uint16_t, 4> {
+    static __device__ __forceinline__ void load(const uint16_t* p, uint16_t (&v)[4]) {
+        uint2 q;
+        asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(q.x), "=r"(q.y) : "l"(p));
+        v[0] = static_cast<uint16_t>(q.x & 0xffffu); v[1] = static_cast<uint16_t>(q.x >> 16);
+        v[2] = static_cast<uint16_t>(q.y & 0xffffu); v[3] = static_cast<uint16_t>(q.y >> 16);
+    }
+};
+
+template <class Tag, int OP, int V, int U>
+__global__ void __launch_bounds__(1024)
+axis_kernel(const typename Tag::raw* __restrict__ x, int64_t outer, int nred, int64_t inner,
+            int64_t* __restrict__ out_idx, typename Tag::raw* __restrict__ out_val) {
+    using R = typename Tag::raw;
+    extern __shared__ __align__(16) uint4 axis_smem[];  // [Y][32][V] CTA merge, then [C][32][V] cluster slots
+    grid_dependency_wait();
+    allow_dependents();
+    const int lane = threadIdx.x & 31;
+    const int y = threadIdx.x >> 5;
+    const int Y = blockDim.x >> 5;
+    const int C = gridDim.x;
+    const int b = blockIdx.x;  // rank in the cluster (the cluster spans x)
+    uint4* cta_slots = axis_smem;
+    uint4* cl_slots = axis_smem + Y * 32 * V;
+    const int64_t i0 = (static_cast<int64_t>(blockIdx.y) * 32 + lane) * V;  // this lane's first column
+    const bool active = i0 < inner;
+    // This warp's part of R: CTA part b of C, then warp part y of Y.
+    const int64_t cb = static_cast<int64_t>(nred) * b / C, ce = static_cast<int64_t>(nred) * (b + 1) / C;
+    const int rs = static_cast<int>(cb + (ce - cb) * y / Y);
+    const int re = static_cast<int>(cb + (ce - cb) * (y + 1) / Y);
+    for (int64_t o = blockIdx.z; o < outer; o += gridDim.z) {
+        const R* col = x + (o * nred) * inner + i0;
+        Cand<Tag> c[V];
+        if (active) {
+            R v0[V];
+            AxisVec<R, V>::load(col, v0);  // row r = 0 seeds every candidate
+#pragma unroll
+            for (int v = 0; v < V; ++v) c[v] = make_cand<Tag, OP>(v0[v], 0);
+            int r = rs;
+            while (r < re) {
+                const int rem = re - r;
+                R buf[U][V];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (u < rem) AxisVec<R, V>::load(col + static_cast<int64_t>(r + u) * inner, buf[u]);
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (u < rem) {
+#pragma unroll
+                        for (int v = 0; v < V; ++v) visit<Tag, OP>(c[v], buf[u][v], r + u);
+                    }
+                if (rem <= U) break;
+                r += U;
+            }
+        }
+        // Merge the Y warps of this CTA, column by column (warp 0).
+        if (active) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) cta_slots[(y * 32 + lane) * V + v] = pack_cand<Tag>(c[v]);
+        }
+        __syncthreads();
+        if (y == 0 && active) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                Cand<Tag> m = c[v];
+                for (int w = 1; w < Y; ++w) m = merge<Tag, OP>(m, unpack_cand<Tag, OP>(cta_slots[(w * 32 + lane) * V + v]));
+                c[v] = m;
+            }
+        }
+        if (C > 1) {
+            if (y == 0 && active) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    const uint4 pk = pack_cand<Tag>(c[v]);
+                    unsigned remote;
+                    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                                 : "=r"(remote)
+                                 : "r"(smem_addr(&cl_slots[(b * 32 + lane) * V + v])), "r"(0));
+                    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "r"(pk.x),
+                                 "r"(pk.y), "r"(pk.z), "r"(pk.w)
+                                 : "memory");
+                }
+            }
+            cluster_barrier();
+            if (b == 0 && y == 0 && active) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    Cand<Tag> m = unpack_cand<Tag, OP>(cl_slots[(0 * 32 + lane) * V + v]);
+                    for (int k = 1; k < C; ++k) m = merge<Tag, OP>(m, unpack_cand<Tag, OP>(cl_slots[(k * 32 + lane) * V + v]));
+                    c[v] = m;
+                }
+            }
+        }
+        if (b == 0 && y == 0 && active) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                if (i0 + v < inner) {
+                    out_idx[o * inner + i0 + v] = c[v].i;
+                    if (out_val) out_val[o * inner + i0 + v] = c[v].v;
+                }
+            }
+        }
+        __syncthreads();  // the CTA merge slots are reused by the next outer index
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Per-warp streaming through shared memory with bulk copies.
 // ---------------------------------------------------------------------------
 constexpr int kMaxStreamWarps = 32;
@@ -837,6 +976,81 @@ cudaError_t launch_stream_t(const argr_plan& p, const Problem& pr) {
     }
 }
 
+template <class Tag, int OP, int V, int U>
+cudaError_t launch_axis_vu(const argr_plan& p, const Problem& pr) {
+    using R = typename Tag::raw;
+    auto kern = axis_kernel<Tag, OP, V, U>;
+    const int Y = p.block / 32;
+    const int C = p.cluster > 1 ? p.cluster : 1;
+    const size_t smem = static_cast<size_t>(Y + (C > 1 ? C : 0)) * 32 * V * sizeof(uint4);
+    static thread_local size_t smem_set = 0;
+    if (smem > 48 * 1024 && smem > smem_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        smem_set = smem;
+    }
+    if (C > 8) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    const int64_t tiles = (pr.inner + 32 * V - 1) / (32 * V);
+    const dim3 grid(static_cast<unsigned>(C), static_cast<unsigned>(tiles), static_cast<unsigned>(p.grid_rows));
+    if (C > 1) {
+        // Refuse a cluster shape the device cannot co-schedule (checked once per shape).
+        static thread_local int checked_block = 0, checked_cluster = 0, checked_ok = 0;
+        if (checked_block != p.block || checked_cluster != C) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = grid;
+            cfg.blockDim = dim3(p.block);
+            cfg.dynamicSmemBytes = smem;
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = static_cast<unsigned>(C);
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+            if (e != cudaSuccess) return e;
+            checked_block = p.block;
+            checked_cluster = C;
+            checked_ok = n > 0;
+        }
+        if (!checked_ok) return cudaErrorInvalidClusterSize;  // reported as ARGR_EUNSUPPORTED
+    }
+    return launch_ex_smem(kern, grid, dim3(p.block), C, smem, p, pr.stream, static_cast<const R*>(pr.x), pr.rows,
+                          pr.cols, pr.inner, pr.out_idx, static_cast<R*>(pr.out_val));
+}
+
+template <class Tag, int OP, int V>
+cudaError_t launch_axis_v(const argr_plan& p, const Problem& pr) {
+    switch (p.unroll) {
+        case 1: return launch_axis_vu<Tag, OP, V, 1>(p, pr);
+        case 2: return launch_axis_vu<Tag, OP, V, 2>(p, pr);
+        case 4: return launch_axis_vu<Tag, OP, V, 4>(p, pr);
+        case 8: return launch_axis_vu<Tag, OP, V, 8>(p, pr);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <class Tag, int OP>
+cudaError_t launch_axis_op(const argr_plan& p, const Problem& pr) {
+    constexpr int VV = sizeof(typename Tag::raw) == 8 ? 2 : 4;
+    return p.vec ? launch_axis_v<Tag, OP, VV>(p, pr) : launch_axis_v<Tag, OP, 1>(p, pr);
+}
+
+template <class Tag>
+cudaError_t launch_axis_t(const argr_plan& p, const Problem& pr) {
+    switch (pr.op) {
+        case kOpMax: return launch_axis_op<Tag, kOpMax>(p, pr);
+        case kOpMin: return launch_axis_op<Tag, kOpMin>(p, pr);
+        case kOpMaxLast: return launch_axis_op<Tag, kOpMaxLast>(p, pr);
+        case kOpMinLast: return launch_axis_op<Tag, kOpMinLast>(p, pr);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 // The device error word of this translation unit: read it, then clear it.
 static inline cudaError_t read_and_clear_error_t(unsigned* out) {
     unsigned v = 0;
@@ -863,6 +1077,9 @@ static inline cudaError_t read_and_clear_error_t(unsigned* out) {
     }                                                                                                         \
     cudaError_t launch_stream_##sfx(const argr_plan& p, const Problem& pr) {                                 \
         return launch_stream_t<Tag>(p, pr);                                                                   \
+    }                                                                                                         \
+    cudaError_t launch_axis_##sfx(const argr_plan& p, const Problem& pr) {                                   \
+        return launch_axis_t<Tag>(p, pr);                                                                     \
     }                                                                                                         \
     cudaError_t read_and_clear_error_##sfx(unsigned* out) { return read_and_clear_error_t(out); }           \
     }

@@ -125,6 +125,7 @@ extern "C" argr_status argreduce_noalloc(const void* x, argr_dtype dtype, int64_
     pr.op = op;
     pr.rows = rows;
     pr.cols = static_cast<int>(cols);
+    pr.inner = 1;
     pr.out_idx = out_idx;
     pr.out_val = out_val;
     pr.scratch = scratch;

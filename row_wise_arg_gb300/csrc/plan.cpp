@@ -173,6 +173,80 @@ argr_status make_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_
     return ARGR_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Non-last axis. A warp covers 32 * V consecutive inner positions; Y warps of
+// a CTA split R; when there are too few column tiles to fill the device, a
+// cluster of C CTAs also splits R (AcceleratedKernels.jl #138: threads along
+// the reduction and a split with a combine step when the outputs do not fill
+// the device; the combine here is distributed shared memory).
+// ---------------------------------------------------------------------------
+static int axis_vec(int dtype) { return elem_size(dtype) == 8 ? 2 : 4; }
+
+static bool axis_vec_ok(int dtype, int64_t inner, uintptr_t x_addr) {
+    const int v = axis_vec(dtype);
+    const int vb = v * elem_size(dtype);  // 16 bytes, or 8 for 16-bit elements
+    return inner % v == 0 && x_addr % vb == 0;
+}
+
+argr_status make_axis_plan(int64_t outer, int64_t reduce, int64_t inner, int dtype, int op, const argr_caps& caps,
+                           bool base_aligned, argr_plan* out) {
+    if (!out) return ARGR_EINVAL;
+    *out = argr_plan{};
+    if (inner < 1 || outer < 0 || !valid_dtype(dtype) || !valid_op(op) || reduce < 1 || reduce > INT_MAX)
+        return ARGR_EINVAL;
+    if (inner == 1) return make_plan(outer, reduce, dtype, op, caps, base_aligned, out);
+    if (!caps_ok(caps)) return ARGR_EINVAL;
+    if (outer == 0) {
+        out->path = ARGR_PATH_NONE;
+        return ARGR_OK;
+    }
+    const bool vec = base_aligned && inner % axis_vec(dtype) == 0;
+    const int64_t v = vec ? axis_vec(dtype) : 1;
+    const int64_t tiles = ceil_div(inner, 32 * v);
+    if (tiles > kMaxGridY) return ARGR_EUNSUPPORTED;
+    const int64_t slots = std::min(outer, kMaxGridY);
+    int64_t y = std::max<int64_t>(1, std::min<int64_t>(8, reduce / 32));
+    int64_t c = 1;
+    const int64_t ctas = slots * tiles;
+    const int64_t want = 2 * static_cast<int64_t>(caps.sm_count);
+    if (ctas < want && outer <= kMaxGridY && caps.max_cluster >= 2) {
+        c = std::min<int64_t>(std::min<int64_t>(16, caps.max_cluster), ceil_div(want, ctas));
+        while (c > 1 && reduce / (c * y) < 16) --c;  // keep at least 16 steps of R per warp
+    }
+    const int64_t steps = reduce / (c * y);
+    out->path = ARGR_PATH_AXIS;
+    out->block = static_cast<int32_t>(32 * y);
+    out->vec = vec ? 1 : 0;
+    out->unroll = steps >= 8 ? 8 : (steps >= 4 ? 4 : (steps >= 2 ? 2 : 1));
+    out->cluster = static_cast<int32_t>(c);
+    out->blocks_per_row = c;
+    out->grid_rows = c > 1 ? outer : slots;
+    out->flags = ARGR_PLAN_PDL;
+    out->scratch_bytes = 0;
+    return ARGR_OK;
+}
+
+argr_status check_axis_plan(const argr_plan& p, int64_t outer, int64_t reduce, int64_t inner, int dtype,
+                            const argr_caps& caps, uintptr_t x_addr) {
+    if (!valid_dtype(dtype) || outer < 0 || inner < 1 || reduce < 1 || reduce > INT_MAX) return ARGR_EINVAL;
+    if (outer == 0) return ARGR_OK;
+    if (p.path != ARGR_PATH_AXIS) return ARGR_EINVAL;
+    if (p.block < 32 || p.block > 1024 || p.block % 32 != 0) return ARGR_EINVAL;
+    if (p.flags & ~ARGR_PLAN_PDL) return ARGR_EINVAL;
+    if (p.unroll != 1 && p.unroll != 2 && p.unroll != 4 && p.unroll != 8) return ARGR_EINVAL;
+    if (p.vec != 0 && p.vec != 1) return ARGR_EINVAL;
+    if (p.vec && !axis_vec_ok(dtype, inner, x_addr)) return ARGR_EINVAL;
+    const int64_t v = p.vec ? axis_vec(dtype) : 1;
+    if (ceil_div(inner, 32 * v) > kMaxGridY) return ARGR_EUNSUPPORTED;
+    if (p.cluster < 1 || p.cluster > 16 || p.blocks_per_row != p.cluster) return ARGR_EINVAL;
+    if (p.cluster > 1 && caps.max_cluster < p.cluster) return ARGR_EUNSUPPORTED;
+    if (p.grid_rows < 1 || p.grid_rows > kMaxGridY) return ARGR_EINVAL;
+    if (p.cluster > 1 && p.grid_rows < outer) return ARGR_EINVAL;  // cluster slots are not reused across outer
+    const int64_t smem = (p.block / 32 + (p.cluster > 1 ? p.cluster : 0)) * 32 * v * 16;
+    if (smem > kMaxDynamicSmem) return ARGR_EINVAL;
+    return ARGR_OK;
+}
+
 argr_status check_plan(const argr_plan& p, int64_t rows, int64_t cols, int dtype, const argr_caps& caps,
                        bool row_aligned) {
     if (!valid_dtype(dtype) || rows < 0 || cols < 1 || cols > INT_MAX) return ARGR_EINVAL;

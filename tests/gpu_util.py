@@ -109,3 +109,33 @@ def forced_plan(path: str, **kw):
 
 def raw_equal(a: np.ndarray, b: np.ndarray) -> bool:
     return a.shape == b.shape and bool((a.view(np.uint8) == b.view(np.uint8)).all())
+
+
+def run_axis(x3: np.ndarray, dtype: str, op: str, plan=None, offset: int = 0):
+    """Reduce the middle axis of raw [outer, R, inner] data on the device
+    through argreduce_axis(); returns (idx [outer, inner], val raw)."""
+    t = torch()
+    outer, R, inner = x3.shape
+    xd, _keep = to_device(x3.reshape(outer, R * inner), dtype, offset=offset, guard=64)
+    n = outer * inner
+    idx_buf, val_buf, g = alloc_out(n, dtype)
+    out_idx = idx_buf[g:g + n]
+    out_val = val_buf[g:g + n]
+    A.argreduce_axis(xd.view(outer, R, inner), 1, op, dtype=dtype, out_idx=out_idx, out_val=out_val, plan=plan)
+    t.cuda.synchronize()
+    check_guards(idx_buf, val_buf, g, n)
+    raw_t = {"f32": np.float32, "f16": np.uint16, "bf16": np.uint16, "f64": np.float64}[dtype]
+    return out_idx.cpu().numpy().reshape(outer, inner), out_val.cpu().numpy().view(raw_t).reshape(outer, inner)
+
+
+def axis_plan(cluster=1, warps=4, vec=1, unroll=8, grid=None, outer=1, pdl=True):
+    p = _lib.argr_plan()
+    p.path = _lib.ARGR_PATH_AXIS
+    p.block = 32 * warps
+    p.vec = vec
+    p.unroll = unroll
+    p.cluster = cluster
+    p.blocks_per_row = cluster
+    p.grid_rows = grid if grid is not None else outer
+    p.flags = _lib.ARGR_PLAN_PDL if pdl else 0
+    return p

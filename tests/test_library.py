@@ -360,3 +360,23 @@ def test_f64_keys_and_prefilter():
                 assert (ka == kb) == equal, (hex(a), hex(b), is_min)
                 if better or equal:  # the pre-test must let every such element through
                     assert prefilter(a, kb, is_min), (hex(a), hex(b), is_min)
+
+
+def test_axis_plans():
+    caps = GB300
+    p = A.argreduce_axis_plan(7, 1000, 1, "f32", "max", caps).as_dict()
+    assert p["path_name"] != "axis"  # inner == 1: the last-axis planner
+    for outer, R, inner, dt in [(1, 100000, 1000, "f32"), (1, 1000, 100000, "f32"), (64, 512, 256, "bf16"),
+                                (128, 4096, 8, "f32"), (16, 2048, 384, "f64"), (3, 5, 7, "f16")]:
+        d = A.argreduce_axis_plan(outer, R, inner, dt, "min", caps).as_dict()
+        assert d["path_name"] == "axis" and d["scratch_bytes"] == 0
+        assert 1 <= d["cluster"] <= 16 and d["block"] % 32 == 0 and d["block"] <= 1024
+        if d["cluster"] > 1:
+            assert d["grid_rows"] == outer
+        v = (2 if dt == "f64" else 4) if d["vec"] else 1
+        tiles = -(-inner // (32 * v))
+        assert (d["grid_rows"] * tiles * d["cluster"]) >= min(2 * 152, d["grid_rows"] * tiles)
+    with pytest.raises(A.ArgreduceError):
+        A.argreduce_axis_plan(1, 0, 5, "f32", "max", caps)
+    assert _lib.argreduce_axis_raw(0x10000, "f32", 0, 10, 5, "max", 0x10000, 0, 0, 0, 0) == _lib.ARGR_OK
+    assert _lib.argreduce_axis_raw(0x10000, "f32", 2, 10, 0, "max", 0x10000, 0, 0, 0, 0) == _lib.ARGR_EINVAL

@@ -170,10 +170,11 @@ class Case:
     recipe: str
     seed: int
     variant: str = ""
+    inner: int = 1  # > 1: reduce the middle axis of [rows (outer), cols (reduce), inner]
 
     @property
     def nbytes(self) -> int:
-        return self.rows * self.cols * ELEM_SIZE[self.dtype]
+        return self.rows * self.cols * self.inner * ELEM_SIZE[self.dtype]
 
 
 def _gauss(rows: int, cols: int, sigma: float, seed: int) -> np.ndarray:
@@ -278,18 +279,36 @@ def make_small_ints(c: Case) -> np.ndarray:
     return encode(rng.integers(0, 8, size=(c.rows, c.cols)).astype(np.float32), c.dtype)
 
 
+def make_axis_mixed(c: Case) -> np.ndarray:
+    """[outer, R, inner] values ~ U(-1, 1) rounded to 1/64 (many ties along R),
+    with 0.1% of the elements replaced by special values (NaN, +-inf, +-0)."""
+    rng = np.random.Generator(np.random.PCG64(c.seed))
+    shape = (c.rows, c.cols, c.inner)
+    vals = np.round(rng.uniform(-1.0, 1.0, size=shape) * 64.0) / 64.0
+    x = encode(vals, c.dtype)
+    a = alphabet(c.dtype)
+    n = x.size
+    k = max(1, n // 1000)
+    pos = rng.integers(0, n, size=k)
+    flat = x.reshape(-1)
+    flat[pos] = a[rng.integers(0, len(a), size=k)]
+    return x
+
+
 RECIPES = {
     "logits": make_logits_1,
     "planted": make_planted,
     "batch_logits": make_batch_logits,
     "uniform_special": make_uniform_special,
     "small_ints": make_small_ints,
+    "axis_mixed": make_axis_mixed,
 }
 
 
 def make(c: Case) -> np.ndarray:
     x = RECIPES[c.recipe](c)
-    assert x.shape == (c.rows, c.cols) and x.flags.c_contiguous
+    shape = (c.rows, c.cols) if c.inner == 1 else (c.rows, c.cols, c.inner)
+    assert x.shape == shape and x.flags.c_contiguous
     return x
 
 
@@ -320,13 +339,21 @@ def config_cases(k: int) -> List[Case]:
     elif k == 5:
         for rows, cols in ((65536, 64), (4096, 8), (4096, 128)):
             out.append(Case(f"narrow_{rows}x{cols}_f32_max", rows, cols, "f32", "max", "small_ints", 5001))
+    elif k == 6:
+        # Reduction over a non-last axis [outer, R, inner] (the next widening of the path):
+        # column ArgMax/ArgMin of tall and wide matrices, a batched middle axis, a small inner extent.
+        out.append(Case("axis_1x100000x1000_f32_max", 1, 100000, "f32", "max", "axis_mixed", 6001, inner=1000))
+        out.append(Case("axis_1x1000x100000_f32_min", 1, 1000, "f32", "min", "axis_mixed", 6002, inner=100000))
+        out.append(Case("axis_64x512x256_bf16_max", 64, 512, "bf16", "max", "axis_mixed", 6003, inner=256))
+        out.append(Case("axis_128x4096x8_f32_max", 128, 4096, "f32", "max", "axis_mixed", 6004, inner=8))
+        out.append(Case("axis_16x2048x384_f64_min", 16, 2048, "f64", "min", "axis_mixed", 6005, inner=384))
     else:
         raise ValueError(k)
     return out
 
 
-def all_cases() -> Iterator[Tuple[int, Case]]:
-    for k in range(1, 6):
+def all_cases(groups=range(1, 6)) -> Iterator[Tuple[int, Case]]:
+    for k in groups:
         for c in config_cases(k):
             yield k, c
 
