@@ -68,9 +68,10 @@ typedef enum {
                               the last CTA to arrive for a row reduces the partials */
     ARGR_PATH_CLUSTER = 3, /* one thread-block cluster of `cluster` CTAs per row, merged
                               through distributed shared memory; no scratch */
-    ARGR_PATH_AXIS = 5,    /* non-last axis (argreduce_axis): a warp covers 32 lanes x V consecutive
-                              inner positions (`vec`: V-element vectors), the CTA's block/32 warps
-                              split R, and a cluster of `cluster` CTAs (1 = none) splits it further */
+    ARGR_PATH_AXIS = 5,    /* non-last axis (argreduce_axis): a warp is `group` column lanes (each
+                              V consecutive inner positions, `vec`: V-element vectors) by 32/group
+                              lanes along R; the CTA's block/32 warps split R, and a cluster of
+                              `cluster` CTAs (1 = none) splits it further. unroll 4 or 8 */
     ARGR_PATH_STREAM = 4   /* every warp streams a contiguous range of rows through its own
                               `stages` shared-memory buffers of `stage_bytes`, filled by bulk
                               (TMA) copies; `group` lanes per row for rows that fit a buffer,
@@ -105,7 +106,7 @@ typedef struct {
 typedef struct {
     int32_t path;           /* argr_path */
     int32_t block;          /* threads per CTA: multiple of 32, 32..1024 */
-    int32_t group;          /* ROWS / STREAM: lanes per row, power of two 1..32 */
+    int32_t group;          /* ROWS / STREAM: lanes per row; AXIS: column lanes per warp; power of two 1..32 */
     int32_t vec;            /* 1: 16-byte vector loads (ROWS needs every row 16-byte aligned) */
     int32_t unroll;         /* loads in flight per thread per step: ROWS 4 or 8; SPLIT/CLUSTER 1,2,4,8 */
     int32_t cluster;        /* CLUSTER: CTAs per cluster, 2..16 */

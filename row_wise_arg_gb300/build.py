@@ -30,8 +30,8 @@ NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-
                      "-I" + INCLUDE, "-I" + CSRC]
 
 SOURCES = ["api.cpp", "plan.cpp", "kernels_f32.cu", "kernels_f16.cu", "kernels_bf16.cu", "kernels_f64.cu",
-           "noalloc.cu"]
-HEADERS = ["device_common.cuh", "kernels_impl.cuh", "internal.h"]
+           "axis_f32.cu", "axis_f16.cu", "axis_bf16.cu", "axis_f64.cu", "noalloc.cu"]
+HEADERS = ["device_common.cuh", "kernels_impl.cuh", "internal.h", "tma.cuh"]
 
 
 def nvcc() -> str:

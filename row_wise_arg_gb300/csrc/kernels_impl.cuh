@@ -264,6 +264,18 @@ __device__ __forceinline__ void cluster_barrier() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Distributed shared memory of another CTA may only be accessed once that CTA
+// is running. Every cluster kernel arrives on the cluster barrier when it
+// starts (cluster_started_arrive) and completes that phase (cluster_started_wait)
+// before its first remote access; by then all CTAs have long arrived, so the
+// wait costs nothing on the critical path.
+__device__ __forceinline__ void cluster_started_arrive() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_started_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 template <class Tag, int OP, int U>
 __global__ void __launch_bounds__(1024)
 cluster_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int64_t* __restrict__ out_idx,
@@ -274,6 +286,8 @@ cluster_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, 
     const int nb = gridDim.x;   // the cluster spans the grid's x dimension
     const int b = blockIdx.x;   // == rank in the cluster
     int parity = 0;
+    bool started = false;
+    cluster_started_arrive();
     grid_dependency_wait();
     allow_dependents();
     for (int64_t r = blockIdx.y; r < rows; r += gridDim.y, parity ^= 1) {
@@ -282,6 +296,10 @@ cluster_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, 
         const Cand<Tag> seed = make_cand<Tag, OP>(x0, 0);
         Cand<Tag> c = scan_share<Tag, OP, U>(row, cols, b, nb, x0);
         c = block_merge<Tag, OP>(c, smem, seed);
+        if (!started) {  // every CTA of the cluster is running before the first push
+            cluster_started_wait();
+            started = true;
+        }
         if (threadIdx.x == 0) {
             const uint4 p = pack_cand<Tag>(c);
             unsigned remote;
@@ -305,6 +323,7 @@ cluster_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, 
         }
         __syncthreads();
     }
+    if (!started) cluster_started_wait();  // complete the start phase even with no rows
 }
 
 // ---------------------------------------------------------------------------
@@ -340,6 +359,8 @@ cluster_bulk_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int c
     const int nt = blockDim.x;
     const unsigned buf = smem_u32(bulk_smem);
     const unsigned bar0 = smem_u32(bars);
+    bool started = false;
+    cluster_started_arrive();
     if (t == 0) {
         for (int p = 0; p < kBulkMaxPieces; ++p) mbar_init(bar0 + 8 * p, 1);
         mbar_init_fence();
@@ -395,6 +416,10 @@ cluster_bulk_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int c
         }
         if (b == nb - 1 && t < cols - tail0) visit<Tag, OP>(c, ld_scalar(row + tail0 + t), tail0 + t);
         c = block_merge<Tag, OP>(c, smem, seed);
+        if (!started) {  // every CTA of the cluster is running before the first push
+            cluster_started_wait();
+            started = true;
+        }
         if (t == 0) {
             const uint4 pk = pack_cand<Tag>(c);
             unsigned remote;
@@ -420,6 +445,7 @@ cluster_bulk_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int c
             if (t == 0) pending = 0;
         }
     }
+    if (!started) cluster_started_wait();  // complete the start phase even with no rows
     if (abort && t == 0) {
         // Copies still in flight into this CTA's buffer: wait for them, bounded.
         for (int p = 0; p < kBulkMaxPieces; ++p)
@@ -430,13 +456,17 @@ cluster_bulk_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int c
 // ---------------------------------------------------------------------------
 // Reduction over a non-last axis: x[outer][R][inner] over R.
 //
-// A warp owns 32 * V consecutive inner positions (V per lane: a 16-byte vector
-// for 4- and 8-byte elements, 8 bytes for 16-bit ones, one element when the
-// columns are not aligned), so every step along R reads one contiguous
-// segment. The Y warps of a CTA take contiguous parts of R and merge per
-// column through shared memory; with a cluster of C CTAs, R is first cut into
-// C parts and the CTAs merge through distributed shared memory into CTA 0.
-// grid = (C, column tiles, outer slots); outer loops over the slots when C == 1.
+// A warp is CG column lanes by 32/CG lanes along R. Column lane cl owns V
+// consecutive inner positions (V per lane: a 16-byte vector for 4- and 8-byte
+// elements, 8 bytes for 16-bit ones, one element when the columns are not
+// aligned), so a CTA tile is CG * V columns and each step along R reads
+// segments of CG * V elements. The R lanes of a column take interleaved steps
+// of the warp's part of R and merge with shuffles; the Y warps of a CTA take
+// contiguous parts of R and merge per column through shared memory; with a
+// cluster of C CTAs, R is first cut into C parts and the CTAs merge through
+// distributed shared memory into CTA 0. Every lane visits its steps in
+// increasing r. grid = (C, column tiles, outer slots); outer loops over the
+// slots when C == 1.
 // ---------------------------------------------------------------------------
 template <typename R, int V>
 struct AxisVec;
@@ -469,91 +499,114 @@ struct AxisVec<uint16_t, 4> {
     }
 };
 
-template <class Tag, int OP, int V, int U>
+template <class Tag, int OP, int V, int U, int CG>
 __global__ void __launch_bounds__(1024)
 axis_kernel(const typename Tag::raw* __restrict__ x, int64_t outer, int nred, int64_t inner,
             int64_t* __restrict__ out_idx, typename Tag::raw* __restrict__ out_val) {
     using R = typename Tag::raw;
-    extern __shared__ __align__(16) uint4 axis_smem[];  // [Y][32][V] CTA merge, then [C][32][V] cluster slots
+    constexpr int RG = 32 / CG;  // lanes of a warp along R for each column lane
+    extern __shared__ __align__(16) uint4 axis_smem[];  // [Y][CG][V] CTA merge, then [C][CG][V] cluster slots
     grid_dependency_wait();
     allow_dependents();
     const int lane = threadIdx.x & 31;
+    const int cl = lane % CG;   // column lane
+    const int rl = lane / CG;   // R lane
     const int y = threadIdx.x >> 5;
     const int Y = blockDim.x >> 5;
     const int C = gridDim.x;
     const int b = blockIdx.x;  // rank in the cluster (the cluster spans x)
     uint4* cta_slots = axis_smem;
-    uint4* cl_slots = axis_smem + Y * 32 * V;
-    const int64_t i0 = (static_cast<int64_t>(blockIdx.y) * 32 + lane) * V;  // this lane's first column
+    uint4* cl_slots = axis_smem + Y * CG * V;
+    bool started = false;
+    if (C > 1) cluster_started_arrive();
+    const int64_t i0 = (static_cast<int64_t>(blockIdx.y) * CG + cl) * V;  // this lane's first column
     const bool active = i0 < inner;
-    // This warp's part of R: CTA part b of C, then warp part y of Y.
+    // This warp's part of R: CTA part b of C, then warp part y of Y; its R
+    // lanes take every RG-th step of that part.
     const int64_t cb = static_cast<int64_t>(nred) * b / C, ce = static_cast<int64_t>(nred) * (b + 1) / C;
     const int rs = static_cast<int>(cb + (ce - cb) * y / Y);
     const int re = static_cast<int>(cb + (ce - cb) * (y + 1) / Y);
     for (int64_t o = blockIdx.z; o < outer; o += gridDim.z) {
         const R* col = x + (o * nred) * inner + i0;
         Cand<Tag> c[V];
-        if (active) {
+        {
             R v0[V];
-            AxisVec<R, V>::load(col, v0);  // row r = 0 seeds every candidate
+            if (active) AxisVec<R, V>::load(col, v0);  // row r = 0 seeds every candidate
 #pragma unroll
-            for (int v = 0; v < V; ++v) c[v] = make_cand<Tag, OP>(v0[v], 0);
-            int r = rs;
+            for (int v = 0; v < V; ++v) c[v] = make_cand<Tag, OP>(active ? v0[v] : R(0), 0);
+        }
+        if (active) {
+            int r = rs + rl;
             while (r < re) {
-                const int rem = re - r;
+                const int rem = re - r;  // > 0
                 R buf[U][V];
 #pragma unroll
                 for (int u = 0; u < U; ++u)
-                    if (u < rem) AxisVec<R, V>::load(col + static_cast<int64_t>(r + u) * inner, buf[u]);
+                    if (u * RG < rem) AxisVec<R, V>::load(col + static_cast<int64_t>(r + u * RG) * inner, buf[u]);
 #pragma unroll
                 for (int u = 0; u < U; ++u)
-                    if (u < rem) {
+                    if (u * RG < rem) {
 #pragma unroll
-                        for (int v = 0; v < V; ++v) visit<Tag, OP>(c[v], buf[u][v], r + u);
+                        for (int v = 0; v < V; ++v) visit<Tag, OP>(c[v], buf[u][v], r + u * RG);
                     }
-                if (rem <= U) break;
-                r += U;
+                if (rem <= U * RG) break;
+                r += U * RG;
+            }
+        }
+        // Merge the R lanes of each column lane (lanes cl, cl + CG, ...).
+#pragma unroll
+        for (int off = CG; off < 32; off <<= 1) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+                const Cand<Tag> other = make_cand<Tag, OP>(shfl_xor_raw(0xffffffffu, c[v].v, off, 32),
+                                                           __shfl_xor_sync(0xffffffffu, c[v].i, off, 32));
+                c[v] = merge<Tag, OP>(c[v], other);
             }
         }
         // Merge the Y warps of this CTA, column by column (warp 0).
-        if (active) {
+        if (rl == 0 && active) {
 #pragma unroll
-            for (int v = 0; v < V; ++v) cta_slots[(y * 32 + lane) * V + v] = pack_cand<Tag>(c[v]);
+            for (int v = 0; v < V; ++v) cta_slots[(y * CG + cl) * V + v] = pack_cand<Tag>(c[v]);
         }
         __syncthreads();
-        if (y == 0 && active) {
+        const bool writer = y == 0 && rl == 0 && active;
+        if (writer) {
 #pragma unroll
             for (int v = 0; v < V; ++v) {
                 Cand<Tag> m = c[v];
-                for (int w = 1; w < Y; ++w) m = merge<Tag, OP>(m, unpack_cand<Tag, OP>(cta_slots[(w * 32 + lane) * V + v]));
+                for (int w = 1; w < Y; ++w) m = merge<Tag, OP>(m, unpack_cand<Tag, OP>(cta_slots[(w * CG + cl) * V + v]));
                 c[v] = m;
             }
         }
         if (C > 1) {
-            if (y == 0 && active) {
+            if (!started) {  // every CTA of the cluster is running before the first push
+                cluster_started_wait();
+                started = true;
+            }
+            if (writer) {
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
                     const uint4 pk = pack_cand<Tag>(c[v]);
                     unsigned remote;
                     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
                                  : "=r"(remote)
-                                 : "r"(smem_addr(&cl_slots[(b * 32 + lane) * V + v])), "r"(0));
+                                 : "r"(smem_addr(&cl_slots[(b * CG + cl) * V + v])), "r"(0));
                     asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "r"(pk.x),
                                  "r"(pk.y), "r"(pk.z), "r"(pk.w)
                                  : "memory");
                 }
             }
             cluster_barrier();
-            if (b == 0 && y == 0 && active) {
+            if (b == 0 && writer) {
 #pragma unroll
                 for (int v = 0; v < V; ++v) {
-                    Cand<Tag> m = unpack_cand<Tag, OP>(cl_slots[(0 * 32 + lane) * V + v]);
-                    for (int k = 1; k < C; ++k) m = merge<Tag, OP>(m, unpack_cand<Tag, OP>(cl_slots[(k * 32 + lane) * V + v]));
+                    Cand<Tag> m = unpack_cand<Tag, OP>(cl_slots[cl * V + v]);
+                    for (int k = 1; k < C; ++k) m = merge<Tag, OP>(m, unpack_cand<Tag, OP>(cl_slots[(k * CG + cl) * V + v]));
                     c[v] = m;
                 }
             }
         }
-        if (b == 0 && y == 0 && active) {
+        if (b == 0 && writer) {
 #pragma unroll
             for (int v = 0; v < V; ++v) {
                 if (i0 + v < inner) {
@@ -564,6 +617,7 @@ axis_kernel(const typename Tag::raw* __restrict__ x, int64_t outer, int nred, in
         }
         __syncthreads();  // the CTA merge slots are reused by the next outer index
     }
+    if (C > 1 && !started) cluster_started_wait();  // complete the start phase even with no work
 }
 
 // ---------------------------------------------------------------------------
@@ -976,13 +1030,13 @@ cudaError_t launch_stream_t(const argr_plan& p, const Problem& pr) {
     }
 }
 
-template <class Tag, int OP, int V, int U>
-cudaError_t launch_axis_vu(const argr_plan& p, const Problem& pr) {
+template <class Tag, int OP, int V, int U, int CG>
+cudaError_t launch_axis_vug(const argr_plan& p, const Problem& pr) {
     using R = typename Tag::raw;
-    auto kern = axis_kernel<Tag, OP, V, U>;
+    auto kern = axis_kernel<Tag, OP, V, U, CG>;
     const int Y = p.block / 32;
     const int C = p.cluster > 1 ? p.cluster : 1;
-    const size_t smem = static_cast<size_t>(Y + (C > 1 ? C : 0)) * 32 * V * sizeof(uint4);
+    const size_t smem = static_cast<size_t>(Y + (C > 1 ? C : 0)) * CG * V * sizeof(uint4);
     static thread_local size_t smem_set = 0;
     if (smem > 48 * 1024 && smem > smem_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -993,7 +1047,7 @@ cudaError_t launch_axis_vu(const argr_plan& p, const Problem& pr) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
-    const int64_t tiles = (pr.inner + 32 * V - 1) / (32 * V);
+    const int64_t tiles = (pr.inner + CG * V - 1) / (CG * V);
     const dim3 grid(static_cast<unsigned>(C), static_cast<unsigned>(tiles), static_cast<unsigned>(p.grid_rows));
     if (C > 1) {
         // Refuse a cluster shape the device cannot co-schedule (checked once per shape).
@@ -1023,15 +1077,22 @@ cudaError_t launch_axis_vu(const argr_plan& p, const Problem& pr) {
                           pr.cols, pr.inner, pr.out_idx, static_cast<R*>(pr.out_val));
 }
 
-template <class Tag, int OP, int V>
-cudaError_t launch_axis_v(const argr_plan& p, const Problem& pr) {
-    switch (p.unroll) {
-        case 1: return launch_axis_vu<Tag, OP, V, 1>(p, pr);
-        case 2: return launch_axis_vu<Tag, OP, V, 2>(p, pr);
-        case 4: return launch_axis_vu<Tag, OP, V, 4>(p, pr);
-        case 8: return launch_axis_vu<Tag, OP, V, 8>(p, pr);
+template <class Tag, int OP, int V, int U>
+cudaError_t launch_axis_vu(const argr_plan& p, const Problem& pr) {
+    switch (p.group) {
+        case 1: return launch_axis_vug<Tag, OP, V, U, 1>(p, pr);
+        case 2: return launch_axis_vug<Tag, OP, V, U, 2>(p, pr);
+        case 4: return launch_axis_vug<Tag, OP, V, U, 4>(p, pr);
+        case 8: return launch_axis_vug<Tag, OP, V, U, 8>(p, pr);
+        case 16: return launch_axis_vug<Tag, OP, V, U, 16>(p, pr);
+        case 32: return launch_axis_vug<Tag, OP, V, U, 32>(p, pr);
         default: return cudaErrorInvalidValue;
     }
+}
+
+template <class Tag, int OP, int V>
+cudaError_t launch_axis_v(const argr_plan& p, const Problem& pr) {
+    return p.unroll == 8 ? launch_axis_vu<Tag, OP, V, 8>(p, pr) : launch_axis_vu<Tag, OP, V, 4>(p, pr);
 }
 
 template <class Tag, int OP>
@@ -1078,8 +1139,11 @@ static inline cudaError_t read_and_clear_error_t(unsigned* out) {
     cudaError_t launch_stream_##sfx(const argr_plan& p, const Problem& pr) {                                 \
         return launch_stream_t<Tag>(p, pr);                                                                   \
     }                                                                                                         \
-    cudaError_t launch_axis_##sfx(const argr_plan& p, const Problem& pr) {                                   \
-        return launch_axis_t<Tag>(p, pr);                                                                     \
-    }                                                                                                         \
     cudaError_t read_and_clear_error_##sfx(unsigned* out) { return read_and_clear_error_t(out); }           \
+    }
+
+// The non-last-axis launcher lives in its own translation unit per type.
+#define ARGR_DEFINE_AXIS_LAUNCHER(sfx, Tag)                                                                  \
+    namespace argr {                                                                                          \
+    cudaError_t launch_axis_##sfx(const argr_plan& p, const Problem& pr) { return launch_axis_t<Tag>(p, pr); } \
     }

@@ -174,11 +174,13 @@ argr_status make_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_
 }
 
 // ---------------------------------------------------------------------------
-// Non-last axis. A warp covers 32 * V consecutive inner positions; Y warps of
-// a CTA split R; when there are too few column tiles to fill the device, a
-// cluster of C CTAs also splits R (AcceleratedKernels.jl #138: threads along
-// the reduction and a split with a combine step when the outputs do not fill
-// the device; the combine here is distributed shared memory).
+// Non-last axis. A warp is CG column lanes (V inner positions each) by 32/CG
+// lanes along R; Y warps of a CTA split R; when the grid still has too few
+// warps, a cluster of C CTAs also splits R (AcceleratedKernels.jl #138:
+// threads along the reduction and a split with a combine step when the
+// outputs do not fill the device; the combine here is distributed shared
+// memory). The rules below reproduce the best of a sweep of CG, Y and C on
+// GB300 for tall, wide, batched, narrow-inner and binary64 shapes.
 // ---------------------------------------------------------------------------
 static int axis_vec(int dtype) { return elem_size(dtype) == 8 ? 2 : 4; }
 
@@ -202,22 +204,35 @@ argr_status make_axis_plan(int64_t outer, int64_t reduce, int64_t inner, int dty
     }
     const bool vec = base_aligned && inner % axis_vec(dtype) == 0;
     const int64_t v = vec ? axis_vec(dtype) : 1;
-    const int64_t tiles = ceil_div(inner, 32 * v);
+    const int64_t es = elem_size(dtype);
+    const int64_t sms = caps.sm_count;
+    // Column lanes: from a full warp of columns (or as many as the columns
+    // need) down to 32-byte segments per step along R, halving while the
+    // grid would have fewer than 4 CTAs per SM; the other lanes go along R.
+    int64_t cg = 32;
+    while (cg > 1 && (cg / 2) * v >= inner) cg >>= 1;
+    const int64_t cg_min = std::max<int64_t>(1, 32 / (v * es));
+    while (cg > cg_min && std::min(outer, kMaxGridY) * ceil_div(inner, cg * v) < 4 * sms) cg >>= 1;
+    const int64_t tiles = ceil_div(inner, cg * v);
     if (tiles > kMaxGridY) return ARGR_EUNSUPPORTED;
     const int64_t slots = std::min(outer, kMaxGridY);
-    int64_t y = std::max<int64_t>(1, std::min<int64_t>(8, reduce / 32));
-    int64_t c = 1;
+    const int64_t rg = 32 / cg;
     const int64_t ctas = slots * tiles;
-    const int64_t want = 2 * static_cast<int64_t>(caps.sm_count);
-    if (ctas < want && outer <= kMaxGridY && caps.max_cluster >= 2) {
-        c = std::min<int64_t>(std::min<int64_t>(16, caps.max_cluster), ceil_div(want, ctas));
-        while (c > 1 && reduce / (c * y) < 16) --c;  // keep at least 16 steps of R per warp
+    // Warps along R: enough for ~16 warps per SM over the grid, each R lane
+    // keeping at least 16 steps.
+    int64_t y = ceil_div(16 * sms, ctas);
+    y = std::max<int64_t>(1, std::min<int64_t>({y, 32, reduce / (rg * 16)}));
+    int64_t c = 1;
+    if (ctas * y < 4 * sms && outer <= kMaxGridY && caps.max_cluster >= 2) {
+        // Still too few warps: a cluster of CTAs splits R further.
+        c = std::min<int64_t>(std::min<int64_t>(16, caps.max_cluster), ceil_div(16 * sms, ctas * y));
+        while (c > 1 && reduce / (c * y * rg) < 16) --c;
     }
-    const int64_t steps = reduce / (c * y);
     out->path = ARGR_PATH_AXIS;
     out->block = static_cast<int32_t>(32 * y);
+    out->group = static_cast<int32_t>(cg);
     out->vec = vec ? 1 : 0;
-    out->unroll = steps >= 8 ? 8 : (steps >= 4 ? 4 : (steps >= 2 ? 2 : 1));
+    out->unroll = 8;
     out->cluster = static_cast<int32_t>(c);
     out->blocks_per_row = c;
     out->grid_rows = c > 1 ? outer : slots;
@@ -233,16 +248,18 @@ argr_status check_axis_plan(const argr_plan& p, int64_t outer, int64_t reduce, i
     if (p.path != ARGR_PATH_AXIS) return ARGR_EINVAL;
     if (p.block < 32 || p.block > 1024 || p.block % 32 != 0) return ARGR_EINVAL;
     if (p.flags & ~ARGR_PLAN_PDL) return ARGR_EINVAL;
-    if (p.unroll != 1 && p.unroll != 2 && p.unroll != 4 && p.unroll != 8) return ARGR_EINVAL;
+    if (p.unroll != 4 && p.unroll != 8) return ARGR_EINVAL;
     if (p.vec != 0 && p.vec != 1) return ARGR_EINVAL;
     if (p.vec && !axis_vec_ok(dtype, inner, x_addr)) return ARGR_EINVAL;
+    const int g = p.group;
+    if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16 && g != 32) return ARGR_EINVAL;
     const int64_t v = p.vec ? axis_vec(dtype) : 1;
-    if (ceil_div(inner, 32 * v) > kMaxGridY) return ARGR_EUNSUPPORTED;
+    if (ceil_div(inner, g * v) > kMaxGridY) return ARGR_EUNSUPPORTED;
     if (p.cluster < 1 || p.cluster > 16 || p.blocks_per_row != p.cluster) return ARGR_EINVAL;
     if (p.cluster > 1 && caps.max_cluster < p.cluster) return ARGR_EUNSUPPORTED;
     if (p.grid_rows < 1 || p.grid_rows > kMaxGridY) return ARGR_EINVAL;
     if (p.cluster > 1 && p.grid_rows < outer) return ARGR_EINVAL;  // cluster slots are not reused across outer
-    const int64_t smem = (p.block / 32 + (p.cluster > 1 ? p.cluster : 0)) * 32 * v * 16;
+    const int64_t smem = (p.block / 32 + (p.cluster > 1 ? p.cluster : 0)) * g * v * 16;
     if (smem > kMaxDynamicSmem) return ARGR_EINVAL;
     return ARGR_OK;
 }

@@ -128,9 +128,10 @@ def run_axis(x3: np.ndarray, dtype: str, op: str, plan=None, offset: int = 0):
     return out_idx.cpu().numpy().reshape(outer, inner), out_val.cpu().numpy().view(raw_t).reshape(outer, inner)
 
 
-def axis_plan(cluster=1, warps=4, vec=1, unroll=8, grid=None, outer=1, pdl=True):
+def axis_plan(cluster=1, warps=4, vec=1, unroll=8, grid=None, outer=1, pdl=True, cg=32):
     p = _lib.argr_plan()
     p.path = _lib.ARGR_PATH_AXIS
+    p.group = cg
     p.block = 32 * warps
     p.vec = vec
     p.unroll = unroll

@@ -53,13 +53,14 @@ def test_axis_forced_geometries(dtype):
         x = fuzz3(dtype, outer, R, inner, seed=outer * 1000 + R + inner)
         for op in W.ALL_OPS:
             check_axis(x, dtype, op)  # the planner's choice
-            for cluster, warps, unroll in ((1, 1, 1), (1, 4, 8), (2, 3, 2), (5, 2, 4), (16, 1, 8)):
-                check_axis(x, dtype, op, plan=axis_plan(cluster, warps, vec=0, unroll=unroll, outer=outer))
+            for cluster, warps, unroll, cg in ((1, 1, 4, 32), (1, 4, 8, 8), (2, 3, 4, 1), (5, 2, 4, 4),
+                                               (16, 1, 8, 16), (3, 2, 8, 2)):
+                check_axis(x, dtype, op, plan=axis_plan(cluster, warps, vec=0, unroll=unroll, outer=outer, cg=cg))
                 if inner % v == 0:
                     check_axis(x, dtype, op, plan=axis_plan(cluster, warps, vec=1, unroll=unroll, outer=outer,
-                                                            pdl=cluster != 2))
+                                                            pdl=cluster != 2, cg=cg))
             if outer > 1:  # fewer outer slots than outer: the CTAs loop
-                check_axis(x, dtype, op, plan=axis_plan(1, 2, vec=0, unroll=4, grid=1))
+                check_axis(x, dtype, op, plan=axis_plan(1, 2, vec=0, unroll=4, grid=1, cg=4))
             check_axis(x, dtype, op, offset=1)  # base not aligned: scalar columns
 
 
@@ -75,6 +76,8 @@ def test_axis_plan_validation():
     for bad in (axis_plan(cluster=2, warps=2, vec=0, outer=4, grid=2),  # a cluster plan may not loop over outer
                 axis_plan(cluster=17, outer=4),
                 axis_plan(cluster=1, unroll=3, outer=4),
+                axis_plan(cluster=1, unroll=2, outer=4),
+                axis_plan(cluster=1, outer=4, cg=3),
                 axis_plan(cluster=1, vec=1, outer=4)):                    # inner 6 is not a multiple of 4
         with pytest.raises(A.ArgreduceError):
             A.argreduce_axis(x, 1, "max", plan=bad)

@@ -374,7 +374,8 @@ def test_axis_plans():
         if d["cluster"] > 1:
             assert d["grid_rows"] == outer
         v = (2 if dt == "f64" else 4) if d["vec"] else 1
-        tiles = -(-inner // (32 * v))
+        assert d["group"] in (1, 2, 4, 8, 16, 32)
+        tiles = -(-inner // (d["group"] * v))
         assert (d["grid_rows"] * tiles * d["cluster"]) >= min(2 * 152, d["grid_rows"] * tiles)
     with pytest.raises(A.ArgreduceError):
         A.argreduce_axis_plan(1, 0, 5, "f32", "max", caps)
