@@ -26,9 +26,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "argreduce_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2, "f64": 3}
+DTYPE_CODE = {"f32": 0, "f16": 1, "bf16": 2, "f64": 3, "i32": 4, "i64": 5}
 OP_CODE = {"max": 0, "min": 1, "max_last": 2, "min_last": 3}
-RAW_NP = {"f32": np.float32, "f16": np.uint16, "bf16": np.uint16, "f64": np.float64}
+RAW_NP = {"f32": np.float32, "f16": np.uint16, "bf16": np.uint16, "f64": np.float64, "i32": np.int32,
+          "i64": np.int64}
 
 _lock = threading.Lock()
 _lib = None
@@ -60,6 +61,9 @@ def _load():
             lib.oracle_argreduce_axis.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                                                   ctypes.c_int64, ctypes.c_int, i64p, ctypes.c_void_p]
             lib.oracle_argreduce_axis.restype = ctypes.c_int
+            lib.oracle_cumreduce.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                             ctypes.c_int, i64p, ctypes.c_void_p]
+            lib.oracle_cumreduce.restype = ctypes.c_int
             lib.oracle_decode_f16.argtypes = [ctypes.c_uint16]
             lib.oracle_decode_f16.restype = ctypes.c_double
             lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
@@ -110,6 +114,28 @@ def argreduce_axis(x: np.ndarray, dtype: str, op: str, want_val: bool = True):
     rc = lib.oracle_argreduce_axis(x.ctypes.data_as(ctypes.c_void_p), DTYPE_CODE[dtype], outer, R, inner,
                                    OP_CODE[op], idx.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
                                    val.ctypes.data_as(ctypes.c_void_p) if val is not None else None)
+    if rc < 0:
+        raise ValueError(f"oracle rejected arguments: shape={x.shape} dtype={dtype} op={op}")
+    return idx, val
+
+
+def cumreduce(x: np.ndarray, dtype: str, op: str, want_val: bool = True):
+    """cummax ("max") / cummin ("min") with indices along the last axis of the
+    2-D raw array ``x``: for every prefix x[r, 0..j], the ArgMax (ArgMin) of
+    that prefix (ties to the earlier index). Returns ``(idx int64[rows, cols],
+    val raw[rows, cols] or None)``."""
+    lib = _load()
+    x = np.ascontiguousarray(x)
+    if x.ndim != 2:
+        raise ValueError("x must be 2-D [rows, cols]")
+    if x.dtype != RAW_NP[dtype]:
+        raise TypeError(f"{dtype} expects raw numpy dtype {RAW_NP[dtype]}, got {x.dtype}")
+    rows, cols = x.shape
+    idx = np.empty((rows, cols), dtype=np.int64)
+    val = np.empty((rows, cols), dtype=x.dtype) if want_val else None
+    rc = lib.oracle_cumreduce(x.ctypes.data_as(ctypes.c_void_p), DTYPE_CODE[dtype], rows, cols, OP_CODE[op],
+                              idx.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                              val.ctypes.data_as(ctypes.c_void_p) if val is not None else None)
     if rc < 0:
         raise ValueError(f"oracle rejected arguments: shape={x.shape} dtype={dtype} op={op}")
     return idx, val

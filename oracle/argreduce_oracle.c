@@ -185,6 +185,67 @@ int oracle_argreduce_axis(const void* x, int dtype, int64_t outer, int64_t R, in
     return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* cummax / cummin with indices (Paddle issue #79670, "Possible fixes": a   */
+/* scan with argmax semantics where ties take the earlier index). For each  */
+/* row and every position j, out[j] is the row's ArgMax (ArgMin) over       */
+/* x[0..j] by the scan above: seed (x[0], 0), replace on a strictly better  */
+/* element, so out[cols-1] equals oracle_argreduce(). Element types: the    */
+/* four floating types and, compared exactly as integers, int32 (code 4)    */
+/* and int64 (code 5). Ops 0 (max) and 1 (min).                             */
+/* ------------------------------------------------------------------------ */
+enum { ORACLE_I32 = 4, ORACLE_I64 = 5 };
+
+static size_t cum_elem_size(int dtype) {
+    if (dtype == ORACLE_I32) return 4;
+    if (dtype == ORACLE_I64) return 8;
+    return elem_size(dtype);
+}
+
+static int64_t read_int(const unsigned char* p, int dtype) {
+    if (dtype == ORACLE_I32) {
+        int32_t v;
+        memcpy(&v, p, 4);
+        return v;
+    }
+    int64_t v;
+    memcpy(&v, p, 8);
+    return v;
+}
+
+int oracle_cumreduce(const void* x, int dtype, int64_t rows, int64_t cols, int op, int64_t* out_idx,
+                     void* out_val) {
+    const size_t es = cum_elem_size(dtype);
+    if (es == 0 || (op != ORACLE_MAX && op != ORACLE_MIN)) return -1;
+    if (rows < 0 || cols < 1 || (rows > 0 && (!x || !out_idx))) return -1;
+    const int is_int = dtype == ORACLE_I32 || dtype == ORACLE_I64;
+    unsigned char* ov = (unsigned char*)out_val;
+    for (int64_t r = 0; r < rows; ++r) {
+        const unsigned char* row = (const unsigned char*)x + (size_t)r * (size_t)cols * es;
+        int64_t best_j = 0;
+        double best_f = is_int ? 0.0 : decode(row, dtype);
+        int64_t best_i = is_int ? read_int(row, dtype) : 0;
+        for (int64_t j = 0; j < cols; ++j) {
+            if (j > 0) {
+                int take;
+                if (is_int) {
+                    const int64_t v = read_int(row + (size_t)j * es, dtype);
+                    take = op == ORACLE_MAX ? v > best_i : v < best_i;
+                    if (take) best_i = v;
+                } else {
+                    const double v = decode(row + (size_t)j * es, dtype);
+                    take = better(v, best_f, op);
+                    if (take) best_f = v;
+                }
+                if (take) best_j = j;
+            }
+            out_idx[(size_t)r * (size_t)cols + (size_t)j] = best_j;
+            if (ov) memcpy(ov + ((size_t)r * (size_t)cols + (size_t)j) * es, row + (size_t)best_j * es, es);
+        }
+    }
+    return 0;
+}
+
 /* Row-parallel wrapper for timing on several host cores: rows are cut into
  * contiguous, independent ranges, one per thread, each scanned exactly as
  * above. Returns the number of threads used (>= 1), or -1 on error. */

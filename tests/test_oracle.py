@@ -476,3 +476,122 @@ def test_axis_mutant_is_caught(name, old, new):
             assert caught, f"axis mutant '{name}' survived"
         finally:
             oracle._lib = saved
+
+
+# ---------------------------------------------------------------------------
+# cummax / cummin with indices (prefix ArgMax / ArgMin).
+# ---------------------------------------------------------------------------
+CUM_DTYPES = ("f32", "f16", "bf16", "f64", "i32", "i64")
+
+
+def cum_rows(dtype, rows, cols, seed):
+    if dtype in ("i32", "i64"):
+        rng = np.random.Generator(np.random.PCG64(seed))
+        info = np.iinfo(np.int32 if dtype == "i32" else np.int64)
+        x = rng.integers(-5, 6, size=(rows, cols)).astype(np.int64)
+        ext = rng.random((rows, cols)) < 0.05
+        x = np.where(ext, np.where(rng.random((rows, cols)) < 0.5, info.min, info.max), x)
+        big = rng.random((rows, cols)) < 0.05
+        x = np.where(big, info.max - rng.integers(0, 3, size=(rows, cols)), x)  # values a double cannot tell apart
+        return x.astype(np.int32 if dtype == "i32" else np.int64)
+    return W.fuzz_rows(dtype, rows, cols, seed=seed, p_special=0.2)
+
+
+@pytest.mark.parametrize("dtype", CUM_DTYPES)
+@pytest.mark.parametrize("op", ("max", "min"))
+def test_cumreduce_prefix_equals_argreduce(dtype, op):
+    """Column j of the scan is the oracle's ArgMax/ArgMin of the prefix 0..j
+    (for the floating types), and a direct running scan in Python (ints)."""
+    x = cum_rows(dtype, 30, 41, seed=7)
+    idx, val = oracle.cumreduce(x, dtype, op)
+    assert raw_equal(val, np.take_along_axis(x, idx, axis=1))
+    if dtype in ("i32", "i64"):
+        for r in range(x.shape[0]):
+            best = 0
+            for j in range(x.shape[1]):
+                v, b = int(x[r, j]), int(x[r, best])
+                if (v > b) if op == "max" else (v < b):
+                    best = j
+                assert idx[r, j] == best
+    else:
+        for j in range(x.shape[1]):
+            pidx, _, _ = oracle.argreduce(np.ascontiguousarray(x[:, :j + 1]), dtype, op)
+            assert (idx[:, j] == pidx).all()
+            assert (idx[:, j] == closed_form(np.ascontiguousarray(x[:, :j + 1]), dtype, op)).all()
+
+
+def test_cumreduce_numpy_accumulate():
+    """NaN-free floats and ints: the values are numpy's maximum/minimum
+    accumulate, and each index is the first position reaching that value."""
+    rng = np.random.Generator(np.random.PCG64(11))
+    for dtype in ("f32", "f64", "i64", "i32"):
+        x = rng.integers(-50, 50, size=(20, 333)).astype(oracle.RAW_NP[dtype])
+        for op, acc in (("max", np.maximum), ("min", np.minimum)):
+            idx, val = oracle.cumreduce(x, dtype, op)
+            assert (val == acc.accumulate(x, axis=1)).all()
+            for r in range(x.shape[0]):
+                first = {}
+                for j, v in enumerate(x[r]):
+                    first.setdefault(v, j)
+                assert all(idx[r, j] == first[val[r, j]] for j in range(x.shape[1]))
+
+
+def test_cumreduce_golden_two_pass():
+    """Paddle issue #79670 (Possible fixes): a tiled two-pass cummax (cummax
+    inside tiles, cummax of the tile maxima, carry folded back) is bit-equal to
+    the one-pass scan. Built here with numpy on int64 data."""
+    rng = np.random.Generator(np.random.PCG64(79670))
+    x = rng.integers(-1000, 1000, size=(1, 65536)).astype(np.int64)
+    _, val = oracle.cumreduce(x, "i64", "max")
+    part = np.maximum.accumulate(x.reshape(512, 128), axis=1)
+    carry = np.maximum.accumulate(part[:, -1])
+    two_pass = np.maximum(part, np.concatenate([[np.iinfo(np.int64).min], carry[:-1]])[:, None]).reshape(1, -1)
+    assert (val == two_pass).all()
+
+
+CUM_MUTANTS = [
+    ("int ties to last", "take = op == ORACLE_MAX ? v > best_i : v < best_i;",
+     "take = op == ORACLE_MAX ? v >= best_i : v <= best_i;"),
+    ("int compared as double", "const int64_t v = read_int(row + (size_t)j * es, dtype);",
+     "const int64_t v = (int64_t)(double)read_int(row + (size_t)j * es, dtype);"),
+    ("output one late", "out_idx[(size_t)r * (size_t)cols + (size_t)j] = best_j;",
+     "out_idx[(size_t)r * (size_t)cols + (size_t)j] = j > 0 && j == best_j ? j - 1 : best_j;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", CUM_MUTANTS, ids=[m[0] for m in CUM_MUTANTS])
+def test_cum_mutant_is_caught(name, old, new):
+    import ctypes
+    if shutil.which("gcc") is None:
+        pytest.skip("no host C compiler")
+    src = open(oracle._SRC).read()
+    assert src.count(old) == 1, old
+    with tempfile.TemporaryDirectory() as d:
+        c, so = os.path.join(d, "m.c"), os.path.join(d, "libm.so")
+        open(c, "w").write(src.replace(old, new))
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", c, "-o", so, "-lm"], check=True)
+        lib = ctypes.CDLL(so)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        lib.oracle_cumreduce.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                         i64p, ctypes.c_void_p]
+        lib.oracle_argreduce.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_int, i64p, ctypes.c_void_p]
+        saved = oracle._lib
+        try:
+            class Shim:
+                pass
+            shim = Shim()
+            shim.oracle_cumreduce = lib.oracle_cumreduce
+            shim.oracle_argreduce = saved.oracle_argreduce if saved else oracle._load().oracle_argreduce
+            oracle._lib = shim
+            caught = False
+            try:
+                for dtype in CUM_DTYPES:
+                    for op in ("max", "min"):
+                        test_cumreduce_prefix_equals_argreduce(dtype, op)
+                test_cumreduce_numpy_accumulate()
+            except AssertionError:
+                caught = True
+            assert caught, f"cum mutant '{name}' survived"
+        finally:
+            oracle._lib = saved
