@@ -52,10 +52,12 @@ WORKLOADS = {
     "wide_rows_last": (-2, "the wide_rows cases with ties to the last index (ONNX select_last_index = 1)"),
     "axis": (6, "ArgMax/ArgMin over a non-last axis: [1,100000,1000], [1,1000,100000], [64,512,256] bf16, "
                 "[128,4096,8], [16,2048,384] f64"),
+    "cum": (7, "cummax/cummin with indices: [1,65536], [1,262144], [64,1024], [1024,64] int64, [4,16384] int32, "
+               "[1,65536] f32/f64, [256,256] bf16"),
 }
-DTYPE_LABEL = {"f32": "f32", "f16": "f16", "bf16": "bf16", "f64": "f64"}
+DTYPE_LABEL = {"f32": "f32", "f16": "f16", "bf16": "bf16", "f64": "f64", "i32": "i32", "i64": "i64"}
 KERNEL_OF_PATH = {"rows": "rows_kernel", "split": "split_kernel", "cluster": "cluster_kernel", "axis": "axis_kernel",
-                  "stream": "stream_kernel", "none": "none"}
+                  "stream": "stream_kernel", "cum": "cum_kernel", "none": "none"}
 
 
 def workload_cases(group: int):
@@ -65,16 +67,31 @@ def workload_cases(group: int):
     return [dataclasses.replace(c, op=c.op + "_last", name=c.name + "_last") for c in W.config_cases(-group)]
 
 
+def is_scan(c: W.Case) -> bool:
+    return c.recipe == "cum_values"
+
+
 def algo_bytes(c: W.Case, with_values: bool = False) -> int:
-    """Algorithmic bytes of one call: the input read once, int64 indices written."""
+    """Algorithmic bytes of one call: the input read once, int64 indices
+    written (one per row, per (outer, inner) column, or per element for the
+    cummax/cummin scan, which also writes one value per element)."""
     es = W.ELEM_SIZE[c.dtype]
+    if is_scan(c):
+        return c.rows * c.cols * (2 * es + 8)
     outputs = c.rows * c.inner
     return c.rows * c.cols * c.inner * es + outputs * 8 + (outputs * es if with_values else 0)
 
 
-def call(A, c: W.Case, x, out_idx, scratch, stream):
+def n_outputs(c: W.Case) -> int:
+    return c.rows * c.cols if is_scan(c) else c.rows * c.inner
+
+
+def call(A, c: W.Case, x, out_idx, scratch, stream, out_val=None):
     """One library call for case c on device data x (flat)."""
-    if c.inner > 1:
+    if is_scan(c):
+        A.argreduce_cum(x.view(c.rows, c.cols), c.op, dtype=c.dtype, out_idx=out_idx, out_val=out_val,
+                        stream=stream)
+    elif c.inner > 1:
         A.argreduce_axis(x.view(c.rows, c.cols, c.inner), 1, c.op, dtype=c.dtype, out_idx=out_idx, scratch=scratch,
                          stream=stream)
     else:
@@ -219,7 +236,10 @@ def oracle_time(cases, inputs, budget_s: float, max_calls: int = None):
     t0 = time.perf_counter()
     while True:
         c = cases[calls % len(cases)]
-        if c.inner > 1:
+        if is_scan(c):
+            oracle.cumreduce(inputs[calls % len(cases)], c.dtype, c.op, want_val=True)
+            used = 1
+        elif c.inner > 1:
             oracle.argreduce_axis(inputs[calls % len(cases)], c.dtype, c.op, want_val=False)
             used = 1
         else:
@@ -239,7 +259,8 @@ def oracle_time(cases, inputs, budget_s: float, max_calls: int = None):
 # GPU timing.
 # ---------------------------------------------------------------------------
 def to_dev(torch, x: np.ndarray, dtype: str):
-    view = {"f32": np.float32, "f16": np.int16, "bf16": np.int16, "f64": np.float64}[dtype]
+    view = {"f32": np.float32, "f16": np.int16, "bf16": np.int16, "f64": np.float64, "i32": np.int32,
+            "i64": np.int64}[dtype]
     return torch.from_numpy(np.ascontiguousarray(x).view(view)).cuda()
 
 
@@ -257,12 +278,13 @@ class GraphSet:
         need = max([A.argreduce_scratch_bytes(c.rows, c.cols, c.dtype, c.op) for c in cases] + [0])
         self.scratch.ensure(max(need, 4096), stream.cuda_stream)
         self.copies = [[x] + [x.clone() for _ in range(copies - 1)] for x in dev_inputs]
-        self.outs = [torch.empty(max(c.rows * c.inner, 1), dtype=torch.int64, device="cuda") for c in cases]
+        self.outs = [torch.empty(max(n_outputs(c), 1), dtype=torch.int64, device="cuda") for c in cases]
+        self.vals = [torch.empty_like(dev_inputs[i]) if is_scan(c) else None for i, c in enumerate(cases)]
         self.graphs = []
 
         def calls(k):
             for i, c in enumerate(cases):
-                call(A, c, self.copies[i][k], self.outs[i], self.scratch, stream)
+                call(A, c, self.copies[i][k], self.outs[i], self.scratch, stream, self.vals[i])
 
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
@@ -329,22 +351,24 @@ def e2e_time(torch, A, cases, inputs, steps, stream):
     """The public call path with host buffers: every step copies the inputs
     from pinned host memory, runs the calls and reads the indices back."""
     hosts = [torch.from_numpy(np.ascontiguousarray(x).view(
-        {"f32": np.float32, "f16": np.int16, "bf16": np.int16, "f64": np.float64}[c.dtype])).pin_memory()
+        {"f32": np.float32, "f16": np.int16, "bf16": np.int16, "f64": np.float64, "i32": np.int32,
+         "i64": np.int64}[c.dtype])).pin_memory()
         for c, x in zip(cases, inputs)]
     devs = [torch.empty_like(h, device="cuda") for h in hosts]
-    outs = [torch.empty(c.rows * c.inner, dtype=torch.int64, device="cuda") for c in cases]
-    host_out = torch.empty(sum(c.rows * c.inner for c in cases), dtype=torch.int64).pin_memory()
+    outs = [torch.empty(n_outputs(c), dtype=torch.int64, device="cuda") for c in cases]
+    vals = [torch.empty_like(d) if is_scan(c) else None for c, d in zip(cases, devs)]
+    host_out = torch.empty(sum(n_outputs(c) for c in cases), dtype=torch.int64).pin_memory()
     scratch = A.Scratch()
     h2d = sum(h.numel() * h.element_size() for h in hosts)
     d2h = host_out.numel() * 8
 
     def step():
         off = 0
-        for c, h, d, o in zip(cases, hosts, devs, outs):
+        for c, h, d, o, v in zip(cases, hosts, devs, outs, vals):
             d.copy_(h, non_blocking=True)
-            call(A, c, d.reshape(-1), o, scratch, stream)
-            host_out[off:off + c.rows * c.inner].copy_(o, non_blocking=True)
-            off += c.rows * c.inner
+            call(A, c, d.reshape(-1), o, scratch, stream, v)
+            host_out[off:off + n_outputs(c)].copy_(o, non_blocking=True)
+            off += n_outputs(c)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -436,7 +460,8 @@ def main():
     plans = {}
     kernels = set()
     for c in cases:
-        p = A.argreduce_axis_plan(c.rows, c.cols, c.inner, c.dtype, c.op).as_dict()
+        p = (A.argreduce_cum_plan(c.rows, c.cols, c.dtype, c.op) if is_scan(c) else
+             A.argreduce_axis_plan(c.rows, c.cols, c.inner, c.dtype, c.op)).as_dict()
         plans[f"{c.rows}x{c.cols}" + (f"x{c.inner}" if c.inner > 1 else "") + f"_{c.dtype}"] = {k: p[k] for k in ("path_name", "blocks_per_row", "cluster",
                                                                     "block", "unroll", "group", "flags")}
         kernels.add(KERNEL_OF_PATH[p["path_name"]])
@@ -483,15 +508,17 @@ def main():
                 if c0.variant == "dup":
                     continue
                 # each case as written, and the same rows with ties to the last index
-                for c in (c0, dataclasses.replace(c0, op=c0.op + "_last", name=c0.name + "_last")):
+                variants = [c0] if is_scan(c0) else [c0, dataclasses.replace(c0, op=c0.op + "_last",
+                                                                             name=c0.name + "_last")]
+                for c in variants:
                     n = max(20, min(4000, int(2e9 / max(c.nbytes, 1) / 50)))
                     s, n, cp, _ = time_group(torch, A, [c], [x], n, 5, stream, exact=False)
                     us = s * 1e6 / n
                     gbs = algo_bytes(c) / (s / n) / 1e9
+                    plan = (A.argreduce_cum_plan(c.rows, c.cols, c.dtype, c.op) if is_scan(c) else
+                            A.argreduce_axis_plan(c.rows, c.cols, c.inner, c.dtype, c.op))
                     table.append({"case": c.name, "us_per_call": round(us, 3), "gbs": round(gbs, 1),
-                                  "frac": round(gbs / peak, 4),
-                                  "path": A.argreduce_axis_plan(c.rows, c.cols, c.inner, c.dtype,
-                                                                c.op).as_dict()["path_name"]})
+                                  "frac": round(gbs / peak, 4), "path": plan.as_dict()["path_name"]})
             del ginputs
         result["configs"] = table
 

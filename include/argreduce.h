@@ -37,12 +37,15 @@ extern "C" {
 /* The same type as cudaStream_t. NULL is the legacy default stream. */
 typedef struct CUstream_st* argr_stream;
 
-/* Element type of x (and of out_val). */
+/* Element type of x (and of out_val). argreduce() and argreduce_axis() take
+ * the floating types; the integer types are for argreduce_cum(). */
 typedef enum {
     ARGR_F32 = 0,  /* IEEE binary32 */
     ARGR_F16 = 1,  /* IEEE binary16 */
     ARGR_BF16 = 2, /* bfloat16 (upper half of binary32) */
-    ARGR_F64 = 3   /* IEEE binary64 */
+    ARGR_F64 = 3,  /* IEEE binary64 */
+    ARGR_I32 = 4,  /* int32: argreduce_cum() only */
+    ARGR_I64 = 5   /* int64: argreduce_cum() only */
 } argr_dtype;
 
 /* ArgMax / ArgMin; ties resolve to the first index, or to the last index for
@@ -72,6 +75,8 @@ typedef enum {
                               V consecutive inner positions, `vec`: V-element vectors) by 32/group
                               lanes along R; the CTA's block/32 warps split R, and a cluster of
                               `cluster` CTAs (1 = none) splits it further. unroll 4 or 8 */
+    ARGR_PATH_CUM = 6,     /* cummax / cummin (argreduce_cum): a row in `cluster` chunks, one CTA
+                              each (1 = none), scanned in tiles of block * 7 elements */
     ARGR_PATH_STREAM = 4   /* every warp streams a contiguous range of rows through its own
                               `stages` shared-memory buffers of `stage_bytes`, filled by bulk
                               (TMA) copies; `group` lanes per row for rows that fit a buffer,
@@ -214,6 +219,30 @@ argr_status argreduce_axis_plan(int64_t outer, int64_t reduce, int64_t inner, ar
 argr_status argreduce_axis_with_plan(const argr_plan* plan, const void* x, argr_dtype dtype, int64_t outer,
                                      int64_t reduce, int64_t inner, argr_op op, int64_t* out_idx, void* out_val,
                                      void* scratch, size_t scratch_bytes, argr_stream stream);
+
+/*
+ * cummax / cummin with indices along the last axis of x[rows, cols]
+ * (op = ARGR_MAX or ARGR_MIN; the *_LAST ops return ARGR_EUNSUPPORTED).
+ * For every position j of every row: out_idx[r * cols + j] is the row's
+ * ArgMax (ArgMin) over x[r, 0..j] by the rules of argreduce() (ties keep the
+ * earlier index; a NaN after x[r, 0] is never chosen; a leading NaN gives 0
+ * everywhere), and out_val[r * cols + j] (optional) the raw bits of that
+ * element. So out_idx[r * cols + cols - 1] equals argreduce()'s result.
+ * Element types: the four floating types and ARGR_I32 / ARGR_I64 (compared
+ * as integers). Paddle issue #79670 ("Possible fixes": a scan with argmax
+ * semantics where ties take the earlier index). Needs no scratch; out_idx
+ * holds rows * cols int64. Errors as for argreduce().
+ */
+argr_status argreduce_cum(const void* x, argr_dtype dtype, int64_t rows, int64_t cols, argr_op op, int64_t* out_idx,
+                          void* out_val, argr_stream stream);
+
+/* The planner for argreduce_cum(). */
+argr_status argreduce_cum_plan(int64_t rows, int64_t cols, argr_dtype dtype, argr_op op, const argr_caps* caps,
+                               argr_plan* out);
+
+/* argreduce_cum() with an explicit ARGR_PATH_CUM plan (re-validated). */
+argr_status argreduce_cum_with_plan(const argr_plan* plan, const void* x, argr_dtype dtype, int64_t rows,
+                                    int64_t cols, argr_op op, int64_t* out_idx, void* out_val, argr_stream stream);
 
 /* Scratch bytes a given plan needs for `rows` rows. */
 size_t argreduce_plan_scratch_bytes(const argr_plan* plan, int64_t rows);

@@ -17,12 +17,14 @@ from typing import Dict, Optional, Tuple
 from . import _lib
 from ._lib import (ARGR_BF16, ARGR_F16, ARGR_F32, ARGR_F64, ARGR_MAX, ARGR_MIN,  # noqa: F401
                    ARGR_OK, ArgreduceError, DTYPE_CODES, OP_CODES, argr_caps, argr_plan, argreduce_axis_plan,
+                   argreduce_cum_plan,
                    argreduce_device_caps,
                    argreduce_plan, argreduce_plan_scratch_bytes, argreduce_read_error, argreduce_scratch_bytes,
                    argreduce_scratch_init, argreduce_status_string, argreduce_version, load, make_caps)
 
 __all__ = [
-    "argreduce", "argreduce_axis", "argreduce_axis_plan", "argmax", "argmin", "argreduce_with_plan", "argreduce_plan", "argreduce_scratch_bytes",
+    "argreduce", "argreduce_axis", "argreduce_axis_plan", "argreduce_cum", "argreduce_cum_plan", "cummax", "cummin",
+    "argmax", "argmin", "argreduce_with_plan", "argreduce_plan", "argreduce_scratch_bytes",
     "argreduce_scratch_init", "argreduce_read_error", "argreduce_device_caps", "argreduce_status_string",
     "argreduce_version", "argreduce_plan_scratch_bytes", "ArgreduceError", "Scratch", "make_caps",
 ]
@@ -38,10 +40,11 @@ def dtype_code(t, dtype: Optional[str]) -> int:
     torch = _torch()
     if dtype is not None:
         code = DTYPE_CODES[dtype]
-        if t.element_size() != {0: 4, 1: 2, 2: 2, 3: 8}[code]:
+        if t.element_size() != {0: 4, 1: 2, 2: 2, 3: 8, 4: 4, 5: 8}[code]:
             raise TypeError(f"dtype {dtype} does not match element size {t.element_size()}")
         return code
-    m = {torch.float32: ARGR_F32, torch.float16: ARGR_F16, torch.bfloat16: ARGR_BF16, torch.float64: ARGR_F64}
+    m = {torch.float32: ARGR_F32, torch.float16: ARGR_F16, torch.bfloat16: ARGR_BF16, torch.float64: ARGR_F64,
+         torch.int32: _lib.ARGR_I32, torch.int64: _lib.ARGR_I64}
     if t.dtype not in m:
         raise TypeError(f"unsupported tensor dtype {t.dtype}; pass dtype= for raw 16-bit storage")
     return m[t.dtype]
@@ -197,6 +200,39 @@ def argreduce_axis(x, dim: int, op="max", *, dtype: Optional[str] = None, with_v
     if st != ARGR_OK:
         raise ArgreduceError(st, "argreduce_axis")
     return out_idx, out_val
+
+
+def argreduce_cum(x, op="max", *, dtype: Optional[str] = None, with_values: bool = True, out_idx=None,
+                  out_val=None, stream=None, plan=None):
+    """cummax ("max") / cummin ("min") with indices along the last axis of a
+    contiguous CUDA tensor: for every position, the ArgMax/ArgMin of the prefix
+    up to it (ties keep the earlier index). Returns (indices, values) shaped
+    like x (values None unless with_values or out_val)."""
+    torch = _torch()
+    if not x.is_cuda or not x.is_contiguous() or x.dim() == 0:
+        raise ValueError("x must be a contiguous CUDA tensor with at least one dimension")
+    cols = x.shape[-1]
+    rows = x.numel() // cols if cols else 0
+    code = dtype_code(x, dtype)
+    if out_idx is None:
+        out_idx = torch.empty(x.shape, dtype=torch.int64, device=x.device)
+    if with_values and out_val is None:
+        out_val = torch.empty_like(x)
+    st_ptr = (stream if isinstance(stream, int) else stream.cuda_stream) if stream is not None else \
+        torch.cuda.current_stream(x.device).cuda_stream
+    st = _lib.argreduce_cum_raw(x.data_ptr(), code, rows, cols, op, out_idx.data_ptr(),
+                                out_val.data_ptr() if out_val is not None else 0, st_ptr, plan)
+    if st != ARGR_OK:
+        raise ArgreduceError(st, "argreduce_cum")
+    return out_idx, out_val
+
+
+def cummax(x, **kw):
+    return argreduce_cum(x, "max", **kw)
+
+
+def cummin(x, **kw):
+    return argreduce_cum(x, "min", **kw)
 
 
 def argmax(x, **kw):

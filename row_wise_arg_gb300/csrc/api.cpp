@@ -56,6 +56,7 @@ bool valid_op(int o) { return o == ARGR_MAX || o == ARGR_MIN || o == ARGR_MAX_LA
 // Checks shared by argreduce() and argreduce_with_plan().
 argr_status check_args(const void* x, int dtype, int64_t rows, int64_t cols, int op, const int64_t* out_idx,
                        const void* out_val) {
+    if (dtype == ARGR_I32 || dtype == ARGR_I64) return ARGR_EUNSUPPORTED;  // integer types: argreduce_cum only
     if (!valid_dtype(dtype) || !valid_op(op)) return ARGR_EINVAL;
     if (rows < 0 || cols < 1 || cols > INT_MAX) return ARGR_EINVAL;
     const int64_t es = elem_size(dtype);
@@ -250,6 +251,77 @@ argr_status argreduce_axis_with_plan(const argr_plan* plan, const void* x, argr_
         if ((s = check_plan(*plan, outer, reduce, dtype, caps, rows_aligned(x, dtype, reduce))) != ARGR_OK) return s;
     }
     return run_axis(*plan, x, dtype, outer, reduce, inner, op, out_idx, out_val, scratch, scratch_bytes, stream);
+}
+
+// ---------------------------------------------------------------------------
+// cummax / cummin.
+// ---------------------------------------------------------------------------
+static argr_status check_cum_args(const void* x, int dtype, int64_t rows, int64_t cols, int op,
+                                  const int64_t* out_idx, const void* out_val) {
+    const int64_t es = elem_size(dtype);
+    if (es == 0 || op < ARGR_MAX || op > ARGR_MIN_LAST) return ARGR_EINVAL;
+    if (op != ARGR_MAX && op != ARGR_MIN) return ARGR_EUNSUPPORTED;
+    if (rows < 0 || cols < 1 || cols > INT_MAX || rows > INT64_MAX / cols / 8) return ARGR_EINVAL;
+    if (rows == 0) return ARGR_OK;
+    if (!x || !out_idx) return ARGR_EINVAL;
+    if (reinterpret_cast<uintptr_t>(x) % es || reinterpret_cast<uintptr_t>(out_idx) % 8) return ARGR_EINVAL;
+    if (out_val && reinterpret_cast<uintptr_t>(out_val) % es) return ARGR_EINVAL;
+    return ARGR_OK;
+}
+
+static argr_status run_cum(const argr_plan& p, const void* x, int dtype, int64_t rows, int64_t cols, int op,
+                           int64_t* out_idx, void* out_val, argr_stream stream) {
+    Problem pr = make_problem(x, dtype, rows, cols, op, out_idx, out_val, nullptr, stream);
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (dtype) {
+        case ARGR_F32: e = launch_cum_f32(p, pr); break;
+        case ARGR_F16: e = launch_cum_f16(p, pr); break;
+        case ARGR_BF16: e = launch_cum_bf16(p, pr); break;
+        case ARGR_F64: e = launch_cum_f64(p, pr); break;
+        case ARGR_I32: e = launch_cum_i32(p, pr); break;
+        case ARGR_I64: e = launch_cum_i64(p, pr); break;
+        default: return ARGR_EINVAL;
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return e == cudaErrorInvalidClusterSize ? ARGR_EUNSUPPORTED : ARGR_ECUDA;
+    }
+    return ARGR_OK;
+}
+
+argr_status argreduce_cum(const void* x, argr_dtype dtype, int64_t rows, int64_t cols, argr_op op, int64_t* out_idx,
+                          void* out_val, argr_stream stream) {
+    argr_status s = check_cum_args(x, dtype, rows, cols, op, out_idx, out_val);
+    if (s != ARGR_OK || rows == 0) return s;
+    argr_caps caps;
+    if ((s = current_caps(&caps)) != ARGR_OK) return s;
+    argr_plan p;
+    if ((s = make_cum_plan(rows, cols, dtype, op, caps, &p)) != ARGR_OK) return s;
+    return run_cum(p, x, dtype, rows, cols, op, out_idx, out_val, stream);
+}
+
+argr_status argreduce_cum_plan(int64_t rows, int64_t cols, argr_dtype dtype, argr_op op, const argr_caps* caps,
+                               argr_plan* out) {
+    if (!out) return ARGR_EINVAL;
+    argr_caps c;
+    if (caps) {
+        c = *caps;
+    } else {
+        argr_status s = current_caps(&c);
+        if (s != ARGR_OK) return s;
+    }
+    return make_cum_plan(rows, cols, dtype, op, c, out);
+}
+
+argr_status argreduce_cum_with_plan(const argr_plan* plan, const void* x, argr_dtype dtype, int64_t rows,
+                                    int64_t cols, argr_op op, int64_t* out_idx, void* out_val, argr_stream stream) {
+    if (!plan) return ARGR_EINVAL;
+    argr_status s = check_cum_args(x, dtype, rows, cols, op, out_idx, out_val);
+    if (s != ARGR_OK || rows == 0) return s;
+    argr_caps caps;
+    if ((s = current_caps(&caps)) != ARGR_OK) return s;
+    if ((s = check_cum_plan(*plan, rows, cols, dtype, op, caps)) != ARGR_OK) return s;
+    return run_cum(*plan, x, dtype, rows, cols, op, out_idx, out_val, stream);
 }
 
 size_t argreduce_plan_scratch_bytes(const argr_plan* plan, int64_t rows) {

@@ -77,4 +77,14 @@ ARGR_DECLARE_LAUNCHERS(bf16)
 ARGR_DECLARE_LAUNCHERS(f64)
 #undef ARGR_DECLARE_LAUNCHERS
 
+// cummax / cummin (argreduce_cum), one translation unit per element type.
+cudaError_t launch_cum_f32(const argr_plan& p, const Problem& pr);
+cudaError_t launch_cum_f16(const argr_plan& p, const Problem& pr);
+cudaError_t launch_cum_bf16(const argr_plan& p, const Problem& pr);
+cudaError_t launch_cum_f64(const argr_plan& p, const Problem& pr);
+cudaError_t launch_cum_i32(const argr_plan& p, const Problem& pr);
+cudaError_t launch_cum_i64(const argr_plan& p, const Problem& pr);
+argr_status make_cum_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_caps& caps, argr_plan* out);
+argr_status check_cum_plan(const argr_plan& p, int64_t rows, int64_t cols, int dtype, int op, const argr_caps& caps);
+
 }  // namespace argr

@@ -59,14 +59,70 @@ int64_t ctas_per_wave(const argr_caps& caps, int block) {
 
 }  // namespace
 
+static bool caps_ok(const argr_caps& c) { return c.sm_count > 0 && c.max_threads_per_sm >= 32; }
+
 int elem_size(int dtype) {
     switch (dtype) {
         case ARGR_F32: return 4;
         case ARGR_F16: return 2;
         case ARGR_BF16: return 2;
         case ARGR_F64: return 8;
+        case ARGR_I32: return 4;
+        case ARGR_I64: return 8;
         default: return 0;
     }
+}
+
+// ---------------------------------------------------------------------------
+// cummax / cummin. A row is cut into C contiguous chunks (a cluster of C CTAs
+// when C > 1) while there are too few rows for the device; each CTA scans
+// tiles of block * 7 elements.
+// ---------------------------------------------------------------------------
+static constexpr int kCumItems = 7;
+
+argr_status make_cum_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_caps& caps, argr_plan* out) {
+    if (!out) return ARGR_EINVAL;
+    *out = argr_plan{};
+    if (elem_size(dtype) == 0 || rows < 0 || cols < 1 || cols > INT_MAX) return ARGR_EINVAL;
+    if (op != ARGR_MAX && op != ARGR_MIN) return (op == ARGR_MAX_LAST || op == ARGR_MIN_LAST) ? ARGR_EUNSUPPORTED
+                                                                                                : ARGR_EINVAL;
+    if (!caps_ok(caps)) return ARGR_EINVAL;
+    if (rows == 0) {
+        out->path = ARGR_PATH_NONE;
+        return ARGR_OK;
+    }
+    int block = 32;
+    while (block < 256 && block * kCumItems < cols) block <<= 1;
+    const int64_t tile = static_cast<int64_t>(block) * kCumItems;
+    int64_t c = 1;
+    const int64_t sms = caps.sm_count;
+    if (rows < 2 * sms && rows <= kMaxGridY && caps.max_cluster >= 2) {
+        c = std::min<int64_t>({16, caps.max_cluster, ceil_div(2 * sms, rows), cols / (2 * tile)});
+        c = std::max<int64_t>(1, c);
+    }
+    out->path = ARGR_PATH_CUM;
+    out->block = block;
+    out->cluster = static_cast<int32_t>(c);
+    out->blocks_per_row = c;
+    out->grid_rows = c > 1 ? rows : std::min(rows, kMaxGridY);
+    out->flags = ARGR_PLAN_PDL;
+    return ARGR_OK;
+}
+
+argr_status check_cum_plan(const argr_plan& p, int64_t rows, int64_t cols, int dtype, int op, const argr_caps& caps) {
+    if (elem_size(dtype) == 0 || rows < 0 || cols < 1 || cols > INT_MAX) return ARGR_EINVAL;
+    if (op != ARGR_MAX && op != ARGR_MIN) return ARGR_EUNSUPPORTED;
+    if (rows == 0) return ARGR_OK;
+    if (p.path != ARGR_PATH_CUM) return ARGR_EINVAL;
+    if (p.block < 32 || p.block > 1024 || p.block % 32 != 0) return ARGR_EINVAL;
+    if (p.flags & ~ARGR_PLAN_PDL) return ARGR_EINVAL;
+    if (p.cluster < 1 || p.cluster > 16 || p.blocks_per_row != p.cluster) return ARGR_EINVAL;
+    if (p.cluster > 1 && caps.max_cluster < p.cluster) return ARGR_EUNSUPPORTED;
+    if (p.grid_rows < 1 || p.grid_rows > kMaxGridY) return ARGR_EINVAL;
+    if (p.cluster > 1 && p.grid_rows < rows) return ARGR_EINVAL;
+    const int64_t smem = static_cast<int64_t>(p.block) * kCumItems * (2 * elem_size(dtype) + 4);
+    if (smem > kMaxDynamicSmem) return ARGR_EINVAL;
+    return ARGR_OK;
 }
 
 size_t plan_scratch(const argr_plan& p, int64_t rows) {
@@ -77,7 +133,6 @@ size_t plan_scratch(const argr_plan& p, int64_t rows) {
     return 0;
 }
 
-static bool caps_ok(const argr_caps& c) { return c.sm_count > 0 && c.max_threads_per_sm >= 32; }
 
 argr_status make_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_caps& caps, bool base_aligned,
                       argr_plan* out) {

@@ -381,3 +381,20 @@ def test_axis_plans():
         A.argreduce_axis_plan(1, 0, 5, "f32", "max", caps)
     assert _lib.argreduce_axis_raw(0x10000, "f32", 0, 10, 5, "max", 0x10000, 0, 0, 0, 0) == _lib.ARGR_OK
     assert _lib.argreduce_axis_raw(0x10000, "f32", 2, 10, 0, "max", 0x10000, 0, 0, 0, 0) == _lib.ARGR_EINVAL
+
+
+def test_cum_plans_and_validation():
+    for rows, cols, dt in [(1, 65536, "i64"), (1, 262144, "i64"), (64, 1024, "i64"), (1024, 64, "i64"),
+                           (4, 16384, "i32"), (1, 65536, "f32"), (256, 256, "bf16"), (1, 3, "f64")]:
+        d = A.argreduce_cum_plan(rows, cols, dt, "max", GB300).as_dict()
+        assert d["path_name"] == "cum" and d["scratch_bytes"] == 0
+        assert 32 <= d["block"] <= 256 and 1 <= d["cluster"] <= 16
+        if d["cluster"] > 1:
+            assert d["grid_rows"] == rows and rows * d["cluster"] <= 2 * 152 + 16
+    with pytest.raises(A.ArgreduceError):
+        A.argreduce_cum_plan(1, 10, "f32", "max_last", GB300)
+    X = 0x10000
+    assert _lib.argreduce_cum_raw(X, "i64", 0, 10, "max", X, 0, 0) == _lib.ARGR_OK
+    assert _lib.argreduce_cum_raw(X, "i64", 2, 0, "max", X, 0, 0) == _lib.ARGR_EINVAL
+    assert _lib.argreduce_cum_raw(X, "i64", 2, 10, "min_last", X, 0, 0) == _lib.ARGR_EUNSUPPORTED
+    assert _lib.argreduce_raw(X, "i64", 2, 10, "max", X, 0, 0, 0, 0) == _lib.ARGR_EUNSUPPORTED

@@ -35,7 +35,7 @@ OPS = ("max", "min")
 LAST_OPS = ("max_last", "min_last")
 ALL_OPS = OPS + LAST_OPS
 
-ELEM_SIZE = {"f32": 4, "f16": 2, "bf16": 2, "f64": 8}
+ELEM_SIZE = {"f32": 4, "f16": 2, "bf16": 2, "f64": 8, "i32": 4, "i64": 8}
 
 
 # ----------------------------------------------------------------------------
@@ -295,6 +295,20 @@ def make_axis_mixed(c: Case) -> np.ndarray:
     return x
 
 
+def make_cum_values(c: Case) -> np.ndarray:
+    """Inputs of the cummax / cummin workloads: integers U{-1000..1000} for
+    the integer types; N(0, 1) with 0.1% special values for the floats."""
+    rng = np.random.Generator(np.random.PCG64(c.seed))
+    if c.dtype in ("i32", "i64"):
+        return rng.integers(-1000, 1001, size=(c.rows, c.cols)).astype(np.int32 if c.dtype == "i32" else np.int64)
+    x = encode(rng.standard_normal((c.rows, c.cols)), c.dtype)
+    a = alphabet(c.dtype)
+    k = max(1, x.size // 1000)
+    flat = x.reshape(-1)
+    flat[rng.integers(0, x.size, size=k)] = a[rng.integers(0, len(a), size=k)]
+    return x
+
+
 RECIPES = {
     "logits": make_logits_1,
     "planted": make_planted,
@@ -302,6 +316,7 @@ RECIPES = {
     "uniform_special": make_uniform_special,
     "small_ints": make_small_ints,
     "axis_mixed": make_axis_mixed,
+    "cum_values": make_cum_values,
 }
 
 
@@ -347,6 +362,12 @@ def config_cases(k: int) -> List[Case]:
         out.append(Case("axis_64x512x256_bf16_max", 64, 512, "bf16", "max", "axis_mixed", 6003, inner=256))
         out.append(Case("axis_128x4096x8_f32_max", 128, 4096, "f32", "max", "axis_mixed", 6004, inner=8))
         out.append(Case("axis_16x2048x384_f64_min", 16, 2048, "f64", "min", "axis_mixed", 6005, inner=384))
+    elif k == 7:
+        # cummax / cummin with indices (the shapes and dtypes of Paddle issue #79670's tables).
+        for rows, cols, dtype, op in ((1, 65536, "i64", "max"), (1, 262144, "i64", "max"), (64, 1024, "i64", "max"),
+                                      (1024, 64, "i64", "min"), (4, 16384, "i32", "max"), (1, 65536, "f32", "max"),
+                                      (1, 65536, "f64", "min"), (256, 256, "bf16", "max")):
+            out.append(Case(f"cum_{rows}x{cols}_{dtype}_{op}", rows, cols, dtype, op, "cum_values", 7001 + cols % 97))
     else:
         raise ValueError(k)
     return out
