@@ -57,7 +57,7 @@ WORKLOADS = {
 }
 DTYPE_LABEL = {"f32": "f32", "f16": "f16", "bf16": "bf16", "f64": "f64", "i32": "i32", "i64": "i64"}
 KERNEL_OF_PATH = {"rows": "rows_kernel", "split": "split_kernel", "cluster": "cluster_kernel", "axis": "axis_kernel",
-                  "stream": "stream_kernel", "cum": "cum_kernel", "none": "none"}
+                  "stream": "stream_kernel", "cum": "cum_kernel", "cum_split": "cum_split_kernel", "none": "none"}
 
 
 def workload_cases(group: int):

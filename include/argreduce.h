@@ -77,6 +77,9 @@ typedef enum {
                               `cluster` CTAs (1 = none) splits it further. unroll 4 or 8 */
     ARGR_PATH_CUM = 6,     /* cummax / cummin (argreduce_cum): a row in `cluster` chunks, one CTA
                               each (1 = none), scanned in tiles of block * 7 elements */
+    ARGR_PATH_CUM_SPLIT = 7, /* cummax / cummin: a row in `blocks_per_row` chunks, one CTA each,
+                              any number of CTAs; chunk aggregates are exchanged through
+                              scratch (rows * blocks_per_row <= 1024) */
     ARGR_PATH_STREAM = 4   /* every warp streams a contiguous range of rows through its own
                               `stages` shared-memory buffers of `stage_bytes`, filled by bulk
                               (TMA) copies; `group` lanes per row for rows that fit a buffer,
@@ -99,11 +102,13 @@ typedef struct {
  * memory by bulk (TMA) copies issued all at once, instead of by loads from
  * every thread. The share must be at most 128 KiB. */
 #define ARGR_PLAN_BULK 2
-/* Plan flag for tests of failure handling (STREAM path only): one bulk copy's
- * barrier is made to expect more bytes than arrive, so the kernel's bounded
- * wait (2 ms under this flag) expires; the kernel records the expiry, skips its
- * work and returns, and argreduce_read_error() reports ARGR_ETIMEOUT. Outputs
- * are undefined. Never set in the planner's plans. */
+/* Plan flag for tests of failure handling (STREAM and CUM_SPLIT paths only).
+ * STREAM: one bulk copy's barrier is made to expect more bytes than arrive, so
+ * the kernel's bounded wait (2 ms under this flag) expires; the kernel records
+ * the expiry, skips its work and returns. CUM_SPLIT: chunk 0 of each row never
+ * publishes its record, so every wait for it expires after 2 ms. Either way
+ * argreduce_read_error() then reports ARGR_ETIMEOUT and outputs are
+ * undefined. Never set in the planner's plans. */
 #define ARGR_PLAN_TEST_EXPIRE 4
 
 /* A launch plan. Produced by argreduce_plan(); tests may edit it to force a
@@ -230,30 +235,42 @@ argr_status argreduce_axis_with_plan(const argr_plan* plan, const void* x, argr_
  * element. So out_idx[r * cols + cols - 1] equals argreduce()'s result.
  * Element types: the four floating types and ARGR_I32 / ARGR_I64 (compared
  * as integers). Paddle issue #79670 ("Possible fixes": a scan with argmax
- * semantics where ties take the earlier index). Needs no scratch; out_idx
- * holds rows * cols int64. Errors as for argreduce().
+ * semantics where ties take the earlier index, and a two-pass tiled scan when
+ * the rows alone do not fill the GPU). out_idx holds rows * cols int64.
+ * Scratch: argreduce_cum_scratch_bytes() bytes (0 when the plan needs none;
+ * then scratch may be NULL), prepared once by argreduce_scratch_init(); the
+ * same buffer may serve argreduce() calls that do not run at the same time.
+ * Errors as for argreduce().
  */
 argr_status argreduce_cum(const void* x, argr_dtype dtype, int64_t rows, int64_t cols, argr_op op, int64_t* out_idx,
-                          void* out_val, argr_stream stream);
+                          void* out_val, void* scratch, size_t scratch_bytes, argr_stream stream);
+
+/* Scratch bytes argreduce_cum() needs for this problem on the current device
+ * (0 = none). */
+size_t argreduce_cum_scratch_bytes(int64_t rows, int64_t cols, argr_dtype dtype, argr_op op);
 
 /* The planner for argreduce_cum(). */
 argr_status argreduce_cum_plan(int64_t rows, int64_t cols, argr_dtype dtype, argr_op op, const argr_caps* caps,
                                argr_plan* out);
 
-/* argreduce_cum() with an explicit ARGR_PATH_CUM plan (re-validated). */
+/* argreduce_cum() with an explicit ARGR_PATH_CUM or ARGR_PATH_CUM_SPLIT plan
+ * (re-validated). */
 argr_status argreduce_cum_with_plan(const argr_plan* plan, const void* x, argr_dtype dtype, int64_t rows,
-                                    int64_t cols, argr_op op, int64_t* out_idx, void* out_val, argr_stream stream);
+                                    int64_t cols, argr_op op, int64_t* out_idx, void* out_val, void* scratch,
+                                    size_t scratch_bytes, argr_stream stream);
 
 /* Scratch bytes a given plan needs for `rows` rows. */
 size_t argreduce_plan_scratch_bytes(const argr_plan* plan, int64_t rows);
 
 /*
  * Synchronise `stream` and read the library's device error words (set by a
- * kernel whose bounded wait for a bulk copy expired; such a kernel skips the
- * rest of its work and returns) and the one in `scratch` (may be NULL).
- * Returns ARGR_ETIMEOUT if any was set (and clears them), ARGR_OK otherwise,
- * ARGR_ECUDA if the stream reports a fault. For tests and benchmarks; it
- * blocks the host.
+ * kernel whose bounded wait expired: for a bulk copy, after which the kernel
+ * skips the rest of its work, or for another CTA's chunk record in the split
+ * scan) and the one in `scratch` (may be NULL). Returns ARGR_ESCRATCH if a
+ * split scan found counters or records its launch did not write (a scratch
+ * buffer that argreduce_scratch_init() never prepared), else ARGR_ETIMEOUT if
+ * any word was set, ARGR_OK otherwise (the words are cleared), and ARGR_ECUDA
+ * if the stream reports a fault. For tests and benchmarks; it blocks the host.
  */
 argr_status argreduce_read_error(void* scratch, argr_stream stream);
 

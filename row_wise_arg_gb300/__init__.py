@@ -203,11 +203,13 @@ def argreduce_axis(x, dim: int, op="max", *, dtype: Optional[str] = None, with_v
 
 
 def argreduce_cum(x, op="max", *, dtype: Optional[str] = None, with_values: bool = True, out_idx=None,
-                  out_val=None, stream=None, plan=None):
+                  out_val=None, scratch: Optional[Scratch] = None, stream=None, plan=None):
     """cummax ("max") / cummin ("min") with indices along the last axis of a
     contiguous CUDA tensor: for every position, the ArgMax/ArgMin of the prefix
     up to it (ties keep the earlier index). Returns (indices, values) shaped
-    like x (values None unless with_values or out_val)."""
+    like x (values None unless with_values or out_val). Runs on ``stream``
+    without synchronising; the split scan uses ``scratch`` (default: the
+    stream's own Scratch)."""
     torch = _torch()
     if not x.is_cuda or not x.is_contiguous() or x.dim() == 0:
         raise ValueError("x must be a contiguous CUDA tensor with at least one dimension")
@@ -220,8 +222,20 @@ def argreduce_cum(x, op="max", *, dtype: Optional[str] = None, with_values: bool
         out_val = torch.empty_like(x)
     st_ptr = (stream if isinstance(stream, int) else stream.cuda_stream) if stream is not None else \
         torch.cuda.current_stream(x.device).cuda_stream
+    if rows == 0:
+        need = 0
+    elif plan is None:
+        need = _lib.argreduce_cum_scratch_bytes(rows, cols, code, op)
+    else:
+        need = argreduce_plan_scratch_bytes(plan, rows)
+    if scratch is None and need:
+        scratch = _default_scratch(x.device.index, st_ptr)
+    if need:
+        scratch.ensure(need, st_ptr)
     st = _lib.argreduce_cum_raw(x.data_ptr(), code, rows, cols, op, out_idx.data_ptr(),
-                                out_val.data_ptr() if out_val is not None else 0, st_ptr, plan)
+                                out_val.data_ptr() if out_val is not None else 0,
+                                scratch.ptr if scratch is not None else 0,
+                                scratch.nbytes if scratch is not None else 0, st_ptr, plan)
     if st != ARGR_OK:
         raise ArgreduceError(st, "argreduce_cum")
     return out_idx, out_val

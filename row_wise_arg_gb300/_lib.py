@@ -18,7 +18,7 @@ ARGR_F32, ARGR_F16, ARGR_BF16, ARGR_F64, ARGR_I32, ARGR_I64 = 0, 1, 2, 3, 4, 5
 ARGR_MAX, ARGR_MIN, ARGR_MAX_LAST, ARGR_MIN_LAST = 0, 1, 2, 3
 (ARGR_OK, ARGR_EINVAL, ARGR_ESCRATCH, ARGR_EUNSUPPORTED, ARGR_ECUDA, ARGR_ETIMEOUT) = range(6)
 ARGR_PATH_NONE, ARGR_PATH_ROWS, ARGR_PATH_SPLIT, ARGR_PATH_CLUSTER, ARGR_PATH_STREAM, ARGR_PATH_AXIS, \
-    ARGR_PATH_CUM = range(7)
+    ARGR_PATH_CUM, ARGR_PATH_CUM_SPLIT = range(8)
 ARGR_PLAN_PDL = 1
 ARGR_PLAN_BULK = 2
 ARGR_PLAN_TEST_EXPIRE = 4
@@ -28,7 +28,7 @@ DTYPE_CODES = {"f32": ARGR_F32, "f16": ARGR_F16, "bf16": ARGR_BF16, "f64": ARGR_
 OP_CODES = {"max": ARGR_MAX, "min": ARGR_MIN, "max_last": ARGR_MAX_LAST, "min_last": ARGR_MIN_LAST}
 PATH_NAMES = {ARGR_PATH_NONE: "none", ARGR_PATH_ROWS: "rows", ARGR_PATH_SPLIT: "split",
               ARGR_PATH_CLUSTER: "cluster", ARGR_PATH_STREAM: "stream", ARGR_PATH_AXIS: "axis",
-              ARGR_PATH_CUM: "cum"}
+              ARGR_PATH_CUM: "cum", ARGR_PATH_CUM_SPLIT: "cum_split"}
 
 # Every function the header declares (checked by the tests).
 EXPORTS = (
@@ -36,7 +36,7 @@ EXPORTS = (
     "argreduce_with_plan", "argreduce_plan_scratch_bytes", "argreduce_read_error",
     "argreduce_device_caps", "argreduce_status_string", "argreduce_version", "argreduce_noalloc",
     "argreduce_axis", "argreduce_axis_plan", "argreduce_axis_with_plan", "argreduce_cum", "argreduce_cum_plan",
-    "argreduce_cum_with_plan",
+    "argreduce_cum_with_plan", "argreduce_cum_scratch_bytes",
 )
 
 
@@ -110,12 +110,15 @@ def load() -> ctypes.CDLL:
         lib.argreduce_axis_with_plan.argtypes = [ctypes.POINTER(argr_plan), vp, i32, i64, i64, i64, i32, vp, vp, vp,
                                                  sz, vp]
         lib.argreduce_axis_with_plan.restype = i32
-        lib.argreduce_cum.argtypes = [vp, i32, i64, i64, i32, vp, vp, vp]
+        lib.argreduce_cum.argtypes = [vp, i32, i64, i64, i32, vp, vp, vp, sz, vp]
         lib.argreduce_cum.restype = i32
         lib.argreduce_cum_plan.argtypes = [i64, i64, i32, i32, ctypes.POINTER(argr_caps), ctypes.POINTER(argr_plan)]
         lib.argreduce_cum_plan.restype = i32
-        lib.argreduce_cum_with_plan.argtypes = [ctypes.POINTER(argr_plan), vp, i32, i64, i64, i32, vp, vp, vp]
+        lib.argreduce_cum_with_plan.argtypes = [ctypes.POINTER(argr_plan), vp, i32, i64, i64, i32, vp, vp, vp, sz,
+                                                vp]
         lib.argreduce_cum_with_plan.restype = i32
+        lib.argreduce_cum_scratch_bytes.argtypes = [i64, i64, i32, i32]
+        lib.argreduce_cum_scratch_bytes.restype = sz
         lib.argreduce_noalloc.argtypes = [vp, i32, i64, i64, i32, vp, vp, vp]
         lib.argreduce_noalloc.restype = i32
         lib.argreduce_version.argtypes = []
@@ -205,10 +208,10 @@ def argreduce_axis_plan(outer: int, reduce: int, inner: int, dtype, op, caps: Op
 
 
 def argreduce_cum_raw(x_ptr: int, dtype, rows: int, cols: int, op, out_idx_ptr: int, out_val_ptr: int,
-                      stream_ptr: int, plan: Optional[argr_plan] = None) -> int:
+                      scratch_ptr: int, scratch_bytes: int, stream_ptr: int, plan: Optional[argr_plan] = None) -> int:
     """argreduce_cum() (or argreduce_cum_with_plan() when a plan is given)."""
     args = (x_ptr or None, _code(DTYPE_CODES, dtype), rows, cols, _code(OP_CODES, op), out_idx_ptr or None,
-            out_val_ptr or None, stream_ptr or None)
+            out_val_ptr or None, scratch_ptr or None, scratch_bytes, stream_ptr or None)
     if plan is None:
         return load().argreduce_cum(*args)
     return load().argreduce_cum_with_plan(ctypes.byref(plan), *args)
@@ -221,6 +224,10 @@ def argreduce_cum_plan(rows: int, cols: int, dtype, op, caps: Optional[argr_caps
     if st != ARGR_OK:
         raise ArgreduceError(st, "argreduce_cum_plan")
     return p
+
+
+def argreduce_cum_scratch_bytes(rows: int, cols: int, dtype, op) -> int:
+    return int(load().argreduce_cum_scratch_bytes(rows, cols, _code(DTYPE_CODES, dtype), _code(OP_CODES, op)))
 
 
 def argreduce_plan_scratch_bytes(plan: argr_plan, rows: int) -> int:

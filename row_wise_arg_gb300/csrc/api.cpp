@@ -270,8 +270,14 @@ static argr_status check_cum_args(const void* x, int dtype, int64_t rows, int64_
 }
 
 static argr_status run_cum(const argr_plan& p, const void* x, int dtype, int64_t rows, int64_t cols, int op,
-                           int64_t* out_idx, void* out_val, argr_stream stream) {
-    Problem pr = make_problem(x, dtype, rows, cols, op, out_idx, out_val, nullptr, stream);
+                           int64_t* out_idx, void* out_val, void* scratch, size_t scratch_bytes,
+                           argr_stream stream) {
+    const size_t need = plan_scratch(p, rows);
+    if (need > 0) {
+        if (!scratch || scratch_bytes < need) return ARGR_ESCRATCH;
+        if (reinterpret_cast<uintptr_t>(scratch) % 16 != 0) return ARGR_ESCRATCH;
+    }
+    Problem pr = make_problem(x, dtype, rows, cols, op, out_idx, out_val, scratch, stream);
     cudaError_t e = cudaErrorInvalidValue;
     switch (dtype) {
         case ARGR_F32: e = launch_cum_f32(p, pr); break;
@@ -290,14 +296,22 @@ static argr_status run_cum(const argr_plan& p, const void* x, int dtype, int64_t
 }
 
 argr_status argreduce_cum(const void* x, argr_dtype dtype, int64_t rows, int64_t cols, argr_op op, int64_t* out_idx,
-                          void* out_val, argr_stream stream) {
+                          void* out_val, void* scratch, size_t scratch_bytes, argr_stream stream) {
     argr_status s = check_cum_args(x, dtype, rows, cols, op, out_idx, out_val);
     if (s != ARGR_OK || rows == 0) return s;
     argr_caps caps;
     if ((s = current_caps(&caps)) != ARGR_OK) return s;
     argr_plan p;
     if ((s = make_cum_plan(rows, cols, dtype, op, caps, &p)) != ARGR_OK) return s;
-    return run_cum(p, x, dtype, rows, cols, op, out_idx, out_val, stream);
+    return run_cum(p, x, dtype, rows, cols, op, out_idx, out_val, scratch, scratch_bytes, stream);
+}
+
+size_t argreduce_cum_scratch_bytes(int64_t rows, int64_t cols, argr_dtype dtype, argr_op op) {
+    argr_caps caps;
+    if (current_caps(&caps) != ARGR_OK) return 0;
+    argr_plan p;
+    if (make_cum_plan(rows, cols, dtype, op, caps, &p) != ARGR_OK) return 0;
+    return p.scratch_bytes;
 }
 
 argr_status argreduce_cum_plan(int64_t rows, int64_t cols, argr_dtype dtype, argr_op op, const argr_caps* caps,
@@ -314,14 +328,15 @@ argr_status argreduce_cum_plan(int64_t rows, int64_t cols, argr_dtype dtype, arg
 }
 
 argr_status argreduce_cum_with_plan(const argr_plan* plan, const void* x, argr_dtype dtype, int64_t rows,
-                                    int64_t cols, argr_op op, int64_t* out_idx, void* out_val, argr_stream stream) {
+                                    int64_t cols, argr_op op, int64_t* out_idx, void* out_val, void* scratch,
+                                    size_t scratch_bytes, argr_stream stream) {
     if (!plan) return ARGR_EINVAL;
     argr_status s = check_cum_args(x, dtype, rows, cols, op, out_idx, out_val);
     if (s != ARGR_OK || rows == 0) return s;
     argr_caps caps;
     if ((s = current_caps(&caps)) != ARGR_OK) return s;
     if ((s = check_cum_plan(*plan, rows, cols, dtype, op, caps)) != ARGR_OK) return s;
-    return run_cum(*plan, x, dtype, rows, cols, op, out_idx, out_val, stream);
+    return run_cum(*plan, x, dtype, rows, cols, op, out_idx, out_val, scratch, scratch_bytes, stream);
 }
 
 size_t argreduce_plan_scratch_bytes(const argr_plan* plan, int64_t rows) {
@@ -363,6 +378,7 @@ argr_status argreduce_read_error(void* scratch, argr_stream stream) {
         }
         any |= word;
     }
+    if (any & 2u) return ARGR_ESCRATCH;  // a split scan met a ticket or record its launch did not write
     return any ? ARGR_ETIMEOUT : ARGR_OK;
 }
 

@@ -87,25 +87,26 @@ struct CumInt {
 using CumI32 = CumInt<int, unsigned>;
 using CumI64 = CumInt<long long, unsigned long long>;
 
+// A prefix result: ordered key and index. Values are not carried through the
+// scan: the value of an index inside the current tile is read back from the
+// tile in shared memory, and the carry-in keeps its own value.
 template <class CT>
-struct Pfx {
+struct KI {
     typename CT::key k;
     int i;
-    typename CT::raw v;
 };
 
 // The later part b replaces the earlier prefix a only when strictly better.
 template <class CT>
-__device__ __forceinline__ Pfx<CT> later(const Pfx<CT>& a, const Pfx<CT>& b) {
+__device__ __forceinline__ KI<CT> later(const KI<CT>& a, const KI<CT>& b) {
     return b.k > a.k ? b : a;
 }
 
 template <class CT>
-__device__ __forceinline__ Pfx<CT> pfx_identity() {
-    Pfx<CT> p;
+__device__ __forceinline__ KI<CT> ki_identity() {
+    KI<CT> p;
     p.k = 0;
     p.i = 0;
-    p.v = typename CT::raw(0);
     return p;
 }
 
@@ -150,16 +151,215 @@ __device__ __forceinline__ T shfl_xor_any(T v, int d) {
 }
 
 template <class CT>
-__device__ __forceinline__ Pfx<CT> shfl_up_pfx(const Pfx<CT>& p, int d) {
-    Pfx<CT> q;
+__device__ __forceinline__ KI<CT> shfl_up_ki(const KI<CT>& p, int d) {
+    KI<CT> q;
     q.k = shfl_up_any(p.k, d);
     q.i = __shfl_up_sync(0xffffffffu, p.i, d);
-    q.v = shfl_up_any(p.v, d);
+    return q;
+}
+
+template <class CT>
+__device__ __forceinline__ KI<CT> shfl_xor_ki(const KI<CT>& p, int d) {
+    KI<CT> q;
+    q.k = shfl_xor_any(p.k, d);
+    q.i = __shfl_xor_sync(0xffffffffu, p.i, d);
     return q;
 }
 
 constexpr int kCumMaxCluster = 16;
+constexpr int kCumLoadsA = 4;  // independent loads in flight per thread in phase A
 
+// Total order for merging aggregates of disjoint ranges: the higher key, then
+// the lower index. Commutative, so the order in which partial aggregates meet
+// does not matter. An empty aggregate is key 0 (it never beats a real prefix,
+// whose key is at least the seed's and whose index is lower on a tie).
+template <class CT>
+__device__ __forceinline__ KI<CT> first_best(const KI<CT>& a, const KI<CT>& b) {
+    return (b.k > a.k || (b.k == a.k && b.i < a.i)) ? b : a;
+}
+
+template <class CT>
+__device__ __forceinline__ KI<CT> warp_first_best(KI<CT> a) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) a = first_best(a, shfl_xor_ki(a, off));
+    return a;
+}
+
+// first_best over the CTA; the result is valid in every thread of warp 0.
+// Ends with warp_tot free for reuse only after the caller's next barrier.
+template <class CT>
+__device__ __forceinline__ KI<CT> block_first_best(KI<CT> a, KI<CT>* warp_tot) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    a = warp_first_best(a);
+    if (lane == 0) warp_tot[warp] = a;
+    __syncthreads();
+    if (warp == 0) a = warp_first_best(lane < nwarps ? warp_tot[lane] : ki_identity<CT>());
+    return a;
+}
+
+// The first tile of row[cb, ce) into registers, in the layout the scan uses
+// (thread t holds elements cb + t + q * NT); phase A reduces it and phase B
+// scans it without loading it again.
+template <class CT, int ITEMS>
+__device__ __forceinline__ void load_first_tile(const typename CT::raw* row, int cb, int ce,
+                                                typename CT::raw (&v)[ITEMS]) {
+    const int nt = blockDim.x;
+    const int n = ce - cb < nt * ITEMS ? ce - cb : nt * ITEMS;
+#pragma unroll
+    for (int q = 0; q < ITEMS; ++q)
+        if (static_cast<int>(threadIdx.x) + q * nt < n) v[q] = ld_scalar(row + cb + threadIdx.x + q * nt);
+}
+
+// Phase A: the aggregate of row[cb, ce) (its first best element): the first
+// tile from v, the rest with kCumLoadsA independent loads in flight per
+// thread. Valid in warp 0.
+template <class CT, int OP, int ITEMS>
+__device__ __forceinline__ KI<CT> chunk_aggregate(const typename CT::raw* row, int cb, int ce,
+                                                  const typename CT::raw (&v)[ITEMS], KI<CT>* warp_tot) {
+    using R = typename CT::raw;
+    using K = typename CT::key;
+    const int nt = blockDim.x;
+    const int t = threadIdx.x;
+    const int tile = nt * ITEMS;
+    const int n0 = ce - cb < tile ? ce - cb : tile;
+    KI<CT> a = ki_identity<CT>();
+#pragma unroll
+    for (int q = 0; q < ITEMS; ++q) {  // increasing indices within the thread: the first best stays
+        if (t + q * nt < n0) {
+            const K k = CT::template elem_key<OP>(v[q]);
+            if (k > a.k) {
+                a.k = k;
+                a.i = cb + t + q * nt;
+            }
+        }
+    }
+    for (int64_t j0 = static_cast<int64_t>(cb) + n0 + t; j0 < ce; j0 += static_cast<int64_t>(kCumLoadsA) * nt) {
+        R w[kCumLoadsA];
+#pragma unroll
+        for (int u = 0; u < kCumLoadsA; ++u)
+            if (j0 + u * nt < ce) w[u] = ld_scalar(row + j0 + u * nt);
+#pragma unroll
+        for (int u = 0; u < kCumLoadsA; ++u) {
+            if (j0 + u * nt < ce) {
+                const K k = CT::template elem_key<OP>(w[u]);
+                if (k > a.k) {
+                    a.k = k;
+                    a.i = static_cast<int>(j0 + u * nt);
+                }
+            }
+        }
+    }
+    return block_first_best(a, warp_tot);
+}
+
+// Phase B: scan row[cb, ce) tile by tile (NT threads x ITEMS consecutive
+// elements per thread), starting from the carry-in (carry, carry_v) = the
+// prefix result just before cb, with the first tile already in v
+// (load_first_tile). Tiles pass through shared memory so that global
+// accesses are coalesced (ITEMS odd: a thread's run of consecutive elements
+// spreads over the banks), and the next tile's loads are issued into
+// registers while the current tile is scanned.
+template <class CT, int OP, int ITEMS>
+__device__ __forceinline__ void scan_chunk(const typename CT::raw* row, int cb, int ce, KI<CT> carry,
+                                           typename CT::raw carry_v, typename CT::raw (&v)[ITEMS],
+                                           int64_t* __restrict__ oi_row, typename CT::raw* __restrict__ ov_row,
+                                           unsigned char* smem, KI<CT>* warp_tot, KI<CT>* s_total) {
+    using R = typename CT::raw;
+    using K = typename CT::key;
+    const int nt = blockDim.x;
+    const int t = threadIdx.x;
+    const int lane = t & 31;
+    const int warp = t >> 5;
+    const int nwarps = nt >> 5;
+    const int tile = nt * ITEMS;
+    R* tin = reinterpret_cast<R*>(smem);                                                 // tile input
+    int* tidx = reinterpret_cast<int*>(smem + static_cast<size_t>(tile) * sizeof(R));  // tile indices
+    int base = cb;
+    int n = ce - cb < tile ? ce - cb : tile;
+    while (n > 0) {
+#pragma unroll
+        for (int q = 0; q < ITEMS; ++q)
+            if (t + q * nt < n) tin[t + q * nt] = v[q];
+        __syncthreads();
+        const int nbase = base + n;
+        const int nn = ce - nbase < tile ? ce - nbase : tile;
+#pragma unroll
+        for (int q = 0; q < ITEMS; ++q)
+            if (t + q * nt < nn) v[q] = ld_scalar(row + nbase + t + q * nt);
+        // thread-local inclusive prefixes of ITEMS consecutive elements
+        KI<CT> p[ITEMS];
+        KI<CT> run = ki_identity<CT>();
+#pragma unroll
+        for (int q = 0; q < ITEMS; ++q) {
+            const int j = t * ITEMS + q;
+            if (j < n) {
+                const K k = CT::template elem_key<OP>(tin[j]);
+                if (k > run.k) {
+                    run.k = k;
+                    run.i = base + j;
+                }
+            }
+            p[q] = run;
+        }
+        // warp inclusive scan of the thread totals
+        KI<CT> ws = run;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const KI<CT> o = shfl_up_ki(ws, d);
+            if (lane >= d) ws = later(o, ws);
+        }
+        KI<CT> excl = shfl_up_ki(ws, 1);
+        if (lane == 0) excl = ki_identity<CT>();
+        if (lane == 31) warp_tot[warp] = ws;
+        __syncthreads();
+        if (warp == 0) {
+            KI<CT> w = lane < nwarps ? warp_tot[lane] : ki_identity<CT>();
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const KI<CT> o = shfl_up_ki(w, d);
+                if (lane >= d) w = later(o, w);
+            }
+            KI<CT> we = shfl_up_ki(w, 1);
+            if (lane == 0) we = ki_identity<CT>();
+            if (lane < nwarps) warp_tot[lane] = we;  // exclusive prefix of each warp
+            if (lane == nwarps - 1) *s_total = w;
+        }
+        __syncthreads();
+        const KI<CT> before = later(later(carry, warp_tot[warp]), excl);
+#pragma unroll
+        for (int q = 0; q < ITEMS; ++q) {
+            const int j = t * ITEMS + q;
+            if (j < n) tidx[j] = later(before, p[q]).i;
+        }
+        const KI<CT> tot = *s_total;
+        __syncthreads();
+        // Coalesced stores. An index before this tile can only be the carry's.
+        int64_t* oi = oi_row + base;
+#pragma unroll
+        for (int q = 0; q < ITEMS; ++q)
+            if (t + q * nt < n) oi[t + q * nt] = tidx[t + q * nt];
+        if (ov_row) {
+            R* ov = ov_row + base;
+#pragma unroll
+            for (int q = 0; q < ITEMS; ++q) {
+                if (t + q * nt < n) {
+                    const int i = tidx[t + q * nt];
+                    ov[t + q * nt] = i >= base ? tin[i - base] : carry_v;
+                }
+            }
+        }
+        if (tot.k > carry.k) {  // carry the tile's best past it
+            carry = tot;
+            carry_v = tin[tot.i - base];
+        }
+        __syncthreads();  // the tile buffers are reused by the next tile
+        base = nbase;
+        n = nn;
+    }
+}
+
+// One CTA per row (C = 1), or a cluster of C CTAs per row whose chunk
+// aggregates are exchanged through distributed shared memory.
 template <class CT, int OP, int ITEMS>
 __global__ void __launch_bounds__(1024)
 cum_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols, int64_t* __restrict__ out_idx,
@@ -167,20 +367,12 @@ cum_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols, int64
     using R = typename CT::raw;
     using K = typename CT::key;
     extern __shared__ __align__(16) unsigned char cum_smem[];
-    __shared__ Pfx<CT> warp_tot[32];
-    __shared__ Pfx<CT> s_total;
+    __shared__ KI<CT> warp_tot[32];
+    __shared__ KI<CT> s_total;
     __shared__ __align__(16) uint4 agg_slots[2][kCumMaxCluster];  // aggregates pushed by earlier CTAs
-    const int nt = blockDim.x;
     const int t = threadIdx.x;
-    const int lane = t & 31;
-    const int warp = t >> 5;
-    const int nwarps = nt >> 5;
     const int C = gridDim.x;
     const int b = blockIdx.x;
-    const int tile = nt * ITEMS;
-    R* tin = reinterpret_cast<R*>(cum_smem);                                                  // tile input
-    int* tidx = reinterpret_cast<int*>(cum_smem + static_cast<size_t>(tile) * sizeof(R));   // tile indices
-    R* tval = reinterpret_cast<R*>(cum_smem + static_cast<size_t>(tile) * (sizeof(R) + 4)); // tile values
     bool started = false;
     if (C > 1) cluster_started_arrive();
     grid_dependency_wait();
@@ -191,44 +383,14 @@ cum_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols, int64
         const int cb = static_cast<int>(static_cast<int64_t>(cols) * b / C);
         const int ce = static_cast<int>(static_cast<int64_t>(cols) * (b + 1) / C);
         const R x0 = ld_scalar(row);
-        Pfx<CT> carry;
+        R v[ITEMS];
+        load_first_tile<CT, ITEMS>(row, cb, ce, v);
+        KI<CT> carry;
         carry.k = CT::template seed_key<OP>(x0);
         carry.i = 0;
-        carry.v = x0;
+        R carry_v = x0;
         if (C > 1) {
-            // Phase A: this chunk's aggregate (first best element), identity-seeded.
-            Pfx<CT> a = pfx_identity<CT>();
-            for (int j = cb + t; j < ce; j += nt) {
-                const R v = ld_scalar(row + j);
-                const K k = CT::template elem_key<OP>(v);
-                if (k > a.k) {
-                    a.k = k;
-                    a.i = j;
-                    a.v = v;
-                }
-            }
-            // CTA merge: higher key wins, equal keys keep the lower index.
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
-                Pfx<CT> o;
-                o.k = __shfl_xor_sync(0xffffffffu, a.k, off);
-                o.i = __shfl_xor_sync(0xffffffffu, a.i, off);
-                o.v = shfl_xor_any(a.v, off);
-                if (o.k > a.k || (o.k == a.k && o.i < a.i)) a = o;
-            }
-            if (lane == 0) warp_tot[warp] = a;
-            __syncthreads();
-            if (warp == 0) {
-                a = lane < nwarps ? warp_tot[lane] : pfx_identity<CT>();
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) {
-                    Pfx<CT> o;
-                    o.k = __shfl_xor_sync(0xffffffffu, a.k, off);
-                    o.i = __shfl_xor_sync(0xffffffffu, a.i, off);
-                    o.v = shfl_xor_any(a.v, off);
-                    if (o.k > a.k || (o.k == a.k && o.i < a.i)) a = o;
-                }
-            }
+            const KI<CT> a = chunk_aggregate<CT, OP, ITEMS>(row, cb, ce, v, warp_tot);
             if (!started) {  // every CTA of the cluster runs before the first remote write
                 cluster_started_wait();
                 started = true;
@@ -250,107 +412,243 @@ cum_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols, int64
             // Fold the aggregates of the earlier chunks, in order, into the carry.
             for (int k = 0; k < b; ++k) {
                 const uint4 pk = agg_slots[parity][k];
-                Pfx<CT> e;
-                e.k = static_cast<K>(static_cast<uint64_t>(pk.x) | (static_cast<uint64_t>(pk.y) << 32));
-                e.i = static_cast<int>(pk.z);
-                if (e.k > carry.k) {
-                    carry.k = e.k;
-                    carry.i = e.i;
-                    carry.v = ld_scalar(row + e.i);  // the winner's raw bits (an L2 hit)
+                const K ek = static_cast<K>(static_cast<uint64_t>(pk.x) | (static_cast<uint64_t>(pk.y) << 32));
+                if (ek > carry.k) {
+                    carry.k = ek;
+                    carry.i = static_cast<int>(pk.z);
+                    carry_v = ld_scalar(row + carry.i);  // the winner's raw bits (an L2 hit)
                 }
             }
         }
-        // Phase B: tiles of this chunk, in order.
-        for (int base = cb; base < ce; base += tile) {
-            const int n = ce - base < tile ? ce - base : tile;
-            for (int j = t; j < n; j += nt) tin[j] = ld_scalar(row + base + j);
-            __syncthreads();
-            // thread-local inclusive prefixes of ITEMS consecutive elements
-            Pfx<CT> p[ITEMS];
-            Pfx<CT> run = pfx_identity<CT>();
-#pragma unroll
-            for (int q = 0; q < ITEMS; ++q) {
-                const int j = t * ITEMS + q;
-                if (j < n) {
-                    const R v = tin[j];
-                    const K k = CT::template elem_key<OP>(v);
-                    if (k > run.k) {
-                        run.k = k;
-                        run.i = base + j;
-                        run.v = v;
-                    }
-                }
-                p[q] = run;
-            }
-            // warp inclusive scan of the thread totals
-            Pfx<CT> ws = run;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const Pfx<CT> o = shfl_up_pfx(ws, d);
-                if (lane >= d) ws = later(o, ws);
-            }
-            Pfx<CT> excl = shfl_up_pfx(ws, 1);
-            if (lane == 0) excl = pfx_identity<CT>();
-            if (lane == 31) warp_tot[warp] = ws;
-            __syncthreads();
-            if (warp == 0) {
-                Pfx<CT> w = lane < nwarps ? warp_tot[lane] : pfx_identity<CT>();
-#pragma unroll
-                for (int d = 1; d < 32; d <<= 1) {
-                    const Pfx<CT> o = shfl_up_pfx(w, d);
-                    if (lane >= d) w = later(o, w);
-                }
-                Pfx<CT> we = shfl_up_pfx(w, 1);
-                if (lane == 0) we = pfx_identity<CT>();
-                if (lane < nwarps) warp_tot[lane] = we;  // exclusive prefix of each warp
-                if (lane == nwarps - 1) s_total = w;
-            }
-            __syncthreads();
-            const Pfx<CT> before = later(later(carry, warp_tot[warp]), excl);
-#pragma unroll
-            for (int q = 0; q < ITEMS; ++q) {
-                const int j = t * ITEMS + q;
-                if (j < n) {
-                    const Pfx<CT> o = later(before, p[q]);
-                    tidx[j] = o.i;
-                    tval[j] = o.v;
-                }
-            }
-            carry = later(carry, s_total);
-            __syncthreads();
-            int64_t* oi = out_idx + r * static_cast<int64_t>(cols) + base;
-            for (int j = t; j < n; j += nt) oi[j] = tidx[j];
-            if (out_val) {
-                R* ov = out_val + r * static_cast<int64_t>(cols) + base;
-                for (int j = t; j < n; j += nt) ov[j] = tval[j];
-            }
-            __syncthreads();  // the tile buffers are reused by the next tile
-        }
+        scan_chunk<CT, OP, ITEMS>(row, cb, ce, carry, carry_v, v, out_idx + r * static_cast<int64_t>(cols),
+                                  out_val ? out_val + r * static_cast<int64_t>(cols) : nullptr, cum_smem, warp_tot,
+                                  &s_total);
     }
     if (C > 1 && !started) cluster_started_wait();  // complete the start phase even with no rows
 }
 
 // ---------------------------------------------------------------------------
-// Launcher.
+// Split scan: a row in `chunks` chunks, one CTA each, any number of CTAs.
+//
+// CTAs take tickets in the order they start (an atomic counter that wraps to
+// zero after the last ticket); ticket k is chunk k % chunks of row k / chunks.
+// After phase A a CTA publishes its chunk's aggregate as one 64-bit record:
+// the low word is index + 1 (0 = not yet published, kNoElement = no element
+// of the chunk has a nonzero key), the high word the key itself for keys of
+// up to 32 bits (wider keys are recomputed from x[index]). It then waits for
+// the records of the earlier chunks of its row, all of which belong to CTAs
+// that took their tickets before it and so are running; their merge with the
+// seed is its carry-in, and phase B follows. No CTA waits on a chain: every
+// record is written straight after its CTA's phase A.
+//
+// Scratch (the argreduce scratch buffer; calls that share it must not run at
+// the same time): a ticket and a done counter in the header, and the records
+// in the region of argreduce's split counters, which must be all-zero between
+// calls. The CTA whose wait finishes last zeroes the records once its own
+// scan is done, so both regions are zero again when the kernel ends.
+// Every wait is bounded: on expiry the CTA records kErrWaitExpired in the
+// scratch error word, counts the missing record as empty and carries on (the
+// outputs of that call are then undefined; the counters still wrap and the
+// records are still cleared).
+// ---------------------------------------------------------------------------
+constexpr unsigned kNoElement = 0xffffffffu;
+constexpr unsigned kErrBadScratch = 2u;  // a ticket or record out of range: scratch not prepared
+
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ unsigned inc_relaxed_gpu(unsigned* counter, unsigned wrap) {
+    unsigned old;
+    asm volatile("atom.relaxed.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(counter), "r"(wrap) : "memory");
+    return old;
+}
+
+// Wait (bounded) until the record at p is published; an empty record on expiry.
+__device__ __forceinline__ unsigned long long wait_record(const unsigned long long* p, unsigned long long limit_ns,
+                                                          unsigned* err) {
+    const unsigned long long t0 = global_timer_ns();
+    for (;;) {
+        const unsigned long long w = ld_acquire_gpu_u64(p);
+        if (static_cast<unsigned>(w) != 0) return w;
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicOr(err, kErrWaitExpired);
+            return kNoElement;
+        }
+        __nanosleep(64);
+    }
+}
+
+template <class CT>
+__device__ __forceinline__ unsigned long long make_record(const KI<CT>& a) {
+    if (a.k == 0) return kNoElement;
+    const unsigned long long lo = static_cast<unsigned>(a.i) + 1u;
+    if constexpr (sizeof(typename CT::key) <= 4) return (static_cast<unsigned long long>(a.k) << 32) | lo;
+    return lo;
+}
+
+template <class CT, int OP, int ITEMS>
+__global__ void __launch_bounds__(1024)
+cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols, int chunks,
+                 int64_t* __restrict__ out_idx, typename CT::raw* __restrict__ out_val,
+                 unsigned char* __restrict__ scratch, int test_expire) {
+    using R = typename CT::raw;
+    using K = typename CT::key;
+    constexpr bool kKeyInRecord = sizeof(K) <= 4;
+    extern __shared__ __align__(16) unsigned char cum_smem[];
+    __shared__ KI<CT> warp_tot[32];
+    __shared__ KI<CT> s_total;
+    __shared__ unsigned s_flag;
+    const int t = threadIdx.x;
+    const int nt = blockDim.x;
+    unsigned* const err = reinterpret_cast<unsigned*>(scratch);
+    unsigned* const ticket_ctr = reinterpret_cast<unsigned*>(scratch + kCumTicketOffset);
+    unsigned* const done_ctr = reinterpret_cast<unsigned*>(scratch + kCumDoneOffset);
+    unsigned long long* const records = reinterpret_cast<unsigned long long*>(scratch + kCumRecordsOffset);
+    const unsigned total = static_cast<unsigned>(rows) * static_cast<unsigned>(chunks);
+    const unsigned long long limit_ns = test_expire ? 2ull * 1000 * 1000 : kWaitLimitNs;
+
+    grid_dependency_wait();  // the previous call's counters and records are settled
+    if (t == 0) s_flag = arrive_acq_rel(ticket_ctr, total - 1);
+    __syncthreads();
+    allow_dependents();
+    const unsigned ticket = s_flag;
+    if (ticket >= total) {  // only with a scratch buffer that was never prepared
+        if (t == 0) atomicOr(err, kErrBadScratch);
+        return;
+    }
+    const int64_t r = ticket / static_cast<unsigned>(chunks);
+    const int c = static_cast<int>(ticket % static_cast<unsigned>(chunks));
+    const R* row = x + r * static_cast<int64_t>(cols);
+    const int cb = static_cast<int>(static_cast<int64_t>(cols) * c / chunks);
+    const int ce = static_cast<int>(static_cast<int64_t>(cols) * (c + 1) / chunks);
+    const R x0 = ld_scalar(row);
+    R v[ITEMS];
+    load_first_tile<CT, ITEMS>(row, cb, ce, v);
+    KI<CT> seed;
+    seed.k = CT::template seed_key<OP>(x0);
+    seed.i = 0;
+
+    const KI<CT> a = chunk_aggregate<CT, OP, ITEMS>(row, cb, ce, v, warp_tot);
+    unsigned long long* const row_records = records + r * chunks;
+    // Publish (the test flag leaves chunk 0's record unset: every wait on it expires).
+    if (t == 0 && !(test_expire && c == 0)) st_release_gpu_u64(row_records + c, make_record(a));
+
+    // Merge the records of chunks 0 .. c-1 (all loads first, then the waits).
+    KI<CT> acc = ki_identity<CT>();
+    for (int j0 = t; j0 < c; j0 += 4 * nt) {
+        unsigned long long w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) w[u] = j0 + u * nt < c ? ld_acquire_gpu_u64(row_records + j0 + u * nt) : kNoElement;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (static_cast<unsigned>(w[u]) == 0) w[u] = wait_record(row_records + j0 + u * nt, limit_ns, err);
+        R xv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const unsigned lo = static_cast<unsigned>(w[u]);
+            if (lo != kNoElement && lo - 1u >= static_cast<unsigned>(cols)) {  // not a record of this call
+                atomicOr(err, kErrBadScratch);
+                w[u] = kNoElement;
+            }
+            if (!kKeyInRecord && static_cast<unsigned>(w[u]) != kNoElement)
+                xv[u] = ld_scalar(row + (static_cast<unsigned>(w[u]) - 1u));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const unsigned lo = static_cast<unsigned>(w[u]);
+            if (lo != kNoElement) {
+                KI<CT> e;
+                if constexpr (kKeyInRecord) {
+                    e.k = static_cast<K>(w[u] >> 32);
+                } else {
+                    e.k = CT::template elem_key<OP>(xv[u]);
+                }
+                e.i = static_cast<int>(lo - 1u);
+                acc = first_best(acc, e);
+            }
+        }
+    }
+    __syncthreads();  // warp_tot is free again (chunk_aggregate's readers are done)
+    acc = block_first_best(acc, warp_tot);
+    unsigned done_old = 0;
+    if (t < 32) {
+        acc = first_best(seed, acc);
+        if (t == 0) {
+            s_total = acc;
+            // Every record this CTA needs has been read (the barrier above);
+            // count it done. The result is only needed after the scan.
+            fence_acq_rel_gpu();
+            done_old = inc_relaxed_gpu(done_ctr, total - 1);
+        }
+    }
+    __syncthreads();
+    const KI<CT> carry = s_total;
+    __syncthreads();  // s_total / warp_tot are reused by the scan
+    const R carry_v = carry.i == 0 ? x0 : ld_scalar(row + carry.i);
+    scan_chunk<CT, OP, ITEMS>(row, cb, ce, carry, carry_v, v, out_idx + r * static_cast<int64_t>(cols),
+                              out_val ? out_val + r * static_cast<int64_t>(cols) : nullptr, cum_smem, warp_tot,
+                              &s_total);
+    // The CTA that counted last clears the records of the whole launch.
+    if (t == 0) {
+        s_flag = done_old == total - 1 ? 1u : 0u;
+        if (s_flag) fence_acq_rel_gpu();
+    }
+    __syncthreads();
+    if (s_flag)
+        for (unsigned j = t; j < total; j += nt) records[j] = 0ull;
+}
+
+// ---------------------------------------------------------------------------
+// Launchers.
 // ---------------------------------------------------------------------------
 constexpr int kCumItems = 7;
 
-inline size_t cum_smem_bytes(int block, int es) { return static_cast<size_t>(block) * kCumItems * (2 * es + 4); }
+inline size_t cum_smem_bytes(int block, int es) { return static_cast<size_t>(block) * kCumItems * (es + 4); }
 
-template <class CT, int OP>
-cudaError_t launch_cum_op(const argr_plan& p, const Problem& pr) {
-    using R = typename CT::raw;
-    auto kern = cum_kernel<CT, OP, kCumItems>;
-    const size_t smem = cum_smem_bytes(p.block, sizeof(R));
-    static thread_local size_t smem_set = 0;
+// Raise the kernel's dynamic shared memory limit when needed; `smem_set` is
+// the caller's record for that one kernel (max and min kernels share a type).
+template <class K>
+cudaError_t set_cum_smem(K kern, size_t smem, size_t& smem_set) {
     if (smem > 48 * 1024 && smem > smem_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         smem_set = smem;
     }
+    return cudaSuccess;
+}
+
+template <class CT, int OP>
+cudaError_t launch_cum_split(const argr_plan& p, const Problem& pr) {
+    using R = typename CT::raw;
+    auto kern = cum_split_kernel<CT, OP, kCumItems>;
+    const size_t smem = cum_smem_bytes(p.block, sizeof(R));
+    static thread_local size_t smem_set = 0;
+    cudaError_t e = set_cum_smem(kern, smem, smem_set);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(static_cast<unsigned>(pr.rows * p.blocks_per_row));
+    return launch_ex_smem(kern, grid, dim3(p.block), 1, smem, p, pr.stream, static_cast<const R*>(pr.x), pr.rows,
+                          pr.cols, static_cast<int>(p.blocks_per_row), pr.out_idx, static_cast<R*>(pr.out_val),
+                          static_cast<unsigned char*>(pr.scratch), (p.flags & ARGR_PLAN_TEST_EXPIRE) ? 1 : 0);
+}
+
+template <class CT, int OP>
+cudaError_t launch_cum_op(const argr_plan& p, const Problem& pr) {
+    using R = typename CT::raw;
+    if (p.path == ARGR_PATH_CUM_SPLIT) return launch_cum_split<CT, OP>(p, pr);
+    auto kern = cum_kernel<CT, OP, kCumItems>;
+    const size_t smem = cum_smem_bytes(p.block, sizeof(R));
+    static thread_local size_t smem_set = 0;
+    cudaError_t e = set_cum_smem(kern, smem, smem_set);
+    if (e != cudaSuccess) return e;
     const int C = p.cluster > 1 ? p.cluster : 1;
     if (C > 8) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
     const dim3 grid(static_cast<unsigned>(C), static_cast<unsigned>(p.grid_rows));
@@ -370,7 +668,7 @@ cudaError_t launch_cum_op(const argr_plan& p, const Problem& pr) {
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
             int n = 0;
-            cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+            e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
             if (e != cudaSuccess) return e;
             checked_block = p.block;
             checked_cluster = C;

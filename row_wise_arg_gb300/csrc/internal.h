@@ -24,10 +24,20 @@ namespace argr {
 //                              one uint32 arrival counter per row slot
 //   [kPartialsOffset, ...)     row_slots * blocks_per_row partials of 16 bytes
 //                              (raw value bits in the low 8 bytes, index in 4)
+//   argreduce_cum's split scan (ARGR_PATH_CUM_SPLIT) uses, in the same buffer:
+//   [kCumTicketOffset, +4)     ticket counter (wraps to 0 after each launch)
+//   [kCumDoneOffset, +4)       done counter (wraps to 0 after each launch)
+//   [kCounterOffset, +8*kCumMaxChunks)
+//                              one 64-bit record per chunk, zeroed again by the
+//                              launch's last CTA, so the split counters stay 0
 constexpr size_t kCounterOffset = 256;
 constexpr int64_t kMaxSplitRows = 2048;  // row slots a multi-CTA split may use
 constexpr size_t kPartialsOffset = kCounterOffset + 4 * kMaxSplitRows;
 constexpr size_t kPartialBytes = 16;
+constexpr size_t kCumTicketOffset = 4;
+constexpr size_t kCumDoneOffset = 8;
+constexpr size_t kCumRecordsOffset = kCounterOffset;
+constexpr int64_t kCumMaxChunks = kMaxSplitRows / 2;  // rows * chunks of one split-scan launch
 
 ARGR_HD inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

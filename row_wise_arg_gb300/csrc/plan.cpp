@@ -79,6 +79,14 @@ int elem_size(int dtype) {
 // tiles of block * 7 elements.
 // ---------------------------------------------------------------------------
 static constexpr int kCumItems = 7;
+// Measured on GB300 (a sweep of cluster and split geometries over rows of
+// 16K..16M elements): clusters win up to 32K elements per row, the split scan
+// beyond, best at about one CTA per 3.5K elements, 76..608 CTAs in total.
+static constexpr int64_t kCumSplitWaves = 4;        // split-scan CTAs per SM at most
+static constexpr int64_t kCumMinChunkTiles = 2;     // rows shorter than 2 x 2 tiles are not split
+static constexpr int64_t kCumMinChunk = 512;        // elements per split-scan or cluster CTA at least
+static constexpr int64_t kCumSplitElems = 3584;     // elements per split-scan CTA the planner aims for
+static constexpr int64_t kCumClusterMaxCols = 32768;
 
 argr_status make_cum_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_caps& caps, argr_plan* out) {
     if (!out) return ARGR_EINVAL;
@@ -94,18 +102,44 @@ argr_status make_cum_plan(int64_t rows, int64_t cols, int dtype, int op, const a
     int block = 32;
     while (block < 256 && block * kCumItems < cols) block <<= 1;
     const int64_t tile = static_cast<int64_t>(block) * kCumItems;
-    int64_t c = 1;
     const int64_t sms = caps.sm_count;
-    if (rows < 2 * sms && rows <= kMaxGridY && caps.max_cluster >= 2) {
-        c = std::min<int64_t>({16, caps.max_cluster, ceil_div(2 * sms, rows), cols / (2 * tile)});
-        c = std::max<int64_t>(1, c);
-    }
-    out->path = ARGR_PATH_CUM;
     out->block = block;
-    out->cluster = static_cast<int32_t>(c);
-    out->blocks_per_row = c;
-    out->grid_rows = c > 1 ? rows : std::min(rows, kMaxGridY);
     out->flags = ARGR_PLAN_PDL;
+    out->cluster = 1;
+    out->blocks_per_row = 1;
+    out->grid_rows = std::min(rows, kMaxGridY);
+    if (rows >= kCumSplitWaves * sms || cols < kCumMinChunkTiles * 2 * tile) {
+        out->path = ARGR_PATH_CUM;  // enough rows, or rows too short to split: one CTA per row
+        return ARGR_OK;
+    }
+    if (cols <= kCumClusterMaxCols && rows <= sms && caps.max_cluster >= 2) {
+        // Short rows: a cluster per row exchanges aggregates through
+        // distributed shared memory, a round trip cheaper than scratch.
+        const int64_t c = std::min<int64_t>({16, caps.max_cluster, ceil_div(2 * sms, rows),
+                                             std::max<int64_t>(2, cols / kCumMinChunk)});
+        out->path = ARGR_PATH_CUM;
+        out->block = 256;
+        out->cluster = static_cast<int32_t>(c);
+        out->blocks_per_row = c;
+        out->grid_rows = rows;
+        return ARGR_OK;
+    }
+    // Long rows: a split scan with one CTA per kCumSplitElems elements in
+    // total, at least half an SM's worth and at most kCumSplitWaves per SM.
+    const int64_t target = std::min(kCumSplitWaves * sms, std::max(sms / 2, ceil_div(rows * cols, kCumSplitElems)));
+    const int64_t chunks = std::min<int64_t>({kCumMaxChunks / rows, ceil_div(target, rows), cols / kCumMinChunk});
+    if (chunks < 2) {
+        out->path = ARGR_PATH_CUM;
+        return ARGR_OK;
+    }
+    const int64_t per_chunk = ceil_div(cols, chunks);
+    int b = 64;
+    while (b < 512 && b * kCumItems < per_chunk) b <<= 1;
+    out->path = ARGR_PATH_CUM_SPLIT;
+    out->block = b;
+    out->blocks_per_row = chunks;
+    out->grid_rows = rows;
+    out->scratch_bytes = plan_scratch(*out, rows);
     return ARGR_OK;
 }
 
@@ -113,20 +147,28 @@ argr_status check_cum_plan(const argr_plan& p, int64_t rows, int64_t cols, int d
     if (elem_size(dtype) == 0 || rows < 0 || cols < 1 || cols > INT_MAX) return ARGR_EINVAL;
     if (op != ARGR_MAX && op != ARGR_MIN) return ARGR_EUNSUPPORTED;
     if (rows == 0) return ARGR_OK;
-    if (p.path != ARGR_PATH_CUM) return ARGR_EINVAL;
     if (p.block < 32 || p.block > 1024 || p.block % 32 != 0) return ARGR_EINVAL;
+    const int64_t smem = static_cast<int64_t>(p.block) * kCumItems * (elem_size(dtype) + 4);
+    if (smem > kMaxDynamicSmem) return ARGR_EINVAL;
+    if (p.path == ARGR_PATH_CUM_SPLIT) {
+        if (p.flags & ~(ARGR_PLAN_PDL | ARGR_PLAN_TEST_EXPIRE)) return ARGR_EINVAL;
+        if (p.cluster != 1 || p.blocks_per_row < 1 || p.blocks_per_row > kCumMaxChunks) return ARGR_EINVAL;
+        if (rows > kCumMaxChunks / p.blocks_per_row) return ARGR_EINVAL;  // records of one launch
+        if (p.grid_rows != rows) return ARGR_EINVAL;
+        return ARGR_OK;
+    }
+    if (p.path != ARGR_PATH_CUM) return ARGR_EINVAL;
     if (p.flags & ~ARGR_PLAN_PDL) return ARGR_EINVAL;
     if (p.cluster < 1 || p.cluster > 16 || p.blocks_per_row != p.cluster) return ARGR_EINVAL;
     if (p.cluster > 1 && caps.max_cluster < p.cluster) return ARGR_EUNSUPPORTED;
     if (p.grid_rows < 1 || p.grid_rows > kMaxGridY) return ARGR_EINVAL;
     if (p.cluster > 1 && p.grid_rows < rows) return ARGR_EINVAL;
-    const int64_t smem = static_cast<int64_t>(p.block) * kCumItems * (2 * elem_size(dtype) + 4);
-    if (smem > kMaxDynamicSmem) return ARGR_EINVAL;
     return ARGR_OK;
 }
 
 size_t plan_scratch(const argr_plan& p, int64_t rows) {
-    (void)rows;
+    if (p.path == ARGR_PATH_CUM_SPLIT)
+        return kCumRecordsOffset + 8 * static_cast<size_t>(rows) * static_cast<size_t>(p.blocks_per_row);
     if (p.path == ARGR_PATH_SPLIT && p.blocks_per_row > 1)
         return kPartialsOffset +
                static_cast<size_t>(p.grid_rows) * static_cast<size_t>(p.blocks_per_row) * kPartialBytes;

@@ -1,8 +1,10 @@
 """GPU parity of cummax / cummin with indices (argreduce_cum) against the CPU
 oracle, bit for bit: the Paddle-issue workloads at full size, and every
 forced geometry (one CTA per row with row loops, clusters of 2..16 CTAs per
-row, tile widths from 32 to 1024 threads) on special-value rows of every
-element type, including leading NaNs and the integer extremes."""
+row, split scans of 2..1024 chunks exchanging aggregates through scratch,
+tile widths from 32 to 1024 threads) on special-value rows of every element
+type, including leading NaNs and the integer extremes; plus the split scan's
+scratch handling (shared with argreduce, graph replay, a forced expiry)."""
 import numpy as np
 import pytest
 
@@ -39,16 +41,27 @@ def cum_plan(cluster=1, block=256, grid=1, pdl=True):
     return p
 
 
-def run_cum(x, dtype, op, plan=None):
+def split_plan(chunks, block=256, rows=1, flags=_lib.ARGR_PLAN_PDL):
+    p = _lib.argr_plan()
+    p.path = _lib.ARGR_PATH_CUM_SPLIT
+    p.block = block
+    p.cluster = 1
+    p.blocks_per_row = chunks
+    p.grid_rows = rows
+    p.flags = flags
+    return p
+
+
+def run_cum(x, dtype, op, plan=None, scratch=None):
     xd = torch.from_numpy(np.ascontiguousarray(x).view(VIEW[dtype])).cuda()
-    idx, val = A.argreduce_cum(xd, op, dtype=dtype, plan=plan)
+    idx, val = A.argreduce_cum(xd, op, dtype=dtype, plan=plan, scratch=scratch)
     torch.cuda.synchronize()
     raw_t = oracle.RAW_NP[dtype]
     return idx.cpu().numpy(), val.cpu().numpy().view(raw_t)
 
 
-def check_cum(x, dtype, op, plan=None):
-    idx, val = run_cum(x, dtype, op, plan)
+def check_cum(x, dtype, op, plan=None, scratch=None):
+    idx, val = run_cum(x, dtype, op, plan, scratch)
     eidx, evalue = oracle.cumreduce(x, dtype, op)
     bad = np.argwhere(idx != eidx)
     assert bad.size == 0, f"{len(bad)} outputs differ, first {bad[:3].tolist()}: got {idx[tuple(bad[0])]} " \
@@ -83,6 +96,9 @@ def test_cum_forced_geometries(dtype):
             for cluster, block in ((1, 32), (1, 1024), (2, 64), (5, 256), (16, 32), (16, 128)):
                 check_cum(x, dtype, op, plan=cum_plan(cluster, block, grid=rows, pdl=cluster != 5))
             check_cum(x, dtype, op, plan=cum_plan(1, 128, grid=1))  # one CTA loops over every row
+            for chunks, block in ((2, 32), (3, 1024), (7, 64), (64, 256)):
+                if rows * chunks <= 1024:  # chunks > cols leaves some chunks empty
+                    check_cum(x, dtype, op, plan=split_plan(chunks, block, rows, flags=chunks % 2))
 
 
 def test_cum_leading_nan_and_extremes():
@@ -116,3 +132,95 @@ def test_cum_rejections():
     with pytest.raises(A.ArgreduceError) as e:
         A.argreduce(xi, "max")  # the integer types are for the scan only
     assert e.value.status == _lib.ARGR_EUNSUPPORTED
+
+
+def test_cum_split_many_chunks():
+    # the planner's split at the pages' lengths, and the largest record count
+    for n, dtype in ((65536, "i64"), (131072, "i64"), (1 << 20, "f32"), (5 << 20, "bf16")):
+        x = cum_rows(dtype, 1, n, seed=n)
+        assert A.argreduce_cum_plan(1, n, dtype, "max").as_dict()["path_name"] == "cum_split"
+        check_cum(x, dtype, "max")
+    x = cum_rows("f64", 2, 300001, seed=5)
+    check_cum(x, "f64", "min", plan=split_plan(512, 128, rows=2))
+    x = cum_rows("f16", 1, 300001, seed=7)
+    check_cum(x, "f16", "max", plan=split_plan(1024, 32, rows=1))
+    x = cum_rows("i32", 1024, 40, seed=6)
+    check_cum(x, "i32", "max", plan=split_plan(1, 32, rows=1024))
+
+
+def test_cum_split_scratch_shared_with_argreduce_and_graphs():
+    """One scratch buffer serves argreduce's split path (per-row counters that
+    must stay zero between calls) and the split scan (records in the same
+    region, cleared by each launch's last CTA) one call after the other, on
+    one stream, eagerly and replayed from CUDA graphs."""
+    from gpu_util import forced_plan
+    sc = A.Scratch()
+    xs = cum_rows("f32", 3, 70001, seed=11)
+    xr = W.fuzz_rows("f32", 3, 3_000_000, seed=12)
+    er, _, _ = oracle.argreduce(xr, "f32", "max")
+    xrd = torch.from_numpy(xr).cuda()
+    rplan = forced_plan("split", bpr=8, grid_rows=3)
+    xsd = torch.from_numpy(xs).cuda()
+    eidx, _ = oracle.cumreduce(xs, "f32", "min")
+    splan = split_plan(40, 256, rows=3)
+    for _ in range(3):
+        idx, _ = A.argreduce_cum(xsd, "min", plan=splan, scratch=sc, with_values=False)
+        got, _ = A.argreduce_with_plan(rplan, xrd, "max", scratch=sc)
+        torch.cuda.synchronize()
+        assert (idx.cpu().numpy() == eidx).all() and (got.cpu().numpy() == er).all()
+    assert A.argreduce_read_error(sc.ptr, 0) == _lib.ARGR_OK
+    s = torch.cuda.Stream()
+    out_i = torch.empty(3, 70001, dtype=torch.int64, device="cuda")
+    out_r = torch.empty(3, dtype=torch.int64, device="cuda")
+    with torch.cuda.stream(s):
+        A.argreduce_cum(xsd, "min", plan=splan, scratch=sc, out_idx=out_i, with_values=False, stream=s)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            A.argreduce_cum(xsd, "min", plan=splan, scratch=sc, out_idx=out_i, with_values=False, stream=s)
+            A.argreduce_with_plan(rplan, xrd, "max", scratch=sc, out_idx=out_r, stream=s)
+            A.argreduce_cum(xsd, "min", scratch=sc, out_idx=out_i, with_values=False, stream=s)
+        for _ in range(5):
+            out_i.zero_()
+            out_r.zero_()
+            g.replay()
+            s.synchronize()
+            assert (out_i.cpu().numpy() == eidx).all() and (out_r.cpu().numpy() == er).all()
+    assert A.argreduce_read_error(sc.ptr, 0) == _lib.ARGR_OK
+
+
+def test_cum_split_bounded_wait_expires():
+    """Chunk 0 never publishes its record (test flag): every other CTA's wait
+    for it gives up after 2 ms, the expiry is reported as ARGR_ETIMEOUT, and
+    the counters and records are left clean, so the next call is exact."""
+    sc = A.Scratch()
+    x = cum_rows("i64", 2, 50000, seed=13)
+    xd = torch.from_numpy(x).cuda()
+    A.argreduce_cum(xd, "max", plan=split_plan(9, 128, rows=2, flags=_lib.ARGR_PLAN_TEST_EXPIRE), scratch=sc)
+    assert A.argreduce_read_error(sc.ptr, 0) == _lib.ARGR_ETIMEOUT
+    assert A.argreduce_read_error(sc.ptr, 0) == _lib.ARGR_OK  # cleared
+    check_cum(x, "i64", "max", plan=split_plan(9, 128, rows=2), scratch=sc)
+    check_cum(x, "i64", "max", plan=split_plan(5, 256, rows=2), scratch=sc)
+    assert A.argreduce_read_error(sc.ptr, 0) == _lib.ARGR_OK
+
+
+def test_cum_split_rejections():
+    x = torch.zeros(4, 100000, device="cuda")
+    o = torch.empty(4, 100000, dtype=torch.int64, device="cuda")
+    p = split_plan(8, 256, rows=4)
+    assert _lib.argreduce_cum_raw(x.data_ptr(), "f32", 4, 100000, "max", o.data_ptr(), 0, 0, 0, 0, p) == \
+        _lib.ARGR_ESCRATCH  # no scratch
+    sc = A.Scratch(nbytes=4096)
+    assert _lib.argreduce_cum_raw(x.data_ptr(), "f32", 4, 100000, "max", o.data_ptr(), 0, sc.ptr + 8, 4000, 0,
+                                  p) == _lib.ARGR_ESCRATCH  # misaligned
+    assert _lib.argreduce_cum_raw(x.data_ptr(), "f32", 4, 100000, "max", o.data_ptr(), 0, sc.ptr, 200, 0,
+                                  p) == _lib.ARGR_ESCRATCH  # too small
+    for bad in (split_plan(257, 256, rows=4), split_plan(8, 256, rows=3), split_plan(8, 48, rows=4),
+                split_plan(8, 256, rows=4, flags=_lib.ARGR_PLAN_BULK)):
+        assert _lib.argreduce_cum_raw(x.data_ptr(), "f32", 4, 100000, "max", o.data_ptr(), 0, sc.ptr, 4096, 0,
+                                      bad) == _lib.ARGR_EINVAL
+    bad = split_plan(8, 256, rows=4)
+    bad.cluster = 2
+    assert _lib.argreduce_cum_raw(x.data_ptr(), "f32", 4, 100000, "max", o.data_ptr(), 0, sc.ptr, 4096, 0,
+                                  bad) == _lib.ARGR_EINVAL
+    torch.cuda.synchronize()

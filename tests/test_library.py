@@ -384,17 +384,78 @@ def test_axis_plans():
 
 
 def test_cum_plans_and_validation():
+    seen = set()
     for rows, cols, dt in [(1, 65536, "i64"), (1, 262144, "i64"), (64, 1024, "i64"), (1024, 64, "i64"),
-                           (4, 16384, "i32"), (1, 65536, "f32"), (256, 256, "bf16"), (1, 3, "f64")]:
+                           (4, 16384, "i32"), (1, 65536, "f32"), (256, 256, "bf16"), (1, 3, "f64"),
+                           (1, 16777216, "i64"), (64, 65536, "f32"), (600, 100000, "f16"), (1, 16384, "i64"),
+                           (200, 30000, "f32"), (4096, 4096, "f32")]:
         d = A.argreduce_cum_plan(rows, cols, dt, "max", GB300).as_dict()
-        assert d["path_name"] == "cum" and d["scratch_bytes"] == 0
-        assert 32 <= d["block"] <= 256 and 1 <= d["cluster"] <= 16
-        if d["cluster"] > 1:
-            assert d["grid_rows"] == rows and rows * d["cluster"] <= 2 * 152 + 16
+        seen.add((d["path_name"], d["cluster"] > 1))
+        if d["path_name"] == "cum_split":
+            # long rows, too few for the GPU: 76..608 CTAs, records of one launch <= 1024
+            chunks = d["blocks_per_row"]
+            assert rows < 4 * 152 and chunks >= 2 and rows * chunks <= 1024
+            assert rows * chunks <= 4 * 152 + rows and (rows * chunks >= 76 or chunks == 1024 // rows or
+                                                       cols // chunks < 1024)
+            assert cols // chunks >= 512
+            assert d["block"] in (64, 128, 256, 512) and (d["block"] * 7 >= -(-cols // chunks) or d["block"] == 512)
+            assert d["scratch_bytes"] == 256 + 8 * rows * chunks and d["cluster"] == 1
+            assert d["grid_rows"] == rows and (cols > 32768 or rows > 152)
+        elif d["cluster"] > 1:
+            # short rows, few of them: one cluster per row
+            assert d["path_name"] == "cum" and cols <= 32768 and rows <= 152 and d["cluster"] <= 16
+            assert d["block"] == 256 and d["grid_rows"] == rows and d["scratch_bytes"] == 0
+            assert d["blocks_per_row"] == d["cluster"]
+        else:
+            assert d["path_name"] == "cum" and d["scratch_bytes"] == 0 and 32 <= d["block"] <= 256
+            assert rows >= 4 * 152 or cols < 4 * 7 * d["block"] or rows > 1024 // 2
+    assert seen == {("cum_split", False), ("cum", True), ("cum", False)}
+    assert A.argreduce_cum_plan(1, 16777216, "i64", "max", GB300).as_dict()["blocks_per_row"] == 608
+    assert A.argreduce_cum_plan(1, 65536, "i64", "max", GB300).as_dict()["blocks_per_row"] == 76
+    assert A.argreduce_cum_plan(4, 16384, "i32", "max", GB300).as_dict()["cluster"] == 16
     with pytest.raises(A.ArgreduceError):
         A.argreduce_cum_plan(1, 10, "f32", "max_last", GB300)
     X = 0x10000
-    assert _lib.argreduce_cum_raw(X, "i64", 0, 10, "max", X, 0, 0) == _lib.ARGR_OK
-    assert _lib.argreduce_cum_raw(X, "i64", 2, 0, "max", X, 0, 0) == _lib.ARGR_EINVAL
-    assert _lib.argreduce_cum_raw(X, "i64", 2, 10, "min_last", X, 0, 0) == _lib.ARGR_EUNSUPPORTED
+    assert _lib.argreduce_cum_raw(X, "i64", 0, 10, "max", X, 0, 0, 0, 0) == _lib.ARGR_OK
+    assert _lib.argreduce_cum_raw(X, "i64", 2, 0, "max", X, 0, 0, 0, 0) == _lib.ARGR_EINVAL
+    assert _lib.argreduce_cum_raw(X, "i64", 2, 10, "min_last", X, 0, 0, 0, 0) == _lib.ARGR_EUNSUPPORTED
     assert _lib.argreduce_raw(X, "i64", 2, 10, "max", X, 0, 0, 0, 0) == _lib.ARGR_EUNSUPPORTED
+
+
+def test_cum_split_index_arithmetic():
+    """Host simulation of the split scan's ticket, chunk and record arithmetic
+    (the kernel's integer formulas, restated): tickets 0..total-1 map to
+    distinct (row, chunk) pairs, every row's chunks partition [0, cols) in
+    order (empty chunks allowed), every 8-byte record lies in the 8 KiB
+    region after the 256-byte header and inside the plan's scratch, and a
+    record's index + 1 never collides with 0 (unpublished) or 0xffffffff
+    (empty chunk)."""
+    for rows, cols, chunks in [(1, 65536, 18), (1, 5, 7), (3, 7, 5), (1024, 1, 1), (1, 2**31 - 1, 1024),
+                               (2, 2**31 - 1, 512), (16, 65536, 64), (5, 4099, 204)]:
+        total = rows * chunks
+        assert total <= 1024
+        seen = set()
+        for ticket in range(total):
+            r, c = divmod(ticket, chunks)
+            seen.add((r, c))
+            word = 256 + 8 * (r * chunks + c)
+            assert 256 <= word and word + 8 <= 256 + 8 * total <= 256 + 8 * 1024 == 8448
+        assert len(seen) == total
+        for c_ in range(chunks):
+            cb = cols * c_ // chunks
+            ce = cols * (c_ + 1) // chunks
+            assert 0 <= cb <= ce <= cols and cb < 2**31 and ce < 2**31
+            if c_ + 1 < chunks:
+                assert ce == cols * (c_ + 1) // chunks  # the next chunk starts where this one ends
+            if ce > cb:
+                assert 1 <= (ce - 1) + 1 < 0xffffffff
+        assert cols * chunks // chunks == cols
+    # the wrapping counters: atom.inc with bound total-1 hands out 0..total-1 and ends at 0
+    for total in (1, 2, 18, 1024):
+        ctr, got = 0, []
+        for _ in range(total):
+            got.append(ctr)
+            ctr = 0 if ctr >= total - 1 else ctr + 1
+        assert got == list(range(total)) and ctr == 0
+
+
