@@ -358,9 +358,11 @@ __device__ __forceinline__ void scan_chunk(const typename CT::raw* row, int cb, 
     }
 }
 
-// One CTA per row (C = 1), or a cluster of C CTAs per row whose chunk
-// aggregates are exchanged through distributed shared memory.
-template <class CT, int OP, int ITEMS>
+// One CTA per row (CLUSTER false: C = 1, the CTA loops over rows), or a
+// cluster of C CTAs per row whose chunk aggregates are exchanged through
+// distributed shared memory. Separate instantiations keep the cluster code out
+// of the one-CTA kernel's registers.
+template <class CT, int OP, int ITEMS, bool CLUSTER>
 __global__ void __launch_bounds__(1024)
 cum_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols, int64_t* __restrict__ out_idx,
            typename CT::raw* __restrict__ out_val) {
@@ -371,10 +373,10 @@ cum_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols, int64
     __shared__ KI<CT> s_total;
     __shared__ __align__(16) uint4 agg_slots[2][kCumMaxCluster];  // aggregates pushed by earlier CTAs
     const int t = threadIdx.x;
-    const int C = gridDim.x;
-    const int b = blockIdx.x;
+    const int C = CLUSTER ? static_cast<int>(gridDim.x) : 1;
+    const int b = CLUSTER ? static_cast<int>(blockIdx.x) : 0;
     bool started = false;
-    if (C > 1) cluster_started_arrive();
+    if (CLUSTER) cluster_started_arrive();
     grid_dependency_wait();
     allow_dependents();
     int parity = 0;
@@ -389,7 +391,7 @@ cum_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols, int64
         carry.k = CT::template seed_key<OP>(x0);
         carry.i = 0;
         R carry_v = x0;
-        if (C > 1) {
+        if constexpr (CLUSTER) {
             const KI<CT> a = chunk_aggregate<CT, OP, ITEMS>(row, cb, ce, v, warp_tot);
             if (!started) {  // every CTA of the cluster runs before the first remote write
                 cluster_started_wait();
@@ -424,7 +426,7 @@ cum_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols, int64
                                   out_val ? out_val + r * static_cast<int64_t>(cols) : nullptr, cum_smem, warp_tot,
                                   &s_total);
     }
-    if (C > 1 && !started) cluster_started_wait();  // complete the start phase even with no rows
+    if (CLUSTER && !started) cluster_started_wait();  // complete the start phase even with no rows
 }
 
 // ---------------------------------------------------------------------------
@@ -641,18 +643,27 @@ template <class CT, int OP>
 cudaError_t launch_cum_op(const argr_plan& p, const Problem& pr) {
     using R = typename CT::raw;
     if (p.path == ARGR_PATH_CUM_SPLIT) return launch_cum_split<CT, OP>(p, pr);
-    auto kern = cum_kernel<CT, OP, kCumItems>;
     const size_t smem = cum_smem_bytes(p.block, sizeof(R));
+    if (p.cluster <= 1) {
+        auto kern1 = cum_kernel<CT, OP, kCumItems, false>;
+        static thread_local size_t smem_set1 = 0;
+        cudaError_t e = set_cum_smem(kern1, smem, smem_set1);
+        if (e != cudaSuccess) return e;
+        return launch_ex_smem(kern1, dim3(1, static_cast<unsigned>(p.grid_rows)), dim3(p.block), 1, smem, p,
+                              pr.stream, static_cast<const R*>(pr.x), pr.rows, pr.cols, pr.out_idx,
+                              static_cast<R*>(pr.out_val));
+    }
+    auto kern = cum_kernel<CT, OP, kCumItems, true>;
     static thread_local size_t smem_set = 0;
     cudaError_t e = set_cum_smem(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
-    const int C = p.cluster > 1 ? p.cluster : 1;
+    const int C = p.cluster;
     if (C > 8) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
     const dim3 grid(static_cast<unsigned>(C), static_cast<unsigned>(p.grid_rows));
-    if (C > 1) {
+    {
         // Refuse a cluster shape the device cannot co-schedule (checked once per shape).
         static thread_local int checked_block = 0, checked_cluster = 0, checked_ok = 0;
         if (checked_block != p.block || checked_cluster != C) {

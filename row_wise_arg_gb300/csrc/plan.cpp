@@ -79,10 +79,13 @@ int elem_size(int dtype) {
 // tiles of block * 7 elements.
 // ---------------------------------------------------------------------------
 static constexpr int kCumItems = 7;
-// Measured on GB300 (a sweep of cluster and split geometries over rows of
-// 16K..16M elements): clusters win up to 32K elements per row, the split scan
-// beyond, best at about one CTA per 3.5K elements, 76..608 CTAs in total.
-static constexpr int64_t kCumSplitWaves = 4;        // split-scan CTAs per SM at most
+// Measured on GB300 (sweeps of one-CTA, cluster and split geometries over
+// rows of 256 to 16M elements): one CTA per row once there are as many rows as
+// SMs (128 threads or fewer when rows are plentiful), clusters up to 32K
+// elements per row, the split scan beyond, best at about one CTA per 3.5K
+// elements: 76..304 CTAs of up to 512 threads for one row, up to 608 CTAs of
+// up to 256 threads for several.
+static constexpr int64_t kCumManyRowsWaves = 4;     // rows per SM from which CTAs shrink
 static constexpr int64_t kCumMinChunkTiles = 2;     // rows shorter than 2 x 2 tiles are not split
 static constexpr int64_t kCumMinChunk = 512;        // elements per split-scan or cluster CTA at least
 static constexpr int64_t kCumSplitElems = 3584;     // elements per split-scan CTA the planner aims for
@@ -99,42 +102,46 @@ argr_status make_cum_plan(int64_t rows, int64_t cols, int dtype, int op, const a
         out->path = ARGR_PATH_NONE;
         return ARGR_OK;
     }
-    int block = 32;
-    while (block < 256 && block * kCumItems < cols) block <<= 1;
-    const int64_t tile = static_cast<int64_t>(block) * kCumItems;
     const int64_t sms = caps.sm_count;
-    out->block = block;
     out->flags = ARGR_PLAN_PDL;
     out->cluster = 1;
     out->blocks_per_row = 1;
     out->grid_rows = std::min(rows, kMaxGridY);
-    if (rows >= kCumSplitWaves * sms || cols < kCumMinChunkTiles * 2 * tile) {
-        out->path = ARGR_PATH_CUM;  // enough rows, or rows too short to split: one CTA per row
+    out->path = ARGR_PATH_CUM;
+    int block = 32;
+    if (rows >= kCumManyRowsWaves * sms) {
+        // Many rows: one CTA per row, small CTAs (more of them resident per
+        // SM, fewer threads held by each barrier), at least two tiles a row.
+        while (block < 128 && 2 * block * kCumItems <= cols) block <<= 1;
+        out->block = block;
         return ARGR_OK;
     }
-    if (cols <= kCumClusterMaxCols && rows <= sms && caps.max_cluster >= 2) {
+    while (block < 256 && block * kCumItems < cols) block <<= 1;
+    out->block = block;
+    const int64_t tile = static_cast<int64_t>(block) * kCumItems;
+    if (cols < kCumMinChunkTiles * 2 * tile || rows >= sms) return ARGR_OK;  // one CTA per row
+    if (cols <= kCumClusterMaxCols && caps.max_cluster >= 2) {
         // Short rows: a cluster per row exchanges aggregates through
         // distributed shared memory, a round trip cheaper than scratch.
         const int64_t c = std::min<int64_t>({16, caps.max_cluster, ceil_div(2 * sms, rows),
                                              std::max<int64_t>(2, cols / kCumMinChunk)});
-        out->path = ARGR_PATH_CUM;
         out->block = 256;
         out->cluster = static_cast<int32_t>(c);
         out->blocks_per_row = c;
         out->grid_rows = rows;
         return ARGR_OK;
     }
-    // Long rows: a split scan with one CTA per kCumSplitElems elements in
-    // total, at least half an SM's worth and at most kCumSplitWaves per SM.
-    const int64_t target = std::min(kCumSplitWaves * sms, std::max(sms / 2, ceil_div(rows * cols, kCumSplitElems)));
+    // Long rows, fewer than the SMs: a split scan with one CTA per
+    // kCumSplitElems elements in total, from half an SM's worth up to two
+    // 512-thread CTAs per SM for one row, or four 256-thread CTAs for more.
+    const int64_t per_sm = rows == 1 ? 2 : 4;
+    const int max_block = rows == 1 ? 512 : 256;
+    const int64_t target = std::min(per_sm * sms, std::max(sms / 2, ceil_div(rows * cols, kCumSplitElems)));
     const int64_t chunks = std::min<int64_t>({kCumMaxChunks / rows, ceil_div(target, rows), cols / kCumMinChunk});
-    if (chunks < 2) {
-        out->path = ARGR_PATH_CUM;
-        return ARGR_OK;
-    }
+    if (chunks < 2) return ARGR_OK;
     const int64_t per_chunk = ceil_div(cols, chunks);
     int b = 64;
-    while (b < 512 && b * kCumItems < per_chunk) b <<= 1;
+    while (b < max_block && b * kCumItems < per_chunk) b <<= 1;
     out->path = ARGR_PATH_CUM_SPLIT;
     out->block = b;
     out->blocks_per_row = chunks;

@@ -388,31 +388,39 @@ def test_cum_plans_and_validation():
     for rows, cols, dt in [(1, 65536, "i64"), (1, 262144, "i64"), (64, 1024, "i64"), (1024, 64, "i64"),
                            (4, 16384, "i32"), (1, 65536, "f32"), (256, 256, "bf16"), (1, 3, "f64"),
                            (1, 16777216, "i64"), (64, 65536, "f32"), (600, 100000, "f16"), (1, 16384, "i64"),
-                           (200, 30000, "f32"), (4096, 4096, "f32")]:
+                           (200, 30000, "f32"), (4096, 4096, "f32"), (65536, 256, "f32"), (256, 65536, "f32"),
+                           (16, 1 << 20, "f64")]:
         d = A.argreduce_cum_plan(rows, cols, dt, "max", GB300).as_dict()
         seen.add((d["path_name"], d["cluster"] > 1))
         if d["path_name"] == "cum_split":
-            # long rows, too few for the GPU: 76..608 CTAs, records of one launch <= 1024
+            # long rows, fewer than the SMs: 76..304 CTAs, records of one launch <= 1024
             chunks = d["blocks_per_row"]
-            assert rows < 4 * 152 and chunks >= 2 and rows * chunks <= 1024
-            assert rows * chunks <= 4 * 152 + rows and (rows * chunks >= 76 or chunks == 1024 // rows or
-                                                       cols // chunks < 1024)
+            assert rows < 152 and chunks >= 2 and rows * chunks <= 1024 and cols > 32768
+            assert rows * chunks <= (2 if rows == 1 else 4) * 152 + rows
+            assert rows * chunks >= 76 or cols // chunks < 1024 or chunks == 1024 // rows
             assert cols // chunks >= 512
-            assert d["block"] in (64, 128, 256, 512) and (d["block"] * 7 >= -(-cols // chunks) or d["block"] == 512)
+            cap = 512 if rows == 1 else 256
+            assert d["block"] in (64, 128, 256, 512) and d["block"] <= cap
+            assert d["block"] * 7 >= -(-cols // chunks) or d["block"] == cap
             assert d["scratch_bytes"] == 256 + 8 * rows * chunks and d["cluster"] == 1
-            assert d["grid_rows"] == rows and (cols > 32768 or rows > 152)
+            assert d["grid_rows"] == rows
         elif d["cluster"] > 1:
-            # short rows, few of them: one cluster per row
-            assert d["path_name"] == "cum" and cols <= 32768 and rows <= 152 and d["cluster"] <= 16
+            # short rows, fewer than the SMs: one cluster per row
+            assert d["path_name"] == "cum" and cols <= 32768 and rows < 152 and d["cluster"] <= 16
             assert d["block"] == 256 and d["grid_rows"] == rows and d["scratch_bytes"] == 0
             assert d["blocks_per_row"] == d["cluster"]
         else:
+            # one CTA per row: as many rows as SMs, or rows too short to split
             assert d["path_name"] == "cum" and d["scratch_bytes"] == 0 and 32 <= d["block"] <= 256
-            assert rows >= 4 * 152 or cols < 4 * 7 * d["block"] or rows > 1024 // 2
+            assert rows >= 152 or cols < 4 * 7 * d["block"]
+            if rows >= 4 * 152:
+                assert d["block"] <= 128 and (d["block"] == 32 or d["block"] * 7 <= cols)
     assert seen == {("cum_split", False), ("cum", True), ("cum", False)}
-    assert A.argreduce_cum_plan(1, 16777216, "i64", "max", GB300).as_dict()["blocks_per_row"] == 608
+    assert A.argreduce_cum_plan(1, 16777216, "i64", "max", GB300).as_dict()["blocks_per_row"] == 304
     assert A.argreduce_cum_plan(1, 65536, "i64", "max", GB300).as_dict()["blocks_per_row"] == 76
     assert A.argreduce_cum_plan(4, 16384, "i32", "max", GB300).as_dict()["cluster"] == 16
+    assert A.argreduce_cum_plan(4096, 4096, "f32", "max", GB300).as_dict()["block"] == 128
+    assert A.argreduce_cum_plan(65536, 256, "f32", "max", GB300).as_dict()["block"] == 32
     with pytest.raises(A.ArgreduceError):
         A.argreduce_cum_plan(1, 10, "f32", "max_last", GB300)
     X = 0x10000
