@@ -86,6 +86,27 @@ def n_outputs(c: W.Case) -> int:
     return c.rows * c.cols if is_scan(c) else c.rows * c.inner
 
 
+class CubCalls:
+    """cub::DeviceReduce::ArgMax/ArgMin on single-row cases (timing
+    comparison): one temporary buffer and one extremum slot per case."""
+
+    def __init__(self, torch, cases):
+        from row_wise_arg_gb300 import cub_compare
+        self.C = cub_compare
+        assert all(c.rows == 1 and c.inner == 1 and c.op in ("max", "min") and not is_scan(c) for c in cases)
+        self.temp = [torch.empty(max(self.C.temp_bytes(c.dtype, c.op, c.cols), 16), dtype=torch.uint8, device="cuda")
+                     for c in cases]
+        self.val = [torch.empty(16, dtype=torch.uint8, device="cuda") for _ in cases]
+
+    def __call__(self, i, c, x, out_idx, stream):
+        self.C.argreduce_raw(x.data_ptr(), c.dtype, c.op, c.cols, self.val[i].data_ptr(), out_idx.data_ptr(),
+                             self.temp[i].data_ptr(), self.temp[i].numel(), stream.cuda_stream)
+
+
+def cub_comparable(cases) -> bool:
+    return all(c.rows == 1 and c.inner == 1 and c.op in ("max", "min") and not is_scan(c) for c in cases)
+
+
 def call(A, c: W.Case, x, out_idx, scratch, stream, out_val=None):
     """One library call for case c on device data x (flat)."""
     if is_scan(c):
@@ -270,7 +291,7 @@ class GraphSet:
     so one replay is `per_graph` steps and consecutive uses of a copy are
     separated by all the other copies' bytes."""
 
-    def __init__(self, torch, A, cases, dev_inputs, copies, per_graph, stream):
+    def __init__(self, torch, A, cases, dev_inputs, copies, per_graph, stream, cub=None):
         self.torch = torch
         self.stream = stream
         self.per_graph = per_graph
@@ -284,7 +305,10 @@ class GraphSet:
 
         def calls(k):
             for i, c in enumerate(cases):
-                call(A, c, self.copies[i][k], self.outs[i], self.scratch, stream, self.vals[i])
+                if cub is not None:
+                    cub(i, c, self.copies[i][k], self.outs[i], stream)
+                else:
+                    call(A, c, self.copies[i][k], self.outs[i], self.scratch, stream, self.vals[i])
 
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
@@ -331,7 +355,7 @@ def copies_for(cases, cap: int = 4096) -> int:
 
 
 def time_group(torch, A, cases, inputs, steps, warmup, stream, dist=None, device=None, clocks=None,
-               exact: bool = True):
+               exact: bool = True, cub=None):
     """Time `steps` steps (each: every case once). With exact=True every graph
     is one step (at most 64 copies); otherwise graphs hold several steps and
     the step count is rounded up to whole replays. Returns (seconds, steps
@@ -340,11 +364,33 @@ def time_group(torch, A, cases, inputs, steps, warmup, stream, dist=None, device
     per_graph = 1 if exact else max(1, math.ceil(copies / 16))
     copies = per_graph * math.ceil(copies / per_graph)
     dev = [to_dev(torch, x, c.dtype).reshape(-1) for c, x in zip(cases, inputs)]
-    gs = GraphSet(torch, A, cases, dev, copies, per_graph, stream)
+    gs = GraphSet(torch, A, cases, dev, copies, per_graph, stream, cub)
     replays = math.ceil(steps / per_graph)
     secs, clk = gs.timed(replays, max(3, math.ceil(warmup / per_graph)), dist, device, clocks)
     del gs, dev
     return secs, replays * per_graph, copies, clk
+
+
+def cub_compare(torch, A, cases, inputs, steps, stream, ours_us):
+    """cub::DeviceReduce::ArgMax/ArgMin, called as a library, timed exactly as
+    the step above (same inputs, copies, graphs and events); its indices are
+    first checked against argreduce() on every case."""
+    cub = CubCalls(torch, cases)
+    agree = True
+    for i, (c, x) in enumerate(zip(cases, inputs)):
+        d = to_dev(torch, x, c.dtype).reshape(-1)
+        mine = torch.empty(1, dtype=torch.int64, device="cuda")
+        theirs = torch.empty(1, dtype=torch.int64, device="cuda")
+        call(A, c, d, mine, A.Scratch(), stream)
+        cub(i, c, d, theirs, stream)
+        torch.cuda.synchronize()
+        agree = agree and int(mine.item()) == int(theirs.item())
+    secs, n, _, _ = time_group(torch, A, cases, inputs, steps, 5, stream, cub=cub)
+    us = secs * 1e6 / (n * len(cases))
+    return {"impl": "cub::DeviceReduce::ArgMax / ArgMin (CCCL, as a library)", "us_per_call": round(us, 4),
+            "argreduce_us_per_call": round(ours_us, 4), "cub_over_argreduce": round(us / ours_us, 3),
+            "steps": n, "same_indices": agree,
+            "note": "timing comparison only: same inputs, rotating copies, one CUDA graph per copy, CUDA events"}
 
 
 def e2e_time(torch, A, cases, inputs, steps, stream):
@@ -422,6 +468,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--no-cub", action="store_true", help="skip the cub::DeviceReduce timing comparison")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -497,6 +544,9 @@ def main():
                          "host_wall_us_per_call": round(wall * 1e6 / (args.e2e_steps * len(cases)), 4),
                          "steps": args.e2e_steps}
 
+    if not args.no_cub and cub_comparable(cases) and (world == 1 or rank == 0):
+        result["cub_compare"] = cub_compare(torch, A, cases, inputs, min(args.steps, 4000), stream, us_per_call)
+
     if not args.no_configs and (world == 1 or rank == 0):
         table = []
         for name, (g, _) in sorted(WORKLOADS.items(), key=lambda kv: kv[1][0]):
@@ -517,8 +567,13 @@ def main():
                     gbs = algo_bytes(c) / (s / n) / 1e9
                     plan = (A.argreduce_cum_plan(c.rows, c.cols, c.dtype, c.op) if is_scan(c) else
                             A.argreduce_axis_plan(c.rows, c.cols, c.inner, c.dtype, c.op))
-                    table.append({"case": c.name, "us_per_call": round(us, 3), "gbs": round(gbs, 1),
-                                  "frac": round(gbs / peak, 4), "path": plan.as_dict()["path_name"]})
+                    row = {"case": c.name, "us_per_call": round(us, 3), "gbs": round(gbs, 1),
+                           "frac": round(gbs / peak, 4), "path": plan.as_dict()["path_name"]}
+                    if not args.no_cub and cub_comparable([c]):
+                        cs, cn, _, _ = time_group(torch, A, [c], [x], n, 5, stream, exact=False,
+                                                  cub=CubCalls(torch, [c]))
+                        row["cub_us_per_call"] = round(cs * 1e6 / cn, 3)
+                    table.append(row)
             del ginputs
         result["configs"] = table
 

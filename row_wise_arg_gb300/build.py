@@ -3,6 +3,8 @@
 Translation units are compiled in parallel into ``row_wise_arg_gb300/_build``
 and linked into ``row_wise_arg_gb300/libargreduce.so`` (CUDA runtime linked
 statically, so the library needs nothing at load time but libc/libstdc++).
+The benchmark's CUB comparison (cub::DeviceReduce::ArgMax/ArgMin called as a
+library) is linked separately into ``row_wise_arg_gb300/libcubcompare.so``.
 
     python -m row_wise_arg_gb300.build [--force] [--verbose-ptxas]
 """
@@ -22,6 +24,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libargreduce.so")
+COMPARE_LIB = os.path.join(PKG, "libcubcompare.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # No fast-math: NaN, signed-zero and subnormal comparisons must follow IEEE 754.
@@ -33,6 +36,7 @@ SOURCES = ["api.cpp", "plan.cpp", "kernels_f32.cu", "kernels_f16.cu", "kernels_b
            "axis_f32.cu", "axis_f16.cu", "axis_bf16.cu", "axis_f64.cu", "cum_f32.cu", "cum_f16.cu", "cum_bf16.cu",
            "cum_f64.cu", "cum_i32.cu", "cum_i64.cu", "noalloc.cu"]
 HEADERS = ["device_common.cuh", "kernels_impl.cuh", "internal.h", "tma.cuh", "cum_impl.cuh"]
+COMPARE_SOURCES = ["compare/cub_argreduce.cu"]
 
 
 def nvcc() -> str:
@@ -43,19 +47,19 @@ def nvcc() -> str:
 
 
 def _deps() -> List[str]:
-    return ([os.path.join(CSRC, s) for s in SOURCES + HEADERS] + [os.path.join(INCLUDE, "argreduce.h"),
-                                                                   os.path.abspath(__file__)])
+    return ([os.path.join(CSRC, s) for s in SOURCES + HEADERS + COMPARE_SOURCES] +
+            [os.path.join(INCLUDE, "argreduce.h"), os.path.abspath(__file__)])
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(COMPARE_LIB):
         return False
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(LIB), os.path.getmtime(COMPARE_LIB))
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
 def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+    obj = os.path.join(BUILD, src.replace("/", "_") + ".o")
     flags = list(NVCC_FLAGS)
     if verbose_ptxas and src.endswith(".cu"):
         flags += ["-Xptxas", "-v"]
@@ -72,14 +76,17 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if not force and not verbose_ptxas and up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
-    with cf.ThreadPoolExecutor(max_workers=min(len(SOURCES), os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc()] + ARCH + ["-shared", "-cudart=static", "-o", tmp] + objs
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    srcs = COMPARE_SOURCES + SOURCES  # the slowest unit first
+    with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
+    n_cmp = len(COMPARE_SOURCES)
+    for out, parts in ((LIB, objs[n_cmp:]), (COMPARE_LIB, objs[:n_cmp])):
+        tmp = out + f".tmp{os.getpid()}"
+        cmd = [nvcc()] + ARCH + ["-shared", "-cudart=static", "-o", tmp] + parts
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, out)
     return LIB
 
 

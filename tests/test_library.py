@@ -467,3 +467,15 @@ def test_cum_split_index_arithmetic():
         assert got == list(range(total)) and ctr == 0
 
 
+
+
+def test_cub_compare_library_exports():
+    """The benchmark's comparison library (cub::DeviceReduce called as a
+    library) is built beside libargreduce.so and exports its two entry points;
+    libargreduce.so itself has no CUB symbol of ours."""
+    import ctypes
+    from row_wise_arg_gb300 import cub_compare
+    lib = ctypes.CDLL(cub_compare.LIB_PATH)
+    for name in ("cubcmp_temp_bytes", "cubcmp_argreduce"):
+        assert hasattr(lib, name)
+    assert not hasattr(_lib.load(), "cubcmp_argreduce")
