@@ -54,6 +54,8 @@ WORKLOADS = {
                 "[128,4096,8], [16,2048,384] f64"),
     "cum": (7, "cummax/cummin with indices: [1,65536], [1,262144], [64,1024], [1024,64] int64, [4,16384] int32, "
                "[1,65536] f32/f64, [256,256] bf16"),
+    "cum_large": (8, "cummax/cummin with indices at bandwidth scale: [1,2^24] int64, [16,2^20] f64, [4096,4096] f32, "
+                     "[256,65536] f32"),
 }
 DTYPE_LABEL = {"f32": "f32", "f16": "f16", "bf16": "bf16", "f64": "f64", "i32": "i32", "i64": "i64"}
 KERNEL_OF_PATH = {"rows": "rows_kernel", "split": "split_kernel", "cluster": "cluster_kernel", "axis": "axis_kernel",
@@ -129,13 +131,25 @@ def load_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+# The sources each workload's kernels and launch plans are built from; a
+# committed traffic figure is used only while they are unchanged.
+_COMMON_SOURCES = ("device_common.cuh", "kernels_impl.cuh", "tma.cuh", "internal.h")
+_WORKLOAD_SOURCES = {
+    "argreduce": _COMMON_SOURCES + ("plan.cpp", "kernels_f32.cu", "kernels_f16.cu", "kernels_bf16.cu",
+                                    "kernels_f64.cu"),
+    "axis": _COMMON_SOURCES + ("plan.cpp", "axis_f32.cu", "axis_f16.cu", "axis_bf16.cu", "axis_f64.cu"),
+    "cum": _COMMON_SOURCES + ("plan_cum.cpp", "cum_impl.cuh", "cum_f32.cu", "cum_f16.cu", "cum_bf16.cu",
+                              "cum_f64.cu", "cum_i32.cu", "cum_i64.cu"),
+}
+
+
+def kernel_source_hash(workload: str) -> str:
+    kind = "cum" if workload.startswith("cum") else "axis" if workload == "axis" else "argreduce"
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "row_wise_arg_gb300", "csrc")
-    for n in sorted(os.listdir(csrc)):
-        if n.endswith((".cu", ".cuh", ".h", ".cpp")):
-            with open(os.path.join(csrc, n), "rb") as f:
-                h.update(n.encode() + b"\0" + f.read())
+    for n in sorted(_WORKLOAD_SOURCES[kind]):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(n.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -145,7 +159,7 @@ def read_traffic(workload: str):
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
-    src = kernel_source_hash()
+    src = kernel_source_hash(workload)
     for line in open(p):
         parts = line.split()
         if line.startswith("#") or len(parts) < 3 or parts[0] != workload:
@@ -296,19 +310,28 @@ class GraphSet:
         self.stream = stream
         self.per_graph = per_graph
         self.scratch = A.Scratch()
-        need = max([A.argreduce_scratch_bytes(c.rows, c.cols, c.dtype, c.op) for c in cases] + [0])
+        need = max([A.argreduce_cum_scratch_bytes(c.rows, c.cols, c.dtype, c.op) if is_scan(c) else
+                    A.argreduce_scratch_bytes(c.rows, c.cols, c.dtype, c.op) for c in cases] + [0])
         self.scratch.ensure(max(need, 4096), stream.cuda_stream)
         self.copies = [[x] + [x.clone() for _ in range(copies - 1)] for x in dev_inputs]
-        self.outs = [torch.empty(max(n_outputs(c), 1), dtype=torch.int64, device="cuda") for c in cases]
-        self.vals = [torch.empty_like(dev_inputs[i]) if is_scan(c) else None for i, c in enumerate(cases)]
+        # Scan outputs (an index and a value per element) rotate with the
+        # inputs, so that every call writes them to HBM; the reductions'
+        # outputs (8 bytes a row) share one buffer per case.
+        n_out = [copies if is_scan(c) else 1 for c in cases]
+        self.outs = [[torch.empty(max(n_outputs(c), 1), dtype=torch.int64, device="cuda") for _ in range(m)]
+                     for c, m in zip(cases, n_out)]
+        self.vals = [[torch.empty_like(dev_inputs[i]) for _ in range(n_out[i])] if is_scan(c) else None
+                     for i, c in enumerate(cases)]
         self.graphs = []
 
         def calls(k):
             for i, c in enumerate(cases):
+                o = self.outs[i][k % n_out[i]]
                 if cub is not None:
-                    cub(i, c, self.copies[i][k], self.outs[i], stream)
+                    cub(i, c, self.copies[i][k], o, stream)
                 else:
-                    call(A, c, self.copies[i][k], self.outs[i], self.scratch, stream, self.vals[i])
+                    call(A, c, self.copies[i][k], o, self.scratch, stream,
+                         self.vals[i][k % n_out[i]] if self.vals[i] is not None else None)
 
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
@@ -349,8 +372,9 @@ class GraphSet:
 
 
 def copies_for(cases, cap: int = 4096) -> int:
-    """Input copies whose total exceeds twice the L2 cache."""
-    step_bytes = sum(c.nbytes for c in cases)
+    """Input copies whose total exceeds twice the L2 cache (inputs and, for
+    the scan, its per-element outputs)."""
+    step_bytes = sum(algo_bytes(c) if is_scan(c) else c.nbytes for c in cases)
     return max(1, min(cap, math.ceil(2 * L2_BYTES / max(step_bytes, 1))))
 
 

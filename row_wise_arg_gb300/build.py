@@ -32,9 +32,10 @@ NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-
                      "-ftz=false", "-prec-div=true", "-prec-sqrt=true",
                      "-I" + INCLUDE, "-I" + CSRC]
 
-SOURCES = ["api.cpp", "plan.cpp", "kernels_f32.cu", "kernels_f16.cu", "kernels_bf16.cu", "kernels_f64.cu",
-           "axis_f32.cu", "axis_f16.cu", "axis_bf16.cu", "axis_f64.cu", "cum_f32.cu", "cum_f16.cu", "cum_bf16.cu",
-           "cum_f64.cu", "cum_i32.cu", "cum_i64.cu", "noalloc.cu"]
+SOURCES = ["api.cpp", "plan.cpp", "plan_cum.cpp",
+           "kernels_f32.cu", "kernels_f16.cu", "kernels_bf16.cu", "kernels_f64.cu",
+           "axis_f32.cu", "axis_f16.cu", "axis_bf16.cu", "axis_f64.cu",
+           "cum_f32.cu", "cum_f16.cu", "cum_bf16.cu", "cum_f64.cu", "cum_i32.cu", "cum_i64.cu", "noalloc.cu"]
 HEADERS = ["device_common.cuh", "kernels_impl.cuh", "internal.h", "tma.cuh", "cum_impl.cuh"]
 COMPARE_SOURCES = ["compare/cub_argreduce.cu"]
 

@@ -73,106 +73,6 @@ int elem_size(int dtype) {
     }
 }
 
-// ---------------------------------------------------------------------------
-// cummax / cummin. A row is cut into C contiguous chunks (a cluster of C CTAs
-// when C > 1) while there are too few rows for the device; each CTA scans
-// tiles of block * 7 elements.
-// ---------------------------------------------------------------------------
-static constexpr int kCumItems = 7;
-// Measured on GB300 (sweeps of one-CTA, cluster and split geometries over
-// rows of 256 to 16M elements): one CTA per row once there are as many rows as
-// SMs (128 threads or fewer when rows are plentiful), clusters up to 32K
-// elements per row, the split scan beyond, best at about one CTA per 3.5K
-// elements: 76..304 CTAs of up to 512 threads for one row, up to 608 CTAs of
-// up to 256 threads for several.
-static constexpr int64_t kCumManyRowsWaves = 4;     // rows per SM from which CTAs shrink
-static constexpr int64_t kCumMinChunkTiles = 2;     // rows shorter than 2 x 2 tiles are not split
-static constexpr int64_t kCumMinChunk = 512;        // elements per split-scan or cluster CTA at least
-static constexpr int64_t kCumSplitElems = 3584;     // elements per split-scan CTA the planner aims for
-static constexpr int64_t kCumClusterMaxCols = 32768;
-
-argr_status make_cum_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_caps& caps, argr_plan* out) {
-    if (!out) return ARGR_EINVAL;
-    *out = argr_plan{};
-    if (elem_size(dtype) == 0 || rows < 0 || cols < 1 || cols > INT_MAX) return ARGR_EINVAL;
-    if (op != ARGR_MAX && op != ARGR_MIN) return (op == ARGR_MAX_LAST || op == ARGR_MIN_LAST) ? ARGR_EUNSUPPORTED
-                                                                                                : ARGR_EINVAL;
-    if (!caps_ok(caps)) return ARGR_EINVAL;
-    if (rows == 0) {
-        out->path = ARGR_PATH_NONE;
-        return ARGR_OK;
-    }
-    const int64_t sms = caps.sm_count;
-    out->flags = ARGR_PLAN_PDL;
-    out->cluster = 1;
-    out->blocks_per_row = 1;
-    out->grid_rows = std::min(rows, kMaxGridY);
-    out->path = ARGR_PATH_CUM;
-    int block = 32;
-    if (rows >= kCumManyRowsWaves * sms) {
-        // Many rows: one CTA per row, small CTAs (more of them resident per
-        // SM, fewer threads held by each barrier), at least two tiles a row.
-        while (block < 128 && 2 * block * kCumItems <= cols) block <<= 1;
-        out->block = block;
-        return ARGR_OK;
-    }
-    while (block < 256 && block * kCumItems < cols) block <<= 1;
-    out->block = block;
-    const int64_t tile = static_cast<int64_t>(block) * kCumItems;
-    if (cols < kCumMinChunkTiles * 2 * tile || rows >= sms) return ARGR_OK;  // one CTA per row
-    if (cols <= kCumClusterMaxCols && caps.max_cluster >= 2) {
-        // Short rows: a cluster per row exchanges aggregates through
-        // distributed shared memory, a round trip cheaper than scratch.
-        const int64_t c = std::min<int64_t>({16, caps.max_cluster, ceil_div(2 * sms, rows),
-                                             std::max<int64_t>(2, cols / kCumMinChunk)});
-        out->block = 256;
-        out->cluster = static_cast<int32_t>(c);
-        out->blocks_per_row = c;
-        out->grid_rows = rows;
-        return ARGR_OK;
-    }
-    // Long rows, fewer than the SMs: a split scan with one CTA per
-    // kCumSplitElems elements in total, from half an SM's worth up to two
-    // 512-thread CTAs per SM for one row, or four 256-thread CTAs for more.
-    const int64_t per_sm = rows == 1 ? 2 : 4;
-    const int max_block = rows == 1 ? 512 : 256;
-    const int64_t target = std::min(per_sm * sms, std::max(sms / 2, ceil_div(rows * cols, kCumSplitElems)));
-    const int64_t chunks = std::min<int64_t>({kCumMaxChunks / rows, ceil_div(target, rows), cols / kCumMinChunk});
-    if (chunks < 2) return ARGR_OK;
-    const int64_t per_chunk = ceil_div(cols, chunks);
-    int b = 64;
-    while (b < max_block && b * kCumItems < per_chunk) b <<= 1;
-    out->path = ARGR_PATH_CUM_SPLIT;
-    out->block = b;
-    out->blocks_per_row = chunks;
-    out->grid_rows = rows;
-    out->scratch_bytes = plan_scratch(*out, rows);
-    return ARGR_OK;
-}
-
-argr_status check_cum_plan(const argr_plan& p, int64_t rows, int64_t cols, int dtype, int op, const argr_caps& caps) {
-    if (elem_size(dtype) == 0 || rows < 0 || cols < 1 || cols > INT_MAX) return ARGR_EINVAL;
-    if (op != ARGR_MAX && op != ARGR_MIN) return ARGR_EUNSUPPORTED;
-    if (rows == 0) return ARGR_OK;
-    if (p.block < 32 || p.block > 1024 || p.block % 32 != 0) return ARGR_EINVAL;
-    const int64_t smem = static_cast<int64_t>(p.block) * kCumItems * (elem_size(dtype) + 4);
-    if (smem > kMaxDynamicSmem) return ARGR_EINVAL;
-    if (p.path == ARGR_PATH_CUM_SPLIT) {
-        if (p.flags & ~(ARGR_PLAN_PDL | ARGR_PLAN_TEST_EXPIRE)) return ARGR_EINVAL;
-        if (p.cluster != 1 || p.blocks_per_row < 1 || p.blocks_per_row > kCumMaxChunks) return ARGR_EINVAL;
-        if (rows > kCumMaxChunks / p.blocks_per_row) return ARGR_EINVAL;  // records of one launch
-        if (p.grid_rows != rows) return ARGR_EINVAL;
-        return ARGR_OK;
-    }
-    if (p.path != ARGR_PATH_CUM) return ARGR_EINVAL;
-    if (p.flags & ~ARGR_PLAN_PDL) return ARGR_EINVAL;
-    if (p.cluster < 1 || p.cluster > 16 || p.blocks_per_row != p.cluster) return ARGR_EINVAL;
-    if (p.cluster > 1 && caps.max_cluster < p.cluster) return ARGR_EUNSUPPORTED;
-    if (p.grid_rows < 1 || p.grid_rows > kMaxGridY) return ARGR_EINVAL;
-    if (p.cluster > 1 && p.grid_rows < rows) return ARGR_EINVAL;
-    return ARGR_OK;
-}
-
 size_t plan_scratch(const argr_plan& p, int64_t rows) {
     if (p.path == ARGR_PATH_CUM_SPLIT)
         return kCumRecordsOffset + 8 * static_cast<size_t>(rows) * static_cast<size_t>(p.blocks_per_row);

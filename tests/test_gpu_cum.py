@@ -80,7 +80,7 @@ def cum_rows(dtype, rows, cols, seed):
     return W.fuzz_rows(dtype, rows, cols, seed=seed, p_special=0.1)
 
 
-@pytest.mark.parametrize("case", W.config_cases(7), ids=lambda c: c.name)
+@pytest.mark.parametrize("case", W.config_cases(7) + W.config_cases(8), ids=lambda c: c.name)
 def test_cum_workload_full_size(case):
     x = W.make(case)
     check_cum(x, case.dtype, case.op)

@@ -329,7 +329,8 @@ def make(c: Case) -> np.ndarray:
 
 # The five workload groups. Seeds are fixed constants.
 def config_cases(k: int) -> List[Case]:
-    """Cases of workload group ``k`` (1..5)."""
+    """Cases of workload group ``k``: 1..5 the reductions, 6 the non-last
+    axis, 7 and 8 the cummax / cummin scans."""
     out: List[Case] = []
     if k == 1:
         out.append(Case("logits_1x32000_f32_max", 1, 32000, "f32", "max", "logits", 1001))
@@ -368,6 +369,11 @@ def config_cases(k: int) -> List[Case]:
                                       (1024, 64, "i64", "min"), (4, 16384, "i32", "max"), (1, 65536, "f32", "max"),
                                       (1, 65536, "f64", "min"), (256, 256, "bf16", "max")):
             out.append(Case(f"cum_{rows}x{cols}_{dtype}_{op}", rows, cols, dtype, op, "cum_values", 7001 + cols % 97))
+    elif k == 8:
+        # cummax / cummin at bandwidth scale (hundreds of MB per call)
+        for rows, cols, dtype, op in ((1, 1 << 24, "i64", "max"), (16, 1 << 20, "f64", "min"),
+                                      (4096, 4096, "f32", "max"), (256, 65536, "f32", "min")):
+            out.append(Case(f"cum_{rows}x{cols}_{dtype}_{op}", rows, cols, dtype, op, "cum_values", 8001 + rows % 97))
     else:
         raise ValueError(k)
     return out
