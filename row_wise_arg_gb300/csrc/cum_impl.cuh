@@ -6,20 +6,18 @@
 // index and a NaN after x[0] is never chosen (Paddle issue #79670, "Possible
 // fixes": a scan with argmax semantics whose ties take the earlier index).
 //
-// Comparisons use ordered integer keys: monotone in the value (reversed for
-// the min op), +0.0 and -0.0 equal, NaN elements key 0 (never better than
-// anything), a NaN x[0] the all-ones key (nothing is better, so every output
-// stays (x[0], 0)). The combine of an earlier prefix a and a later part b is
-// "b if b.key > a.key, else a": associative, so any scan tree reproduces the
-// sequential scan, and key-0 elements act as its identity.
+// The combine of an earlier prefix a and a later part b is "b if b.key >
+// a.key, else a" (keys below): associative, so any scan tree reproduces the
+// sequential scan.
 //
-// Decomposition: a row is cut into C contiguous chunks, one CTA each (a
-// thread-block cluster when C > 1). Phase A (C > 1): every CTA reduces its
-// chunk to an aggregate and pushes it into the shared memory of every later
-// CTA of the cluster; after one cluster barrier each CTA folds the aggregates
-// before it into its carry-in. Phase B: the CTA scans its chunk tile by tile
-// (NT threads x ITEMS elements; tiles loaded and stored through shared memory
-// so that global accesses are coalesced, ITEMS odd so that a thread's run of
+// Decomposition: a row is one CTA's, or is cut into C contiguous chunks, one
+// CTA each: a thread-block cluster (C <= 16) or a split scan (any C). Phase A
+// (C > 1): every CTA reduces its chunk to an aggregate and hands it to the
+// later chunks (distributed shared memory in a cluster, records in scratch
+// for the split scan); each CTA folds the aggregates before its chunk into
+// its carry-in. Phase B: the CTA scans its chunk tile by tile (NT threads x
+// ITEMS elements; tiles loaded and stored through shared memory so that
+// global accesses are coalesced, ITEMS odd so that a thread's run of
 // consecutive elements spreads over the banks), carrying the running prefix.
 #pragma once
 
@@ -28,40 +26,48 @@
 
 namespace argr {
 
-// Ordered keys for the scan. Key type u32 for elements up to 4 bytes, u64 for 8.
+// Comparison keys for the scan: "b replaces a" is b.k > a.k for both ops.
+// Floating types of up to 4 bytes compare as binary32 values, negated for
+// the min op: an IEEE comparison is false on NaN, so a NaN element never
+// replaces anything and a NaN seed (x[0]) is never replaced, and -0.0 equals
+// +0.0. The identity (an empty prefix) is the lowest key, -inf: an element
+// enters a prefix only when its key is strictly greater, so a prefix whose
+// key is -inf is the identity, never an element, while the seed enters
+// without that test and is always a real element. binary64 uses ordered
+// 64-bit integer keys (GB300's FP64 pipe is too slow to compare at memory
+// speed) and the integers their order as unsigned keys; there the identity
+// is key 0 and the same argument holds.
 struct CumF32 {
     using raw = float;
-    using key = unsigned;
-    template <int OP> static __device__ __forceinline__ unsigned ordered(unsigned b) {
-        unsigned u = (b & 0x7fffffffu) == 0 ? 0x80000000u : ((b & 0x80000000u) ? ~b : (b | 0x80000000u));
-        return kIsMin<OP> ? ~u : u;
-    }
-    template <int OP> static __device__ __forceinline__ unsigned elem_key(float v) {
-        const unsigned b = __float_as_uint(v);
-        return (b & 0x7fffffffu) > 0x7f800000u ? 0u : ordered<OP>(b);
-    }
-    template <int OP> static __device__ __forceinline__ unsigned seed_key(float v) {
-        const unsigned b = __float_as_uint(v);
-        return (b & 0x7fffffffu) > 0x7f800000u ? ~0u : ordered<OP>(b);
+    using key = float;
+    template <int OP> static __device__ __forceinline__ float elem_key(float v) { return kIsMin<OP> ? -v : v; }
+    template <int OP> static __device__ __forceinline__ float seed_key(float v) { return elem_key<OP>(v); }
+    static __device__ __forceinline__ float identity() { return __int_as_float(0xff800000); }
+    static __device__ __forceinline__ unsigned long long to_bits(float k) { return __float_as_uint(k); }
+    static __device__ __forceinline__ float from_bits(unsigned long long b) {
+        return __uint_as_float(static_cast<unsigned>(b));
     }
 };
-template <unsigned kInf>
+template <bool BF16>
 struct Cum16 {
     using raw = uint16_t;
-    using key = unsigned;
-    template <int OP> static __device__ __forceinline__ unsigned ordered(unsigned b) {
-        unsigned u = (b & 0x7fffu) == 0 ? 0x8000u : ((b & 0x8000u) ? (~b & 0xffffu) : (b | 0x8000u));
-        return kIsMin<OP> ? (~u & 0xffffu) : u;
+    using key = float;
+    static __device__ __forceinline__ float widen(uint16_t v) {
+        if constexpr (BF16) return __uint_as_float(static_cast<unsigned>(v) << 16);
+        return __half2float(__ushort_as_half(v));
     }
-    template <int OP> static __device__ __forceinline__ unsigned elem_key(uint16_t v) {
-        return (v & 0x7fffu) > kInf ? 0u : ordered<OP>(v);
+    template <int OP> static __device__ __forceinline__ float elem_key(uint16_t v) {
+        return kIsMin<OP> ? -widen(v) : widen(v);
     }
-    template <int OP> static __device__ __forceinline__ unsigned seed_key(uint16_t v) {
-        return (v & 0x7fffu) > kInf ? ~0u : ordered<OP>(v);
+    template <int OP> static __device__ __forceinline__ float seed_key(uint16_t v) { return elem_key<OP>(v); }
+    static __device__ __forceinline__ float identity() { return __int_as_float(0xff800000); }
+    static __device__ __forceinline__ unsigned long long to_bits(float k) { return __float_as_uint(k); }
+    static __device__ __forceinline__ float from_bits(unsigned long long b) {
+        return __uint_as_float(static_cast<unsigned>(b));
     }
 };
-using CumF16 = Cum16<0x7c00u>;
-using CumBF16 = Cum16<0x7f80u>;
+using CumF16 = Cum16<false>;
+using CumBF16 = Cum16<true>;
 struct CumF64 {
     using raw = unsigned long long;  // binary64 bit patterns
     using key = unsigned long long;
@@ -71,6 +77,9 @@ struct CumF64 {
     template <int OP> static __device__ __forceinline__ unsigned long long seed_key(unsigned long long b) {
         return TagF64::seed_key<OP>(b);
     }
+    static __device__ __forceinline__ unsigned long long identity() { return 0ull; }
+    static __device__ __forceinline__ unsigned long long to_bits(unsigned long long k) { return k; }
+    static __device__ __forceinline__ unsigned long long from_bits(unsigned long long b) { return b; }
 };
 template <typename I, typename U>
 struct CumInt {
@@ -83,6 +92,9 @@ struct CumInt {
         return kIsMin<OP> ? static_cast<U>(~u) : u;
     }
     template <int OP> static __device__ __forceinline__ U seed_key(I v) { return elem_key<OP>(v); }
+    static __device__ __forceinline__ U identity() { return 0; }
+    static __device__ __forceinline__ unsigned long long to_bits(U k) { return k; }
+    static __device__ __forceinline__ U from_bits(unsigned long long b) { return static_cast<U>(b); }
 };
 using CumI32 = CumInt<int, unsigned>;
 using CumI64 = CumInt<long long, unsigned long long>;
@@ -105,7 +117,7 @@ __device__ __forceinline__ KI<CT> later(const KI<CT>& a, const KI<CT>& b) {
 template <class CT>
 __device__ __forceinline__ KI<CT> ki_identity() {
     KI<CT> p;
-    p.k = 0;
+    p.k = CT::identity();
     p.i = 0;
     return p;
 }
@@ -252,6 +264,97 @@ __device__ __forceinline__ KI<CT> chunk_aggregate(const typename CT::raw* row, i
     return block_first_best(a, warp_tot);
 }
 
+// One tile of phase B: row[base, base + n) (n == NT * ITEMS when FULL, which
+// drops the bounds tests), whose elements are in v; loads the next tile
+// (nn elements from nbase) into v while scanning, writes the outputs and
+// moves the carry past the tile.
+template <class CT, int OP, int ITEMS, bool FULL>
+__device__ __forceinline__ void scan_tile(const typename CT::raw* row, int base, int n, int nbase, int nn,
+                                          KI<CT>& carry, typename CT::raw& carry_v, typename CT::raw (&v)[ITEMS],
+                                          int64_t* __restrict__ oi_row, typename CT::raw* __restrict__ ov_row,
+                                          typename CT::raw* tin, int* tidx, KI<CT>* warp_tot, KI<CT>* s_total) {
+    using K = typename CT::key;
+    const int nt = blockDim.x;
+    const int t = threadIdx.x;
+    const int lane = t & 31;
+    const int warp = t >> 5;
+    const int nwarps = nt >> 5;
+#pragma unroll
+    for (int q = 0; q < ITEMS; ++q)
+        if (FULL || t + q * nt < n) tin[t + q * nt] = v[q];
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < ITEMS; ++q)
+        if (t + q * nt < nn) v[q] = ld_scalar(row + nbase + t + q * nt);
+    // thread-local inclusive prefixes of ITEMS consecutive elements
+    KI<CT> p[ITEMS];
+    KI<CT> run = ki_identity<CT>();
+#pragma unroll
+    for (int q = 0; q < ITEMS; ++q) {
+        const int j = t * ITEMS + q;
+        if (FULL || j < n) {
+            const K k = CT::template elem_key<OP>(tin[j]);
+            if (k > run.k) {
+                run.k = k;
+                run.i = base + j;
+            }
+        }
+        p[q] = run;
+    }
+    // warp inclusive scan of the thread totals
+    KI<CT> ws = run;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const KI<CT> o = shfl_up_ki(ws, d);
+        if (lane >= d) ws = later(o, ws);
+    }
+    KI<CT> excl = shfl_up_ki(ws, 1);
+    if (lane == 0) excl = ki_identity<CT>();
+    if (lane == 31) warp_tot[warp] = ws;
+    __syncthreads();
+    if (warp == 0) {
+        KI<CT> w = lane < nwarps ? warp_tot[lane] : ki_identity<CT>();
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const KI<CT> o = shfl_up_ki(w, d);
+            if (lane >= d) w = later(o, w);
+        }
+        KI<CT> we = shfl_up_ki(w, 1);
+        if (lane == 0) we = ki_identity<CT>();
+        if (lane < nwarps) warp_tot[lane] = we;  // exclusive prefix of each warp
+        if (lane == nwarps - 1) *s_total = w;
+    }
+    __syncthreads();
+    const KI<CT> before = later(later(carry, warp_tot[warp]), excl);
+#pragma unroll
+    for (int q = 0; q < ITEMS; ++q) {
+        const int j = t * ITEMS + q;
+        if (FULL || j < n) tidx[j] = later(before, p[q]).i;
+    }
+    const KI<CT> tot = *s_total;
+    __syncthreads();
+    // Coalesced stores. An index before this tile can only be the carry's.
+    int64_t* oi = oi_row + base;
+#pragma unroll
+    for (int q = 0; q < ITEMS; ++q)
+        if (FULL || t + q * nt < n) oi[t + q * nt] = tidx[t + q * nt];
+    if (ov_row) {
+        typename CT::raw* ov = ov_row + base;
+#pragma unroll
+        for (int q = 0; q < ITEMS; ++q) {
+            if (FULL || t + q * nt < n) {
+                const int i = tidx[t + q * nt];
+                ov[t + q * nt] = i >= base ? tin[i - base] : carry_v;
+            }
+        }
+    }
+    if (tot.k > carry.k) {  // carry the tile's best past it
+        carry = tot;
+        carry_v = tin[tot.i - base];
+    }
+    __syncthreads();  // the tile buffers are reused by the next tile
+}
+
 // Phase B: scan row[cb, ce) tile by tile (NT threads x ITEMS consecutive
 // elements per thread), starting from the carry-in (carry, carry_v) = the
 // prefix result just before cb, with the first tile already in v
@@ -265,94 +368,20 @@ __device__ __forceinline__ void scan_chunk(const typename CT::raw* row, int cb, 
                                            int64_t* __restrict__ oi_row, typename CT::raw* __restrict__ ov_row,
                                            unsigned char* smem, KI<CT>* warp_tot, KI<CT>* s_total) {
     using R = typename CT::raw;
-    using K = typename CT::key;
-    const int nt = blockDim.x;
-    const int t = threadIdx.x;
-    const int lane = t & 31;
-    const int warp = t >> 5;
-    const int nwarps = nt >> 5;
-    const int tile = nt * ITEMS;
+    const int tile = static_cast<int>(blockDim.x) * ITEMS;
     R* tin = reinterpret_cast<R*>(smem);                                                 // tile input
     int* tidx = reinterpret_cast<int*>(smem + static_cast<size_t>(tile) * sizeof(R));  // tile indices
     int base = cb;
     int n = ce - cb < tile ? ce - cb : tile;
     while (n > 0) {
-#pragma unroll
-        for (int q = 0; q < ITEMS; ++q)
-            if (t + q * nt < n) tin[t + q * nt] = v[q];
-        __syncthreads();
         const int nbase = base + n;
         const int nn = ce - nbase < tile ? ce - nbase : tile;
-#pragma unroll
-        for (int q = 0; q < ITEMS; ++q)
-            if (t + q * nt < nn) v[q] = ld_scalar(row + nbase + t + q * nt);
-        // thread-local inclusive prefixes of ITEMS consecutive elements
-        KI<CT> p[ITEMS];
-        KI<CT> run = ki_identity<CT>();
-#pragma unroll
-        for (int q = 0; q < ITEMS; ++q) {
-            const int j = t * ITEMS + q;
-            if (j < n) {
-                const K k = CT::template elem_key<OP>(tin[j]);
-                if (k > run.k) {
-                    run.k = k;
-                    run.i = base + j;
-                }
-            }
-            p[q] = run;
-        }
-        // warp inclusive scan of the thread totals
-        KI<CT> ws = run;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const KI<CT> o = shfl_up_ki(ws, d);
-            if (lane >= d) ws = later(o, ws);
-        }
-        KI<CT> excl = shfl_up_ki(ws, 1);
-        if (lane == 0) excl = ki_identity<CT>();
-        if (lane == 31) warp_tot[warp] = ws;
-        __syncthreads();
-        if (warp == 0) {
-            KI<CT> w = lane < nwarps ? warp_tot[lane] : ki_identity<CT>();
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const KI<CT> o = shfl_up_ki(w, d);
-                if (lane >= d) w = later(o, w);
-            }
-            KI<CT> we = shfl_up_ki(w, 1);
-            if (lane == 0) we = ki_identity<CT>();
-            if (lane < nwarps) warp_tot[lane] = we;  // exclusive prefix of each warp
-            if (lane == nwarps - 1) *s_total = w;
-        }
-        __syncthreads();
-        const KI<CT> before = later(later(carry, warp_tot[warp]), excl);
-#pragma unroll
-        for (int q = 0; q < ITEMS; ++q) {
-            const int j = t * ITEMS + q;
-            if (j < n) tidx[j] = later(before, p[q]).i;
-        }
-        const KI<CT> tot = *s_total;
-        __syncthreads();
-        // Coalesced stores. An index before this tile can only be the carry's.
-        int64_t* oi = oi_row + base;
-#pragma unroll
-        for (int q = 0; q < ITEMS; ++q)
-            if (t + q * nt < n) oi[t + q * nt] = tidx[t + q * nt];
-        if (ov_row) {
-            R* ov = ov_row + base;
-#pragma unroll
-            for (int q = 0; q < ITEMS; ++q) {
-                if (t + q * nt < n) {
-                    const int i = tidx[t + q * nt];
-                    ov[t + q * nt] = i >= base ? tin[i - base] : carry_v;
-                }
-            }
-        }
-        if (tot.k > carry.k) {  // carry the tile's best past it
-            carry = tot;
-            carry_v = tin[tot.i - base];
-        }
-        __syncthreads();  // the tile buffers are reused by the next tile
+        if (n == tile)
+            scan_tile<CT, OP, ITEMS, true>(row, base, n, nbase, nn, carry, carry_v, v, oi_row, ov_row, tin, tidx,
+                                           warp_tot, s_total);
+        else
+            scan_tile<CT, OP, ITEMS, false>(row, base, n, nbase, nn, carry, carry_v, v, oi_row, ov_row, tin, tidx,
+                                            warp_tot, s_total);
         base = nbase;
         n = nn;
     }
@@ -400,7 +429,7 @@ cum_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols, int64
             if (t < C - b - 1) {
                 // Push this chunk's aggregate (key and index; the winner's raw
                 // value is reloaded by whoever needs it) to the later CTA b + 1 + t.
-                const uint64_t kk = static_cast<uint64_t>(a.k);
+                const uint64_t kk = CT::to_bits(a.k);
                 unsigned remote;
                 asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
                              : "=r"(remote)
@@ -414,7 +443,7 @@ cum_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols, int64
             // Fold the aggregates of the earlier chunks, in order, into the carry.
             for (int k = 0; k < b; ++k) {
                 const uint4 pk = agg_slots[parity][k];
-                const K ek = static_cast<K>(static_cast<uint64_t>(pk.x) | (static_cast<uint64_t>(pk.y) << 32));
+                const K ek = CT::from_bits(static_cast<uint64_t>(pk.x) | (static_cast<uint64_t>(pk.y) << 32));
                 if (ek > carry.k) {
                     carry.k = ek;
                     carry.i = static_cast<int>(pk.z);
@@ -488,9 +517,9 @@ __device__ __forceinline__ unsigned long long wait_record(const unsigned long lo
 
 template <class CT>
 __device__ __forceinline__ unsigned long long make_record(const KI<CT>& a) {
-    if (a.k == 0) return kNoElement;
+    if (a.k == CT::identity()) return kNoElement;
     const unsigned long long lo = static_cast<unsigned>(a.i) + 1u;
-    if constexpr (sizeof(typename CT::key) <= 4) return (static_cast<unsigned long long>(a.k) << 32) | lo;
+    if constexpr (sizeof(typename CT::key) <= 4) return (CT::to_bits(a.k) << 32) | lo;
     return lo;
 }
 
@@ -567,7 +596,7 @@ cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols,
             if (lo != kNoElement) {
                 KI<CT> e;
                 if constexpr (kKeyInRecord) {
-                    e.k = static_cast<K>(w[u] >> 32);
+                    e.k = CT::from_bits(w[u] >> 32);
                 } else {
                     e.k = CT::template elem_key<OP>(xv[u]);
                 }

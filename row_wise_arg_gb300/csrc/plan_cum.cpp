@@ -30,8 +30,8 @@ static constexpr int kCumItems = 7;
 // rows of 256 to 16M elements): one CTA per row once there are as many rows as
 // SMs (128 threads or fewer when rows are plentiful), clusters up to 32K
 // elements per row, the split scan beyond, best at about one CTA per 3.5K
-// elements: 76..304 CTAs of up to 512 threads for one row, up to 608 CTAs of
-// up to 256 threads for several.
+// elements: 76..304 CTAs of up to 512 threads for one row, up to 1024 CTAs of
+// up to 128 threads for several.
 static constexpr int64_t kCumManyRowsWaves = 4;     // rows per SM from which CTAs shrink
 static constexpr int64_t kCumMinChunkTiles = 2;     // rows shorter than 2 x 2 tiles are not split
 static constexpr int64_t kCumMinChunk = 512;        // elements per split-scan or cluster CTA at least
@@ -80,10 +80,11 @@ argr_status make_cum_plan(int64_t rows, int64_t cols, int dtype, int op, const a
     }
     // Long rows, fewer than the SMs: a split scan with one CTA per
     // kCumSplitElems elements in total, from half an SM's worth up to two
-    // 512-thread CTAs per SM for one row, or four 256-thread CTAs for more.
-    const int64_t per_sm = rows == 1 ? 2 : 4;
-    const int max_block = rows == 1 ? 512 : 256;
-    const int64_t target = std::min(per_sm * sms, std::max(sms / 2, ceil_div(rows * cols, kCumSplitElems)));
+    // 512-thread CTAs per SM for one row, or as many 128-thread CTAs as the
+    // records allow for several rows.
+    const int64_t max_ctas = rows == 1 ? 2 * sms : kCumMaxChunks;
+    const int max_block = rows == 1 ? 512 : 128;
+    const int64_t target = std::min(max_ctas, std::max(sms / 2, ceil_div(rows * cols, kCumSplitElems)));
     const int64_t chunks = std::min<int64_t>({kCumMaxChunks / rows, ceil_div(target, rows), cols / kCumMinChunk});
     if (chunks < 2) return ARGR_OK;
     const int64_t per_chunk = ceil_div(cols, chunks);

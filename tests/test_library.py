@@ -396,10 +396,10 @@ def test_cum_plans_and_validation():
             # long rows, fewer than the SMs: 76..304 CTAs, records of one launch <= 1024
             chunks = d["blocks_per_row"]
             assert rows < 152 and chunks >= 2 and rows * chunks <= 1024 and cols > 32768
-            assert rows * chunks <= (2 if rows == 1 else 4) * 152 + rows
+            assert rows * chunks <= (2 * 152 + 1 if rows == 1 else 1024)
             assert rows * chunks >= 76 or cols // chunks < 1024 or chunks == 1024 // rows
             assert cols // chunks >= 512
-            cap = 512 if rows == 1 else 256
+            cap = 512 if rows == 1 else 128
             assert d["block"] in (64, 128, 256, 512) and d["block"] <= cap
             assert d["block"] * 7 >= -(-cols // chunks) or d["block"] == cap
             assert d["scratch_bytes"] == 256 + 8 * rows * chunks and d["cluster"] == 1
