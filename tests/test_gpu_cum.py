@@ -224,3 +224,49 @@ def test_cum_split_rejections():
     assert _lib.argreduce_cum_raw(x.data_ptr(), "f32", 4, 100000, "max", o.data_ptr(), 0, sc.ptr, 4096, 0,
                                   bad) == _lib.ARGR_EINVAL
     torch.cuda.synchronize()
+
+
+def test_cum_int_max_row_f16():
+    """[1, INT32_MAX] fp16, the widest admitted row (4 GiB in, 16 GiB of
+    indices, 4 GiB of values): zeros with a planted ladder of maxima and two
+    minima, so every output is known by construction; checked at the ladder's
+    edges, the last element and random positions, under the planner's split
+    scan, a 1024-chunk split, a cluster and a single CTA."""
+    free, _ = torch.cuda.mem_get_info()
+    if free < 30 * 2**30:
+        pytest.skip("needs ~26 GiB of device memory")
+    n = 2**31 - 1
+    p1, p2, p3 = 1000, 2**30 + 7, n - 2
+    q1 = 5
+    x = torch.zeros((1, n), dtype=torch.float16, device="cuda")
+    x[0, p1], x[0, p2], x[0, p3] = 1.0, 2.0, 3.0
+    x[0, q1], x[0, n - 1] = -1.0, -2.0
+    out_i = torch.empty((1, n), dtype=torch.int64, device="cuda")
+    out_v = torch.empty((1, n), dtype=torch.float16, device="cuda")
+    rng = np.random.Generator(np.random.PCG64(2**31))
+    pos = np.unique(np.concatenate([rng.integers(0, n, size=2000),
+                                    [0, 1, q1 - 1, q1, q1 + 1, p1 - 1, p1, p1 + 1, p2 - 1, p2, p2 + 1,
+                                     p3 - 1, p3, p3 + 1, n - 2, n - 1]]))
+    pos = pos[(pos >= 0) & (pos < n)]
+    pos_t = torch.from_numpy(pos).cuda()
+
+    def want(op):
+        if op == "max":
+            return np.select([pos < p1, pos < p2, pos < p3], [0, p1, p2], p3)
+        return np.select([pos < q1, pos < n - 1], [0, q1], n - 1)
+
+    vals = {0: 0.0, p1: 1.0, p2: 2.0, p3: 3.0, q1: -1.0, n - 1: -2.0}
+    plans = [None, split_plan(1024, 512, rows=1), cum_plan(16, 1024, grid=1), cum_plan(1, 1024, grid=1)]
+    for plan in plans:
+        for op in ("max", "min"):
+            out_i.fill_(-7)
+            A.argreduce_cum(x, op, out_idx=out_i, out_val=out_v, plan=plan)
+            torch.cuda.synchronize()
+            got = out_i[0, pos_t].cpu().numpy()
+            w = want(op)
+            assert (got == w).all(), (plan.as_dict() if plan is not None else "planner", op,
+                                      pos[got != w][:5], got[got != w][:5], w[got != w][:5])
+            gv = out_v[0, pos_t].float().cpu().numpy()
+            assert (gv == np.array([vals[int(i)] for i in w], dtype=np.float32)).all()
+    del x, out_i, out_v
+    torch.cuda.empty_cache()
