@@ -79,7 +79,8 @@ typedef enum {
                               each (1 = none), scanned in tiles of block * 7 elements */
     ARGR_PATH_CUM_SPLIT = 7, /* cummax / cummin: a row in `blocks_per_row` chunks, one CTA each,
                               any number of CTAs; chunk aggregates are exchanged through
-                              scratch (rows * blocks_per_row <= 1024) */
+                              scratch (rows * blocks_per_row <= 65536; above 1024 the
+                              records need a scratch buffer of more than 1 MiB) */
     ARGR_PATH_STREAM = 4   /* every warp streams a contiguous range of rows through its own
                               `stages` shared-memory buffers of `stage_bytes`, filled by bulk
                               (TMA) copies; `group` lanes per row for rows that fit a buffer,
@@ -110,6 +111,13 @@ typedef struct {
  * argreduce_read_error() then reports ARGR_ETIMEOUT and outputs are
  * undefined. Never set in the planner's plans. */
 #define ARGR_PLAN_TEST_EXPIRE 4
+/* Plan flag (CUM_SPLIT path): each CTA copies its whole chunk (at most 80 KiB)
+ * into shared memory with bulk (TMA) copies and scans it there, so the input
+ * is read from memory once; without it, phase B reads the chunk again (from
+ * L2 while the chunks in flight fit it). Measured slower on GB300 at every
+ * size (two CTAs per SM alternate loading and scanning), so the planner does
+ * not set it. */
+#define ARGR_PLAN_STASH 8
 
 /* A launch plan. Produced by argreduce_plan(); tests may edit it to force a
  * path and pass it to argreduce_with_plan(), which re-validates it. */

@@ -265,10 +265,11 @@ __device__ __forceinline__ KI<CT> chunk_aggregate(const typename CT::raw* row, i
 }
 
 // One tile of phase B: row[base, base + n) (n == NT * ITEMS when FULL, which
-// drops the bounds tests), whose elements are in v; loads the next tile
-// (nn elements from nbase) into v while scanning, writes the outputs and
-// moves the carry past the tile.
-template <class CT, int OP, int ITEMS, bool FULL>
+// drops the bounds tests). Unless STASHED (the tile is already in shared
+// memory at tin), its elements are in v: they are stored to tin and the next
+// tile (nn elements from nbase) is loaded into v while this one is scanned.
+// Writes the outputs and moves the carry past the tile.
+template <class CT, int OP, int ITEMS, bool FULL, bool STASHED>
 __device__ __forceinline__ void scan_tile(const typename CT::raw* row, int base, int n, int nbase, int nn,
                                           KI<CT>& carry, typename CT::raw& carry_v, typename CT::raw (&v)[ITEMS],
                                           int64_t* __restrict__ oi_row, typename CT::raw* __restrict__ ov_row,
@@ -279,13 +280,15 @@ __device__ __forceinline__ void scan_tile(const typename CT::raw* row, int base,
     const int lane = t & 31;
     const int warp = t >> 5;
     const int nwarps = nt >> 5;
+    if constexpr (!STASHED) {
 #pragma unroll
-    for (int q = 0; q < ITEMS; ++q)
-        if (FULL || t + q * nt < n) tin[t + q * nt] = v[q];
-    __syncthreads();
+        for (int q = 0; q < ITEMS; ++q)
+            if (FULL || t + q * nt < n) tin[t + q * nt] = v[q];
+        __syncthreads();
 #pragma unroll
-    for (int q = 0; q < ITEMS; ++q)
-        if (t + q * nt < nn) v[q] = ld_scalar(row + nbase + t + q * nt);
+        for (int q = 0; q < ITEMS; ++q)
+            if (t + q * nt < nn) v[q] = ld_scalar(row + nbase + t + q * nt);
+    }
     // thread-local inclusive prefixes of ITEMS consecutive elements
     KI<CT> p[ITEMS];
     KI<CT> run = ki_identity<CT>();
@@ -377,13 +380,100 @@ __device__ __forceinline__ void scan_chunk(const typename CT::raw* row, int cb, 
         const int nbase = base + n;
         const int nn = ce - nbase < tile ? ce - nbase : tile;
         if (n == tile)
-            scan_tile<CT, OP, ITEMS, true>(row, base, n, nbase, nn, carry, carry_v, v, oi_row, ov_row, tin, tidx,
-                                           warp_tot, s_total);
+            scan_tile<CT, OP, ITEMS, true, false>(row, base, n, nbase, nn, carry, carry_v, v, oi_row, ov_row, tin,
+                                                  tidx, warp_tot, s_total);
         else
-            scan_tile<CT, OP, ITEMS, false>(row, base, n, nbase, nn, carry, carry_v, v, oi_row, ov_row, tin, tidx,
-                                            warp_tot, s_total);
+            scan_tile<CT, OP, ITEMS, false, false>(row, base, n, nbase, nn, carry, carry_v, v, oi_row, ov_row, tin,
+                                                   tidx, warp_tot, s_total);
         base = nbase;
         n = nn;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Stashed chunks (split scan with ARGR_PLAN_STASH): the CTA's whole chunk is
+// copied into shared memory once, by 1-D bulk (TMA) copies of its 16-byte
+// aligned middle plus plain loads of the ragged head and tail, and both phases
+// read it there. The stash starts at the chunk's address modulo 16, so that
+// the aligned middle lands on 16-byte aligned shared memory.
+// ---------------------------------------------------------------------------
+constexpr unsigned kStashPieceBytes = 16384;  // bulk copies in flight at once, up to 5 for 80 KiB
+
+template <class CT>
+__device__ __forceinline__ typename CT::raw* stash_fill(const typename CT::raw* row, int cb, int ce,
+                                                       unsigned char* smem, unsigned long long* bar,
+                                                       unsigned long long limit_ns, unsigned* err) {
+    using R = typename CT::raw;
+    constexpr int es = sizeof(R);
+    const int t = threadIdx.x;
+    const int nt = blockDim.x;
+    const uintptr_t g0 = reinterpret_cast<uintptr_t>(row + cb);
+    const uintptr_t g1 = reinterpret_cast<uintptr_t>(row + ce);
+    R* stash = reinterpret_cast<R*>(smem + (g0 & 15));
+    const uintptr_t a0 = (g0 + 15) & ~static_cast<uintptr_t>(15);
+    const uintptr_t a1 = g1 & ~static_cast<uintptr_t>(15);
+    const bool bulk = a1 > a0;
+    const int n = ce - cb;
+    const int head = bulk ? static_cast<int>((a0 - g0) / es) : n;  // elements before the aligned middle
+    const int tail = bulk ? static_cast<int>((a1 - g0) / es) : n;  // first element after it
+    const unsigned barp = smem_u32(bar);
+    if (t == 0 && bulk) {
+        mbar_init(barp, 1);
+        mbar_init_fence();
+        const unsigned bytes = static_cast<unsigned>(a1 - a0);
+        mbar_arrive_expect_tx(barp, bytes);
+        const unsigned dst = smem_u32(stash) + static_cast<unsigned>(a0 - g0);
+        for (unsigned off = 0; off < bytes; off += kStashPieceBytes) {
+            const unsigned len = bytes - off < kStashPieceBytes ? bytes - off : kStashPieceBytes;
+            bulk_copy_g2s(dst + off, reinterpret_cast<const void*>(a0 + off), len, barp);
+        }
+    }
+    for (int j = t; j < head; j += nt) stash[j] = ld_scalar(row + cb + j);
+    for (int j = tail + t; j < n; j += nt) stash[j] = ld_scalar(row + cb + j);
+    __syncthreads();  // the barrier is initialised before anyone waits on it
+    if (bulk && !mbar_wait_bounded(barp, 0, limit_ns)) {
+        atomicOr(err, kErrWaitExpired);
+        mbar_wait_bounded(barp, 0, limit_ns);  // let a late copy land before the CTA moves on
+    }
+    __syncthreads();
+    return stash;
+}
+
+// Phase A on a stashed chunk: its first best element, valid in warp 0.
+template <class CT, int OP>
+__device__ __forceinline__ KI<CT> stash_aggregate(const typename CT::raw* stash, int cb, int ce, KI<CT>* warp_tot) {
+    using K = typename CT::key;
+    KI<CT> a = ki_identity<CT>();
+    const int n = ce - cb;
+    for (int j = threadIdx.x; j < n; j += blockDim.x) {  // increasing indices within the thread
+        const K k = CT::template elem_key<OP>(stash[j]);
+        if (k > a.k) {
+            a.k = k;
+            a.i = cb + j;
+        }
+    }
+    return block_first_best(a, warp_tot);
+}
+
+// Phase B on a stashed chunk: the tiles are windows of the stash.
+template <class CT, int OP, int ITEMS>
+__device__ __forceinline__ void scan_stash(const typename CT::raw* row, typename CT::raw* stash, int cb, int ce,
+                                           KI<CT> carry, typename CT::raw carry_v, int64_t* __restrict__ oi_row,
+                                           typename CT::raw* __restrict__ ov_row, int* tidx, KI<CT>* warp_tot,
+                                           KI<CT>* s_total) {
+    using R = typename CT::raw;
+    const int tile = static_cast<int>(blockDim.x) * ITEMS;
+    R unused[ITEMS];
+    for (int base = cb; base < ce;) {
+        const int n = ce - base < tile ? ce - base : tile;
+        R* tin = stash + (base - cb);
+        if (n == tile)
+            scan_tile<CT, OP, ITEMS, true, true>(row, base, n, 0, 0, carry, carry_v, unused, oi_row, ov_row, tin,
+                                                 tidx, warp_tot, s_total);
+        else
+            scan_tile<CT, OP, ITEMS, false, true>(row, base, n, 0, 0, carry, carry_v, unused, oi_row, ov_row, tin,
+                                                  tidx, warp_tot, s_total);
+        base += n;
     }
 }
 
@@ -523,7 +613,7 @@ __device__ __forceinline__ unsigned long long make_record(const KI<CT>& a) {
     return lo;
 }
 
-template <class CT, int OP, int ITEMS>
+template <class CT, int OP, int ITEMS, bool STASH>
 __global__ void __launch_bounds__(1024)
 cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols, int chunks,
                  int64_t* __restrict__ out_idx, typename CT::raw* __restrict__ out_val,
@@ -535,13 +625,14 @@ cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols,
     __shared__ KI<CT> warp_tot[32];
     __shared__ KI<CT> s_total;
     __shared__ unsigned s_flag;
+    __shared__ __align__(8) unsigned long long stash_bar;
     const int t = threadIdx.x;
     const int nt = blockDim.x;
+    const unsigned total = static_cast<unsigned>(rows) * static_cast<unsigned>(chunks);
     unsigned* const err = reinterpret_cast<unsigned*>(scratch);
     unsigned* const ticket_ctr = reinterpret_cast<unsigned*>(scratch + kCumTicketOffset);
     unsigned* const done_ctr = reinterpret_cast<unsigned*>(scratch + kCumDoneOffset);
-    unsigned long long* const records = reinterpret_cast<unsigned long long*>(scratch + kCumRecordsOffset);
-    const unsigned total = static_cast<unsigned>(rows) * static_cast<unsigned>(chunks);
+    unsigned long long* const records = reinterpret_cast<unsigned long long*>(scratch + cum_records_offset(total));
     const unsigned long long limit_ns = test_expire ? 2ull * 1000 * 1000 : kWaitLimitNs;
 
     grid_dependency_wait();  // the previous call's counters and records are settled
@@ -560,12 +651,19 @@ cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols,
     const int ce = static_cast<int>(static_cast<int64_t>(cols) * (c + 1) / chunks);
     const R x0 = ld_scalar(row);
     R v[ITEMS];
-    load_first_tile<CT, ITEMS>(row, cb, ce, v);
+    R* stash = nullptr;
+    KI<CT> a;
+    if constexpr (STASH) {
+        stash = stash_fill<CT>(row, cb, ce, cum_smem, &stash_bar, limit_ns, err);
+        a = stash_aggregate<CT, OP>(stash, cb, ce, warp_tot);
+    } else {
+        load_first_tile<CT, ITEMS>(row, cb, ce, v);
+        a = chunk_aggregate<CT, OP, ITEMS>(row, cb, ce, v, warp_tot);
+    }
     KI<CT> seed;
     seed.k = CT::template seed_key<OP>(x0);
     seed.i = 0;
 
-    const KI<CT> a = chunk_aggregate<CT, OP, ITEMS>(row, cb, ce, v, warp_tot);
     unsigned long long* const row_records = records + r * chunks;
     // Publish (the test flag leaves chunk 0's record unset: every wait on it expires).
     if (t == 0 && !(test_expire && c == 0)) st_release_gpu_u64(row_records + c, make_record(a));
@@ -622,9 +720,13 @@ cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols,
     const KI<CT> carry = s_total;
     __syncthreads();  // s_total / warp_tot are reused by the scan
     const R carry_v = carry.i == 0 ? x0 : ld_scalar(row + carry.i);
-    scan_chunk<CT, OP, ITEMS>(row, cb, ce, carry, carry_v, v, out_idx + r * static_cast<int64_t>(cols),
-                              out_val ? out_val + r * static_cast<int64_t>(cols) : nullptr, cum_smem, warp_tot,
-                              &s_total);
+    int64_t* const oi_row = out_idx + r * static_cast<int64_t>(cols);
+    R* const ov_row = out_val ? out_val + r * static_cast<int64_t>(cols) : nullptr;
+    if constexpr (STASH)
+        scan_stash<CT, OP, ITEMS>(row, stash, cb, ce, carry, carry_v, oi_row, ov_row,
+                                  reinterpret_cast<int*>(cum_smem + kCumStashBytes + 16), warp_tot, &s_total);
+    else
+        scan_chunk<CT, OP, ITEMS>(row, cb, ce, carry, carry_v, v, oi_row, ov_row, cum_smem, warp_tot, &s_total);
     // The CTA that counted last clears the records of the whole launch.
     if (t == 0) {
         s_flag = done_old == total - 1 ? 1u : 0u;
@@ -654,11 +756,13 @@ cudaError_t set_cum_smem(K kern, size_t smem, size_t& smem_set) {
     return cudaSuccess;
 }
 
-template <class CT, int OP>
-cudaError_t launch_cum_split(const argr_plan& p, const Problem& pr) {
+template <class CT, int OP, bool STASH>
+cudaError_t launch_cum_split_s(const argr_plan& p, const Problem& pr) {
     using R = typename CT::raw;
-    auto kern = cum_split_kernel<CT, OP, kCumItems>;
-    const size_t smem = cum_smem_bytes(p.block, sizeof(R));
+    auto kern = cum_split_kernel<CT, OP, kCumItems, STASH>;
+    // Stash: the chunk (16 bytes of slack for its alignment) and the tile indices.
+    const size_t smem = STASH ? kCumStashBytes + 16 + static_cast<size_t>(p.block) * kCumItems * 4
+                              : cum_smem_bytes(p.block, sizeof(R));
     static thread_local size_t smem_set = 0;
     cudaError_t e = set_cum_smem(kern, smem, smem_set);
     if (e != cudaSuccess) return e;
@@ -666,6 +770,12 @@ cudaError_t launch_cum_split(const argr_plan& p, const Problem& pr) {
     return launch_ex_smem(kern, grid, dim3(p.block), 1, smem, p, pr.stream, static_cast<const R*>(pr.x), pr.rows,
                           pr.cols, static_cast<int>(p.blocks_per_row), pr.out_idx, static_cast<R*>(pr.out_val),
                           static_cast<unsigned char*>(pr.scratch), (p.flags & ARGR_PLAN_TEST_EXPIRE) ? 1 : 0);
+}
+
+template <class CT, int OP>
+cudaError_t launch_cum_split(const argr_plan& p, const Problem& pr) {
+    if (p.flags & ARGR_PLAN_STASH) return launch_cum_split_s<CT, OP, true>(p, pr);
+    return launch_cum_split_s<CT, OP, false>(p, pr);
 }
 
 template <class CT, int OP>

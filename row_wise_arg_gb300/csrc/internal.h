@@ -28,8 +28,13 @@ namespace argr {
 //   [kCumTicketOffset, +4)     ticket counter (wraps to 0 after each launch)
 //   [kCumDoneOffset, +4)       done counter (wraps to 0 after each launch)
 //   [kCounterOffset, +8*kCumMaxChunks)
-//                              one 64-bit record per chunk, zeroed again by the
+//                              one 64-bit record per chunk for launches of up to
+//                              kCumMaxChunks chunks, zeroed again by the
 //                              launch's last CTA, so the split counters stay 0
+//   [kCumBigRecordsOffset, +8*chunks)
+//                              the records of larger launches (up to
+//                              kCumMaxChunksBig chunks), zeroed the same way;
+//                              argreduce's partials never reach this offset
 constexpr size_t kCounterOffset = 256;
 constexpr int64_t kMaxSplitRows = 2048;  // row slots a multi-CTA split may use
 constexpr size_t kPartialsOffset = kCounterOffset + 4 * kMaxSplitRows;
@@ -37,7 +42,14 @@ constexpr size_t kPartialBytes = 16;
 constexpr size_t kCumTicketOffset = 4;
 constexpr size_t kCumDoneOffset = 8;
 constexpr size_t kCumRecordsOffset = kCounterOffset;
-constexpr int64_t kCumMaxChunks = kMaxSplitRows / 2;  // rows * chunks of one split-scan launch
+constexpr int64_t kCumMaxChunks = kMaxSplitRows / 2;  // rows * chunks of a split scan, small region
+constexpr size_t kCumBigRecordsOffset = size_t(1) << 20;
+constexpr int64_t kCumMaxChunksBig = 65536;           // rows * chunks of a split scan, large region
+constexpr int64_t kMaxPartials = (kCumBigRecordsOffset - kPartialsOffset) / kPartialBytes;
+constexpr int64_t kCumStashBytes = 80 * 1024;         // a stashed split-scan chunk, at most
+ARGR_HD inline size_t cum_records_offset(int64_t total_chunks) {
+    return total_chunks <= kCumMaxChunks ? kCounterOffset : kCumBigRecordsOffset;
+}
 
 ARGR_HD inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

@@ -74,8 +74,10 @@ int elem_size(int dtype) {
 }
 
 size_t plan_scratch(const argr_plan& p, int64_t rows) {
-    if (p.path == ARGR_PATH_CUM_SPLIT)
-        return kCumRecordsOffset + 8 * static_cast<size_t>(rows) * static_cast<size_t>(p.blocks_per_row);
+    if (p.path == ARGR_PATH_CUM_SPLIT) {
+        const int64_t total = rows * p.blocks_per_row;
+        return cum_records_offset(total) + 8 * static_cast<size_t>(total);
+    }
     if (p.path == ARGR_PATH_SPLIT && p.blocks_per_row > 1)
         return kPartialsOffset +
                static_cast<size_t>(p.grid_rows) * static_cast<size_t>(p.blocks_per_row) * kPartialBytes;
@@ -293,6 +295,8 @@ argr_status check_plan(const argr_plan& p, int64_t rows, int64_t cols, int dtype
             // A split row owns its partial slots and counter: no row loop, and
             // at most kMaxSplitRows counters exist.
             if (p.blocks_per_row > 1 && (p.grid_rows < rows || p.grid_rows > kMaxSplitRows)) return ARGR_EINVAL;
+            // The partials stay below the split scan's large record region.
+            if (p.blocks_per_row > 1 && p.grid_rows * p.blocks_per_row > kMaxPartials) return ARGR_EINVAL;
             return ARGR_OK;
         }
         case ARGR_PATH_STREAM: {

@@ -85,6 +85,10 @@ argr_status make_cum_plan(int64_t rows, int64_t cols, int dtype, int op, const a
     const int64_t max_ctas = rows == 1 ? 2 * sms : kCumMaxChunks;
     const int max_block = rows == 1 ? 512 : 128;
     const int64_t target = std::min(max_ctas, std::max(sms / 2, ceil_div(rows * cols, kCumSplitElems)));
+    // (ARGR_PLAN_STASH is not chosen: stashing 80 KiB chunks reads the input
+    // once but leaves two CTAs per SM alternating a load burst and a compute
+    // burst, measured slower than re-reading from L2 or memory: [1,2^24]
+    // int64 128 vs 111 us, [16,2^20] f64 131 vs 110 us.)
     const int64_t chunks = std::min<int64_t>({kCumMaxChunks / rows, ceil_div(target, rows), cols / kCumMinChunk});
     if (chunks < 2) return ARGR_OK;
     const int64_t per_chunk = ceil_div(cols, chunks);
@@ -106,10 +110,16 @@ argr_status check_cum_plan(const argr_plan& p, int64_t rows, int64_t cols, int d
     const int64_t smem = static_cast<int64_t>(p.block) * kCumItems * (elem_size(dtype) + 4);
     if (smem > kMaxDynamicSmem) return ARGR_EINVAL;
     if (p.path == ARGR_PATH_CUM_SPLIT) {
-        if (p.flags & ~(ARGR_PLAN_PDL | ARGR_PLAN_TEST_EXPIRE)) return ARGR_EINVAL;
-        if (p.cluster != 1 || p.blocks_per_row < 1 || p.blocks_per_row > kCumMaxChunks) return ARGR_EINVAL;
-        if (rows > kCumMaxChunks / p.blocks_per_row) return ARGR_EINVAL;  // records of one launch
+        if (p.flags & ~(ARGR_PLAN_PDL | ARGR_PLAN_TEST_EXPIRE | ARGR_PLAN_STASH)) return ARGR_EINVAL;
+        if (p.cluster != 1 || p.blocks_per_row < 1 || p.blocks_per_row > kCumMaxChunksBig) return ARGR_EINVAL;
+        if (rows > kCumMaxChunksBig / p.blocks_per_row) return ARGR_EINVAL;  // records of one launch
         if (p.grid_rows != rows) return ARGR_EINVAL;
+        if (p.flags & ARGR_PLAN_STASH) {
+            // The largest chunk fits the stash; stash and tile indices fit one CTA.
+            if (ceil_div(cols, p.blocks_per_row) * elem_size(dtype) > kCumStashBytes) return ARGR_EINVAL;
+            if (kCumStashBytes + 16 + static_cast<int64_t>(p.block) * kCumItems * 4 > kMaxDynamicSmem)
+                return ARGR_EINVAL;
+        }
         return ARGR_OK;
     }
     if (p.path != ARGR_PATH_CUM) return ARGR_EINVAL;

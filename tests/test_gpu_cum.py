@@ -52,16 +52,24 @@ def split_plan(chunks, block=256, rows=1, flags=_lib.ARGR_PLAN_PDL):
     return p
 
 
-def run_cum(x, dtype, op, plan=None, scratch=None):
-    xd = torch.from_numpy(np.ascontiguousarray(x).view(VIEW[dtype])).cuda()
+STASH = 8  # ARGR_PLAN_STASH
+
+
+def run_cum(x, dtype, op, plan=None, scratch=None, offset=0):
+    """The scan of x on the GPU; `offset` elements of padding in front move
+    the base pointer off its allocation's alignment."""
+    flat = np.ascontiguousarray(x).view(VIEW[dtype]).reshape(-1)
+    buf = torch.zeros(flat.size + offset, dtype=getattr(torch, str(flat.dtype)), device="cuda")
+    buf[offset:] = torch.from_numpy(flat).cuda()
+    xd = buf[offset:].view(x.shape)
     idx, val = A.argreduce_cum(xd, op, dtype=dtype, plan=plan, scratch=scratch)
     torch.cuda.synchronize()
     raw_t = oracle.RAW_NP[dtype]
     return idx.cpu().numpy(), val.cpu().numpy().view(raw_t)
 
 
-def check_cum(x, dtype, op, plan=None, scratch=None):
-    idx, val = run_cum(x, dtype, op, plan, scratch)
+def check_cum(x, dtype, op, plan=None, scratch=None, offset=0):
+    idx, val = run_cum(x, dtype, op, plan, scratch, offset)
     eidx, evalue = oracle.cumreduce(x, dtype, op)
     bad = np.argwhere(idx != eidx)
     assert bad.size == 0, f"{len(bad)} outputs differ, first {bad[:3].tolist()}: got {idx[tuple(bad[0])]} " \
@@ -99,6 +107,10 @@ def test_cum_forced_geometries(dtype):
             for chunks, block in ((2, 32), (3, 1024), (7, 64), (64, 256)):
                 if rows * chunks <= 1024:  # chunks > cols leaves some chunks empty
                     check_cum(x, dtype, op, plan=split_plan(chunks, block, rows, flags=chunks % 2))
+            # stashed chunks (bulk copies of the aligned middle, plain loads of the ends)
+            for chunks, block, off in ((1, 512, 0), (3, 128, 1), (5, 1024, 3), (64, 64, 2)):
+                if -(-cols // chunks) * W.ELEM_SIZE[dtype] <= 80 * 1024:
+                    check_cum(x, dtype, op, plan=split_plan(chunks, block, rows, flags=1 | STASH), offset=off)
 
 
 def test_cum_leading_nan_and_extremes():
@@ -215,8 +227,12 @@ def test_cum_split_rejections():
                                   p) == _lib.ARGR_ESCRATCH  # misaligned
     assert _lib.argreduce_cum_raw(x.data_ptr(), "f32", 4, 100000, "max", o.data_ptr(), 0, sc.ptr, 200, 0,
                                   p) == _lib.ARGR_ESCRATCH  # too small
-    for bad in (split_plan(257, 256, rows=4), split_plan(8, 256, rows=3), split_plan(8, 48, rows=4),
-                split_plan(8, 256, rows=4, flags=_lib.ARGR_PLAN_BULK)):
+    # more than 1024 chunks keep their records 1 MiB into the scratch buffer
+    assert _lib.argreduce_cum_raw(x.data_ptr(), "f32", 4, 100000, "max", o.data_ptr(), 0, sc.ptr, 4096, 0,
+                                  split_plan(257, 256, rows=4)) == _lib.ARGR_ESCRATCH
+    for bad in (split_plan(16385, 256, rows=4), split_plan(8, 256, rows=3), split_plan(8, 48, rows=4),
+                split_plan(8, 256, rows=4, flags=_lib.ARGR_PLAN_BULK),
+                split_plan(1, 256, rows=4, flags=STASH)):  # a 400 KB chunk does not fit the stash
         assert _lib.argreduce_cum_raw(x.data_ptr(), "f32", 4, 100000, "max", o.data_ptr(), 0, sc.ptr, 4096, 0,
                                       bad) == _lib.ARGR_EINVAL
     bad = split_plan(8, 256, rows=4)
@@ -270,3 +286,54 @@ def test_cum_int_max_row_f16():
             assert (gv == np.array([vals[int(i)] for i in w], dtype=np.float32)).all()
     del x, out_i, out_v
     torch.cuda.empty_cache()
+
+
+def test_cum_stash_and_large_record_region():
+    """Split scans of more than 1024 chunks keep their records 1 MiB into the
+    scratch buffer: with and without stashed chunks, from misaligned bases,
+    alternating with argreduce's split path on one buffer, and 80 KiB
+    stashes of a 96 MiB row."""
+    from gpu_util import forced_plan
+    sc = A.Scratch()
+    x = cum_rows("f32", 2, 300001, seed=21)
+    for plan in (split_plan(1000, 128, rows=2, flags=1 | STASH), split_plan(1000, 64, rows=2),
+                 split_plan(2500, 32, rows=2, flags=STASH), split_plan(16, 512, rows=2, flags=STASH)):
+        for off in (0, 1):
+            check_cum(x, "f32", "max", plan=plan, scratch=sc, offset=off)
+    xr = W.fuzz_rows("bf16", 4, 1_000_000, seed=22)
+    er, _, _ = oracle.argreduce(xr, "bf16", "min")
+    xrd = torch.from_numpy(xr.view(np.int16)).cuda()
+    rplan = forced_plan("split", bpr=16, grid_rows=4)
+    for _ in range(2):
+        check_cum(x, "f32", "min", plan=split_plan(1500, 128, rows=2, flags=STASH), scratch=sc)
+        got, _ = A.argreduce_with_plan(rplan, xrd, "min", dtype="bf16", scratch=sc)
+        torch.cuda.synchronize()
+        assert (got.cpu().numpy() == er).all()
+    assert A.argreduce_read_error(sc.ptr, 0) == _lib.ARGR_OK
+    # stashed 80 KiB chunks of 12M int64 elements (96 MiB, 1229 chunks) in one row, from an odd base
+    n = 12 << 20
+    big = cum_rows("i64", 1, n, seed=23)
+    check_cum(big, "i64", "max", plan=split_plan(1229, 512, rows=1, flags=1 | STASH), offset=1)
+    # the forced expiry with stashed chunks
+    # (16 chunks of a 300001-element f32 row: 75 KB each, within the 80 KiB stash)
+    A.argreduce_cum(torch.from_numpy(x).cuda(), "max", plan=split_plan(16, 256, rows=2, flags=STASH | 4),
+                    scratch=sc)
+    assert A.argreduce_read_error(sc.ptr, 0) == _lib.ARGR_ETIMEOUT
+    check_cum(x, "f32", "max", plan=split_plan(16, 256, rows=2, flags=STASH), scratch=sc)
+    assert A.argreduce_read_error(sc.ptr, 0) == _lib.ARGR_OK
+
+
+def test_split_partials_stay_below_the_scan_records():
+    """argreduce's split partials may not reach 1 MiB into the scratch
+    buffer, where large split scans keep their records."""
+    from gpu_util import forced_plan
+    x = torch.zeros(2048, 100000, device="cuda")
+    o = torch.empty(2048, dtype=torch.int64, device="cuda")
+    sc = A.Scratch(nbytes=4 << 20)
+    ok = forced_plan("split", bpr=31, grid_rows=2048)   # 63488 partials: below 1 MiB
+    bad = forced_plan("split", bpr=32, grid_rows=2048)  # 65536 partials: beyond
+    assert _lib.argreduce_with_plan_raw(ok, x.data_ptr(), "f32", 2048, 100000, "max", o.data_ptr(), 0, sc.ptr,
+                                        sc.nbytes, 0) == _lib.ARGR_OK
+    assert _lib.argreduce_with_plan_raw(bad, x.data_ptr(), "f32", 2048, 100000, "max", o.data_ptr(), 0, sc.ptr,
+                                        sc.nbytes, 0) == _lib.ARGR_EINVAL
+    torch.cuda.synchronize()

@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import row_wise_arg_gb300 as A
@@ -392,7 +393,15 @@ def test_cum_plans_and_validation():
                            (16, 1 << 20, "f64")]:
         d = A.argreduce_cum_plan(rows, cols, dt, "max", GB300).as_dict()
         seen.add((d["path_name"], d["cluster"] > 1))
-        if d["path_name"] == "cum_split":
+        es = {"f32": 4, "f16": 2, "bf16": 2, "f64": 8, "i32": 4, "i64": 8}[dt]
+        if d["path_name"] == "cum_split" and d["flags"] & 8:
+            # ARGR_PLAN_STASH: inputs of 32 MiB and more, chunks that fit 80 KiB of shared memory
+            chunks = d["blocks_per_row"]
+            assert rows * cols * es >= 32 << 20 and -(-cols // chunks) * es <= 80 * 1024 and d["block"] == 512
+            assert chunks >= -(-76 // rows) and rows * chunks <= 65536
+            total = rows * chunks
+            assert d["scratch_bytes"] == (256 if total <= 1024 else 1 << 20) + 8 * total
+        elif d["path_name"] == "cum_split":
             # long rows, fewer than the SMs: 76..304 CTAs, records of one launch <= 1024
             chunks = d["blocks_per_row"]
             assert rows < 152 and chunks >= 2 and rows * chunks <= 1024 and cols > 32768
@@ -416,7 +425,8 @@ def test_cum_plans_and_validation():
             if rows >= 4 * 152:
                 assert d["block"] <= 128 and (d["block"] == 32 or d["block"] * 7 <= cols)
     assert seen == {("cum_split", False), ("cum", True), ("cum", False)}
-    assert A.argreduce_cum_plan(1, 16777216, "i64", "max", GB300).as_dict()["blocks_per_row"] == 304
+    big = A.argreduce_cum_plan(1, 16777216, "i64", "max", GB300).as_dict()
+    assert big["blocks_per_row"] == 304 and big["flags"] & 8 == 0  # the stash is a forced-plan option
     assert A.argreduce_cum_plan(1, 65536, "i64", "max", GB300).as_dict()["blocks_per_row"] == 76
     assert A.argreduce_cum_plan(4, 16384, "i32", "max", GB300).as_dict()["cluster"] == 16
     assert A.argreduce_cum_plan(4096, 4096, "f32", "max", GB300).as_dict()["block"] == 128
@@ -439,15 +449,22 @@ def test_cum_split_index_arithmetic():
     record's index + 1 never collides with 0 (unpublished) or 0xffffffff
     (empty chunk)."""
     for rows, cols, chunks in [(1, 65536, 18), (1, 5, 7), (3, 7, 5), (1024, 1, 1), (1, 2**31 - 1, 1024),
-                               (2, 2**31 - 1, 512), (16, 65536, 64), (5, 4099, 204)]:
+                               (2, 2**31 - 1, 512), (16, 65536, 64), (5, 4099, 204), (1, 2**31 - 1, 65536),
+                               (16, 2**20, 4096), (1, 1025, 1025)]:
         total = rows * chunks
-        assert total <= 1024
+        assert total <= 65536
+        region = 256 if total <= 1024 else 1 << 20
+        if region == 256:
+            assert region + 8 * total <= 8448  # inside the split counters' region
+        else:
+            # beyond every argreduce partial: 8448 + 16 * (grid_rows * blocks_per_row) <= 1 MiB
+            assert 8448 + 16 * ((1 << 20) - 8448) // 16 <= region
         seen = set()
         for ticket in range(total):
             r, c = divmod(ticket, chunks)
             seen.add((r, c))
-            word = 256 + 8 * (r * chunks + c)
-            assert 256 <= word and word + 8 <= 256 + 8 * total <= 256 + 8 * 1024 == 8448
+            word = region + 8 * (r * chunks + c)
+            assert region <= word and word + 8 <= region + 8 * total
         assert len(seen) == total
         for c_ in range(chunks):
             cb = cols * c_ // chunks
@@ -459,7 +476,7 @@ def test_cum_split_index_arithmetic():
                 assert 1 <= (ce - 1) + 1 < 0xffffffff
         assert cols * chunks // chunks == cols
     # the wrapping counters: atom.inc with bound total-1 hands out 0..total-1 and ends at 0
-    for total in (1, 2, 18, 1024):
+    for total in (1, 2, 18, 1024, 65536):
         ctr, got = 0, []
         for _ in range(total):
             got.append(ctr)
@@ -479,3 +496,52 @@ def test_cub_compare_library_exports():
     for name in ("cubcmp_temp_bytes", "cubcmp_argreduce"):
         assert hasattr(lib, name)
     assert not hasattr(_lib.load(), "cubcmp_argreduce")
+
+
+def _stash_fill_plan(g0, n, es, stash_bytes=80 * 1024, piece=16384):
+    """The split scan's stash arithmetic (stash_fill), restated: the chunk
+    [g0, g0 + n*es) goes to shared offset (g0 % 16) onward; its 16-byte
+    aligned middle by bulk copies of at most `piece` bytes, the head and the
+    tail element by element."""
+    g1 = g0 + n * es
+    a0 = (g0 + 15) & ~15
+    a1 = g1 & ~15
+    bulk = a1 > a0
+    head = (a0 - g0) // es if bulk else n
+    tail = (a1 - g0) // es if bulk else n
+    stash = g0 & 15  # shared offset of element 0 of the chunk
+    copies = []
+    if bulk:
+        dst = stash + (a0 - g0)
+        off = 0
+        while off < a1 - a0:
+            ln = min(piece, a1 - a0 - off)
+            copies.append((dst + off, a0 + off, ln))
+            off += ln
+    return head, tail, stash, copies
+
+
+def test_cum_stash_fill_arithmetic():
+    """Every element of a stashed chunk is written exactly once (head and tail
+    by threads, the middle by bulk copies whose global and shared addresses
+    and sizes are multiples of 16, at most 16 KiB each), and the stash stays
+    within its 80 KiB + 16 bytes of shared memory, before the tile indices."""
+    stash_bytes = 80 * 1024
+    for es in (2, 4, 8):
+        cap = stash_bytes // es
+        for phase in range(0, 16, es):
+            for n in (1, 2, 3, 7, 8, 9, 15, 16, 17, 31, 33, 100, 4095, cap - 1, cap):
+                g0 = 0x7f0000000000 + 4096 * 3 + phase
+                head, tail, stash, copies = _stash_fill_plan(g0, n, es)
+                covered = np.zeros(n, dtype=np.int64)
+                covered[:head] += 1
+                covered[tail:] += 1
+                for dst, src, ln in copies:
+                    assert dst % 16 == 0 and src % 16 == 0 and ln % 16 == 0 and 0 < ln <= 16384
+                    first = (src - g0) // es
+                    assert (src - g0) % es == 0 and dst - stash == src - g0
+                    covered[first:first + ln // es] += 1
+                assert (covered == 1).all(), (es, phase, n)
+                assert 0 <= head <= tail <= n and (head == n) == (not copies)
+                assert stash + n * es <= stash_bytes + 16  # the tile indices start at stash_bytes + 16
+                assert len(copies) <= 5
