@@ -385,7 +385,13 @@ def time_group(torch, A, cases, inputs, steps, warmup, stream, dist=None, device
     the step count is rounded up to whole replays. Returns (seconds, steps
     timed, copies, clocks)."""
     copies = copies_for(cases, cap=64 if exact else 4096)
-    per_graph = 1 if exact else max(1, math.ceil(copies / 16))
+    if exact:
+        per_graph = 1
+    else:
+        # About 16 calls per graph (as in the timed step) so that a graph
+        # launch is not charged to a single call, within 2 GiB of copies.
+        step_bytes = sum(algo_bytes(c) if is_scan(c) else c.nbytes for c in cases)
+        per_graph = max(1, math.ceil(copies / 16), min(math.ceil(16 / len(cases)), (2 << 30) // max(step_bytes, 1)))
     copies = per_graph * math.ceil(copies / per_graph)
     dev = [to_dev(torch, x, c.dtype).reshape(-1) for c, x in zip(cases, inputs)]
     gs = GraphSet(torch, A, cases, dev, copies, per_graph, stream, cub)
