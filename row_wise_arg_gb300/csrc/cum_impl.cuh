@@ -744,18 +744,6 @@ constexpr int kCumItems = 7;
 
 inline size_t cum_smem_bytes(int block, int es) { return static_cast<size_t>(block) * kCumItems * (es + 4); }
 
-// Raise the kernel's dynamic shared memory limit when needed; `smem_set` is
-// the caller's record for that one kernel (max and min kernels share a type).
-template <class K>
-cudaError_t set_cum_smem(K kern, size_t smem, size_t& smem_set) {
-    if (smem > 48 * 1024 && smem > smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        smem_set = smem;
-    }
-    return cudaSuccess;
-}
-
 template <class CT, int OP, bool STASH>
 cudaError_t launch_cum_split_s(const argr_plan& p, const Problem& pr) {
     using R = typename CT::raw;
@@ -763,8 +751,8 @@ cudaError_t launch_cum_split_s(const argr_plan& p, const Problem& pr) {
     // Stash: the chunk (16 bytes of slack for its alignment) and the tile indices.
     const size_t smem = STASH ? kCumStashBytes + 16 + static_cast<size_t>(p.block) * kCumItems * 4
                               : cum_smem_bytes(p.block, sizeof(R));
-    static thread_local size_t smem_set = 0;
-    cudaError_t e = set_cum_smem(kern, smem, smem_set);
+    static KernelLaunchCache cache;
+    cudaError_t e = ensure_smem_limit(kern, smem, cache);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(pr.rows * p.blocks_per_row));
     return launch_ex_smem(kern, grid, dim3(p.block), 1, smem, p, pr.stream, static_cast<const R*>(pr.x), pr.rows,
@@ -785,47 +773,27 @@ cudaError_t launch_cum_op(const argr_plan& p, const Problem& pr) {
     const size_t smem = cum_smem_bytes(p.block, sizeof(R));
     if (p.cluster <= 1) {
         auto kern1 = cum_kernel<CT, OP, kCumItems, false>;
-        static thread_local size_t smem_set1 = 0;
-        cudaError_t e = set_cum_smem(kern1, smem, smem_set1);
+        static KernelLaunchCache cache1;
+        cudaError_t e = ensure_smem_limit(kern1, smem, cache1);
         if (e != cudaSuccess) return e;
         return launch_ex_smem(kern1, dim3(1, static_cast<unsigned>(p.grid_rows)), dim3(p.block), 1, smem, p,
                               pr.stream, static_cast<const R*>(pr.x), pr.rows, pr.cols, pr.out_idx,
                               static_cast<R*>(pr.out_val));
     }
     auto kern = cum_kernel<CT, OP, kCumItems, true>;
-    static thread_local size_t smem_set = 0;
-    cudaError_t e = set_cum_smem(kern, smem, smem_set);
+    static KernelLaunchCache cache;
+    cudaError_t e = ensure_smem_limit(kern, smem, cache);
     if (e != cudaSuccess) return e;
     const int C = p.cluster;
     if (C > 8) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = allow_big_cluster(kern, cache);
         if (e != cudaSuccess) return e;
     }
     const dim3 grid(static_cast<unsigned>(C), static_cast<unsigned>(p.grid_rows));
-    {
-        // Refuse a cluster shape the device cannot co-schedule (checked once per shape).
-        static thread_local int checked_block = 0, checked_cluster = 0, checked_ok = 0;
-        if (checked_block != p.block || checked_cluster != C) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = grid;
-            cfg.blockDim = dim3(p.block);
-            cfg.dynamicSmemBytes = smem;
-            cudaLaunchAttribute attr;
-            attr.id = cudaLaunchAttributeClusterDimension;
-            attr.val.clusterDim.x = static_cast<unsigned>(C);
-            attr.val.clusterDim.y = 1;
-            attr.val.clusterDim.z = 1;
-            cfg.attrs = &attr;
-            cfg.numAttrs = 1;
-            int n = 0;
-            e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-            if (e != cudaSuccess) return e;
-            checked_block = p.block;
-            checked_cluster = C;
-            checked_ok = n > 0;
-        }
-        if (!checked_ok) return cudaErrorInvalidClusterSize;  // reported as ARGR_EUNSUPPORTED
-    }
+    bool ok = false;  // refuse a cluster shape the device cannot co-schedule
+    e = cluster_fits(kern, grid, p.block, C, smem, cache, &ok);
+    if (e != cudaSuccess) return e;
+    if (!ok) return cudaErrorInvalidClusterSize;  // reported as ARGR_EUNSUPPORTED
     return launch_ex_smem(kern, grid, dim3(p.block), C, smem, p, pr.stream, static_cast<const R*>(pr.x), pr.rows,
                           pr.cols, pr.out_idx, static_cast<R*>(pr.out_val));
 }

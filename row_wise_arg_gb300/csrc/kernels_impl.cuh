@@ -27,6 +27,9 @@
 // Row offsets are 64-bit.
 #pragma once
 
+#include <atomic>
+#include <mutex>
+
 #include "device_common.cuh"
 #include "internal.h"
 #include "tma.cuh"
@@ -772,6 +775,103 @@ stream_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, i
 }
 
 // ---------------------------------------------------------------------------
+// Per-device launch facts: a kernel's raised dynamic shared memory limit, its
+// permission for 16-CTA clusters, and whether a cluster shape fits the device.
+// Kernel attributes belong to the current device, so each is recorded per
+// device; the records are shared by every host thread (atomics, or a mutex
+// for the occupancy answers).
+// ---------------------------------------------------------------------------
+constexpr int kLaunchCacheDevices = 64;
+
+struct KernelLaunchCache {
+    std::atomic<size_t> smem_limit[kLaunchCacheDevices];  // dynamic shared memory already allowed
+    std::atomic<bool> big_cluster[kLaunchCacheDevices];   // non-portable cluster size allowed
+    struct Fit {
+        int dev, block, cluster;
+        size_t smem;
+        bool ok;
+    };
+    std::mutex mu;
+    Fit fits[16];
+    int n_fits;
+};
+
+inline cudaError_t launch_device(int* dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e == cudaSuccess && (*dev < 0 || *dev >= kLaunchCacheDevices)) *dev = -1;  // not cached
+    return e;
+}
+
+// Raise the kernel's dynamic shared memory limit to `smem` on the current device if needed.
+template <class K>
+cudaError_t ensure_smem_limit(K kern, size_t smem, KernelLaunchCache& c) {
+    if (smem <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = launch_device(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && c.smem_limit[dev].load(std::memory_order_acquire) >= smem) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e == cudaSuccess && dev >= 0) {
+        size_t cur = c.smem_limit[dev].load(std::memory_order_relaxed);
+        while (cur < smem && !c.smem_limit[dev].compare_exchange_weak(cur, smem, std::memory_order_release)) {
+        }
+    }
+    return e;
+}
+
+// Allow clusters of more than 8 CTAs for the kernel on the current device.
+template <class K>
+cudaError_t allow_big_cluster(K kern, KernelLaunchCache& c) {
+    int dev = 0;
+    cudaError_t e = launch_device(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && c.big_cluster[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess && dev >= 0) c.big_cluster[dev].store(true, std::memory_order_release);
+    return e;
+}
+
+// Whether the current device can co-schedule clusters of `cluster` CTAs of
+// `block` threads with `smem` bytes of dynamic shared memory (answers cached).
+template <class K>
+cudaError_t cluster_fits(K kern, dim3 grid, int block, int cluster, size_t smem, KernelLaunchCache& c, bool* ok) {
+    int dev = 0;
+    cudaError_t e = launch_device(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0) {
+        std::lock_guard<std::mutex> lk(c.mu);
+        for (int i = 0; i < c.n_fits && i < 16; ++i) {
+            const KernelLaunchCache::Fit& f = c.fits[i];
+            if (f.dev == dev && f.block == block && f.cluster == cluster && f.smem == smem) {
+                *ok = f.ok;
+                return cudaSuccess;
+            }
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    *ok = n > 0;
+    if (dev >= 0) {
+        std::lock_guard<std::mutex> lk(c.mu);
+        c.fits[c.n_fits % 16] = KernelLaunchCache::Fit{dev, block, cluster, smem, *ok};
+        ++c.n_fits;
+    }
+    return cudaSuccess;
+}
+
+// ---------------------------------------------------------------------------
 // Launchers. Every launch goes through cudaLaunchKernelEx so that it can carry
 // the programmatic-dependent-launch attribute (plan flag ARGR_PLAN_PDL) and,
 // on the cluster path, the cluster shape.
@@ -885,34 +985,17 @@ template <class Tag, int OP, int U>
 cudaError_t launch_cluster_u(const argr_plan& p, const Problem& pr) {
     using R = typename Tag::raw;
     auto kern = cluster_kernel<Tag, OP, U>;
+    static KernelLaunchCache cache;
     if (p.cluster > 8) {
         // Cluster sizes above the portable 8 must be enabled per kernel.
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        cudaError_t e = allow_big_cluster(kern, cache);
         if (e != cudaSuccess) return e;
     }
     const dim3 grid(static_cast<unsigned>(p.cluster), static_cast<unsigned>(p.grid_rows));
-    // Refuse a cluster shape the device cannot co-schedule (checked once per
-    // kernel, block size and cluster size).
-    static thread_local int checked_block = 0, checked_cluster = 0, checked_ok = 0;
-    if (checked_block != p.block || checked_cluster != p.cluster) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = grid;
-        cfg.blockDim = dim3(p.block);
-        cudaLaunchAttribute attr;
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = static_cast<unsigned>(p.cluster);
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
-        int n = 0;
-        cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-        if (e != cudaSuccess) return e;
-        checked_block = p.block;
-        checked_cluster = p.cluster;
-        checked_ok = n > 0;
-    }
-    if (!checked_ok) return cudaErrorInvalidClusterSize;  // reported as ARGR_EUNSUPPORTED
+    bool ok = false;  // refuse a cluster shape the device cannot co-schedule
+    cudaError_t e = cluster_fits(kern, grid, p.block, p.cluster, 0, cache, &ok);
+    if (e != cudaSuccess) return e;
+    if (!ok) return cudaErrorInvalidClusterSize;  // reported as ARGR_EUNSUPPORTED
     return launch_ex(kern, grid, dim3(p.block), p.cluster, p, pr.stream, static_cast<const R*>(pr.x), pr.rows,
                      pr.cols, pr.out_idx, static_cast<R*>(pr.out_val));
 }
@@ -929,40 +1012,18 @@ cudaError_t launch_cluster_bulk(const argr_plan& p, const Problem& pr) {
     using R = typename Tag::raw;
     auto kern = cluster_bulk_kernel<Tag, OP>;
     const size_t smem = cluster_bulk_smem(p, pr.cols, sizeof(R));
-    static thread_local size_t smem_set = 0;
-    if (smem > 48 * 1024 && smem > smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        smem_set = smem;
-    }
+    static KernelLaunchCache cache;
+    cudaError_t e = ensure_smem_limit(kern, smem, cache);
+    if (e != cudaSuccess) return e;
     if (p.cluster > 8) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = allow_big_cluster(kern, cache);
         if (e != cudaSuccess) return e;
     }
     const dim3 grid(static_cast<unsigned>(p.cluster), static_cast<unsigned>(p.grid_rows));
-    static thread_local int checked_block = 0, checked_cluster = 0, checked_ok = 0;
-    static thread_local size_t checked_smem = 0;
-    if (checked_block != p.block || checked_cluster != p.cluster || checked_smem != smem) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = grid;
-        cfg.blockDim = dim3(p.block);
-        cfg.dynamicSmemBytes = smem;
-        cudaLaunchAttribute attr;
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = static_cast<unsigned>(p.cluster);
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
-        int n = 0;
-        cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-        if (e != cudaSuccess) return e;
-        checked_block = p.block;
-        checked_cluster = p.cluster;
-        checked_smem = smem;
-        checked_ok = n > 0;
-    }
-    if (!checked_ok) return cudaErrorInvalidClusterSize;  // reported as ARGR_EUNSUPPORTED
+    bool ok = false;
+    e = cluster_fits(kern, grid, p.block, p.cluster, smem, cache, &ok);
+    if (e != cudaSuccess) return e;
+    if (!ok) return cudaErrorInvalidClusterSize;  // reported as ARGR_EUNSUPPORTED
     return launch_ex_smem(kern, grid, dim3(p.block), p.cluster, smem, p, pr.stream, static_cast<const R*>(pr.x),
                           pr.rows, pr.cols, pr.out_idx, static_cast<R*>(pr.out_val));
 }
@@ -995,12 +1056,9 @@ cudaError_t launch_stream_g(const argr_plan& p, const Problem& pr) {
     using R = typename Tag::raw;
     auto kern = stream_kernel<Tag, OP, G>;
     const size_t smem = static_cast<size_t>(p.block / 32) * p.stages * p.stage_bytes;
-    static thread_local size_t smem_set = 0;
-    if (smem > 48 * 1024 && smem > smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        smem_set = smem;
-    }
+    static KernelLaunchCache cache;
+    cudaError_t e = ensure_smem_limit(kern, smem, cache);
+    if (e != cudaSuccess) return e;
     return launch_ex_smem(kern, dim3(static_cast<unsigned>(p.grid_rows)), dim3(p.block), 1, smem, p, pr.stream,
                           static_cast<const R*>(pr.x), pr.rows, pr.cols, pr.out_idx, static_cast<R*>(pr.out_val),
                           p.stages, p.stage_bytes, p.flags);
@@ -1037,41 +1095,20 @@ cudaError_t launch_axis_vug(const argr_plan& p, const Problem& pr) {
     const int Y = p.block / 32;
     const int C = p.cluster > 1 ? p.cluster : 1;
     const size_t smem = static_cast<size_t>(Y + (C > 1 ? C : 0)) * CG * V * sizeof(uint4);
-    static thread_local size_t smem_set = 0;
-    if (smem > 48 * 1024 && smem > smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        smem_set = smem;
-    }
+    static KernelLaunchCache cache;
+    cudaError_t e = ensure_smem_limit(kern, smem, cache);
+    if (e != cudaSuccess) return e;
     if (C > 8) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = allow_big_cluster(kern, cache);
         if (e != cudaSuccess) return e;
     }
     const int64_t tiles = (pr.inner + CG * V - 1) / (CG * V);
     const dim3 grid(static_cast<unsigned>(C), static_cast<unsigned>(tiles), static_cast<unsigned>(p.grid_rows));
     if (C > 1) {
-        // Refuse a cluster shape the device cannot co-schedule (checked once per shape).
-        static thread_local int checked_block = 0, checked_cluster = 0, checked_ok = 0;
-        if (checked_block != p.block || checked_cluster != C) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = grid;
-            cfg.blockDim = dim3(p.block);
-            cfg.dynamicSmemBytes = smem;
-            cudaLaunchAttribute attr;
-            attr.id = cudaLaunchAttributeClusterDimension;
-            attr.val.clusterDim.x = static_cast<unsigned>(C);
-            attr.val.clusterDim.y = 1;
-            attr.val.clusterDim.z = 1;
-            cfg.attrs = &attr;
-            cfg.numAttrs = 1;
-            int n = 0;
-            cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-            if (e != cudaSuccess) return e;
-            checked_block = p.block;
-            checked_cluster = C;
-            checked_ok = n > 0;
-        }
-        if (!checked_ok) return cudaErrorInvalidClusterSize;  // reported as ARGR_EUNSUPPORTED
+        bool ok = false;  // refuse a cluster shape the device cannot co-schedule
+        e = cluster_fits(kern, grid, p.block, C, smem, cache, &ok);
+        if (e != cudaSuccess) return e;
+        if (!ok) return cudaErrorInvalidClusterSize;  // reported as ARGR_EUNSUPPORTED
     }
     return launch_ex_smem(kern, grid, dim3(p.block), C, smem, p, pr.stream, static_cast<const R*>(pr.x), pr.rows,
                           pr.cols, pr.inner, pr.out_idx, static_cast<R*>(pr.out_val));

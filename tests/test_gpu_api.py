@@ -237,3 +237,52 @@ def test_int_max_row_f16():
     assert int(idx[0]) == 0
     del x
     torch.cuda.empty_cache()
+
+
+def test_concurrent_host_threads():
+    """Four host threads call the library at once (ctypes releases the GIL),
+    each on its own stream and scratch: cluster launches with their
+    co-scheduling check, raised shared-memory limits (bulk cluster plans, the
+    stashed scan) and split scans share the per-device launch records without
+    corrupting them or each other's results."""
+    import threading
+    xs = [W.fuzz_rows("f32", 3, 200001 + 17 * k, seed=70 + k) for k in range(4)]
+    want = [oracle.argreduce(x, "f32", "max")[0] for x in xs]
+    want_cum = [oracle.cumreduce(np.ascontiguousarray(x[:, :50000]), "f32", "min")[0] for x in xs]
+    dev = [torch.from_numpy(x).cuda() for x in xs]
+    dev_cum = [torch.from_numpy(np.ascontiguousarray(x[:, :50000])).cuda() for x in xs]
+    errors = []
+
+    def stash_plan():
+        p = _lib.argr_plan()
+        p.path, p.block, p.cluster, p.blocks_per_row, p.grid_rows, p.flags = _lib.ARGR_PATH_CUM_SPLIT, 256, 1, 8, 3, 1 | 8
+        return p
+
+    def worker(k):
+        try:
+            s = torch.cuda.Stream()
+            sc = A.Scratch()
+            plans = [None, forced_plan("cluster", cluster=16, block=512, unroll=8, grid_rows=3),
+                     forced_plan("cluster", cluster=8, block=256, unroll=4, grid_rows=3, bulk=True)]
+            with torch.cuda.stream(s):
+                for it in range(20):
+                    p = plans[(it + k) % 3]
+                    if p is None:
+                        idx, _ = A.argreduce(dev[k], "max", scratch=sc, stream=s)
+                    else:
+                        idx, _ = A.argreduce_with_plan(p, dev[k], "max", scratch=sc, stream=s)
+                    ci, _ = A.argreduce_cum(dev_cum[k], "min", scratch=sc, stream=s, with_values=False,
+                                            plan=stash_plan() if it % 2 else None)
+                    s.synchronize()
+                    if not (idx.cpu().numpy() == want[k]).all() or not (ci.cpu().numpy() == want_cum[k]).all():
+                        errors.append((k, it))
+                        return
+        except Exception as e:  # surfaced below
+            errors.append((k, repr(e)))
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
