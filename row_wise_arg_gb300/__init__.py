@@ -94,6 +94,27 @@ def _default_scratch(device_index: int, stream_ptr: int) -> Scratch:
         return s
 
 
+_need_lock = threading.Lock()
+_need_cache: Dict[Tuple[int, int, int, int, int, bool], int] = {}
+
+
+def _scratch_need(device_index: int, rows: int, cols: int, code: int, opc: int, cum: bool = False) -> int:
+    """Scratch bytes of the planner's plan for this problem on this device,
+    asked once per (device, shape, type, op): the planner is a pure function
+    of them and the device's properties."""
+    if rows == 0:
+        return 0
+    key = (device_index, rows, cols, code, opc, cum)
+    need = _need_cache.get(key)
+    if need is None:
+        need = (argreduce_cum_scratch_bytes if cum else argreduce_scratch_bytes)(rows, cols, code, opc)
+        with _need_lock:
+            if len(_need_cache) > 4096:
+                _need_cache.clear()
+            _need_cache[key] = need
+    return need
+
+
 def _prepare(x, op, dtype, with_values, out_idx, out_val):
     torch = _torch()
     if not x.is_cuda:
@@ -126,7 +147,7 @@ def argreduce(x, op="max", *, dtype: Optional[str] = None, with_values: bool = F
     rows, cols, code, opc, out_idx, out_val = _prepare(x, op, dtype, with_values, out_idx, out_val)
     st_ptr = (stream if isinstance(stream, int) else stream.cuda_stream) if stream is not None else \
         torch.cuda.current_stream(x.device).cuda_stream
-    need = argreduce_scratch_bytes(rows, cols, code, opc) if rows else 0
+    need = _scratch_need(x.device.index, rows, cols, code, opc)
     if scratch is None and need:
         scratch = _default_scratch(x.device.index, st_ptr)
     if need:
@@ -226,7 +247,7 @@ def argreduce_cum(x, op="max", *, dtype: Optional[str] = None, with_values: bool
     if rows == 0:
         need = 0
     elif plan is None:
-        need = argreduce_cum_scratch_bytes(rows, cols, code, op)
+        need = _scratch_need(x.device.index, rows, cols, code, _lib._code(OP_CODES, op), cum=True)
     else:
         need = argreduce_plan_scratch_bytes(plan, rows)
     if scratch is None and need:
