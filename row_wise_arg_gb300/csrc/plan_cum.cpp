@@ -67,12 +67,16 @@ argr_status make_cum_plan(int64_t rows, int64_t cols, int dtype, int op, const a
     out->block = block;
     const int64_t tile = static_cast<int64_t>(block) * kCumItems;
     if (cols < kCumMinChunkTiles * 2 * tile || rows >= sms) return ARGR_OK;  // one CTA per row
-    if (cols <= kCumClusterMaxCols && caps.max_cluster >= 2) {
+    const int64_t es = elem_size(dtype);
+    if ((cols <= kCumClusterMaxCols || (es <= 4 && cols <= 2 * kCumClusterMaxCols)) && caps.max_cluster >= 2) {
         // Short rows: a cluster per row exchanges aggregates through
-        // distributed shared memory, a round trip cheaper than scratch.
+        // distributed shared memory, a round trip cheaper than scratch. Up to
+        // 64K elements of 4 bytes or less, 1024-thread CTAs keep each CTA's
+        // chunk in one tile ([1,65536] f32 7.9 -> 6.9 us); the 64-bit scan
+        // kernels spill at that size and stay with the split scan.
         const int64_t c = std::min<int64_t>({16, caps.max_cluster, ceil_div(2 * sms, rows),
                                              std::max<int64_t>(2, cols / kCumMinChunk)});
-        out->block = 256;
+        out->block = cols <= kCumClusterMaxCols ? 256 : 1024;
         out->cluster = static_cast<int32_t>(c);
         out->blocks_per_row = c;
         out->grid_rows = rows;

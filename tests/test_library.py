@@ -412,11 +412,13 @@ def test_cum_plans_and_validation():
             assert d["block"] in (64, 128, 256, 512) and d["block"] <= cap
             assert d["block"] * 7 >= -(-cols // chunks) or d["block"] == cap
             assert d["scratch_bytes"] == 256 + 8 * rows * chunks and d["cluster"] == 1
-            assert d["grid_rows"] == rows
+            assert d["grid_rows"] == rows and cols > 32768 and (es == 8 or cols > 65536)
         elif d["cluster"] > 1:
             # short rows, fewer than the SMs: one cluster per row
-            assert d["path_name"] == "cum" and cols <= 32768 and rows < 152 and d["cluster"] <= 16
-            assert d["block"] == 256 and d["grid_rows"] == rows and d["scratch_bytes"] == 0
+            assert d["path_name"] == "cum" and rows < 152 and d["cluster"] <= 16
+            assert cols <= 32768 or (es <= 4 and cols <= 65536)
+            assert d["block"] == (256 if cols <= 32768 else 1024)
+            assert d["grid_rows"] == rows and d["scratch_bytes"] == 0
             assert d["blocks_per_row"] == d["cluster"]
         else:
             # one CTA per row: as many rows as SMs, or rows too short to split
