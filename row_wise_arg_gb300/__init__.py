@@ -36,19 +36,40 @@ def _torch():
     return torch
 
 
+_ELEM_SIZE = {ARGR_F32: 4, ARGR_F16: 2, ARGR_BF16: 2, ARGR_F64: 8, _lib.ARGR_I32: 4, _lib.ARGR_I64: 8}
+_tensor_codes: Optional[dict] = None
+_raw_stream = None
+
+
 def dtype_code(t, dtype: Optional[str]) -> int:
     """Element type code for a tensor; raw 16-bit tensors need ``dtype``."""
-    torch = _torch()
+    global _tensor_codes
     if dtype is not None:
         code = DTYPE_CODES[dtype]
-        if t.element_size() != {0: 4, 1: 2, 2: 2, 3: 8, 4: 4, 5: 8}[code]:
+        if t.element_size() != _ELEM_SIZE[code]:
             raise TypeError(f"dtype {dtype} does not match element size {t.element_size()}")
         return code
-    m = {torch.float32: ARGR_F32, torch.float16: ARGR_F16, torch.bfloat16: ARGR_BF16, torch.float64: ARGR_F64,
-         torch.int32: _lib.ARGR_I32, torch.int64: _lib.ARGR_I64}
-    if t.dtype not in m:
+    if _tensor_codes is None:
+        torch = _torch()
+        _tensor_codes = {torch.float32: ARGR_F32, torch.float16: ARGR_F16, torch.bfloat16: ARGR_BF16,
+                         torch.float64: ARGR_F64, torch.int32: _lib.ARGR_I32, torch.int64: _lib.ARGR_I64}
+    code = _tensor_codes.get(t.dtype)
+    if code is None:
         raise TypeError(f"unsupported tensor dtype {t.dtype}; pass dtype= for raw 16-bit storage")
-    return m[t.dtype]
+    return code
+
+
+def _stream_ptr(stream, device_index: int) -> int:
+    """The cudaStream_t to launch on: `stream` (a torch stream or a raw
+    handle), else torch's current stream on the device."""
+    global _raw_stream
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    if _raw_stream is None:
+        torch = _torch()
+        f = getattr(torch._C, "_cuda_getCurrentRawStream", None)  # no Stream object per call
+        _raw_stream = f if f is not None else (lambda d: torch.cuda.current_stream(d).cuda_stream)
+    return _raw_stream(device_index)
 
 
 class Scratch:
@@ -116,22 +137,24 @@ def _scratch_need(device_index: int, rows: int, cols: int, code: int, opc: int, 
 
 
 def _prepare(x, op, dtype, with_values, out_idx, out_val):
-    torch = _torch()
     if not x.is_cuda:
         raise ValueError("x must be a CUDA tensor (the library has no CPU path)")
-    if x.dim() == 0:
+    shape = x.shape
+    if len(shape) == 0:
         raise ValueError("x must have at least one dimension")
     if not x.is_contiguous():
         raise ValueError("x must be contiguous (row-major, reduced over its last axis)")
-    cols = x.shape[-1]
+    cols = shape[-1]
     rows = x.numel() // cols if cols else 0
     code = dtype_code(x, dtype)
-    lead = tuple(x.shape[:-1])
-    if out_idx is None:
-        out_idx = torch.empty(lead, dtype=torch.int64, device=x.device)
-    if with_values and out_val is None:
-        out_val = torch.empty(lead, dtype=x.dtype, device=x.device)
-    return rows, cols, code, _lib._code(OP_CODES, op), out_idx, out_val
+    opc = OP_CODES[op] if isinstance(op, str) else int(op)
+    if out_idx is None or (with_values and out_val is None):
+        torch = _torch()
+        if out_idx is None:
+            out_idx = torch.empty(shape[:-1], dtype=torch.int64, device=x.device)
+        if with_values and out_val is None:
+            out_val = torch.empty(shape[:-1], dtype=x.dtype, device=x.device)
+    return rows, cols, code, opc, out_idx, out_val
 
 
 def argreduce(x, op="max", *, dtype: Optional[str] = None, with_values: bool = False, out_idx=None, out_val=None,
@@ -143,19 +166,18 @@ def argreduce(x, op="max", *, dtype: Optional[str] = None, with_values: bool = F
     ``x[..., index]`` (else ``None``). Runs on ``stream`` (default: torch's
     current stream) without synchronising.
     """
-    torch = _torch()
     rows, cols, code, opc, out_idx, out_val = _prepare(x, op, dtype, with_values, out_idx, out_val)
-    st_ptr = (stream if isinstance(stream, int) else stream.cuda_stream) if stream is not None else \
-        torch.cuda.current_stream(x.device).cuda_stream
-    need = _scratch_need(x.device.index, rows, cols, code, opc)
+    dev = x.get_device()
+    st_ptr = _stream_ptr(stream, dev)
+    need = _scratch_need(dev, rows, cols, code, opc)
     if scratch is None and need:
-        scratch = _default_scratch(x.device.index, st_ptr)
+        scratch = _default_scratch(dev, st_ptr)
     if need:
         scratch.ensure(need, st_ptr)
-    st = _lib.argreduce_raw(x.data_ptr(), code, rows, cols, opc, out_idx.data_ptr(),
-                            out_val.data_ptr() if out_val is not None else 0,
-                            scratch.ptr if scratch is not None else 0,
-                            scratch.nbytes if scratch is not None else 0, st_ptr)
+    st = _lib.load().argreduce(x.data_ptr(), code, rows, cols, opc, out_idx.data_ptr(),
+                               out_val.data_ptr() if out_val is not None else None,
+                               scratch.ptr if scratch is not None else None,
+                               scratch.nbytes if scratch is not None else 0, st_ptr or None)
     if st != ARGR_OK:
         raise ArgreduceError(st, "argreduce")
     return out_idx, out_val
@@ -166,8 +188,7 @@ def argreduce_with_plan(plan: argr_plan, x, op="max", *, dtype: Optional[str] = 
     """argreduce() with an explicit (possibly forced) plan."""
     torch = _torch()
     rows, cols, code, opc, out_idx, out_val = _prepare(x, op, dtype, with_values, out_idx, out_val)
-    st_ptr = (stream if isinstance(stream, int) else stream.cuda_stream) if stream is not None else \
-        torch.cuda.current_stream(x.device).cuda_stream
+    st_ptr = _stream_ptr(stream, x.get_device())
     need = argreduce_plan_scratch_bytes(plan, rows)
     if scratch is None and need:
         scratch = _default_scratch(x.device.index, st_ptr)
@@ -205,8 +226,7 @@ def argreduce_axis(x, dim: int, op="max", *, dtype: Optional[str] = None, with_v
         out_idx = torch.empty(shape, dtype=torch.int64, device=x.device)
     if with_values and out_val is None:
         out_val = torch.empty(shape, dtype=x.dtype, device=x.device)
-    st_ptr = (stream if isinstance(stream, int) else stream.cuda_stream) if stream is not None else \
-        torch.cuda.current_stream(x.device).cuda_stream
+    st_ptr = _stream_ptr(stream, x.get_device())
     need = 0
     if inner == 1 and outer > 0 and reduce > 0:
         need = argreduce_plan_scratch_bytes(plan, outer) if plan is not None else \
@@ -242,8 +262,7 @@ def argreduce_cum(x, op="max", *, dtype: Optional[str] = None, with_values: bool
         out_idx = torch.empty(x.shape, dtype=torch.int64, device=x.device)
     if with_values and out_val is None:
         out_val = torch.empty_like(x)
-    st_ptr = (stream if isinstance(stream, int) else stream.cuda_stream) if stream is not None else \
-        torch.cuda.current_stream(x.device).cuda_stream
+    st_ptr = _stream_ptr(stream, x.get_device())
     if rows == 0:
         need = 0
     elif plan is None:
