@@ -118,6 +118,11 @@ typedef struct {
  * size (two CTAs per SM alternate loading and scanning), so the planner does
  * not set it. */
 #define ARGR_PLAN_STASH 8
+/* Plan flag (CUM_SPLIT path, not with ARGR_PLAN_STASH): decoupled look-back.
+ * Every chunk also publishes its inclusive prefix once known, and a CTA reads
+ * back only to the nearest one, so chunks can be one tile each (read once,
+ * from registers) at any chunk count; two record words per chunk. */
+#define ARGR_PLAN_LOOKBACK 16
 
 /* A launch plan. Produced by argreduce_plan(); tests may edit it to force a
  * path and pass it to argreduce_with_plan(), which re-validates it. */

@@ -613,7 +613,54 @@ __device__ __forceinline__ unsigned long long make_record(const KI<CT>& a) {
     return lo;
 }
 
-template <class CT, int OP, int ITEMS, bool STASH>
+// Wait (bounded) until chunk j publishes its inclusive prefix or its
+// aggregate, and return whichever is there; an empty record on expiry.
+__device__ __forceinline__ unsigned long long wait_either(const unsigned long long* incl,
+                                                          const unsigned long long* agg,
+                                                          unsigned long long limit_ns, unsigned* err) {
+    const unsigned long long t0 = global_timer_ns();
+    for (;;) {
+        unsigned long long w = ld_acquire_gpu_u64(incl);
+        if (static_cast<unsigned>(w) != 0) return w;
+        w = ld_acquire_gpu_u64(agg);
+        if (static_cast<unsigned>(w) != 0) return w;
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicOr(err, kErrWaitExpired);
+            return kNoElement;
+        }
+        __nanosleep(64);
+    }
+}
+
+// A published record of row `row` as a prefix result (false: none, or not a
+// record of this call, which is reported). Index 0 is the seed's: its key is
+// the seed key (for a NaN x[0] that is not elem_key's).
+template <class CT, int OP>
+__device__ __forceinline__ bool decode_record(unsigned long long w, const typename CT::raw* row, int cols,
+                                              const KI<CT>& seed, unsigned* err, KI<CT>* e) {
+    const unsigned lo = static_cast<unsigned>(w);
+    if (lo == 0 || lo == kNoElement) return false;
+    if (lo - 1u >= static_cast<unsigned>(cols)) {  // not a record of this call
+        atomicOr(err, kErrBadScratch);
+        return false;
+    }
+    e->i = static_cast<int>(lo - 1u);
+    if constexpr (sizeof(typename CT::key) <= 4) {
+        e->k = CT::from_bits(w >> 32);
+    } else {
+        e->k = e->i == 0 ? seed.k : CT::template elem_key<OP>(ld_scalar(row + e->i));
+    }
+    return true;
+}
+
+// Split scan, LOOKBACK variant (decoupled look-back): every chunk publishes
+// its aggregate and, once its carry-in is known, its inclusive prefix (chunk
+// 0 only the latter). A CTA reads the records of the chunks before its own,
+// one per thread, nearest first, down to the nearest inclusive prefix, so
+// the work per CTA does not grow with the chunk count; merging an inclusive
+// prefix with aggregates it already covers is harmless (first_best is
+// idempotent). Records: [aggregate, inclusive] per chunk.
+template <class CT, int OP, int ITEMS, bool STASH, bool LOOKBACK>
 __global__ void __launch_bounds__(1024)
 cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols, int chunks,
                  int64_t* __restrict__ out_idx, typename CT::raw* __restrict__ out_val,
@@ -625,14 +672,17 @@ cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols,
     __shared__ KI<CT> warp_tot[32];
     __shared__ KI<CT> s_total;
     __shared__ unsigned s_flag;
+    __shared__ int s_near;
     __shared__ __align__(8) unsigned long long stash_bar;
     const int t = threadIdx.x;
     const int nt = blockDim.x;
     const unsigned total = static_cast<unsigned>(rows) * static_cast<unsigned>(chunks);
+    constexpr unsigned kWords = LOOKBACK ? 2u : 1u;  // record words per chunk
     unsigned* const err = reinterpret_cast<unsigned*>(scratch);
     unsigned* const ticket_ctr = reinterpret_cast<unsigned*>(scratch + kCumTicketOffset);
     unsigned* const done_ctr = reinterpret_cast<unsigned*>(scratch + kCumDoneOffset);
-    unsigned long long* const records = reinterpret_cast<unsigned long long*>(scratch + cum_records_offset(total));
+    unsigned long long* const records =
+        reinterpret_cast<unsigned long long*>(scratch + cum_records_offset(static_cast<int64_t>(kWords) * total));
     const unsigned long long limit_ns = test_expire ? 2ull * 1000 * 1000 : kWaitLimitNs;
 
     grid_dependency_wait();  // the previous call's counters and records are settled
@@ -664,19 +714,54 @@ cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols,
     seed.k = CT::template seed_key<OP>(x0);
     seed.i = 0;
 
-    unsigned long long* const row_records = records + r * chunks;
+    unsigned long long* const row_records = records + kWords * (r * chunks);
+    KI<CT> acc = ki_identity<CT>();
+    if constexpr (LOOKBACK) {
+        // Publish: chunk 0 its inclusive prefix (seed and aggregate), the others
+        // their aggregate (the test flag leaves chunk 0's record unset).
+        if (t == 0 && !(test_expire && c == 0)) {
+            if (c == 0)
+                st_release_gpu_u64(row_records + 1, make_record(first_best(seed, a)));
+            else
+                st_release_gpu_u64(row_records + 2 * c, make_record(a));
+        }
+        // Look back in windows of one chunk per thread, nearest first.
+        for (int j_hi = c - 1; j_hi >= 0; j_hi -= nt) {
+            const int j = j_hi - t;
+            unsigned long long w = 0;
+            bool is_incl = false;
+            if (j >= 0) {
+                w = ld_acquire_gpu_u64(row_records + 2 * j + 1);
+                is_incl = static_cast<unsigned>(w) != 0;
+                if (!is_incl) w = ld_acquire_gpu_u64(row_records + 2 * j);
+            }
+            if (t == 0) s_near = nt;
+            __syncthreads();
+            if (is_incl) atomicMin(&s_near, t);
+            __syncthreads();
+            const int near = s_near;  // the nearest chunk with an inclusive prefix, if any in this window
+            if (j >= 0 && t <= near) {
+                if (static_cast<unsigned>(w) == 0)
+                    w = wait_either(row_records + 2 * j + 1, row_records + 2 * j, limit_ns, err);
+                KI<CT> e;
+                if (decode_record<CT, OP>(w, row, cols, seed, err, &e)) acc = first_best(acc, e);
+            }
+            __syncthreads();  // s_near is rewritten by the next window
+            if (near < nt) break;
+        }
+    } else {
+    unsigned long long* const row_rec1 = row_records;
     // Publish (the test flag leaves chunk 0's record unset: every wait on it expires).
-    if (t == 0 && !(test_expire && c == 0)) st_release_gpu_u64(row_records + c, make_record(a));
+    if (t == 0 && !(test_expire && c == 0)) st_release_gpu_u64(row_rec1 + c, make_record(a));
 
     // Merge the records of chunks 0 .. c-1 (all loads first, then the waits).
-    KI<CT> acc = ki_identity<CT>();
     for (int j0 = t; j0 < c; j0 += 4 * nt) {
         unsigned long long w[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) w[u] = j0 + u * nt < c ? ld_acquire_gpu_u64(row_records + j0 + u * nt) : kNoElement;
+        for (int u = 0; u < 4; ++u) w[u] = j0 + u * nt < c ? ld_acquire_gpu_u64(row_rec1 + j0 + u * nt) : kNoElement;
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-            if (static_cast<unsigned>(w[u]) == 0) w[u] = wait_record(row_records + j0 + u * nt, limit_ns, err);
+            if (static_cast<unsigned>(w[u]) == 0) w[u] = wait_record(row_rec1 + j0 + u * nt, limit_ns, err);
         R xv[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -703,6 +788,7 @@ cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols,
             }
         }
     }
+    }
     __syncthreads();  // warp_tot is free again (chunk_aggregate's readers are done)
     acc = block_first_best(acc, warp_tot);
     unsigned done_old = 0;
@@ -710,6 +796,8 @@ cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols,
         acc = first_best(seed, acc);
         if (t == 0) {
             s_total = acc;
+            // LOOKBACK: the inclusive prefix of this chunk, for the chunks after it.
+            if (LOOKBACK && c > 0) st_release_gpu_u64(row_records + 2 * c + 1, make_record(first_best(acc, a)));
             // Every record this CTA needs has been read (the barrier above);
             // count it done. The result is only needed after the scan.
             fence_acq_rel_gpu();
@@ -734,7 +822,7 @@ cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols,
     }
     __syncthreads();
     if (s_flag)
-        for (unsigned j = t; j < total; j += nt) records[j] = 0ull;
+        for (unsigned j = t; j < kWords * total; j += nt) records[j] = 0ull;
 }
 
 // ---------------------------------------------------------------------------
@@ -744,10 +832,10 @@ constexpr int kCumItems = 7;
 
 inline size_t cum_smem_bytes(int block, int es) { return static_cast<size_t>(block) * kCumItems * (es + 4); }
 
-template <class CT, int OP, bool STASH>
+template <class CT, int OP, bool STASH, bool LOOKBACK>
 cudaError_t launch_cum_split_s(const argr_plan& p, const Problem& pr) {
     using R = typename CT::raw;
-    auto kern = cum_split_kernel<CT, OP, kCumItems, STASH>;
+    auto kern = cum_split_kernel<CT, OP, kCumItems, STASH, LOOKBACK>;
     // Stash: the chunk (16 bytes of slack for its alignment) and the tile indices.
     const size_t smem = STASH ? kCumStashBytes + 16 + static_cast<size_t>(p.block) * kCumItems * 4
                               : cum_smem_bytes(p.block, sizeof(R));
@@ -762,8 +850,9 @@ cudaError_t launch_cum_split_s(const argr_plan& p, const Problem& pr) {
 
 template <class CT, int OP>
 cudaError_t launch_cum_split(const argr_plan& p, const Problem& pr) {
-    if (p.flags & ARGR_PLAN_STASH) return launch_cum_split_s<CT, OP, true>(p, pr);
-    return launch_cum_split_s<CT, OP, false>(p, pr);
+    if (p.flags & ARGR_PLAN_STASH) return launch_cum_split_s<CT, OP, true, false>(p, pr);
+    if (p.flags & ARGR_PLAN_LOOKBACK) return launch_cum_split_s<CT, OP, false, true>(p, pr);
+    return launch_cum_split_s<CT, OP, false, false>(p, pr);
 }
 
 template <class CT, int OP>

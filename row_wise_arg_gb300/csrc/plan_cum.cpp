@@ -68,12 +68,15 @@ argr_status make_cum_plan(int64_t rows, int64_t cols, int dtype, int op, const a
     const int64_t tile = static_cast<int64_t>(block) * kCumItems;
     if (cols < kCumMinChunkTiles * 2 * tile || rows >= sms) return ARGR_OK;  // one CTA per row
     const int64_t es = elem_size(dtype);
-    if ((cols <= kCumClusterMaxCols || (es <= 4 && cols <= 2 * kCumClusterMaxCols)) && caps.max_cluster >= 2) {
+    const bool wide_cluster = es <= 4 && cols <= 2 * kCumClusterMaxCols && rows * 16 <= 2 * sms && caps.max_cluster >= 16;
+    if ((cols <= kCumClusterMaxCols || wide_cluster) && caps.max_cluster >= 2) {
         // Short rows: a cluster per row exchanges aggregates through
         // distributed shared memory, a round trip cheaper than scratch. Up to
-        // 64K elements of 4 bytes or less, 1024-thread CTAs keep each CTA's
-        // chunk in one tile ([1,65536] f32 7.9 -> 6.9 us); the 64-bit scan
-        // kernels spill at that size and stay with the split scan.
+        // 64K elements of 4 bytes or less, while clusters of 16 fit, 1024-thread
+        // CTAs keep each CTA's chunk in one tile ([1,65536] f32 7.9 -> 6.9 us);
+        // the 64-bit scan kernels spill at that size and stay with the split
+        // scan, and so do more rows ([64,65536] f32: clusters of 5 x 1024
+        // 39 us, the split 26 us).
         const int64_t c = std::min<int64_t>({16, caps.max_cluster, ceil_div(2 * sms, rows),
                                              std::max<int64_t>(2, cols / kCumMinChunk)});
         out->block = cols <= kCumClusterMaxCols ? 256 : 1024;
@@ -89,6 +92,9 @@ argr_status make_cum_plan(int64_t rows, int64_t cols, int dtype, int op, const a
     const int64_t max_ctas = rows == 1 ? 2 * sms : kCumMaxChunks;
     const int max_block = rows == 1 ? 512 : 128;
     const int64_t target = std::min(max_ctas, std::max(sms / 2, ceil_div(rows * cols, kCumSplitElems)));
+    // (ARGR_PLAN_LOOKBACK is not chosen either: one-tile chunks behind a serial
+    // ticket / load / look-back / scan chain per CTA measured slower on long
+    // rows, [1,2^24] int64 116 vs 110 us.)
     // (ARGR_PLAN_STASH is not chosen: stashing 80 KiB chunks reads the input
     // once but leaves two CTAs per SM alternating a load burst and a compute
     // burst, measured slower than re-reading from L2 or memory: [1,2^24]
@@ -114,9 +120,12 @@ argr_status check_cum_plan(const argr_plan& p, int64_t rows, int64_t cols, int d
     const int64_t smem = static_cast<int64_t>(p.block) * kCumItems * (elem_size(dtype) + 4);
     if (smem > kMaxDynamicSmem) return ARGR_EINVAL;
     if (p.path == ARGR_PATH_CUM_SPLIT) {
-        if (p.flags & ~(ARGR_PLAN_PDL | ARGR_PLAN_TEST_EXPIRE | ARGR_PLAN_STASH)) return ARGR_EINVAL;
-        if (p.cluster != 1 || p.blocks_per_row < 1 || p.blocks_per_row > kCumMaxChunksBig) return ARGR_EINVAL;
-        if (rows > kCumMaxChunksBig / p.blocks_per_row) return ARGR_EINVAL;  // records of one launch
+        if (p.flags & ~(ARGR_PLAN_PDL | ARGR_PLAN_TEST_EXPIRE | ARGR_PLAN_STASH | ARGR_PLAN_LOOKBACK))
+            return ARGR_EINVAL;
+        if ((p.flags & ARGR_PLAN_STASH) && (p.flags & ARGR_PLAN_LOOKBACK)) return ARGR_EINVAL;
+        const int64_t words = (p.flags & ARGR_PLAN_LOOKBACK) ? 2 : 1;  // record words per chunk
+        if (p.cluster != 1 || p.blocks_per_row < 1 || p.blocks_per_row > kCumMaxChunksBig / words) return ARGR_EINVAL;
+        if (rows > kCumMaxChunksBig / words / p.blocks_per_row) return ARGR_EINVAL;  // records of one launch
         if (p.grid_rows != rows) return ARGR_EINVAL;
         if (p.flags & ARGR_PLAN_STASH) {
             // The largest chunk fits the stash; stash and tile indices fit one CTA.

@@ -53,6 +53,7 @@ def split_plan(chunks, block=256, rows=1, flags=_lib.ARGR_PLAN_PDL):
 
 
 STASH = 8  # ARGR_PLAN_STASH
+LOOKBACK = 16  # ARGR_PLAN_LOOKBACK
 
 
 def run_cum(x, dtype, op, plan=None, scratch=None, offset=0):
@@ -107,6 +108,10 @@ def test_cum_forced_geometries(dtype):
             for chunks, block in ((2, 32), (3, 1024), (7, 64), (64, 256)):
                 if rows * chunks <= 1024:  # chunks > cols leaves some chunks empty
                     check_cum(x, dtype, op, plan=split_plan(chunks, block, rows, flags=chunks % 2))
+            # decoupled look-back (inclusive prefixes), chunks of up to a tile and beyond
+            for chunks, block in ((2, 64), (3, 1024), (9, 32), (100, 128)):
+                if rows * chunks * 2 <= 65536:
+                    check_cum(x, dtype, op, plan=split_plan(chunks, block, rows, flags=(chunks % 2) | LOOKBACK))
             # stashed chunks (bulk copies of the aligned middle, plain loads of the ends)
             for chunks, block, off in ((1, 512, 0), (3, 128, 1), (5, 1024, 3), (64, 64, 2)):
                 if -(-cols // chunks) * W.ELEM_SIZE[dtype] <= 80 * 1024:
@@ -337,3 +342,36 @@ def test_split_partials_stay_below_the_scan_records():
     assert _lib.argreduce_with_plan_raw(bad, x.data_ptr(), "f32", 2048, 100000, "max", o.data_ptr(), 0, sc.ptr,
                                         sc.nbytes, 0) == _lib.ARGR_EINVAL
     torch.cuda.synchronize()
+
+
+def test_cum_lookback_long_rows_and_scratch():
+    """The decoupled look-back at large chunk counts (windows of one chunk per
+    thread, several windows back), one-tile chunks of long rows, the forced
+    expiry, and one scratch buffer shared with argreduce's split path."""
+    from gpu_util import forced_plan
+    sc = A.Scratch()
+    x = cum_rows("f32", 2, 300001, seed=31)
+    for chunks, block in ((4096, 32), (1000, 64), (300, 128)):
+        for off in (0, 3):
+            check_cum(x, "f32", "max", plan=split_plan(chunks, block, rows=2, flags=1 | LOOKBACK), scratch=sc,
+                      offset=off)
+    for dtype, n, block in (("i64", 1 << 20, 512), ("f64", 3 << 20, 256), ("bf16", 1 << 24, 512)):
+        big = cum_rows(dtype, 1, n, seed=n % 1000)
+        chunks = -(-n // (block * 7))  # one tile per chunk
+        check_cum(big, dtype, "min", plan=split_plan(chunks, block, rows=1, flags=1 | LOOKBACK), scratch=sc)
+    xi = cum_rows("i32", 16, 70000, seed=32)
+    check_cum(xi, "i32", "max", plan=split_plan(1024, 64, rows=16, flags=LOOKBACK), scratch=sc)
+    xr = W.fuzz_rows("f32", 3, 2_000_000, seed=33)
+    er, _, _ = oracle.argreduce(xr, "f32", "max")
+    got, _ = A.argreduce_with_plan(forced_plan("split", bpr=12, grid_rows=3), torch.from_numpy(xr).cuda(), "max",
+                                   scratch=sc)
+    torch.cuda.synchronize()
+    assert (got.cpu().numpy() == er).all()
+    assert A.argreduce_read_error(sc.ptr, 0) == _lib.ARGR_OK
+    A.argreduce_cum(torch.from_numpy(x).cuda(), "max", plan=split_plan(600, 128, rows=2, flags=LOOKBACK | 4),
+                    scratch=sc)
+    assert A.argreduce_read_error(sc.ptr, 0) == _lib.ARGR_ETIMEOUT
+    check_cum(x, "f32", "max", plan=split_plan(600, 128, rows=2, flags=LOOKBACK), scratch=sc)
+    assert A.argreduce_read_error(sc.ptr, 0) == _lib.ARGR_OK
+    assert _lib.argreduce_cum_raw(0x10000, "f32", 2, 300001, "max", 0x10000, 0, sc.ptr, sc.nbytes, 0,
+                                  split_plan(8, 128, rows=2, flags=LOOKBACK | STASH)) == _lib.ARGR_EINVAL

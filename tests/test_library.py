@@ -412,11 +412,11 @@ def test_cum_plans_and_validation():
             assert d["block"] in (64, 128, 256, 512) and d["block"] <= cap
             assert d["block"] * 7 >= -(-cols // chunks) or d["block"] == cap
             assert d["scratch_bytes"] == 256 + 8 * rows * chunks and d["cluster"] == 1
-            assert d["grid_rows"] == rows and cols > 32768 and (es == 8 or cols > 65536)
+            assert d["grid_rows"] == rows and cols > 32768 and (es == 8 or cols > 65536 or rows * 16 > 304)
         elif d["cluster"] > 1:
             # short rows, fewer than the SMs: one cluster per row
             assert d["path_name"] == "cum" and rows < 152 and d["cluster"] <= 16
-            assert cols <= 32768 or (es <= 4 and cols <= 65536)
+            assert cols <= 32768 or (es <= 4 and cols <= 65536 and rows * 16 <= 304)
             assert d["block"] == (256 if cols <= 32768 else 1024)
             assert d["grid_rows"] == rows and d["scratch_bytes"] == 0
             assert d["blocks_per_row"] == d["cluster"]
@@ -547,3 +547,16 @@ def test_cum_stash_fill_arithmetic():
                 assert 0 <= head <= tail <= n and (head == n) == (not copies)
                 assert stash + n * es <= stash_bytes + 16  # the tile indices start at stash_bytes + 16
                 assert len(copies) <= 5
+
+
+def test_cum_lookback_scratch_size():
+    """A look-back split scan keeps two record words per chunk ([aggregate,
+    inclusive prefix]); past 1024 words they move 1 MiB into the buffer."""
+    for rows, chunks, want in ((1, 76, 256 + 16 * 76), (1, 512, 256 + 16 * 512), (1, 513, (1 << 20) + 16 * 513),
+                               (4, 4681, (1 << 20) + 16 * 4 * 4681)):
+        p = _lib.argr_plan()
+        p.path, p.block, p.cluster, p.blocks_per_row, p.grid_rows = _lib.ARGR_PATH_CUM_SPLIT, 512, 1, chunks, rows
+        p.flags = _lib.ARGR_PLAN_PDL | _lib.ARGR_PLAN_LOOKBACK
+        assert _lib.argreduce_plan_scratch_bytes(p, rows) == want
+        p.flags = _lib.ARGR_PLAN_PDL
+        assert _lib.argreduce_plan_scratch_bytes(p, rows) == (256 if rows * chunks <= 1024 else 1 << 20) + 8 * rows * chunks
