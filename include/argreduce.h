@@ -77,6 +77,10 @@ typedef enum {
                               `cluster` CTAs (1 = none) splits it further. unroll 4 or 8 */
     ARGR_PATH_CUM = 6,     /* cummax / cummin (argreduce_cum): a row in `cluster` chunks, one CTA
                               each (1 = none), scanned in tiles of block * 7 elements */
+    ARGR_PATH_CUM_STREAM = 8, /* cummax / cummin: tiles of block * 7 elements (`blocks_per_row` =
+                              tiles per row) taken in ticket order by `grid_rows` CTAs, each
+                              tile read once; carries by decoupled look-back through scratch
+                              (rows * blocks_per_row <= 32768) */
     ARGR_PATH_CUM_SPLIT = 7, /* cummax / cummin: a row in `blocks_per_row` chunks, one CTA each,
                               any number of CTAs; chunk aggregates are exchanged through
                               scratch (rows * blocks_per_row <= 65536; above 1024 the

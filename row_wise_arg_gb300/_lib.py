@@ -18,7 +18,7 @@ ARGR_F32, ARGR_F16, ARGR_BF16, ARGR_F64, ARGR_I32, ARGR_I64 = 0, 1, 2, 3, 4, 5
 ARGR_MAX, ARGR_MIN, ARGR_MAX_LAST, ARGR_MIN_LAST = 0, 1, 2, 3
 (ARGR_OK, ARGR_EINVAL, ARGR_ESCRATCH, ARGR_EUNSUPPORTED, ARGR_ECUDA, ARGR_ETIMEOUT) = range(6)
 ARGR_PATH_NONE, ARGR_PATH_ROWS, ARGR_PATH_SPLIT, ARGR_PATH_CLUSTER, ARGR_PATH_STREAM, ARGR_PATH_AXIS, \
-    ARGR_PATH_CUM, ARGR_PATH_CUM_SPLIT = range(8)
+    ARGR_PATH_CUM, ARGR_PATH_CUM_SPLIT, ARGR_PATH_CUM_STREAM = range(9)
 ARGR_PLAN_PDL = 1
 ARGR_PLAN_BULK = 2
 ARGR_PLAN_TEST_EXPIRE = 4
@@ -30,7 +30,7 @@ DTYPE_CODES = {"f32": ARGR_F32, "f16": ARGR_F16, "bf16": ARGR_BF16, "f64": ARGR_
 OP_CODES = {"max": ARGR_MAX, "min": ARGR_MIN, "max_last": ARGR_MAX_LAST, "min_last": ARGR_MIN_LAST}
 PATH_NAMES = {ARGR_PATH_NONE: "none", ARGR_PATH_ROWS: "rows", ARGR_PATH_SPLIT: "split",
               ARGR_PATH_CLUSTER: "cluster", ARGR_PATH_STREAM: "stream", ARGR_PATH_AXIS: "axis",
-              ARGR_PATH_CUM: "cum", ARGR_PATH_CUM_SPLIT: "cum_split"}
+              ARGR_PATH_CUM: "cum", ARGR_PATH_CUM_SPLIT: "cum_split", ARGR_PATH_CUM_STREAM: "cum_stream"}
 
 # Every function the header declares (checked by the tests).
 EXPORTS = (

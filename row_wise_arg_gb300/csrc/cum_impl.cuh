@@ -826,6 +826,222 @@ cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols,
 }
 
 // ---------------------------------------------------------------------------
+// Streaming scan (ARGR_PATH_CUM_STREAM): a fixed grid of CTAs (about two per
+// SM) takes tiles in ticket order, any number of tiles per CTA, each tile
+// read once. For a tile the CTA scans it locally (identity-seeded), publishes
+// the tile's total as its aggregate, looks back (decoupled look-back, as in
+// the split scan's LOOKBACK variant) for its carry-in, publishes its inclusive
+// prefix and writes its outputs; the next ticket's tile is being loaded into
+// registers all the while. Tickets come from an atomic counter, so a tile
+// only waits for tiles with earlier tickets, taken by CTAs that are running.
+// Records: [aggregate, inclusive] per tile. The CTA that leaves last clears
+// the records and the ticket counter.
+// ---------------------------------------------------------------------------
+template <class CT, int OP, int ITEMS>
+__device__ __forceinline__ void stream_load(const typename CT::raw* x, int cols, int tiles_per_row, unsigned ticket,
+                                            typename CT::raw (&v)[ITEMS]) {
+    const int nt = blockDim.x;
+    const int tile = nt * ITEMS;
+    const int64_t r = ticket / static_cast<unsigned>(tiles_per_row);
+    const int base = static_cast<int>(ticket % static_cast<unsigned>(tiles_per_row)) * tile;
+    const int n = cols - base < tile ? cols - base : tile;
+    const typename CT::raw* src = x + r * static_cast<int64_t>(cols) + base;
+#pragma unroll
+    for (int q = 0; q < ITEMS; ++q)
+        if (static_cast<int>(threadIdx.x) + q * nt < n) v[q] = ld_scalar(src + threadIdx.x + q * nt);
+}
+
+template <class CT, int OP, int ITEMS>
+__global__ void __launch_bounds__(1024)
+cum_stream_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols, int tiles_per_row,
+                  int64_t* __restrict__ out_idx, typename CT::raw* __restrict__ out_val,
+                  unsigned char* __restrict__ scratch, int test_expire) {
+    using R = typename CT::raw;
+    using K = typename CT::key;
+    extern __shared__ __align__(16) unsigned char cum_smem[];
+    __shared__ KI<CT> warp_tot[32];  // the local scan's warp prefixes
+    __shared__ KI<CT> lb_tot[32];    // the look-back's reduction
+    __shared__ KI<CT> s_total;
+    __shared__ KI<CT> s_carry;
+    __shared__ unsigned s_ticket;
+    __shared__ int s_near;
+    const int nt = blockDim.x;
+    const int t = threadIdx.x;
+    const int lane = t & 31;
+    const int warp = t >> 5;
+    const int nwarps = nt >> 5;
+    const int tile = nt * ITEMS;
+    const unsigned total = static_cast<unsigned>(rows) * static_cast<unsigned>(tiles_per_row);
+    unsigned* const err = reinterpret_cast<unsigned*>(scratch);
+    unsigned* const ticket_ctr = reinterpret_cast<unsigned*>(scratch + kCumTicketOffset);
+    unsigned* const done_ctr = reinterpret_cast<unsigned*>(scratch + kCumDoneOffset);
+    unsigned long long* const records =
+        reinterpret_cast<unsigned long long*>(scratch + cum_records_offset(2 * static_cast<int64_t>(total)));
+    const unsigned long long limit_ns = test_expire ? 2ull * 1000 * 1000 : kWaitLimitNs;
+    R* tin = reinterpret_cast<R*>(cum_smem);
+    int* tidx = reinterpret_cast<int*>(cum_smem + static_cast<size_t>(tile) * sizeof(R));
+
+    // Tickets are taken one tile ahead: a CTA holds `ticket` (being scanned)
+    // and `next` (being loaded), and asks for the one after during the scan.
+    grid_dependency_wait();  // the previous call's counters and records are settled
+    if (t == 0) {
+        s_ticket = atomicAdd(ticket_ctr, 1u);
+        s_near = static_cast<int>(s_ticket < total ? atomicAdd(ticket_ctr, 1u) : total);
+    }
+    __syncthreads();
+    allow_dependents();
+    unsigned ticket = s_ticket;
+    unsigned next = static_cast<unsigned>(s_near);
+    // Each CTA takes at most two tickets past the last tile, so a first ticket
+    // at or above total + 2 * grid comes from a scratch buffer never prepared.
+    if (ticket >= total + 2 * gridDim.x) {
+        if (t == 0) atomicOr(err, kErrBadScratch);
+        return;
+    }
+    __syncthreads();  // s_near is reused by the look-back
+    R v[ITEMS];
+    if (ticket < total) stream_load<CT, OP, ITEMS>(x, cols, tiles_per_row, ticket, v);
+    while (ticket < total) {
+        const int64_t r = ticket / static_cast<unsigned>(tiles_per_row);
+        const int j = static_cast<int>(ticket % static_cast<unsigned>(tiles_per_row));
+        const int base = j * tile;
+        const int n = cols - base < tile ? cols - base : tile;
+        const R* row = x + r * static_cast<int64_t>(cols);
+        unsigned long long* const row_records = records + 2 * (r * tiles_per_row);
+#pragma unroll
+        for (int q = 0; q < ITEMS; ++q)
+            if (t + q * nt < n) tin[t + q * nt] = v[q];
+        unsigned after = total;  // thread 0: the ticket after `next`, asked for now, read at the end
+        if (t == 0 && next < total) after = atomicAdd(ticket_ctr, 1u);
+        __syncthreads();
+        if (next < total) stream_load<CT, OP, ITEMS>(x, cols, tiles_per_row, next, v);  // overlaps the rest
+
+        // Local scan: thread prefixes, warp scan, warp totals; s_total = the tile's total.
+        KI<CT> p[ITEMS];
+        KI<CT> run = ki_identity<CT>();
+#pragma unroll
+        for (int q = 0; q < ITEMS; ++q) {
+            const int jj = t * ITEMS + q;
+            if (jj < n) {
+                const K k = CT::template elem_key<OP>(tin[jj]);
+                if (k > run.k) {
+                    run.k = k;
+                    run.i = base + jj;
+                }
+            }
+            p[q] = run;
+        }
+        KI<CT> ws = run;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const KI<CT> o = shfl_up_ki(ws, d);
+            if (lane >= d) ws = later(o, ws);
+        }
+        KI<CT> excl = shfl_up_ki(ws, 1);
+        if (lane == 0) excl = ki_identity<CT>();
+        if (lane == 31) warp_tot[warp] = ws;
+        __syncthreads();
+        if (warp == 0) {
+            KI<CT> w = lane < nwarps ? warp_tot[lane] : ki_identity<CT>();
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const KI<CT> o = shfl_up_ki(w, d);
+                if (lane >= d) w = later(o, w);
+            }
+            KI<CT> we = shfl_up_ki(w, 1);
+            if (lane == 0) we = ki_identity<CT>();
+            if (lane < nwarps) warp_tot[lane] = we;  // exclusive prefix of each warp
+            if (lane == nwarps - 1) s_total = w;
+        }
+        __syncthreads();
+        const KI<CT> agg = s_total;
+        const R x0 = ld_scalar(row);
+        KI<CT> seed;
+        seed.k = CT::template seed_key<OP>(x0);
+        seed.i = 0;
+
+        // Carry-in: the seed for a row's first tile, else the look-back.
+        KI<CT> acc = ki_identity<CT>();
+        if (j == 0) {
+            if (t == 0 && !test_expire) st_release_gpu_u64(row_records + 1, make_record(first_best(seed, agg)));
+        } else {
+            if (t == 0) st_release_gpu_u64(row_records + 2 * j, make_record(agg));
+            for (int j_hi = j - 1; j_hi >= 0; j_hi -= nt) {
+                const int jb = j_hi - t;
+                unsigned long long w = 0;
+                bool is_incl = false;
+                if (jb >= 0) {
+                    w = ld_acquire_gpu_u64(row_records + 2 * jb + 1);
+                    is_incl = static_cast<unsigned>(w) != 0;
+                    if (!is_incl) w = ld_acquire_gpu_u64(row_records + 2 * jb);
+                }
+                if (t == 0) s_near = nt;
+                __syncthreads();
+                if (is_incl) atomicMin(&s_near, t);
+                __syncthreads();
+                const int near = s_near;
+                if (jb >= 0 && t <= near) {
+                    if (static_cast<unsigned>(w) == 0)
+                        w = wait_either(row_records + 2 * jb + 1, row_records + 2 * jb, limit_ns, err);
+                    KI<CT> e;
+                    if (decode_record<CT, OP>(w, row, cols, seed, err, &e)) acc = first_best(acc, e);
+                }
+                __syncthreads();  // s_near is rewritten by the next window
+                if (near < nt) break;
+            }
+        }
+        acc = block_first_best(acc, lb_tot);
+        if (t == 0) {
+            const KI<CT> carry = first_best(seed, acc);
+            s_carry = carry;
+            if (j > 0) st_release_gpu_u64(row_records + 2 * j + 1, make_record(first_best(carry, agg)));
+        }
+        __syncthreads();
+        const KI<CT> carry = s_carry;
+        const R carry_v = carry.i == 0 ? x0 : ld_scalar(row + carry.i);  // before the tile: an L2 hit
+
+        // Outputs: the carry, the warp's exclusive prefix and the lane's, then the thread's own prefixes.
+        const KI<CT> before = later(later(carry, warp_tot[warp]), excl);
+#pragma unroll
+        for (int q = 0; q < ITEMS; ++q) {
+            const int jj = t * ITEMS + q;
+            if (jj < n) tidx[jj] = later(before, p[q]).i;
+        }
+        __syncthreads();
+        int64_t* oi = out_idx + r * static_cast<int64_t>(cols) + base;
+#pragma unroll
+        for (int q = 0; q < ITEMS; ++q)
+            if (t + q * nt < n) oi[t + q * nt] = tidx[t + q * nt];
+        if (out_val) {
+            R* ov = out_val + r * static_cast<int64_t>(cols) + base;
+#pragma unroll
+            for (int q = 0; q < ITEMS; ++q) {
+                if (t + q * nt < n) {
+                    const int i = tidx[t + q * nt];
+                    ov[t + q * nt] = i >= base ? tin[i - base] : carry_v;
+                }
+            }
+        }
+        if (t == 0) s_ticket = after;
+        __syncthreads();  // tin, tidx, the shared totals are reused by the next tile
+        ticket = next;
+        next = s_ticket;
+    }
+    // The CTA that leaves last clears the records and resets the ticket counter.
+    if (t == 0) {
+        fence_acq_rel_gpu();
+        const unsigned old = inc_relaxed_gpu(done_ctr, gridDim.x - 1);
+        s_ticket = old == gridDim.x - 1 ? 1u : 0u;
+        if (s_ticket) fence_acq_rel_gpu();
+    }
+    __syncthreads();
+    if (s_ticket) {
+        for (unsigned k = t; k < 2 * total; k += nt) records[k] = 0ull;
+        if (t == 0) *ticket_ctr = 0u;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Launchers.
 // ---------------------------------------------------------------------------
 constexpr int kCumItems = 7;
@@ -856,9 +1072,24 @@ cudaError_t launch_cum_split(const argr_plan& p, const Problem& pr) {
 }
 
 template <class CT, int OP>
+cudaError_t launch_cum_stream(const argr_plan& p, const Problem& pr) {
+    using R = typename CT::raw;
+    auto kern = cum_stream_kernel<CT, OP, kCumItems>;
+    const size_t smem = cum_smem_bytes(p.block, sizeof(R));
+    static KernelLaunchCache cache;
+    cudaError_t e = ensure_smem_limit(kern, smem, cache);
+    if (e != cudaSuccess) return e;
+    return launch_ex_smem(kern, dim3(static_cast<unsigned>(p.grid_rows)), dim3(p.block), 1, smem, p, pr.stream,
+                          static_cast<const R*>(pr.x), pr.rows, pr.cols, static_cast<int>(p.blocks_per_row),
+                          pr.out_idx, static_cast<R*>(pr.out_val), static_cast<unsigned char*>(pr.scratch),
+                          (p.flags & ARGR_PLAN_TEST_EXPIRE) ? 1 : 0);
+}
+
+template <class CT, int OP>
 cudaError_t launch_cum_op(const argr_plan& p, const Problem& pr) {
     using R = typename CT::raw;
     if (p.path == ARGR_PATH_CUM_SPLIT) return launch_cum_split<CT, OP>(p, pr);
+    if (p.path == ARGR_PATH_CUM_STREAM) return launch_cum_stream<CT, OP>(p, pr);
     const size_t smem = cum_smem_bytes(p.block, sizeof(R));
     if (p.cluster <= 1) {
         auto kern1 = cum_kernel<CT, OP, kCumItems, false>;

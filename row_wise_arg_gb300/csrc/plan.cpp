@@ -74,8 +74,9 @@ int elem_size(int dtype) {
 }
 
 size_t plan_scratch(const argr_plan& p, int64_t rows) {
-    if (p.path == ARGR_PATH_CUM_SPLIT) {
-        const int64_t words = rows * p.blocks_per_row * ((p.flags & ARGR_PLAN_LOOKBACK) ? 2 : 1);
+    if (p.path == ARGR_PATH_CUM_SPLIT || p.path == ARGR_PATH_CUM_STREAM) {
+        const int64_t words =
+            rows * p.blocks_per_row * ((p.path == ARGR_PATH_CUM_STREAM || (p.flags & ARGR_PLAN_LOOKBACK)) ? 2 : 1);
         return cum_records_offset(words) + 8 * static_cast<size_t>(words);
     }
     if (p.path == ARGR_PATH_SPLIT && p.blocks_per_row > 1)

@@ -135,6 +135,15 @@ argr_status check_cum_plan(const argr_plan& p, int64_t rows, int64_t cols, int d
         }
         return ARGR_OK;
     }
+    if (p.path == ARGR_PATH_CUM_STREAM) {
+        if (p.flags & ~(ARGR_PLAN_PDL | ARGR_PLAN_TEST_EXPIRE)) return ARGR_EINVAL;
+        // exactly the tiles of a row; two record words per tile in one launch
+        if (p.cluster != 1 || p.blocks_per_row != ceil_div(cols, static_cast<int64_t>(p.block) * kCumItems))
+            return ARGR_EINVAL;
+        if (rows > kCumMaxChunksBig / 2 / p.blocks_per_row) return ARGR_EINVAL;
+        if (p.grid_rows < 1 || p.grid_rows > kMaxGridY) return ARGR_EINVAL;
+        return ARGR_OK;
+    }
     if (p.path != ARGR_PATH_CUM) return ARGR_EINVAL;
     if (p.flags & ~ARGR_PLAN_PDL) return ARGR_EINVAL;
     if (p.cluster < 1 || p.cluster > 16 || p.blocks_per_row != p.cluster) return ARGR_EINVAL;

@@ -53,6 +53,17 @@ def split_plan(chunks, block=256, rows=1, flags=_lib.ARGR_PLAN_PDL):
 
 
 STASH = 8  # ARGR_PLAN_STASH
+
+
+def stream_plan(cols, block=256, rows=1, grid=16, flags=_lib.ARGR_PLAN_PDL):
+    p = _lib.argr_plan()
+    p.path = _lib.ARGR_PATH_CUM_STREAM
+    p.block = block
+    p.cluster = 1
+    p.blocks_per_row = -(-cols // (block * 7))  # tiles per row
+    p.grid_rows = grid  # CTAs
+    p.flags = flags
+    return p
 LOOKBACK = 16  # ARGR_PLAN_LOOKBACK
 
 
@@ -108,6 +119,9 @@ def test_cum_forced_geometries(dtype):
             for chunks, block in ((2, 32), (3, 1024), (7, 64), (64, 256)):
                 if rows * chunks <= 1024:  # chunks > cols leaves some chunks empty
                     check_cum(x, dtype, op, plan=split_plan(chunks, block, rows, flags=chunks % 2))
+            # streaming scan: tiles in ticket order over a fixed grid (1 CTA walks every tile)
+            for block, grid in ((32, 1), (128, 3), (1024, 16), (64, 304)):
+                check_cum(x, dtype, op, plan=stream_plan(cols, block, rows, grid, flags=grid % 2))
             # decoupled look-back (inclusive prefixes), chunks of up to a tile and beyond
             for chunks, block in ((2, 64), (3, 1024), (9, 32), (100, 128)):
                 if rows * chunks * 2 <= 65536:
@@ -375,3 +389,55 @@ def test_cum_lookback_long_rows_and_scratch():
     assert A.argreduce_read_error(sc.ptr, 0) == _lib.ARGR_OK
     assert _lib.argreduce_cum_raw(0x10000, "f32", 2, 300001, "max", 0x10000, 0, sc.ptr, sc.nbytes, 0,
                                   split_plan(8, 128, rows=2, flags=LOOKBACK | STASH)) == _lib.ARGR_EINVAL
+
+
+def test_cum_stream_long_rows_graphs_and_scratch():
+    """The streaming scan on long rows of every width class, from misaligned
+    bases, in CUDA-graph replays (the ticket counter must come back to zero
+    after every launch), through a forced expiry, and on one scratch buffer
+    with argreduce's split path and the split scan."""
+    from gpu_util import forced_plan
+    sc = A.Scratch()
+    for dtype, rows, n, block, grid in (("i64", 1, 1 << 20, 512, 304), ("f64", 2, 3 << 20, 256, 608),
+                                        ("bf16", 1, 1 << 24, 512, 304), ("f32", 7, 300001, 128, 1000),
+                                        ("i32", 3, 1 << 20, 1024, 152)):
+        x = cum_rows(dtype, rows, n, seed=n % 997 + rows)
+        check_cum(x, dtype, "min" if rows % 2 else "max", plan=stream_plan(n, block, rows, grid), scratch=sc,
+                  offset=rows % 3)
+    x = cum_rows("f32", 2, 400001, seed=41)
+    xd = torch.from_numpy(x).cuda()
+    eidx, _ = oracle.cumreduce(x, "f32", "max")
+    xr = W.fuzz_rows("f32", 3, 2_000_000, seed=42)
+    er, _, _ = oracle.argreduce(xr, "f32", "max")
+    xrd = torch.from_numpy(xr).cuda()
+    rplan = forced_plan("split", bpr=12, grid_rows=3)
+    s = torch.cuda.Stream()
+    out_i = torch.empty(2, 400001, dtype=torch.int64, device="cuda")
+    out_r = torch.empty(3, dtype=torch.int64, device="cuda")
+    plan = stream_plan(400001, 256, rows=2, grid=300)
+    with torch.cuda.stream(s):
+        A.argreduce_cum(xd, "max", plan=plan, scratch=sc, out_idx=out_i, with_values=False, stream=s)
+        A.argreduce_with_plan(rplan, xrd, "max", scratch=sc, out_idx=out_r, stream=s)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            A.argreduce_cum(xd, "max", plan=plan, scratch=sc, out_idx=out_i, with_values=False, stream=s)
+            A.argreduce_with_plan(rplan, xrd, "max", scratch=sc, out_idx=out_r, stream=s)
+            A.argreduce_cum(xd, "max", plan=split_plan(40, 128, rows=2), scratch=sc, out_idx=out_i,
+                            with_values=False, stream=s)
+            A.argreduce_cum(xd, "max", plan=plan, scratch=sc, out_idx=out_i, with_values=False, stream=s)
+        for _ in range(5):
+            out_i.zero_()
+            out_r.zero_()
+            g.replay()
+            s.synchronize()
+            assert (out_i.cpu().numpy() == eidx).all() and (out_r.cpu().numpy() == er).all()
+    assert A.argreduce_read_error(sc.ptr, 0) == _lib.ARGR_OK
+    A.argreduce_cum(xd, "max", plan=stream_plan(400001, 256, rows=2, grid=64, flags=4), scratch=sc)
+    assert A.argreduce_read_error(sc.ptr, 0) == _lib.ARGR_ETIMEOUT
+    check_cum(x, "f32", "max", plan=stream_plan(400001, 256, rows=2, grid=64), scratch=sc)
+    assert A.argreduce_read_error(sc.ptr, 0) == _lib.ARGR_OK
+    bad = stream_plan(400001, 256, rows=2, grid=64)
+    bad.blocks_per_row += 1  # not the row's tile count
+    assert _lib.argreduce_cum_raw(xd.data_ptr(), "f32", 2, 400001, "max", out_i.data_ptr(), 0, sc.ptr, sc.nbytes, 0,
+                                  bad) == _lib.ARGR_EINVAL

@@ -560,3 +560,13 @@ def test_cum_lookback_scratch_size():
         assert _lib.argreduce_plan_scratch_bytes(p, rows) == want
         p.flags = _lib.ARGR_PLAN_PDL
         assert _lib.argreduce_plan_scratch_bytes(p, rows) == (256 if rows * chunks <= 1024 else 1 << 20) + 8 * rows * chunks
+
+
+def test_cum_stream_scratch_size():
+    """The streaming scan keeps [aggregate, inclusive prefix] per tile."""
+    for rows, cols, block, want in ((1, 65536, 512, 256 + 16 * 19), (1, 1 << 24, 512, (1 << 20) + 16 * 4682),
+                                    (3, 1 << 20, 1024, 256 + 16 * 3 * 147)):
+        p = _lib.argr_plan()
+        p.path, p.block, p.cluster, p.grid_rows = _lib.ARGR_PATH_CUM_STREAM, block, 1, 304
+        p.blocks_per_row = -(-cols // (block * 7))
+        assert _lib.argreduce_plan_scratch_bytes(p, rows) == want
