@@ -108,5 +108,7 @@ cudaError_t launch_cum_i32(const argr_plan& p, const Problem& pr);
 cudaError_t launch_cum_i64(const argr_plan& p, const Problem& pr);
 argr_status make_cum_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_caps& caps, argr_plan* out);
 argr_status check_cum_plan(const argr_plan& p, int64_t rows, int64_t cols, int dtype, int op, const argr_caps& caps);
+// Scratch bytes of a cummax / cummin plan (records of the split and streaming scans).
+size_t cum_plan_scratch(const argr_plan& p, int64_t rows);
 
 }  // namespace argr

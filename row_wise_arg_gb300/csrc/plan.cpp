@@ -74,11 +74,8 @@ int elem_size(int dtype) {
 }
 
 size_t plan_scratch(const argr_plan& p, int64_t rows) {
-    if (p.path == ARGR_PATH_CUM_SPLIT || p.path == ARGR_PATH_CUM_STREAM) {
-        const int64_t words =
-            rows * p.blocks_per_row * ((p.path == ARGR_PATH_CUM_STREAM || (p.flags & ARGR_PLAN_LOOKBACK)) ? 2 : 1);
-        return cum_records_offset(words) + 8 * static_cast<size_t>(words);
-    }
+    if (p.path == ARGR_PATH_CUM || p.path == ARGR_PATH_CUM_SPLIT || p.path == ARGR_PATH_CUM_STREAM)
+        return cum_plan_scratch(p, rows);
     if (p.path == ARGR_PATH_SPLIT && p.blocks_per_row > 1)
         return kPartialsOffset +
                static_cast<size_t>(p.grid_rows) * static_cast<size_t>(p.blocks_per_row) * kPartialBytes;

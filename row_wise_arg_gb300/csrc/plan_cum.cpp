@@ -112,6 +112,13 @@ argr_status make_cum_plan(int64_t rows, int64_t cols, int dtype, int op, const a
     return ARGR_OK;
 }
 
+size_t cum_plan_scratch(const argr_plan& p, int64_t rows) {
+    if (p.path != ARGR_PATH_CUM_SPLIT && p.path != ARGR_PATH_CUM_STREAM) return 0;
+    const int64_t words =
+        rows * p.blocks_per_row * ((p.path == ARGR_PATH_CUM_STREAM || (p.flags & ARGR_PLAN_LOOKBACK)) ? 2 : 1);
+    return cum_records_offset(words) + 8 * static_cast<size_t>(words);
+}
+
 argr_status check_cum_plan(const argr_plan& p, int64_t rows, int64_t cols, int dtype, int op, const argr_caps& caps) {
     if (elem_size(dtype) == 0 || rows < 0 || cols < 1 || cols > INT_MAX) return ARGR_EINVAL;
     if (op != ARGR_MAX && op != ARGR_MIN) return ARGR_EUNSUPPORTED;
