@@ -77,14 +77,14 @@ typedef enum {
                               `cluster` CTAs (1 = none) splits it further. unroll 4 or 8 */
     ARGR_PATH_CUM = 6,     /* cummax / cummin (argreduce_cum): a row in `cluster` chunks, one CTA
                               each (1 = none), scanned in tiles of block * 7 elements */
+    ARGR_PATH_CUM_SPLIT = 7, /* cummax / cummin: a row in `blocks_per_row` chunks, one CTA each,
+                              any number of CTAs; chunk aggregates are exchanged through
+                              scratch (rows * blocks_per_row <= 65536; above 1024 record
+                              words the records need a scratch buffer of more than 1 MiB) */
     ARGR_PATH_CUM_STREAM = 8, /* cummax / cummin: tiles of block * 7 elements (`blocks_per_row` =
                               tiles per row) taken in ticket order by `grid_rows` CTAs, each
                               tile read once; carries by decoupled look-back through scratch
-                              (rows * blocks_per_row <= 32768) */
-    ARGR_PATH_CUM_SPLIT = 7, /* cummax / cummin: a row in `blocks_per_row` chunks, one CTA each,
-                              any number of CTAs; chunk aggregates are exchanged through
-                              scratch (rows * blocks_per_row <= 65536; above 1024 the
-                              records need a scratch buffer of more than 1 MiB) */
+                              (rows * blocks_per_row <= 32768). Not chosen by the planner */
     ARGR_PATH_STREAM = 4   /* every warp streams a contiguous range of rows through its own
                               `stages` shared-memory buffers of `stage_bytes`, filled by bulk
                               (TMA) copies; `group` lanes per row for rows that fit a buffer,
@@ -107,13 +107,14 @@ typedef struct {
  * memory by bulk (TMA) copies issued all at once, instead of by loads from
  * every thread. The share must be at most 128 KiB. */
 #define ARGR_PLAN_BULK 2
-/* Plan flag for tests of failure handling (STREAM and CUM_SPLIT paths only).
- * STREAM: one bulk copy's barrier is made to expect more bytes than arrive, so
- * the kernel's bounded wait (2 ms under this flag) expires; the kernel records
- * the expiry, skips its work and returns. CUM_SPLIT: chunk 0 of each row never
- * publishes its record, so every wait for it expires after 2 ms. Either way
- * argreduce_read_error() then reports ARGR_ETIMEOUT and outputs are
- * undefined. Never set in the planner's plans. */
+/* Plan flag for tests of failure handling (STREAM, CUM_SPLIT and CUM_STREAM
+ * paths only). STREAM: one bulk copy's barrier is made to expect more bytes
+ * than arrive, so the kernel's bounded wait (2 ms under this flag) expires;
+ * the kernel records the expiry, skips its work and returns. CUM_SPLIT and
+ * CUM_STREAM: the first chunk (tile) of each row never publishes its record,
+ * so every wait for it expires after 2 ms. Either way argreduce_read_error()
+ * then reports ARGR_ETIMEOUT and outputs are undefined. Never set in the
+ * planner's plans. */
 #define ARGR_PLAN_TEST_EXPIRE 4
 /* Plan flag (CUM_SPLIT path): each CTA copies its whole chunk (at most 80 KiB)
  * into shared memory with bulk (TMA) copies and scans it there, so the input
@@ -141,9 +142,10 @@ typedef struct {
     int32_t stages;         /* STREAM: buffers per warp, 1..4 */
     int32_t stage_bytes;    /* STREAM: bytes per buffer, multiple of 16, 1 KiB..64 KiB */
     int32_t reserved;       /* 0 */
-    int64_t blocks_per_row; /* SPLIT / CLUSTER: CTAs that share one row */
-    int64_t grid_rows;      /* SPLIT / CLUSTER: row slots in the grid (rows loop over them);
-                               ROWS / STREAM: number of CTAs */
+    int64_t blocks_per_row; /* SPLIT / CLUSTER / CUM: CTAs that share one row; CUM_SPLIT: chunks
+                               per row; CUM_STREAM: tiles per row */
+    int64_t grid_rows;      /* SPLIT / CLUSTER / CUM: row slots in the grid (rows loop over them;
+                               CUM_SPLIT: the rows); ROWS / STREAM / CUM_STREAM: number of CTAs */
     uint64_t scratch_bytes; /* bytes of scratch this plan needs (0 = none) */
 } argr_plan;
 
@@ -270,8 +272,8 @@ size_t argreduce_cum_scratch_bytes(int64_t rows, int64_t cols, argr_dtype dtype,
 argr_status argreduce_cum_plan(int64_t rows, int64_t cols, argr_dtype dtype, argr_op op, const argr_caps* caps,
                                argr_plan* out);
 
-/* argreduce_cum() with an explicit ARGR_PATH_CUM or ARGR_PATH_CUM_SPLIT plan
- * (re-validated). */
+/* argreduce_cum() with an explicit ARGR_PATH_CUM, ARGR_PATH_CUM_SPLIT or
+ * ARGR_PATH_CUM_STREAM plan (re-validated). */
 argr_status argreduce_cum_with_plan(const argr_plan* plan, const void* x, argr_dtype dtype, int64_t rows,
                                     int64_t cols, argr_op op, int64_t* out_idx, void* out_val, void* scratch,
                                     size_t scratch_bytes, argr_stream stream);
@@ -283,9 +285,10 @@ size_t argreduce_plan_scratch_bytes(const argr_plan* plan, int64_t rows);
  * Synchronise `stream` and read the library's device error words (set by a
  * kernel whose bounded wait expired: for a bulk copy, after which the kernel
  * skips the rest of its work, or for another CTA's chunk record in the split
- * scan) and the one in `scratch` (may be NULL). Returns ARGR_ESCRATCH if a
- * split scan found counters or records its launch did not write (a scratch
- * buffer that argreduce_scratch_init() never prepared), else ARGR_ETIMEOUT if
+ * or streaming scan) and the one in `scratch` (may be NULL). Returns
+ * ARGR_ESCRATCH if a split or streaming scan found counters or records its
+ * launch did not write (a scratch buffer that argreduce_scratch_init() never
+ * prepared), else ARGR_ETIMEOUT if
  * any word was set, ARGR_OK otherwise (the words are cleared), and ARGR_ECUDA
  * if the stream reports a fault. For tests and benchmarks; it blocks the host.
  */
