@@ -128,6 +128,11 @@ typedef struct {
  * back only to the nearest one, so chunks can be one tile each (read once,
  * from registers) at any chunk count; two record words per chunk. */
 #define ARGR_PLAN_LOOKBACK 16
+/* Plan flag (ROWS path with vec = 1 and group 16 or 32): software-pipelined
+ * loads. Every lane issues the next batch of `unroll` 16-byte loads before it
+ * compares the current batch, so its loads stay in flight while it compares;
+ * twice the registers for loaded data, so at most 256 threads per CTA. */
+#define ARGR_PLAN_PIPELINE 32
 
 /* A launch plan. Produced by argreduce_plan(); tests may edit it to force a
  * path and pass it to argreduce_with_plan(), which re-validates it. */

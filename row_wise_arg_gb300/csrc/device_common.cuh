@@ -51,6 +51,9 @@ template <int OP> constexpr bool kIsLast = (OP & 2) != 0;
 // worse than, so it never wins; a NaN candidate (only ever x[0]) gets the
 // all-ones key, so nothing displaces it. Neither sentinel is the key of a
 // number, so "strictly better" decides exactly as the IEEE comparison does.
+// The row scans skip the NaN test: order_key() of a NaN lies outside the keys of
+// numbers, above kLimit (the key of the best infinity) or below every key of
+// a number, so one comparison with kLimit excludes it.
 // ---------------------------------------------------------------------------
 struct TagF32 {
     using raw = float;
@@ -90,18 +93,25 @@ struct TagF64 {
     using key = unsigned long long;
     static constexpr unsigned long long kSign = 0x8000000000000000ull;
     static constexpr unsigned long long kInfBits = 0x7FF0000000000000ull;
-    // Monotone key of a non-NaN value (larger key = better for OP).
-    template <int OP> static __device__ __forceinline__ unsigned long long ordered(unsigned long long b) {
-        const unsigned long long mag = b & ~kSign;
-        unsigned long long u = mag == 0 ? kSign : ((b & kSign) ? ~b : (b | kSign));
-        if constexpr (kIsMin<OP>) u = ~u;
-        return u;
+    // Key of a value (larger key = better for OP), monotone on the numbers.
+    // ArgMax: a negative value maps to its two's complement negation -b,
+    // which gives -0.0 the key kSign of +0.0, a positive one to b with the
+    // sign bit set. ArgMin uses the ArgMax key of the negated value (sign bit
+    // flipped). The keys of numbers lie in [0x0010000000000000, kLimit];
+    // NaNs whose sign bit (after the flip) is clear map above that range,
+    // the others below it.
+    template <int OP> static __device__ __forceinline__ unsigned long long order_key(unsigned long long b) {
+        if constexpr (kIsMin<OP>) b ^= kSign;
+        const unsigned long long s = static_cast<unsigned long long>(static_cast<long long>(b) >> 63);
+        return ((b ^ s) - s) ^ (~s & kSign);
     }
+    // The key of the best infinity (+inf for ArgMax, -inf for ArgMin).
+    static constexpr unsigned long long kLimit = 0xFFF0000000000000ull;
     template <int OP> static __device__ __forceinline__ unsigned long long elem_key(unsigned long long b) {
-        return (b & ~kSign) > kInfBits ? 0ull : ordered<OP>(b);
+        return (b & ~kSign) > kInfBits ? 0ull : order_key<OP>(b);
     }
     template <int OP> static __device__ __forceinline__ unsigned long long seed_key(unsigned long long b) {
-        return (b & ~kSign) > kInfBits ? ~0ull : ordered<OP>(b);
+        return (b & ~kSign) > kInfBits ? ~0ull : order_key<OP>(b);
     }
     template <int OP> static __device__ __forceinline__ bool better(unsigned long long a, unsigned long long b) {
         return a > b;
@@ -127,28 +137,23 @@ __device__ __forceinline__ Cand<Tag> make_cand(typename Tag::raw v, int i) {
 template <class Tag, int OP>
 __device__ __forceinline__ void visit(Cand<Tag>& c, typename Tag::raw x, int j) {
     if constexpr (sizeof(typename Tag::raw) == 8) {
-        // binary64: a 32-bit pre-test on the high word first. f(x) equals the
-        // high half of x's key, except for -0.0 under ArgMax, where it is one
-        // below (the key of -0.0 is that of +0.0), and it is at least that
-        // high half for NaNs. An element with f(x) + 1 < high half of the
-        // candidate's key can be neither better nor equal and is skipped with
-        // a few integer operations; the full 64-bit key is only formed for the
-        // rare elements that pass.
-        const unsigned hi = static_cast<unsigned>(x >> 32);
-        unsigned f = hi ^ (static_cast<unsigned>(static_cast<int>(hi) >> 31) | 0x80000000u);
-        if constexpr (kIsMin<OP>) f = ~f;
-        const unsigned kh = static_cast<unsigned>(c.k >> 32);
-        if (f >= kh || f + 1u == kh) {
-            const typename Tag::key k = Tag::template elem_key<OP>(x);
-            if (Tag::template better<OP>(k, c.k) || (kIsLast<OP> && k == c.k)) {
-                c.v = x;
-                c.k = k;
-                c.i = j;
-            }
+        // binary64: order_key() without the NaN test. A NaN whose key lies above
+        // kLimit is excluded by the first comparison; one whose key lies
+        // below every key of a number is never better than the candidate nor
+        // equal to it (the candidate is a number or the all-ones NaN seed).
+        const typename Tag::key k = Tag::template order_key<OP>(x);
+        if (k <= Tag::kLimit && (kIsLast<OP> ? k >= c.k : k > c.k)) {
+            c.v = x;
+            c.k = k;
+            c.i = j;
         }
     } else {
+        // "better or equal" is one IEEE comparison (>= / <=, false on NaN).
         const typename Tag::key k = Tag::template elem_key<OP>(x);
-        if (Tag::template better<OP>(k, c.k) || (kIsLast<OP> && k == c.k)) {
+        bool take;
+        if constexpr (kIsLast<OP>) take = kIsMin<OP> ? k <= c.k : k >= c.k;
+        else take = Tag::template better<OP>(k, c.k);
+        if (take) {
             c.v = x;
             c.k = k;
             c.i = j;

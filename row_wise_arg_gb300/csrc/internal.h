@@ -47,6 +47,7 @@ constexpr size_t kCumBigRecordsOffset = size_t(1) << 20;
 constexpr int64_t kCumMaxChunksBig = 65536;           // rows * chunks of a split scan, large region
 constexpr int64_t kMaxPartials = (kCumBigRecordsOffset - kPartialsOffset) / kPartialBytes;
 constexpr int64_t kCumStashBytes = 80 * 1024;         // a stashed split-scan chunk, at most
+constexpr int kPipeMaxBlock = 256;  // threads per CTA of the pipelined rows kernel (its registers)
 ARGR_HD inline size_t cum_records_offset(int64_t total_chunks) {
     return total_chunks <= kCumMaxChunks ? kCounterOffset : kCumBigRecordsOffset;
 }

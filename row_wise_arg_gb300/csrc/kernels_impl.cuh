@@ -39,8 +39,8 @@ namespace argr {
 // ---------------------------------------------------------------------------
 // G lanes per row.
 // ---------------------------------------------------------------------------
-template <class Tag, int OP, int G, bool VEC, int U>
-__global__ void __launch_bounds__(1024)
+template <class Tag, int OP, int G, bool VEC, int U, bool PIPE>
+__global__ void __launch_bounds__(PIPE ? kPipeMaxBlock : 1024)
 rows_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int64_t* __restrict__ out_idx,
             typename Tag::raw* __restrict__ out_val) {
     using R = typename Tag::raw;
@@ -68,18 +68,44 @@ rows_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int
             for (int u = 0; u < U; ++u) buf[u] = (u * G < rem) ? ld_stream16(rv + v0 + u * G) : make_uint4(0, 0, 0, 0);
             // Lane 0 of the group always holds vector 0, whose first element is x[0].
             c = make_cand<Tag, OP>(shfl_raw(gmask, vec_elem<R>(buf[0], 0), 0, G), 0);
+            if constexpr (PIPE) {
+                // Software pipeline: the next batch's loads are issued before
+                // the current batch is scanned, so a lane always has loads in
+                // flight while it compares.
+                for (;;) {
+                    const bool more = rem > G * U;
+                    uint4 nxt[U];
+                    int v1 = v0, rem1 = 0;
+                    if (more) {
+                        v1 = v0 + G * U;
+                        rem1 = nvec - v1;
 #pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (u * G < rem) visit_vec<Tag, OP>(c, buf[u], (v0 + u * G) * E);
-            while (rem > G * U) {
-                v0 += G * U;
-                rem = nvec - v0;
+                        for (int u = 0; u < U; ++u)
+                            nxt[u] = (u * G < rem1) ? ld_stream16(rv + v1 + u * G) : make_uint4(0, 0, 0, 0);
+                    }
+                    #pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        if (u * G < rem) visit_vec<Tag, OP>(c, buf[u], (v0 + u * G) * E);
+                    if (!more) break;
+                    v0 = v1;
+                    rem = rem1;
 #pragma unroll
-                for (int u = 0; u < U; ++u)
-                    if (u * G < rem) buf[u] = ld_stream16(rv + v0 + u * G);
+                    for (int u = 0; u < U; ++u) buf[u] = nxt[u];
+                }
+            } else {
+                #pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        if (u * G < rem) visit_vec<Tag, OP>(c, buf[u], (v0 + u * G) * E);
+                while (rem > G * U) {
+                    v0 += G * U;
+                    rem = nvec - v0;
 #pragma unroll
-                for (int u = 0; u < U; ++u)
-                    if (u * G < rem) visit_vec<Tag, OP>(c, buf[u], (v0 + u * G) * E);
+                    for (int u = 0; u < U; ++u)
+                        if (u * G < rem) buf[u] = ld_stream16(rv + v0 + u * G);
+                    #pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        if (u * G < rem) visit_vec<Tag, OP>(c, buf[u], (v0 + u * G) * E);
+                }
             }
         } else {
             int j0 = lg;
@@ -914,11 +940,16 @@ cudaError_t launch_rows_gu(const argr_plan& p, const Problem& pr) {
     const dim3 grid(static_cast<unsigned>(p.grid_rows));
     const R* x = static_cast<const R*>(pr.x);
     R* ov = static_cast<R*>(pr.out_val);
+    if constexpr (G >= 16) {
+        if (p.flags & ARGR_PLAN_PIPELINE)  // check_plan admits it only with vec and G >= 16
+            return launch_ex(rows_kernel<Tag, OP, G, true, U, true>, grid, dim3(p.block), 1, p, pr.stream, x,
+                             pr.rows, pr.cols, pr.out_idx, ov);
+    }
     if (p.vec)
-        return launch_ex(rows_kernel<Tag, OP, G, true, U>, grid, dim3(p.block), 1, p, pr.stream, x, pr.rows, pr.cols,
-                         pr.out_idx, ov);
-    return launch_ex(rows_kernel<Tag, OP, G, false, U>, grid, dim3(p.block), 1, p, pr.stream, x, pr.rows, pr.cols,
-                     pr.out_idx, ov);
+        return launch_ex(rows_kernel<Tag, OP, G, true, U, false>, grid, dim3(p.block), 1, p, pr.stream, x, pr.rows,
+                         pr.cols, pr.out_idx, ov);
+    return launch_ex(rows_kernel<Tag, OP, G, false, U, false>, grid, dim3(p.block), 1, p, pr.stream, x, pr.rows,
+                     pr.cols, pr.out_idx, ov);
 }
 
 template <class Tag, int OP, int G>

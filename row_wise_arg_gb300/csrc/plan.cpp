@@ -15,7 +15,8 @@
 //  * otherwise (very wide rows) a row is split over several CTAs of the whole
 //    device, about one wave in total (more CTAs than one wave was measured
 //    slower on the pages' H200, and the merge cost grows with the CTA count),
-//    while every thread keeps at least kMinBytesPerThread of the row.
+//    while every CTA keeps at least kMinSplitShare of the row; rows too short
+//    for that get one CTA (or, 16-32 KB rows of many elements, one warp).
 // Every default plan launches as a programmatic dependent of the previous grid
 // in the stream, which hides launch latency between back-to-back calls.
 #include <algorithm>
@@ -34,12 +35,13 @@ constexpr int kManyRowsUnroll = 8;         // 16-byte loads in flight per lane o
 constexpr int kBlock = 256;                // threads per CTA on every path
 constexpr int kRowsUnroll = 4;             // loads in flight per lane on the rows path
 constexpr int kSplitUnroll = 4;            // vector loads in flight per thread on the split path
-constexpr int64_t kMinBytesPerThread = 16; // one 16-byte vector per thread at least
 constexpr int64_t kRowsWaves = 8;          // rows path: grid of at most this many waves (grid-stride beyond)
 constexpr int64_t kMaxGridY = 65535;       // hardware limit of gridDim.y
 constexpr int64_t kMaxBlocksPerRow = 65535;
 constexpr int64_t kClusterMaxCtaBytes = 128 * 1024;  // largest share of a row per cluster CTA
 constexpr int64_t kMaxDynamicSmem = 227 * 1024;        // dynamic shared memory one CTA may use
+constexpr int64_t kPipeDeepWarpsPerSm = 16;  // resident warps of the 8-deep pipelined rows kernel (registers)
+constexpr int64_t kMinSplitShare = 32768;    // a row is shared by several CTAs only in pieces of this size
 
 int64_t ceil_div(int64_t a, int64_t b) { return a / b + (a % b != 0); }
 
@@ -122,15 +124,28 @@ argr_status make_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_
         // Enough rows: no row is split.
         if (row_bytes <= kWarpRowBytes) {
             // Measured on GB300: 128-thread CTAs with 8 loads in flight per
-            // lane, a whole warp for rows of 16 KB and more, half a warp below.
-            const int g = row_bytes >= 16384 ? 32 : 16;
+            // lane, a whole warp for rows of 16 KB and more (4 KB for
+            // 2- and 4-byte elements: [65536,1024] f32 38.4 -> 37.9 us,
+            // [8192,4096] f16 13.2 -> 12.2 us), half a warp below.
+            const int g = (row_bytes >= 16384 || (es <= 4 && row_bytes >= 4096)) ? 32 : 16;
             out->path = ARGR_PATH_ROWS;
             out->group = g;
-            // 32 KB binary64 rows: 256-thread CTAs
-            // measured 10% faster ([4096,4096] f64 30.4 -> 27.6 us).
-            out->block = (es == 8 && row_bytes >= kWarpRowBytes) ? 2 * kManyRowsBlock : kManyRowsBlock;
+            // 256-thread CTAs for 32 KB binary64 rows ([4096,4096] f64 30.4 ->
+            // 27.6 us) and 16-bit rows of 16 KB and more ([4096,8192] bf16
+            // 13.7 -> 13.0 us).
+            const bool wide_ctas = (es == 8 && row_bytes >= kWarpRowBytes) || (es == 2 && row_bytes >= 16384);
+            out->block = wide_ctas ? 2 * kManyRowsBlock : kManyRowsBlock;
             out->vec = aligned ? 1 : 0;
             out->unroll = kManyRowsUnroll;
+            // Long rows (16 KB of binary32, 32 KB of binary64): software-
+            // pipelined loads, 8 deep while the rows fit the warps that kernel
+            // keeps resident, else 4 deep ([4096,4096] f32 11.9 -> 11.5 us,
+            // f64 24.3 -> 23.9 us; [2048,8192] f32 13.2 -> 12.7 us).
+            const bool pipe_rows = (es == 4 && row_bytes >= 16384) || (es == 8 && row_bytes >= kWarpRowBytes);
+            if (aligned && pipe_rows) {
+                out->flags |= ARGR_PLAN_PIPELINE;
+                out->unroll = rows <= kPipeDeepWarpsPerSm * caps.sm_count ? 8 : 4;
+            }
             out->grid_rows = std::min(ceil_div(rows, out->block / g), kRowsWaves * ctas_per_wave(caps, out->block));
             out->blocks_per_row = 1;
         } else {
@@ -167,17 +182,38 @@ argr_status make_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_
         }
     }
 
-    // Very wide rows: split each row over CTAs, about one wave in total.
+    // Very wide rows: split each row over CTAs, about one wave in total, each
+    // CTA with at least kMinSplitShare of the row: below that the merge of
+    // the partials costs more than the extra CTAs gain ([256,8192] f32 over
+    // 4 CTAs 6.6 us, one CTA per row 4.0 us).
     const int64_t by_wave = std::max<int64_t>(1, wave / rows);
-    const int64_t by_work = std::max<int64_t>(1, row_bytes / (kBlock * kMinBytesPerThread));
+    const int64_t by_work = std::max<int64_t>(1, row_bytes / kMinSplitShare);
     const int64_t bpr = std::min({by_wave, by_work, kMaxBlocksPerRow});
     out->path = ARGR_PATH_SPLIT;
     out->unroll = kSplitUnroll;
     out->blocks_per_row = bpr;
     out->grid_rows = rows;  // rows < one wave <= kMaxGridY here
     if (bpr == 1) {
-        // One CTA per row, as on the many-rows path: small CTAs, 8 loads in flight.
-        out->block = kManyRowsBlock;
+        const int64_t sms = caps.sm_count;
+        if (aligned && rows > 4 * sms && cols <= 4096 && es >= 4 && row_bytes >= 16384) {
+            // Rows of 16-32 KB with at most 4096 elements: a warp per row with
+            // 8-deep pipelined loads ([1024,4096] f64 10.0 -> 8.9 us,
+            // [1200,4096] f32 5.5 -> 5.2 us).
+            out->path = ARGR_PATH_ROWS;
+            out->group = 32;
+            out->vec = 1;
+            out->block = kManyRowsBlock;
+            out->unroll = 8;
+            out->flags |= ARGR_PLAN_PIPELINE;
+            out->grid_rows = ceil_div(rows, kManyRowsBlock / 32);
+            out->blocks_per_row = 1;
+            out->scratch_bytes = 0;
+            return ARGR_OK;
+        }
+        // One CTA per row with 8 loads in flight per thread: 256 threads while
+        // there are few rows per SM ([512,8192] f32 5.8 -> 5.4 us), else 128
+        // as on the many-rows path.
+        out->block = rows <= 4 * sms ? kBlock : kManyRowsBlock;
         out->unroll = kManyRowsUnroll;
         out->grid_rows = std::min(rows, kMaxGridY);
     }
@@ -282,8 +318,11 @@ argr_status check_plan(const argr_plan& p, int64_t rows, int64_t cols, int dtype
     if (!valid_dtype(dtype) || rows < 0 || cols < 1 || cols > INT_MAX) return ARGR_EINVAL;
     if (rows == 0) return ARGR_OK;
     if (p.block < 32 || p.block > 1024 || p.block % 32 != 0) return ARGR_EINVAL;
-    if (p.flags & ~(ARGR_PLAN_PDL | ARGR_PLAN_BULK | ARGR_PLAN_TEST_EXPIRE)) return ARGR_EINVAL;
+    if (p.flags & ~(ARGR_PLAN_PDL | ARGR_PLAN_BULK | ARGR_PLAN_TEST_EXPIRE | ARGR_PLAN_PIPELINE)) return ARGR_EINVAL;
     if ((p.flags & ARGR_PLAN_BULK) && p.path != ARGR_PATH_CLUSTER) return ARGR_EINVAL;
+    if ((p.flags & ARGR_PLAN_PIPELINE) &&
+        (p.path != ARGR_PATH_ROWS || p.vec != 1 || p.group < 16 || p.block > kPipeMaxBlock))
+        return ARGR_EINVAL;
     if ((p.flags & ARGR_PLAN_TEST_EXPIRE) && p.path != ARGR_PATH_STREAM) return ARGR_EINVAL;
     switch (p.path) {
         case ARGR_PATH_ROWS: {

@@ -81,6 +81,8 @@ def forced_plan(path: str, **kw):
         p.unroll = kw.get("unroll", 4)
         p.grid_rows = kw.get("grid", 64)
         p.blocks_per_row = 1
+        if kw.get("pipeline"):
+            p.flags |= _lib.ARGR_PLAN_PIPELINE
     elif path == "split":
         p.path = _lib.ARGR_PATH_SPLIT
         p.blocks_per_row = kw["bpr"]

@@ -103,8 +103,13 @@ def test_forced_plan_validation():
         forced_plan("split", bpr=2, grid_rows=4, unroll=3),
         forced_plan("cluster", cluster=17, grid_rows=4),
         forced_plan("cluster", cluster=1, grid_rows=4),
+        forced_plan("rows", group=8, vec=1, pipeline=True),             # pipelined: 16 or 32 lanes per row
+        forced_plan("rows", group=32, vec=0, pipeline=True),            # pipelined: vector loads only
+        forced_plan("rows", group=32, vec=1, block=512, pipeline=True),  # pipelined: at most 256 threads
+        forced_plan("split", bpr=1, grid_rows=4),                       # pipelined: rows path only (set below)
     ]
     bad[1].unroll = 5
+    bad[-1].flags |= _lib.ARGR_PLAN_PIPELINE
     for p in bad:
         with pytest.raises(A.ArgreduceError) as e:
             A.argreduce_with_plan(p, x, "max")

@@ -51,8 +51,10 @@ def test_fuzz_argreduce():
         if kind == "planner":
             plan = None
         elif kind == "rows":
-            plan = forced_plan("rows", group=int(rng.choice([1, 2, 4, 8, 16, 32])), vec=int(rng.integers(2)),
-                               block=block, unroll=int(rng.choice([4, 8])), grid=int(rng.integers(1, 200)))
+            group, vec = int(rng.choice([1, 2, 4, 8, 16, 32])), int(rng.integers(2))
+            plan = forced_plan("rows", group=group, vec=vec, block=block, unroll=int(rng.choice([4, 8])),
+                               grid=int(rng.integers(1, 200)),
+                               pipeline=group >= 16 and vec == 1 and block <= 256 and it % 2 == 0)
         elif kind == "split":
             bpr = int(rng.choice([1, 2, 3, 8, 40]))
             plan = forced_plan("split", bpr=bpr, grid_rows=rows if bpr > 1 else int(rng.integers(1, rows + 1)),

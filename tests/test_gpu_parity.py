@@ -82,6 +82,11 @@ def test_rows_path(dtype, group):
             if (cols * es) % 16 == 0:
                 check(x, dtype, op, plan=forced_plan("rows", group=group, vec=1, grid=5))
                 check(x, dtype, op, plan=forced_plan("rows", group=group, vec=1, grid=7, unroll=8, pdl=False))
+                if group >= 16:  # software-pipelined loads
+                    check(x, dtype, op, plan=forced_plan("rows", group=group, vec=1, grid=5, block=64,
+                                                         pipeline=True))
+                    check(x, dtype, op, plan=forced_plan("rows", group=group, vec=1, grid=2, unroll=8,
+                                                         pipeline=True, pdl=False))
 
 
 @pytest.mark.parametrize("dtype", W.DTYPES)

@@ -77,7 +77,7 @@ H200_LIKE = A.make_caps(132)
 TINY = A.make_caps(2, 2048)
 
 CONFIG_SHAPES = [(1, 32000), (1, 202048), (1, 262144), (8, 202048), (32, 202048), (4096, 4096),
-                 (65536, 1024), (65536, 64), (4096, 8), (4096, 128)]
+                 (65536, 1024), (65536, 64), (4096, 8), (4096, 128), (2048, 8192), (8192, 2048)]
 
 
 @pytest.mark.parametrize("caps", [GB300, H200_LIKE, TINY], ids=["152sm", "132sm", "2sm"])
@@ -89,6 +89,8 @@ def test_plan_geometry(caps, dtype):
         p = A.argreduce_plan(rows, cols, dtype, "max", caps)
         d = p.as_dict()
         assert d["block"] % 32 == 0 and 32 <= d["block"] <= 1024
+        if d["flags"] & _lib.ARGR_PLAN_PIPELINE:  # what check_plan admits for pipelined loads
+            assert d["path_name"] == "rows" and d["vec"] == 1 and d["group"] >= 16 and d["block"] <= 256
         if d["path_name"] == "rows":
             assert d["group"] in (1, 2, 4, 8, 16, 32)
             if d["vec"]:
@@ -128,6 +130,39 @@ def test_plan_paths_for_configs():
     for cols in (8, 64, 128):
         d = path(65536 if cols == 64 else 4096, cols)
         assert d["path_name"] == "rows" and d["vec"] == 1 and d["group"] <= 8
+    # medium rows: warp per row from 4 KB of binary32; pipelined loads from
+    # 16 KB (binary32) / 32 KB (binary64) rows, 8 deep while the rows fit
+    # 16 warps per SM, else 4 deep
+    pipe = _lib.ARGR_PLAN_PIPELINE
+    d = path(65536, 1024)
+    assert d["group"] == 32 and not d["flags"] & pipe and d["unroll"] == 8
+    d = path(65536, 1024, "f64")
+    assert d["group"] == 16 and not d["flags"] & pipe
+    d = path(4096, 4096)
+    assert d["group"] == 32 and d["flags"] & pipe and d["unroll"] == 4 and d["block"] == 128
+    d = path(2048, 8192)
+    assert d["group"] == 32 and d["flags"] & pipe and d["unroll"] == 8
+    d = path(4096, 4096, "f64")
+    assert d["group"] == 32 and d["flags"] & pipe and d["unroll"] == 4 and d["block"] == 256
+    d = path(8192, 2048, "f64")
+    assert d["group"] == 32 and not d["flags"] & pipe
+    assert not path(4096, 4095)["flags"] & pipe  # rows not 16-byte aligned: no vector loads
+    # 16-bit rows: a warp from 4 KB, 256-thread CTAs from 16 KB, no pipelining
+    d = path(8192, 4096, "f16")
+    assert d["group"] == 32 and d["block"] == 128 and not d["flags"] & pipe
+    d = path(4096, 8192, "bf16")
+    assert d["group"] == 32 and d["block"] == 256 and not d["flags"] & pipe
+    # rows below one wave: a row is shared by CTAs only in pieces of 32 KB or more
+    for rows, cols, dt in ((256, 8192, "f32"), (512, 4096, "f64")):
+        d = path(rows, cols, dt)
+        assert d["path_name"] == "split" and d["blocks_per_row"] == 1 and d["block"] == 256, d
+    d = path(1024, 8192)
+    assert d["path_name"] == "split" and d["blocks_per_row"] == 1 and d["block"] == 128
+    d = path(1024, 4096, "f64")  # 32 KB rows of 4096 elements: pipelined warp per row
+    assert d["path_name"] == "rows" and d["group"] == 32 and d["flags"] & pipe and d["unroll"] == 8
+    assert path(1024, 4095, "f64")["path_name"] == "split"  # not aligned
+    d = path(256, 202048)
+    assert d["path_name"] == "split" and d["blocks_per_row"] == 4
 
 
 def test_split_rows_capped():
@@ -251,6 +286,42 @@ def sim_rows_lane(cols, es, vec, G, U, lg):
     return out
 
 
+def sim_rows_pipe_lane(nvec, G, U, lg):
+    """Vectors one lane of the pipelined rows loop loads and visits (same
+    arithmetic as rows_kernel with PIPE): returns (loaded, visited) in order."""
+    v0 = lg
+    rem = i32(nvec - v0)
+    loaded = [i32(v0 + u * G) for u in range(U) if i32(u * G) < rem]
+    visited = []
+    while True:
+        more = rem > i32(G * U)
+        if more:
+            v1 = i32(v0 + G * U)
+            rem1 = i32(nvec - v1)
+            loaded.extend(i32(v1 + u * G) for u in range(U) if i32(u * G) < rem1)
+        visited.extend(i32(v0 + u * G) for u in range(U) if i32(u * G) < rem)
+        if not more:
+            break
+        v0, rem = v1, rem1
+    return loaded, visited
+
+
+def test_rows_pipeline_partition_exact():
+    for G in (16, 32):
+        for U in (4, 8):
+            for nvec in range(1, 600):
+                seen = []
+                for lg in range(G):
+                    loaded, visited = sim_rows_pipe_lane(nvec, G, U, lg)
+                    assert loaded == visited and visited == sorted(visited)
+                    assert all(0 <= v < nvec for v in loaded)
+                    seen.extend(visited)
+                assert sorted(seen) == list(range(nvec))
+    # v1 = v0 + G*U is formed only while it stays below nvec = cols / E, and a
+    # 16-byte vector holds E >= 2 elements, so nvec <= INT32_MAX / 2: no overflow.
+    assert (2**31 - 1) // 2 + 32 * 8 < 2**31
+
+
 def test_rows_partition_exact():
     for es in (2, 4, 8):
         for G in (1, 2, 4, 8, 16, 32):
@@ -314,31 +385,34 @@ def f64_bits(v):
     return struct.unpack("<Q", struct.pack("<d", v))[0]
 
 
-def ordered(b, is_min):
-    mag = b & ~SIGN & M64
-    u = SIGN if mag == 0 else ((~b & M64) if b & SIGN else (b | SIGN))
-    return (~u & M64) if is_min else u
+def key64(b, is_min):
+    """TagF64::order_key(): negative values to -b (two's complement), positive
+    ones to b with the sign bit set; ArgMin takes the key of the negated value."""
+    if is_min:
+        b ^= SIGN
+    s = M64 if b & SIGN else 0
+    return (((b ^ s) - s) & M64) ^ (~s & SIGN)
+
+
+def limit64(is_min):
+    return 0xFFF0000000000000
 
 
 def elem_key(b, is_min):
-    return 0 if (b & ~SIGN & M64) > INF_BITS else ordered(b, is_min)
+    return 0 if (b & ~SIGN & M64) > INF_BITS else key64(b, is_min)
 
 
 def seed_key(b, is_min):
-    return M64 if (b & ~SIGN & M64) > INF_BITS else ordered(b, is_min)
+    return M64 if (b & ~SIGN & M64) > INF_BITS else key64(b, is_min)
 
 
-def prefilter(b, cand_key, is_min):
-    hi = b >> 32
-    s = 0xFFFFFFFF if hi & 0x80000000 else 0
-    f = hi ^ (s | 0x80000000)
-    if is_min:
-        f = ~f & 0xFFFFFFFF
-    kh = cand_key >> 32
-    return f >= kh or ((f + 1) & 0xFFFFFFFF) == kh
+def row_scan_takes(b, cand_key, is_min, last):
+    """The row scans' f64 update test (no NaN test, one limit comparison)."""
+    k = key64(b, is_min)
+    return k <= limit64(is_min) and (k > cand_key or (last and k == cand_key))
 
 
-def test_f64_keys_and_prefilter():
+def test_f64_keys_and_row_scan_test():
     import math
     import random
     specials = [0.0, -0.0, 5e-324, -5e-324, 2.2250738585072014e-308, -2.2250738585072014e-308, 1.0, -1.0,
@@ -359,8 +433,18 @@ def test_f64_keys_and_prefilter():
                 ka, kb = elem_key(a, is_min), seed_key(b, is_min)
                 assert (ka > kb) == better, (hex(a), hex(b), is_min)
                 assert (ka == kb) == equal, (hex(a), hex(b), is_min)
-                if better or equal:  # the pre-test must let every such element through
-                    assert prefilter(a, kb, is_min), (hex(a), hex(b), is_min)
+                assert row_scan_takes(a, kb, is_min, False) == better, (hex(a), hex(b), is_min)
+                assert row_scan_takes(a, kb, is_min, True) == (better or equal), (hex(a), hex(b), is_min)
+    # the key range of the numbers and where the NaNs fall
+    for is_min in (False, True):
+        lo_key, hi_key = key64(f64_bits(-math.inf), is_min), key64(f64_bits(math.inf), is_min)
+        if is_min:
+            lo_key, hi_key = hi_key, lo_key
+        assert hi_key == limit64(is_min) and lo_key >= 1
+        for nan in (0x7FF0000000000001, 0x7FF8000000000000, 0x7FFFFFFFFFFFFFFF, 0xFFF0000000000001,
+                    0xFFF8000000000000, 0xFFFFFFFFFFFFFFFF):
+            k = key64(nan, is_min)
+            assert k > hi_key or k < lo_key, (hex(nan), is_min)
 
 
 def test_axis_plans():
