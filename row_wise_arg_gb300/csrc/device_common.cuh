@@ -25,6 +25,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace argr {
 
 // Ops: ArgMax and ArgMin, first occurrence (0, 1) and last occurrence (2, 3:
@@ -277,6 +279,89 @@ __device__ __forceinline__ void visit_vec(Cand<Tag>& c, const uint4& v, int j0) 
     constexpr int E = 16 / sizeof(R);
 #pragma unroll
     for (int k = 0; k < E; ++k) visit<Tag, OP>(c, vec_elem<R>(v, k), j0 + k);
+}
+
+// ---------------------------------------------------------------------------
+// Vector scanners: visit a thread's 16-byte vectors in increasing index order,
+// starting from its candidate so far, then return the updated candidate. The
+// generic scanner visits the elements one by one.
+// ---------------------------------------------------------------------------
+template <class Tag, int OP, bool PAIRED = (sizeof(typename Tag::raw) == 2)>
+struct VecScan {
+    Cand<Tag> c;
+    __device__ __forceinline__ explicit VecScan(const Cand<Tag>& c0) : c(c0) {}
+    __device__ __forceinline__ void visit(const uint4& v, int j0) { visit_vec<Tag, OP>(c, v, j0); }
+    __device__ __forceinline__ Cand<Tag> finish() const { return c; }
+};
+
+// 16-bit elements come two to a 32-bit word: the elements at even and at odd
+// positions of the vectors a thread visits form two subsequences, each
+// scanned by the exact sequential rule against its own candidate, both
+// seeded with the thread's candidate so far. Per word, one packed comparison
+// (setp on the 16-bit pair, false on NaN) gives each subsequence's update
+// predicate, two selects update the indices, and one packed max / min (which
+// ignores NaNs) the keys. The two candidates then merge by the usual rule;
+// each is the best of {seed} and its subsequence with ties to the earlier
+// (later) index, so the merge is that of the whole sequence. The kept key is
+// the winning element itself except that a zero may carry the other sign
+// (packed max / min of equal zeros); cand_value() reads zeros back. A NaN
+// candidate (only x[0] can be one) is never displaced, so it skips the scan.
+template <class Tag, int OP>
+struct VecScan<Tag, OP, true> {
+    static constexpr bool kBF = std::is_same<Tag, TagBF16>::value;
+    uint32_t kv;    // keys of the two candidates as raw 16-bit patterns (low half: even positions)
+    int ie, io;     // index of the even candidate; index - 1 of the odd one
+    Cand<Tag> c0;
+    bool frozen;
+    __device__ __forceinline__ explicit VecScan(const Cand<Tag>& c)
+        : kv(static_cast<uint32_t>(c.v) * 0x10001u), ie(c.i), io(c.i - 1), c0(c), frozen(c.k != c.k) {}
+    __device__ __forceinline__ void word(uint32_t w, int j) {
+        // p: element j (low half) takes the even candidate, q: element j + 1 the odd one
+#define ARGR_PAIR_SEL(CMP, TY)                                                                   \
+    asm("{\n\t.reg .pred p, q;\n\tsetp." CMP "." TY " p|q, %2, %3;\n\t"                        \
+        "selp.b32 %0, %4, %0, p;\n\tselp.b32 %1, %4, %1, q;\n\t}"                              \
+        : "+r"(ie), "+r"(io)                                                                      \
+        : "r"(w), "r"(kv), "r"(j))
+        if constexpr (kBF) {
+            if constexpr (OP == kOpMax) ARGR_PAIR_SEL("gt", "bf16x2");
+            else if constexpr (OP == kOpMin) ARGR_PAIR_SEL("lt", "bf16x2");
+            else if constexpr (OP == kOpMaxLast) ARGR_PAIR_SEL("ge", "bf16x2");
+            else ARGR_PAIR_SEL("le", "bf16x2");
+            if constexpr (kIsMin<OP>) asm("min.bf16x2 %0, %0, %1;" : "+r"(kv) : "r"(w));
+            else asm("max.bf16x2 %0, %0, %1;" : "+r"(kv) : "r"(w));
+        } else {
+            if constexpr (OP == kOpMax) ARGR_PAIR_SEL("gt", "f16x2");
+            else if constexpr (OP == kOpMin) ARGR_PAIR_SEL("lt", "f16x2");
+            else if constexpr (OP == kOpMaxLast) ARGR_PAIR_SEL("ge", "f16x2");
+            else ARGR_PAIR_SEL("le", "f16x2");
+            if constexpr (kIsMin<OP>) asm("min.f16x2 %0, %0, %1;" : "+r"(kv) : "r"(w));
+            else asm("max.f16x2 %0, %0, %1;" : "+r"(kv) : "r"(w));
+        }
+#undef ARGR_PAIR_SEL
+    }
+    __device__ __forceinline__ void visit(const uint4& v, int j0) {
+        if (frozen) return;
+        word(v.x, j0);
+        word(v.y, j0 + 2);
+        word(v.z, j0 + 4);
+        word(v.w, j0 + 6);
+    }
+    __device__ __forceinline__ Cand<Tag> finish() const {
+        if (frozen) return c0;
+        const Cand<Tag> a = make_cand<Tag, OP>(static_cast<uint16_t>(kv & 0xffffu), ie);
+        const Cand<Tag> b = make_cand<Tag, OP>(static_cast<uint16_t>(kv >> 16), io + 1);
+        return merge<Tag, OP>(a, b);
+    }
+};
+
+// The raw bits of a candidate's element for out_val. The paired 16-bit scan
+// may keep a zero of the other sign, so a zero is read back from the row.
+template <class Tag>
+__device__ __forceinline__ typename Tag::raw cand_value(const Cand<Tag>& c, const typename Tag::raw* row) {
+    if constexpr (sizeof(typename Tag::raw) == 2) {
+        if ((c.v & 0x7fffu) == 0) return ld_scalar(row + c.i);
+    }
+    return c.v;
 }
 
 }  // namespace argr

@@ -68,6 +68,7 @@ rows_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int
             for (int u = 0; u < U; ++u) buf[u] = (u * G < rem) ? ld_stream16(rv + v0 + u * G) : make_uint4(0, 0, 0, 0);
             // Lane 0 of the group always holds vector 0, whose first element is x[0].
             c = make_cand<Tag, OP>(shfl_raw(gmask, vec_elem<R>(buf[0], 0), 0, G), 0);
+            VecScan<Tag, OP> scan(c);
             if constexpr (PIPE) {
                 // Software pipeline: the next batch's loads are issued before
                 // the current batch is scanned, so a lane always has loads in
@@ -85,7 +86,7 @@ rows_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int
                     }
                     #pragma unroll
                     for (int u = 0; u < U; ++u)
-                        if (u * G < rem) visit_vec<Tag, OP>(c, buf[u], (v0 + u * G) * E);
+                        if (u * G < rem) scan.visit(buf[u], (v0 + u * G) * E);
                     if (!more) break;
                     v0 = v1;
                     rem = rem1;
@@ -95,7 +96,7 @@ rows_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int
             } else {
                 #pragma unroll
                     for (int u = 0; u < U; ++u)
-                        if (u * G < rem) visit_vec<Tag, OP>(c, buf[u], (v0 + u * G) * E);
+                        if (u * G < rem) scan.visit(buf[u], (v0 + u * G) * E);
                 while (rem > G * U) {
                     v0 += G * U;
                     rem = nvec - v0;
@@ -104,9 +105,10 @@ rows_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int
                         if (u * G < rem) buf[u] = ld_stream16(rv + v0 + u * G);
                     #pragma unroll
                     for (int u = 0; u < U; ++u)
-                        if (u * G < rem) visit_vec<Tag, OP>(c, buf[u], (v0 + u * G) * E);
+                        if (u * G < rem) scan.visit(buf[u], (v0 + u * G) * E);
                 }
             }
+            c = scan.finish();
         } else {
             int j0 = lg;
             int rem = cols - j0;
@@ -131,7 +133,7 @@ rows_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int
         c = group_merge<Tag, OP, G>(c, gmask);
         if (lg == 0) {
             out_idx[r] = c.i;
-            if (out_val) out_val[r] = c.v;
+            if (out_val) out_val[r] = cand_value<Tag>(c, row);
         }
     }
 }
@@ -165,6 +167,7 @@ __device__ __forceinline__ Cand<Tag> scan_share(const typename Tag::raw* __restr
 
     int v0 = vb + t;
     if (v0 < ve) {
+        VecScan<Tag, OP> scan(c);
         for (;;) {
             const int rem = ve - v0;
             uint4 buf[U];
@@ -173,10 +176,11 @@ __device__ __forceinline__ Cand<Tag> scan_share(const typename Tag::raw* __restr
                 if (u * nt < rem) buf[u] = ld_stream16(rv + v0 + u * nt);
 #pragma unroll
             for (int u = 0; u < U; ++u)
-                if (u * nt < rem) visit_vec<Tag, OP>(c, buf[u], head + (v0 + u * nt) * E);
+                if (u * nt < rem) scan.visit(buf[u], head + (v0 + u * nt) * E);
             if (rem <= U * nt) break;
             v0 += U * nt;
         }
+        c = scan.finish();
     }
     if (b == nb - 1 && t < cols - tail0) visit<Tag, OP>(c, ld_scalar(row + tail0 + t), tail0 + t);
     return c;
@@ -251,7 +255,7 @@ split_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, in
             if (nb == 1) {
                 if (lane == 0) {
                     out_idx[r] = c.i;
-                    if (out_val) out_val[r] = c.v;
+                    if (out_val) out_val[r] = cand_value<Tag>(c, row);
                 }
             } else {
                 // Multi-CTA row: publish the partial, then arrive. The arrival
@@ -273,7 +277,7 @@ split_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, in
                     m = group_merge<Tag, OP, 32>(m, 0xffffffffu);
                     if (lane == 0) {
                         out_idx[r] = m.i;
-                        if (out_val) out_val[r] = m.v;
+                        if (out_val) out_val[r] = cand_value<Tag>(m, row);
                     }
                 }
             }
@@ -347,7 +351,7 @@ cluster_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, 
             m = group_merge<Tag, OP, 32>(m, 0xffffffffu);
             if (threadIdx.x == 0) {
                 out_idx[r] = m.i;
-                if (out_val) out_val[r] = m.v;
+                if (out_val) out_val[r] = cand_value<Tag>(m, row);
             }
         }
         __syncthreads();
