@@ -457,13 +457,14 @@ class E2EStep:
         self.host_out.copy_(self.dev_out, non_blocking=True)
 
 
-def e2e_time(torch, A, cases, inputs, steps, stream):
-    """End-to-end steps (E2EStep) captured as two CUDA graphs and replayed
-    alternately on two streams: step k+1's input copy overlaps step k's
-    calls, as a pipelined application would run them. Also times the same
-    steps issued eagerly from Python on one stream (host-bound: the binding
-    costs several microseconds a call). Returns (device seconds for `steps`
-    pipelined steps, host wall seconds, eager device seconds, h2d, d2h)."""
+def e2e_time(torch, A, cases, inputs, steps, stream, depth=2):
+    """End-to-end steps (E2EStep) captured as `depth` CUDA graphs (each with
+    its own buffers) and replayed in rotation on `depth` streams, so up to
+    `depth` steps are in flight: later steps' input copies overlap earlier
+    steps' calls, as a pipelined application would run them. Also times the
+    same steps issued eagerly from Python on one stream (host-bound: the
+    binding costs several microseconds a call). Returns (device seconds for
+    `steps` pipelined steps, host wall seconds, eager device seconds, h2d, d2h)."""
     offs, total = [], 0
     for c in cases:
         offs.append(total)
@@ -471,10 +472,10 @@ def e2e_time(torch, A, cases, inputs, steps, stream):
     host_in = torch.empty(total, dtype=torch.uint8).pin_memory()
     for c, x, o in zip(cases, inputs, offs):
         host_in[o:o + c.nbytes].copy_(torch.from_numpy(np.ascontiguousarray(x).reshape(-1).view(np.uint8)))
-    pair = [E2EStep(torch, A, cases, inputs, host_in, offs) for _ in range(2)]
+    pair = [E2EStep(torch, A, cases, inputs, host_in, offs) for _ in range(depth)]
     h2d = host_in.numel()  # the bytes copied, alignment gaps included
     d2h = pair[0].host_out.numel() * 8
-    streams = [stream, torch.cuda.Stream()]
+    streams = [stream] + [torch.cuda.Stream() for _ in range(depth - 1)]
 
     # eager: one step after another on one stream
     with torch.cuda.stream(stream):
@@ -491,7 +492,7 @@ def e2e_time(torch, A, cases, inputs, steps, stream):
         eager = e0.elapsed_time(e1) / 1e3
 
     graphs = []
-    for k in range(2):
+    for k in range(depth):
         with torch.cuda.stream(streams[k]):
             pair[k](streams[k])  # warm-up outside the capture
             streams[k].synchronize()
@@ -500,21 +501,23 @@ def e2e_time(torch, A, cases, inputs, steps, stream):
                 pair[k](streams[k])
             graphs.append(g)
     torch.cuda.synchronize()
-    for k in range(4):
-        with torch.cuda.stream(streams[k % 2]):
-            graphs[k % 2].replay()
+    for k in range(2 * depth):
+        with torch.cuda.stream(streams[k % depth]):
+            graphs[k % depth].replay()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    joined = torch.cuda.Event()
     t0 = time.perf_counter()
     e0.record(streams[0])
-    streams[1].wait_event(e0)
+    for s in streams[1:]:
+        s.wait_event(e0)
     for k in range(steps):
-        with torch.cuda.stream(streams[k % 2]):
-            graphs[k % 2].replay()
-    joined.record(streams[1])
-    streams[0].wait_event(joined)
+        with torch.cuda.stream(streams[k % depth]):
+            graphs[k % depth].replay()
+    for s in streams[1:]:
+        joined = torch.cuda.Event()
+        joined.record(s)
+        streams[0].wait_event(joined)
     e1.record(streams[0])
     e1.synchronize()
     wall = time.perf_counter() - t0
@@ -557,6 +560,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--e2e-depth", type=int, default=3, help="end-to-end steps in flight (graphs in rotation)")
     ap.add_argument("--no-cub", action="store_true", help="skip the cub::DeviceReduce timing comparison")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -627,16 +631,18 @@ def main():
                           "bytes_per_launch_avg": step_bytes / len(cases)}
 
     if world == 1 or rank == 0:
-        dev_s, wall, eager_s, h2d, d2h = e2e_time(torch, A, cases, inputs, args.e2e_steps, stream)
+        dev_s, wall, eager_s, h2d, d2h = e2e_time(torch, A, cases, inputs, args.e2e_steps, stream,
+                                                  max(2, args.e2e_depth))
         ncall = args.e2e_steps * len(cases)
         result["e2e"] = {"value": round(dev_s * 1e6 / ncall, 4), "unit": "us/call",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                          "host_wall_us_per_call": round(wall * 1e6 / ncall, 4),
                          "eager_python_us_per_call": round(eager_s * 1e6 / ncall, 4),
-                         "steps": args.e2e_steps,
+                         "steps": args.e2e_steps, "steps_in_flight": max(2, args.e2e_depth),
                          "method": "each step copies its inputs from pinned host memory and reads its indices "
-                                   "back; steps captured as two CUDA graphs replayed alternately on two streams, "
-                                   "so one step's input copy overlaps the previous step's calls"}
+                                   "back; steps captured as CUDA graphs (one per step in flight, each with its "
+                                   "own buffers) replayed in rotation on as many streams, so later steps' input "
+                                   "copies overlap earlier steps' calls"}
 
     if not args.no_cub and cub_comparable(cases) and (world == 1 or rank == 0):
         result["cub_compare"] = cub_compare(torch, A, cases, inputs, min(args.steps, 4000), stream, us_per_call)

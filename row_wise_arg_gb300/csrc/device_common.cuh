@@ -286,12 +286,71 @@ __device__ __forceinline__ void visit_vec(Cand<Tag>& c, const uint4& v, int j0) 
 // starting from its candidate so far, then return the updated candidate. The
 // generic scanner visits the elements one by one.
 // ---------------------------------------------------------------------------
-template <class Tag, int OP, bool PAIRED = (sizeof(typename Tag::raw) == 2)>
-struct VecScan {
+template <class Tag, int OP>
+struct VecScanElems {
     Cand<Tag> c;
-    __device__ __forceinline__ explicit VecScan(const Cand<Tag>& c0) : c(c0) {}
+    __device__ __forceinline__ explicit VecScanElems(const Cand<Tag>& c0) : c(c0) {}
     __device__ __forceinline__ void visit(const uint4& v, int j0) { visit_vec<Tag, OP>(c, v, j0); }
     __device__ __forceinline__ Cand<Tag> finish() const { return c; }
+};
+template <class Tag, int OP, bool PAIRED = (sizeof(typename Tag::raw) == 2)>
+struct VecScan : VecScanElems<Tag, OP> {
+    using VecScanElems<Tag, OP>::VecScanElems;
+};
+
+// binary32: the key is the value itself, so only (key, index) is carried.
+template <int OP>
+struct VecScan<TagF32, OP, false> {
+    float k;
+    int i;
+    __device__ __forceinline__ explicit VecScan(const Cand<TagF32>& c) : k(c.k), i(c.i) {}
+    __device__ __forceinline__ void el(float x, int j) {
+        bool take;  // "better or equal" is one IEEE comparison (false on NaN)
+        if constexpr (kIsLast<OP>) take = kIsMin<OP> ? x <= k : x >= k;
+        else take = TagF32::better<OP>(x, k);
+        if (take) {
+            k = x;
+            i = j;
+        }
+    }
+    __device__ __forceinline__ void visit(const uint4& v, int j0) {
+        el(__uint_as_float(v.x), j0);
+        el(__uint_as_float(v.y), j0 + 1);
+        el(__uint_as_float(v.z), j0 + 2);
+        el(__uint_as_float(v.w), j0 + 3);
+    }
+    __device__ __forceinline__ Cand<TagF32> finish() const { return Cand<TagF32>{k, k, i}; }
+};
+
+// binary64: only (key, index) is carried and the value is rebuilt from the
+// key at the end (order_key() is invertible on the numbers, except that both
+// zeros share a key: cand_value() reads zeros back). An unchanged candidate is
+// returned as it came, which keeps a NaN x[0] exact.
+template <int OP>
+struct VecScan<TagF64, OP, false> {
+    unsigned long long k;
+    int i;
+    Cand<TagF64> c0;
+    __device__ __forceinline__ explicit VecScan(const Cand<TagF64>& c) : k(c.k), i(c.i), c0(c) {}
+    __device__ __forceinline__ void el(unsigned long long x, int j) {
+        const unsigned long long kx = TagF64::order_key<OP>(x);
+        if (kx <= TagF64::kLimit && (kIsLast<OP> ? kx >= k : kx > k)) {
+            k = kx;
+            i = j;
+        }
+    }
+    __device__ __forceinline__ void visit(const uint4& v, int j0) {
+        el(static_cast<unsigned long long>(v.y) << 32 | v.x, j0);
+        el(static_cast<unsigned long long>(v.w) << 32 | v.z, j0 + 1);
+    }
+    __device__ __forceinline__ Cand<TagF64> finish() const {
+        if (k == c0.k && i == c0.i) return c0;
+        // inverse of order_key: keys with the sign bit set are b | kSign,
+        // the others -b; ArgMin flips the sign bit back
+        unsigned long long b = (k & TagF64::kSign) ? (k ^ TagF64::kSign) : (0ull - k);
+        if constexpr (kIsMin<OP>) b ^= TagF64::kSign;
+        return Cand<TagF64>{b, k, i};
+    }
 };
 
 // 16-bit elements come two to a 32-bit word: the elements at even and at odd
@@ -354,12 +413,15 @@ struct VecScan<Tag, OP, true> {
     }
 };
 
-// The raw bits of a candidate's element for out_val. The paired 16-bit scan
-// may keep a zero of the other sign, so a zero is read back from the row.
+// The raw bits of a candidate's element for out_val. The 16-bit and binary64
+// vector scans may hold a zero of the other sign, so a zero is read back from
+// the row.
 template <class Tag>
 __device__ __forceinline__ typename Tag::raw cand_value(const Cand<Tag>& c, const typename Tag::raw* row) {
     if constexpr (sizeof(typename Tag::raw) == 2) {
         if ((c.v & 0x7fffu) == 0) return ld_scalar(row + c.i);
+    } else if constexpr (sizeof(typename Tag::raw) == 8) {
+        if ((c.v & ~TagF64::kSign) == 0) return ld_scalar(row + c.i);
     }
     return c.v;
 }
