@@ -203,8 +203,37 @@ __device__ __forceinline__ uint16_t shfl_raw(unsigned m, uint16_t v, int src, in
 
 // Butterfly over groups of G lanes (G a power of two <= 32); every lane of
 // the group ends with the group's merged candidate.
+// Whole-warp merge of candidates with 32-bit (binary32) keys through the warp
+// reduction unit. The key maps to an unsigned integer with the same order
+// (-0.0 first becomes +0.0 by adding +0.0, so both zeros map alike); one
+// reduction finds the best key, a second the lowest index holding it (the
+// highest, for the last-occurrence ops), and the value comes from a lane with
+// that index (lanes with the same index hold the same element). When x[0] is
+// NaN every candidate is (x[0], 0), so all keys map alike there too. Every
+// lane gets the result; all 32 lanes must take part.
+template <class Tag, int OP>
+__device__ __forceinline__ Cand<Tag> warp_merge_redux(const Cand<Tag>& c) {
+    const unsigned b = __float_as_uint(c.k + 0.0f);
+    unsigned u = b ^ (static_cast<unsigned>(static_cast<int>(b) >> 31) | 0x80000000u);
+    if constexpr (kIsMin<OP>) u = ~u;
+    const unsigned best = __reduce_max_sync(0xffffffffu, u);
+    const bool has = u == best;
+    int win;
+    if constexpr (kIsLast<OP>)
+        win = static_cast<int>(__reduce_max_sync(0xffffffffu, has ? static_cast<unsigned>(c.i) + 1u : 0u)) - 1;
+    else
+        win = static_cast<int>(__reduce_min_sync(0xffffffffu, has ? static_cast<unsigned>(c.i) : 0xffffffffu));
+    const int src = __ffs(__ballot_sync(0xffffffffu, c.i == win)) - 1;
+    Cand<Tag> r;
+    r.v = shfl_raw(0xffffffffu, c.v, src, 32);
+    r.k = __shfl_sync(0xffffffffu, c.k, src);
+    r.i = win;
+    return r;
+}
+
 template <class Tag, int OP, int G>
 __device__ __forceinline__ Cand<Tag> group_merge(Cand<Tag> c, unsigned mask) {
+    if constexpr (G == 32 && sizeof(typename Tag::key) == 4) return warp_merge_redux<Tag, OP>(c);
 #pragma unroll
     for (int off = G / 2; off >= 1; off >>= 1) {
         const Cand<Tag> o = make_cand<Tag, OP>(shfl_xor_raw(mask, c.v, off, G), __shfl_xor_sync(mask, c.i, off, G));
