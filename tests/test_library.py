@@ -654,3 +654,19 @@ def test_cum_stream_scratch_size():
         p.path, p.block, p.cluster, p.grid_rows = _lib.ARGR_PATH_CUM_STREAM, block, 1, 304
         p.blocks_per_row = -(-cols // (block * 7))
         assert _lib.argreduce_plan_scratch_bytes(p, rows) == want
+
+
+def test_warp_collectives_not_short_circuited():
+    """Every lane named in a warp collective's mask must execute it, or the
+    others wait for it forever. A collective written after `&&`, `||` or `?`
+    in the same expression is skipped by the lanes that short-circuit, so
+    device code computes collectives into variables first."""
+    import glob
+    pat = re.compile(r"(&&|\|\||\?)[^;{}]*\b__\w+_sync\(")
+    bad = []
+    for path in sorted(glob.glob(os.path.join(ROOT, "row_wise_arg_gb300", "csrc", "*.cu*"))):
+        for n, line in enumerate(open(path), 1):
+            code = line.split("//")[0]
+            if pat.search(code):
+                bad.append(f"{os.path.basename(path)}:{n}: {line.strip()}")
+    assert not bad, bad
