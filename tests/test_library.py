@@ -124,6 +124,11 @@ def test_plan_paths_for_configs():
         assert d["path_name"] == "cluster" and d["cluster"] >= 8, d
         assert rows * d["cluster"] <= 2 * 152 and d["scratch_bytes"] == 0
         assert d["flags"] & _lib.ARGR_PLAN_PDL
+        if rows == 1:  # one batch of loads covers a CTA's share
+            assert d["unroll"] * d["block"] * 16 * d["cluster"] >= cols * 4
+    # one row with >= 48 KB per CTA: 1024 threads; more rows or smaller shares: 512 or fewer
+    assert path(1, 202048)["block"] == 1024 and path(1, 262144)["block"] == 1024
+    assert path(1, 202048, "bf16")["block"] == 512 and path(8, 202048)["block"] == 512
     d = path(1, 10_000_000)  # too wide for one cluster: split over the device
     assert d["path_name"] == "split" and d["blocks_per_row"] > 152
     assert path(4096, 4096)["path_name"] == "rows" and path(4096, 4096)["group"] == 32
