@@ -105,6 +105,29 @@ class CubCalls:
                              self.temp[i].data_ptr(), self.temp[i].numel(), stream.cuda_stream)
 
 
+class ThreadPerRowCalls:
+    """The thread-per-row kernel (one thread scans a whole row: the pages'
+    narrow-row design) as a forced plan of the same library, for the narrow
+    configs' comparison: scalar loads as on the pages, or 16-byte vector
+    loads (`vec`, rows 16-byte aligned), 256 threads, 4 loads in flight."""
+
+    def __init__(self, A, cases, vec):
+        from row_wise_arg_gb300 import _lib
+        self.A = A
+        self.plans = []
+        for c in cases:
+            p = _lib.argr_plan()
+            p.path, p.block, p.group, p.vec, p.unroll = _lib.ARGR_PATH_ROWS, 256, 1, int(vec), 4
+            p.flags = _lib.ARGR_PLAN_PDL
+            p.blocks_per_row = 1
+            p.grid_rows = min(-(-c.rows // 256), 65535)
+            self.plans.append(p)
+
+    def __call__(self, i, c, x, out_idx, stream):
+        self.A.argreduce_with_plan(self.plans[i], x.view(c.rows, c.cols), c.op, dtype=c.dtype, out_idx=out_idx,
+                                   stream=stream)
+
+
 def cub_comparable(cases) -> bool:
     return all(c.rows == 1 and c.inner == 1 and c.op in ("max", "min") and not is_scan(c) for c in cases)
 
@@ -673,6 +696,17 @@ def main():
                         cs, cn, _, _ = time_group(torch, A, [c], [x], n, 5, stream, exact=False,
                                                   cub=CubCalls(torch, [c]))
                         row["cub_us_per_call"] = round(cs * 1e6 / cn, 3)
+                    if name == "narrow":
+                        # the narrow-row target: no slower than a thread-per-row kernel
+                        tpr = {}
+                        aligned = c.cols * W.ELEM_SIZE[c.dtype] % 16 == 0
+                        for label, vec in (("scalar_loads", False), ("vector_loads", True)):
+                            if vec and not aligned:
+                                continue
+                            ts, tn, _, _ = time_group(torch, A, [c], [x], n, 5, stream, exact=False,
+                                                      cub=ThreadPerRowCalls(A, [c], vec))
+                            tpr[label] = round(ts * 1e6 / tn, 3)
+                        row["thread_per_row_us_per_call"] = tpr
                     table.append(row)
             del ginputs
         result["configs"] = table
