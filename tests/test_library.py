@@ -450,6 +450,24 @@ def test_f64_keys_and_row_scan_test():
                     0xFFF8000000000000, 0xFFFFFFFFFFFFFFFF):
             k = key64(nan, is_min)
             assert k > hi_key or k < lo_key, (hex(nan), is_min)
+    # the binary64 vector scan rebuilds a value from its key (VecScan<TagF64>::finish):
+    # exact for every nonzero number; both zeros share a key and come back as one
+    # of them, which is why cand_value() reads zeros back from the row
+    for is_min in (False, True):
+        for b in vals:
+            if dv[b] != dv[b]:
+                continue  # NaNs never become a scan's candidate through a key
+            got = key_value64(key64(b, is_min), is_min)
+            if b & ~SIGN & M64:
+                assert got == b, (hex(b), is_min)
+            else:
+                assert got in (0, SIGN), (hex(b), is_min)
+
+
+def key_value64(k, is_min):
+    """Inverse of key64 on the numbers (VecScan<TagF64>::finish)."""
+    b = (k ^ SIGN) if k & SIGN else ((0 - k) & M64)
+    return b ^ SIGN if is_min else b
 
 
 def test_axis_plans():
