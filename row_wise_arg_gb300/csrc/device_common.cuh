@@ -247,13 +247,17 @@ __device__ __forceinline__ Cand<Tag> group_merge(Cand<Tag> c, unsigned mask) {
     // Reductions for whole warps and for 16-lane groups of binary64 keys
     // (measured: below that the few shuffle rounds are faster; [4096,128]
     // f32, 8 lanes per row: 2.06 us with shuffles, 2.48 us with reductions).
-    if constexpr (G == 32 || (G == 16 && sizeof(typename Tag::key) == 8)) return group_merge_redux<Tag, OP>(c, mask);
+    if constexpr (G == 32 || (G == 16 && sizeof(typename Tag::key) == 8)) {
+        return group_merge_redux<Tag, OP>(c, mask);
+    } else {
 #pragma unroll
-    for (int off = G / 2; off >= 1; off >>= 1) {
-        const Cand<Tag> o = make_cand<Tag, OP>(shfl_xor_raw(mask, c.v, off, G), __shfl_xor_sync(mask, c.i, off, G));
-        c = merge<Tag, OP>(c, o);
+        for (int off = G / 2; off >= 1; off >>= 1) {
+            const Cand<Tag> o =
+                make_cand<Tag, OP>(shfl_xor_raw(mask, c.v, off, G), __shfl_xor_sync(mask, c.i, off, G));
+            c = merge<Tag, OP>(c, o);
+        }
+        return c;
     }
-    return c;
 }
 
 // Whole-CTA merge. Every thread passes its candidate; the merged candidate is
@@ -396,6 +400,36 @@ struct VecScan<TagF64, OP, false> {
     }
 };
 
+// One packed step over a 32-bit word w of two 16-bit elements against the
+// packed keys kv of two candidates (low half against low half): a packed
+// comparison (setp on the pair, false on NaN) decides each candidate's update,
+// which sets its index to j (ia: low, ib: high), and a packed max / min
+// (which ignores NaNs) updates the keys.
+template <class Tag, int OP>
+__device__ __forceinline__ void pair_step(uint32_t& kv, int& ia, int& ib, uint32_t w, int j) {
+#define ARGR_PAIR_SEL(CMP, TY)                                                                   \
+    asm("{\n\t.reg .pred p, q;\n\tsetp." CMP "." TY " p|q, %2, %3;\n\t"                        \
+        "selp.b32 %0, %4, %0, p;\n\tselp.b32 %1, %4, %1, q;\n\t}"                              \
+        : "+r"(ia), "+r"(ib)                                                                      \
+        : "r"(w), "r"(kv), "r"(j))
+    if constexpr (std::is_same<Tag, TagBF16>::value) {
+        if constexpr (OP == kOpMax) ARGR_PAIR_SEL("gt", "bf16x2");
+        else if constexpr (OP == kOpMin) ARGR_PAIR_SEL("lt", "bf16x2");
+        else if constexpr (OP == kOpMaxLast) ARGR_PAIR_SEL("ge", "bf16x2");
+        else ARGR_PAIR_SEL("le", "bf16x2");
+        if constexpr (kIsMin<OP>) asm("min.bf16x2 %0, %0, %1;" : "+r"(kv) : "r"(w));
+        else asm("max.bf16x2 %0, %0, %1;" : "+r"(kv) : "r"(w));
+    } else {
+        if constexpr (OP == kOpMax) ARGR_PAIR_SEL("gt", "f16x2");
+        else if constexpr (OP == kOpMin) ARGR_PAIR_SEL("lt", "f16x2");
+        else if constexpr (OP == kOpMaxLast) ARGR_PAIR_SEL("ge", "f16x2");
+        else ARGR_PAIR_SEL("le", "f16x2");
+        if constexpr (kIsMin<OP>) asm("min.f16x2 %0, %0, %1;" : "+r"(kv) : "r"(w));
+        else asm("max.f16x2 %0, %0, %1;" : "+r"(kv) : "r"(w));
+    }
+#undef ARGR_PAIR_SEL
+}
+
 // 16-bit elements come two to a 32-bit word: the elements at even and at odd
 // positions of the vectors a thread visits form two subsequences, each
 // scanned by the exact sequential rule against its own candidate, both
@@ -410,37 +444,14 @@ struct VecScan<TagF64, OP, false> {
 // candidate (only x[0] can be one) is never displaced, so it skips the scan.
 template <class Tag, int OP>
 struct VecScan<Tag, OP, true> {
-    static constexpr bool kBF = std::is_same<Tag, TagBF16>::value;
     uint32_t kv;    // keys of the two candidates as raw 16-bit patterns (low half: even positions)
     int ie, io;     // index of the even candidate; index - 1 of the odd one
     Cand<Tag> c0;
     bool frozen;
     __device__ __forceinline__ explicit VecScan(const Cand<Tag>& c)
         : kv(static_cast<uint32_t>(c.v) * 0x10001u), ie(c.i), io(c.i - 1), c0(c), frozen(c.k != c.k) {}
-    __device__ __forceinline__ void word(uint32_t w, int j) {
-        // p: element j (low half) takes the even candidate, q: element j + 1 the odd one
-#define ARGR_PAIR_SEL(CMP, TY)                                                                   \
-    asm("{\n\t.reg .pred p, q;\n\tsetp." CMP "." TY " p|q, %2, %3;\n\t"                        \
-        "selp.b32 %0, %4, %0, p;\n\tselp.b32 %1, %4, %1, q;\n\t}"                              \
-        : "+r"(ie), "+r"(io)                                                                      \
-        : "r"(w), "r"(kv), "r"(j))
-        if constexpr (kBF) {
-            if constexpr (OP == kOpMax) ARGR_PAIR_SEL("gt", "bf16x2");
-            else if constexpr (OP == kOpMin) ARGR_PAIR_SEL("lt", "bf16x2");
-            else if constexpr (OP == kOpMaxLast) ARGR_PAIR_SEL("ge", "bf16x2");
-            else ARGR_PAIR_SEL("le", "bf16x2");
-            if constexpr (kIsMin<OP>) asm("min.bf16x2 %0, %0, %1;" : "+r"(kv) : "r"(w));
-            else asm("max.bf16x2 %0, %0, %1;" : "+r"(kv) : "r"(w));
-        } else {
-            if constexpr (OP == kOpMax) ARGR_PAIR_SEL("gt", "f16x2");
-            else if constexpr (OP == kOpMin) ARGR_PAIR_SEL("lt", "f16x2");
-            else if constexpr (OP == kOpMaxLast) ARGR_PAIR_SEL("ge", "f16x2");
-            else ARGR_PAIR_SEL("le", "f16x2");
-            if constexpr (kIsMin<OP>) asm("min.f16x2 %0, %0, %1;" : "+r"(kv) : "r"(w));
-            else asm("max.f16x2 %0, %0, %1;" : "+r"(kv) : "r"(w));
-        }
-#undef ARGR_PAIR_SEL
-    }
+    // element j (low half) may take the even candidate, element j + 1 the odd one
+    __device__ __forceinline__ void word(uint32_t w, int j) { pair_step<Tag, OP>(kv, ie, io, w, j); }
     __device__ __forceinline__ void visit(const uint4& v, int j0) {
         if (frozen) return;
         word(v.x, j0);

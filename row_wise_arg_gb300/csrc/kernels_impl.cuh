@@ -528,9 +528,13 @@ struct AxisVec<unsigned long long, 2> {
 };
 template <>
 struct AxisVec<uint16_t, 4> {
-    static __device__ __forceinline__ void load(const uint16_t* p, uint16_t (&v)[4]) {
+    static __device__ __forceinline__ uint2 load_words(const uint16_t* p) {
         uint2 q;
         asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(q.x), "=r"(q.y) : "l"(p));
+        return q;
+    }
+    static __device__ __forceinline__ void load(const uint16_t* p, uint16_t (&v)[4]) {
+        const uint2 q = load_words(p);
         v[0] = static_cast<uint16_t>(q.x & 0xffffu); v[1] = static_cast<uint16_t>(q.x >> 16);
         v[2] = static_cast<uint16_t>(q.y & 0xffffu); v[3] = static_cast<uint16_t>(q.y >> 16);
     }
@@ -566,13 +570,41 @@ axis_kernel(const typename Tag::raw* __restrict__ x, int64_t outer, int nred, in
     for (int64_t o = blockIdx.z; o < outer; o += gridDim.z) {
         const R* col = x + (o * nred) * inner + i0;
         Cand<Tag> c[V];
-        {
-            R v0[V];
-            if (active) AxisVec<R, V>::load(col, v0);  // row r = 0 seeds every candidate
+        R v0[V];
+        if (active) AxisVec<R, V>::load(col, v0);  // row r = 0 seeds every candidate
 #pragma unroll
-            for (int v = 0; v < V; ++v) c[v] = make_cand<Tag, OP>(active ? v0[v] : R(0), 0);
-        }
-        if (active) {
+        for (int v = 0; v < V; ++v) c[v] = make_cand<Tag, OP>(active ? v0[v] : R(0), 0);
+        if constexpr (sizeof(R) == 2 && V == 4) {
+            // 16-bit columns, two to a 32-bit word: two independent scans per
+            // packed step (pair_step), both with the row's index. A column
+            // whose x[0] is NaN keeps (x[0], 0) (nothing displaces it), which
+            // is restored after the loop since the packed max moves its key.
+            if (active) {
+                uint32_t kv0 = static_cast<uint32_t>(v0[0]) | static_cast<uint32_t>(v0[1]) << 16;
+                uint32_t kv1 = static_cast<uint32_t>(v0[2]) | static_cast<uint32_t>(v0[3]) << 16;
+                int ix[4] = {0, 0, 0, 0};
+                int r = rs + rl;
+                while (r < re) {
+                    const int rem = re - r;  // > 0
+                    uint2 buf[U];
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        if (u * RG < rem) buf[u] = AxisVec<R, 4>::load_words(col + static_cast<int64_t>(r + u * RG) * inner);
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        if (u * RG < rem) {
+                            pair_step<Tag, OP>(kv0, ix[0], ix[1], buf[u].x, r + u * RG);
+                            pair_step<Tag, OP>(kv1, ix[2], ix[3], buf[u].y, r + u * RG);
+                        }
+                    if (rem <= U * RG) break;
+                    r += U * RG;
+                }
+                const uint32_t keys[4] = {kv0 & 0xffffu, kv0 >> 16, kv1 & 0xffffu, kv1 >> 16};
+#pragma unroll
+                for (int v = 0; v < V; ++v)
+                    if (c[v].k == c[v].k) c[v] = make_cand<Tag, OP>(static_cast<R>(keys[v]), ix[v]);
+            }
+        } else if (active) {
             int r = rs + rl;
             while (r < re) {
                 const int rem = re - r;  // > 0
@@ -648,7 +680,14 @@ axis_kernel(const typename Tag::raw* __restrict__ x, int64_t outer, int nred, in
             for (int v = 0; v < V; ++v) {
                 if (i0 + v < inner) {
                     out_idx[o * inner + i0 + v] = c[v].i;
-                    if (out_val) out_val[o * inner + i0 + v] = c[v].v;
+                    if (out_val) {
+                        R val = c[v].v;
+                        // the packed 16-bit scan may keep a zero of the other sign: read zeros back
+                        if constexpr (sizeof(R) == 2 && V == 4) {
+                            if ((val & 0x7fffu) == 0) val = ld_scalar(col + static_cast<int64_t>(c[v].i) * inner + v);
+                        }
+                        out_val[o * inner + i0 + v] = val;
+                    }
                 }
             }
         }
