@@ -224,6 +224,20 @@ argr_status argreduce_with_plan(const argr_plan* plan, const void* x, argr_dtype
                                 size_t scratch_bytes, argr_stream stream);
 
 /*
+ * The checks argreduce_with_plan() applies to a plan, against the given device
+ * properties instead of the current device's: path, CTA size, lanes per row,
+ * loads in flight, flags (each only on the paths it applies to), grid limits
+ * and the cluster size (ARGR_EUNSUPPORTED above caps->max_cluster). Covers the
+ * last-axis paths (NONE, ROWS, SPLIT, CLUSTER, STREAM). rows_aligned != 0 says
+ * every row of the input starts on a 16-byte boundary (vector loads allowed).
+ * Returns ARGR_OK, ARGR_EINVAL or ARGR_EUNSUPPORTED as argreduce_with_plan()
+ * would; pure host code (#32092 Testing: every dispatch path, simulated device
+ * capacities), so forced plans can be checked without a GPU.
+ */
+argr_status argreduce_plan_check(const argr_plan* plan, int64_t rows, int64_t cols, argr_dtype dtype,
+                                 const argr_caps* caps, int rows_aligned);
+
+/*
  * ArgMax / ArgMin over a non-last axis: x is row-major [outer, reduce, inner]
  * and the result is out_idx[outer, inner] (int64, the position along the
  * reduced axis), out_val[outer, inner] optional. Element (o, r, i) is at

@@ -19,13 +19,14 @@ from ._lib import (ARGR_BF16, ARGR_F16, ARGR_F32, ARGR_F64, ARGR_MAX, ARGR_MIN, 
                    ARGR_OK, ArgreduceError, DTYPE_CODES, OP_CODES, argr_caps, argr_plan, argreduce_axis_plan,
                    argreduce_cum_plan, argreduce_cum_scratch_bytes,
                    argreduce_device_caps,
-                   argreduce_plan, argreduce_plan_scratch_bytes, argreduce_read_error, argreduce_scratch_bytes,
+                   argreduce_plan, argreduce_plan_check, argreduce_plan_scratch_bytes, argreduce_read_error,
+                   argreduce_scratch_bytes,
                    argreduce_scratch_init, argreduce_status_string, argreduce_version, load, make_caps)
 
 __all__ = [
     "argreduce", "argreduce_axis", "argreduce_axis_plan", "argreduce_cum", "argreduce_cum_plan",
     "argreduce_cum_scratch_bytes", "cummax", "cummin",
-    "argmax", "argmin", "argreduce_with_plan", "argreduce_plan", "argreduce_scratch_bytes",
+    "argmax", "argmin", "argreduce_with_plan", "argreduce_plan", "argreduce_plan_check", "argreduce_scratch_bytes",
     "argreduce_scratch_init", "argreduce_read_error", "argreduce_device_caps", "argreduce_status_string",
     "argreduce_version", "argreduce_plan_scratch_bytes", "ArgreduceError", "Scratch", "make_caps",
 ]

@@ -39,7 +39,7 @@ EXPORTS = (
     "argreduce_with_plan", "argreduce_plan_scratch_bytes", "argreduce_read_error",
     "argreduce_device_caps", "argreduce_status_string", "argreduce_version", "argreduce_noalloc",
     "argreduce_axis", "argreduce_axis_plan", "argreduce_axis_with_plan", "argreduce_cum", "argreduce_cum_plan",
-    "argreduce_cum_with_plan", "argreduce_cum_scratch_bytes",
+    "argreduce_cum_with_plan", "argreduce_cum_scratch_bytes", "argreduce_plan_check",
 )
 
 
@@ -97,6 +97,8 @@ def load() -> ctypes.CDLL:
         lib.argreduce_plan.restype = i32
         lib.argreduce_with_plan.argtypes = [ctypes.POINTER(argr_plan), vp, i32, i64, i64, i32, vp, vp, vp, sz, vp]
         lib.argreduce_with_plan.restype = i32
+        lib.argreduce_plan_check.argtypes = [ctypes.POINTER(argr_plan), i64, i64, i32, ctypes.POINTER(argr_caps), i32]
+        lib.argreduce_plan_check.restype = i32
         lib.argreduce_plan_scratch_bytes.argtypes = [ctypes.POINTER(argr_plan), i64]
         lib.argreduce_plan_scratch_bytes.restype = sz
         lib.argreduce_read_error.argtypes = [vp, vp]
@@ -188,6 +190,14 @@ def argreduce_plan(rows: int, cols: int, dtype, op, caps: Optional[argr_caps] = 
     if st != ARGR_OK:
         raise ArgreduceError(st, "argreduce_plan")
     return p
+
+
+def argreduce_plan_check(plan: argr_plan, rows: int, cols: int, dtype, caps: argr_caps,
+                         rows_aligned: bool = True) -> int:
+    """Status argreduce_with_plan() would give this plan on a device with `caps`
+    (no GPU needed)."""
+    return load().argreduce_plan_check(ctypes.byref(plan), rows, cols, _code(DTYPE_CODES, dtype),
+                                       ctypes.byref(caps), 1 if rows_aligned else 0)
 
 
 def argreduce_axis_raw(x_ptr: int, dtype, outer: int, reduce: int, inner: int, op, out_idx_ptr: int,

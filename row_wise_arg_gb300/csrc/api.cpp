@@ -185,6 +185,12 @@ argr_status argreduce_with_plan(const argr_plan* plan, const void* x, argr_dtype
     return run(*plan, make_problem(x, dtype, rows, cols, op, out_idx, out_val, scratch, stream), scratch_bytes);
 }
 
+argr_status argreduce_plan_check(const argr_plan* plan, int64_t rows, int64_t cols, argr_dtype dtype,
+                                 const argr_caps* caps, int rows_aligned) {
+    if (!plan || !caps) return ARGR_EINVAL;
+    return check_plan(*plan, rows, cols, dtype, *caps, rows_aligned != 0);
+}
+
 // ---------------------------------------------------------------------------
 // Reduction over a non-last axis.
 // ---------------------------------------------------------------------------

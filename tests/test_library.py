@@ -693,3 +693,54 @@ def test_warp_collectives_not_short_circuited():
             if pat.search(code):
                 bad.append(f"{os.path.basename(path)}:{n}: {line.strip()}")
     assert not bad, bad
+
+
+def test_plan_check_without_a_gpu():
+    """argreduce_plan_check() applies argreduce_with_plan()'s checks against
+    simulated device properties: the planner's own plans always pass, and each
+    rule of a forced plan is enforced (ARGR_PLAN_PIPELINE only on vector rows
+    plans with 16 or 32 lanes and at most 256 threads)."""
+    from row_wise_arg_gb300 import _lib as L
+    rng = np.random.Generator(np.random.PCG64(77))
+    shapes = CONFIG_SHAPES + [(1, 1), (3, 7), (2, 5000), (70000, 3), (1024, 4096), (256, 8192), (512, 8192)]
+    shapes += [(int(rng.integers(1, 5000)), int(rng.integers(1, 300000))) for _ in range(40)]
+    for caps in (GB300, H200_LIKE, TINY):
+        for dt in ("f32", "f16", "bf16", "f64"):
+            for rows, cols in shapes:
+                p = A.argreduce_plan(rows, cols, dt, "max", caps)
+                assert A.argreduce_plan_check(p, rows, cols, dt, caps) == L.ARGR_OK, (rows, cols, dt, p)
+
+    def rows_plan(group=32, vec=1, block=128, unroll=4, pipe=True):
+        p = L.argr_plan()
+        p.path, p.group, p.vec, p.block, p.unroll = L.ARGR_PATH_ROWS, group, vec, block, unroll
+        p.flags = L.ARGR_PLAN_PDL | (L.ARGR_PLAN_PIPELINE if pipe else 0)
+        p.grid_rows, p.blocks_per_row = 64, 1
+        return p
+
+    chk = lambda p, aligned=True, rows=4096, cols=4096: A.argreduce_plan_check(p, rows, cols, "f32", GB300, aligned)
+    assert chk(rows_plan()) == L.ARGR_OK
+    assert chk(rows_plan(group=16, block=256, unroll=8)) == L.ARGR_OK
+    assert chk(rows_plan(group=8)) == L.ARGR_EINVAL          # pipelined: 16 or 32 lanes per row
+    assert chk(rows_plan(vec=0)) == L.ARGR_EINVAL            # pipelined: vector loads only
+    assert chk(rows_plan(block=512)) == L.ARGR_EINVAL        # pipelined: at most 256 threads
+    assert chk(rows_plan(pipe=False, block=512)) == L.ARGR_OK
+    assert chk(rows_plan(pipe=False), aligned=False) == L.ARGR_EINVAL  # vector loads need aligned rows
+    assert chk(rows_plan(pipe=False, vec=0), aligned=False) == L.ARGR_OK
+    assert chk(rows_plan(pipe=False, unroll=5)) == L.ARGR_EINVAL
+    assert chk(rows_plan(pipe=False, group=3)) == L.ARGR_EINVAL
+    assert chk(rows_plan(), rows=0) == L.ARGR_OK             # nothing to launch
+    sp = L.argr_plan()
+    sp.path, sp.block, sp.unroll, sp.blocks_per_row, sp.grid_rows = L.ARGR_PATH_SPLIT, 256, 4, 4, 4
+    sp.flags = L.ARGR_PLAN_PDL
+    assert chk(sp, rows=4, cols=1 << 20) == L.ARGR_OK
+    sp.flags |= L.ARGR_PLAN_PIPELINE
+    assert chk(sp, rows=4, cols=1 << 20) == L.ARGR_EINVAL    # pipelining is a rows-path flag
+    sp.flags = L.ARGR_PLAN_PDL
+    sp.grid_rows = 2
+    assert chk(sp, rows=4, cols=1 << 20) == L.ARGR_EINVAL    # a split row may not loop
+    cp = L.argr_plan()
+    cp.path, cp.block, cp.unroll, cp.cluster, cp.blocks_per_row, cp.grid_rows = L.ARGR_PATH_CLUSTER, 512, 8, 16, 16, 1
+    assert chk(cp, rows=1, cols=202048) == L.ARGR_OK
+    assert A.argreduce_plan_check(cp, 1, 202048, "f32", A.make_caps(152, max_cluster=8)) == L.ARGR_EUNSUPPORTED
+    cp.cluster = cp.blocks_per_row = 17
+    assert chk(cp, rows=1, cols=202048) == L.ARGR_EINVAL
