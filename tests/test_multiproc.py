@@ -32,9 +32,11 @@ def _worker(rank, world, port, out_dir):
     dist.destroy_process_group()
 
 
-def test_max_over_ranks_gloo(tmp_path):
+def test_max_over_ranks_gloo(tmp_path, monkeypatch):
     torch = pytest.importorskip("torch")
     import torch.multiprocessing as mp
+    # CPU ranks: no GPU is visible to them, also where one is present
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "")
     mp.start_processes(_worker, args=(2, free_port(), str(tmp_path)), nprocs=2, start_method="spawn")
     for rank in range(2):
         d = json.load(open(tmp_path / f"rank{rank}.json"))
@@ -49,7 +51,7 @@ def test_reference_arm_under_torchrun():
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(free_port()), "bench.py", "--impl", "reference",
            "--gpus", "2", "--steps", "4", "--warmup", "3"]
-    env = dict(os.environ, OMP_NUM_THREADS="1")
+    env = dict(os.environ, OMP_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")  # CPU ranks, also on a GPU machine
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
