@@ -744,3 +744,20 @@ def test_plan_check_without_a_gpu():
     assert A.argreduce_plan_check(cp, 1, 202048, "f32", A.make_caps(152, max_cluster=8)) == L.ARGR_EUNSUPPORTED
     cp.cluster = cp.blocks_per_row = 17
     assert chk(cp, rows=1, cols=202048) == L.ARGR_EINVAL
+
+
+def test_bench_thread_per_row_plans_are_valid():
+    """The thread-per-row plans bench.py times beside the narrow configs pass the
+    library's own plan checks (scalar loads always, vector loads on aligned rows)."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    from row_wise_arg_gb300 import _lib as L
+    for c in W.config_cases(5):
+        aligned = c.cols * W.ELEM_SIZE[c.dtype] % 16 == 0
+        for vec in (False, True):
+            p = bench.ThreadPerRowCalls(A, [c], vec).plans[0]
+            assert p.group == 1 and p.path == L.ARGR_PATH_ROWS
+            want = L.ARGR_OK if (aligned or not vec) else L.ARGR_EINVAL
+            assert A.argreduce_plan_check(p, c.rows, c.cols, c.dtype, GB300, aligned) == want, (c.name, vec)
