@@ -509,11 +509,13 @@ def test_cum_plans_and_validation():
             total = rows * chunks
             assert d["scratch_bytes"] == (256 if total <= 1024 else 1 << 20) + 8 * total
         elif d["path_name"] == "cum_split":
-            # long rows, fewer than the SMs: 76..304 CTAs, records of one launch <= 1024
+            # long rows, fewer than the SMs: 76..304 CTAs (38 for one row of <= 64K
+            # elements), records of one launch <= 1024
             chunks = d["blocks_per_row"]
             assert rows < 152 and chunks >= 2 and rows * chunks <= 1024 and cols > 32768
             assert rows * chunks <= (2 * 152 + 1 if rows == 1 else 1024)
-            assert rows * chunks >= 76 or cols // chunks < 1024 or chunks == 1024 // rows
+            floor = 38 if rows == 1 and cols <= 65536 else 76
+            assert rows * chunks >= floor or cols // chunks < 1024 or chunks == 1024 // rows
             assert cols // chunks >= 512
             cap = 512 if rows == 1 else 128
             assert d["block"] in (64, 128, 256, 512) and d["block"] <= cap
@@ -536,7 +538,9 @@ def test_cum_plans_and_validation():
     assert seen == {("cum_split", False), ("cum", True), ("cum", False)}
     big = A.argreduce_cum_plan(1, 16777216, "i64", "max", GB300).as_dict()
     assert big["blocks_per_row"] == 304 and big["flags"] & 8 == 0  # the stash is a forced-plan option
-    assert A.argreduce_cum_plan(1, 65536, "i64", "max", GB300).as_dict()["blocks_per_row"] == 76
+    d = A.argreduce_cum_plan(1, 65536, "i64", "max", GB300).as_dict()  # the pages' 65536-element int64 row
+    assert d["blocks_per_row"] == 38 and d["block"] == 256
+    assert A.argreduce_cum_plan(1, 131072, "i64", "max", GB300).as_dict()["blocks_per_row"] == 76
     assert A.argreduce_cum_plan(4, 16384, "i32", "max", GB300).as_dict()["cluster"] == 16
     assert A.argreduce_cum_plan(4096, 4096, "f32", "max", GB300).as_dict()["block"] == 128
     assert A.argreduce_cum_plan(65536, 256, "f32", "max", GB300).as_dict()["block"] == 32
