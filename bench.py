@@ -191,6 +191,71 @@ def read_traffic(workload: str):
     return None
 
 
+def read_config_traffic():
+    """Per-case ncu figures of the reduction configs, from the committed
+    summary, if taken on the current kernel and planner sources: {case name:
+    (DRAM bytes per launch, kernel ns per launch)}."""
+    p = os.path.join(ROOT, "profiles", "traffic_configs.txt")
+    if not os.path.exists(p):
+        return {}
+    src = kernel_source_hash("wide_rows")
+    out = {}
+    for line in open(p):
+        parts = line.split()
+        if line.startswith("#") or len(parts) < 4:
+            continue
+        if parts[3] == src:
+            out[parts[0]] = (float(parts[1]), float(parts[2]))
+    return out
+
+
+def config_group_cases(groups=range(1, 6)):
+    """The reduction configs' cases as the per-config table lists them: the
+    duplicated-extreme variants of the wide rows are left out (same shape and
+    time as the unique ones)."""
+    return [c for g in groups for c in W.config_cases(g) if c.variant != "dup"]
+
+
+def ncu_cases(torch, A):
+    """One planner call per reduction config case, in table order, each on
+    its own freshly allocated input (for one ncu capture of every case: the
+    i-th captured launch is the i-th case printed)."""
+    for c in config_group_cases():
+        x = W.make(c)
+        d = to_dev(torch, x, c.dtype).view(c.rows, c.cols)
+        out = torch.empty(c.rows, dtype=torch.int64, device="cuda")
+        A.argreduce(d, c.op, dtype=c.dtype, out_idx=out)
+        torch.cuda.synchronize()
+        print(c.name, flush=True)
+        del d, out
+
+
+def summarize_ncu(csv_path: str):
+    """Turn an ncu CSV of `--ncu-cases` (metrics dram__bytes_read.sum,
+    dram__bytes_write.sum, gpu__time_duration.sum) into the lines of
+    profiles/traffic_configs.txt: case, bytes, ns, source hash."""
+    import csv
+    rows = {}
+    with open(csv_path) as f:
+        lines = [l for l in f if l.startswith('"')]
+    for r in csv.DictReader(lines):
+        rid = int(r["ID"])
+        unit = r.get("Metric Unit", "")
+        v = float(r["Metric Value"].replace(",", ""))
+        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6, "GB": 1e9,
+                 "nsecond": 1, "usecond": 1e3, "msecond": 1e6, "ns": 1, "us": 1e3, "ms": 1e6}.get(unit, 1)
+        rows.setdefault(rid, {})[r["Metric Name"]] = v * scale
+    ids = sorted(rows)
+    cases = config_group_cases()
+    if len(ids) != len(cases):
+        raise SystemExit(f"{len(ids)} launches captured for {len(cases)} cases")
+    src = kernel_source_hash("wide_rows")
+    for c, i in zip(cases, ids):
+        m = rows[i]
+        b = m["dram__bytes_read.sum"] + m["dram__bytes_write.sum"]
+        print(f"{c.name} {b:.0f} {m['gpu__time_duration.sum']:.0f} {src}")
+
+
 # ---------------------------------------------------------------------------
 # Clock sampling during the timed region.
 # ---------------------------------------------------------------------------
@@ -424,6 +489,51 @@ def time_group(torch, A, cases, inputs, steps, warmup, stream, dist=None, device
     return secs, replays * per_graph, copies, clk
 
 
+def isolated_time(torch, A, c, x, stream, calls: int = 200) -> float:
+    """Latency of one call on its own: one call per CUDA graph (input copies
+    rotated so every call reads HBM), CUDA events around each replay, the
+    host waiting for each before the next; the median in microseconds. Each
+    figure includes the graph launch's own device-side cost."""
+    copies = max(1, min(64, copies_for([c])))
+    dev = [to_dev(torch, x, c.dtype).reshape(-1)]
+    gs = GraphSet(torch, A, [c], dev, copies, 1, stream)
+    ts = []
+    with torch.cuda.stream(stream):
+        for k in range(calls + 5):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gs.graphs[k % len(gs.graphs)].replay()
+            e1.record(stream)
+            e1.synchronize()
+            if k >= 5:
+                ts.append(e0.elapsed_time(e1) * 1e3)
+    del gs, dev
+    return statistics.median(ts)
+
+
+def cpu_time(c: W.Case, x, budget_s: float = 0.3):
+    """The oracle as it stands on one case: all host cores over rows for the
+    many-row reductions, one core otherwise; repeated until `budget_s`.
+    Returns (us per call, cores)."""
+    import oracle
+    t0 = time.perf_counter()
+    n = 0
+    cores = 1
+    while True:
+        if is_scan(c):
+            oracle.cumreduce(x, c.dtype, c.op, want_val=True)
+        elif c.inner > 1:
+            oracle.argreduce_axis(x, c.dtype, c.op, want_val=False)
+        else:
+            threads = min(os.cpu_count() or 1, c.rows) if c.rows > 1 else 1
+            _, _, cores = oracle.argreduce(x, c.dtype, c.op, threads=threads, want_val=False)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return el * 1e6 / n, cores
+
+
 def cub_compare(torch, A, cases, inputs, steps, stream, ours_us):
     """cub::DeviceReduce::ArgMax/ArgMin, called as a library, timed exactly as
     the step above (same inputs, copies, graphs and events); its indices are
@@ -547,6 +657,77 @@ def e2e_time(torch, A, cases, inputs, steps, stream, depth=2):
     return e0.elapsed_time(e1) / 1e3, wall, eager, h2d, d2h
 
 
+def config_table(torch, A, args, stream, peak):
+    """Every workload case (the reductions' configs 1-5 in both tie rules, the
+    non-last axis, the scans), timed like the step (graphs of about 16 calls
+    on rotating L2-cold inputs), plus for each: its isolated single-call
+    latency, the oracle's time on the host cores, and the ncu DRAM figures of
+    profiles/traffic_configs.txt where they match the sources. Returns (the
+    full table, a compact one of configs 1-5)."""
+    table, compact = [], []
+    traffic = read_config_traffic()
+    for name, (g, _) in sorted(WORKLOADS.items(), key=lambda kv: kv[1][0]):
+        if g < 0:
+            continue
+        gcases = W.config_cases(g)
+        ginputs = [W.make(c) for c in gcases]
+        for c0, x in zip(gcases, ginputs):
+            if c0.variant == "dup":
+                continue
+            # each case as written, and the same rows with ties to the last index
+            variants = [c0] if is_scan(c0) else [c0, dataclasses.replace(c0, op=c0.op + "_last",
+                                                                         name=c0.name + "_last")]
+            for c in variants:
+                n = max(20, min(4000, int(2e9 / max(c.nbytes, 1) / 50)))
+                s, n, cp, _ = time_group(torch, A, [c], [x], n, 5, stream, exact=False)
+                us = s * 1e6 / n
+                gbs = algo_bytes(c) / (s / n) / 1e9
+                plan = (A.argreduce_cum_plan(c.rows, c.cols, c.dtype, c.op) if is_scan(c) else
+                        A.argreduce_axis_plan(c.rows, c.cols, c.inner, c.dtype, c.op))
+                path = plan.as_dict()["path_name"]
+                row = {"case": c.name, "us_per_call": round(us, 3), "gbs": round(gbs, 1),
+                       "frac": round(gbs / peak, 4), "path": path}
+                if c is c0:
+                    row["isolated_us"] = round(isolated_time(torch, A, c, x, stream), 3)
+                    if not args.no_cpu_baseline:
+                        cu, cores = cpu_time(c, x)
+                        row["cpu_us_per_call"] = round(cu, 1)
+                        row["cpu_cores"] = cores
+                    if c.name in traffic:
+                        tb, tns = traffic[c.name]
+                        row["ncu_dram_bytes"] = int(tb)
+                        row["ncu_gbs"] = round(tb / tns, 1)
+                        row["ncu_frac"] = round(tb / tns / peak, 4)
+                if not args.no_cub and cub_comparable([c]):
+                    cs, cn, _, _ = time_group(torch, A, [c], [x], n, 5, stream, exact=False,
+                                              cub=CubCalls(torch, [c]))
+                    row["cub_us_per_call"] = round(cs * 1e6 / cn, 3)
+                if name == "narrow":
+                    # the narrow-row target: no slower than a thread-per-row kernel
+                    tpr = {}
+                    aligned = c.cols * W.ELEM_SIZE[c.dtype] % 16 == 0
+                    for label, vec in (("scalar_loads", False), ("vector_loads", True)):
+                        if vec and not aligned:
+                            continue
+                        ts, tn, _, _ = time_group(torch, A, [c], [x], n, 5, stream, exact=False,
+                                                  cub=ThreadPerRowCalls(A, [c], vec))
+                        tpr[label] = round(ts * 1e6 / tn, 3)
+                    row["thread_per_row_us_per_call"] = tpr
+                table.append(row)
+                if c is c0 and 1 <= g <= 5:
+                    short = c.name.split("_", 1)[1].replace("_unique", "")
+                    item = f"{short} {row['us_per_call']:.2f} {row['frac']:.3f} {path[:2]} iso{row['isolated_us']:.2f}"
+                    if "cpu_us_per_call" in row:
+                        item += f" cpu{row['cpu_us_per_call']:.0f}/{row['cpu_cores']}"
+                    if "ncu_frac" in row:
+                        item += f" ncu{row['ncu_frac']:.3f}"
+                    compact.append(item)
+        del ginputs
+    legend = ("case: us/call (graphs of ~16 calls, L2-cold inputs), frac of measured HBM peak, path, "
+              "isolated single-call us, oracle us/cores, ncu DRAM frac")
+    return table, {"legend": legend, "rows": compact}
+
+
 # ---------------------------------------------------------------------------
 def reference_arm(args, rank, world, dist):
     """The oracle on host cores, on the same workload and metric."""
@@ -585,9 +766,23 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--e2e-depth", type=int, default=3, help="end-to-end steps in flight (graphs in rotation)")
     ap.add_argument("--no-cub", action="store_true", help="skip the cub::DeviceReduce timing comparison")
+    ap.add_argument("--ncu-cases", action="store_true",
+                    help="no timing: one planner call per reduction config case, for an ncu capture")
+    ap.add_argument("--ncu-summarize", metavar="CSV",
+                    help="no GPU: print profiles/traffic_configs.txt lines from an ncu CSV of --ncu-cases")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.ncu_summarize:
+        summarize_ncu(args.ncu_summarize)
+        return 0
+    if args.ncu_cases:
+        import torch
+        from row_wise_arg_gb300.build import build
+        build()
+        import row_wise_arg_gb300 as A
+        ncu_cases(torch, A)
+        return 0
 
     rank, world, local, dist = dist_setup(args.gpus)
     if args.impl == "reference":
@@ -670,52 +865,17 @@ def main():
     if not args.no_cub and cub_comparable(cases) and (world == 1 or rank == 0):
         result["cub_compare"] = cub_compare(torch, A, cases, inputs, min(args.steps, 4000), stream, us_per_call)
 
-    if not args.no_configs and (world == 1 or rank == 0):
-        table = []
-        for name, (g, _) in sorted(WORKLOADS.items(), key=lambda kv: kv[1][0]):
-            if g < 0:
-                continue
-            gcases = W.config_cases(g)
-            ginputs = [W.make(c) for c in gcases]
-            for c0, x in zip(gcases, ginputs):
-                if c0.variant == "dup":
-                    continue
-                # each case as written, and the same rows with ties to the last index
-                variants = [c0] if is_scan(c0) else [c0, dataclasses.replace(c0, op=c0.op + "_last",
-                                                                             name=c0.name + "_last")]
-                for c in variants:
-                    n = max(20, min(4000, int(2e9 / max(c.nbytes, 1) / 50)))
-                    s, n, cp, _ = time_group(torch, A, [c], [x], n, 5, stream, exact=False)
-                    us = s * 1e6 / n
-                    gbs = algo_bytes(c) / (s / n) / 1e9
-                    plan = (A.argreduce_cum_plan(c.rows, c.cols, c.dtype, c.op) if is_scan(c) else
-                            A.argreduce_axis_plan(c.rows, c.cols, c.inner, c.dtype, c.op))
-                    row = {"case": c.name, "us_per_call": round(us, 3), "gbs": round(gbs, 1),
-                           "frac": round(gbs / peak, 4), "path": plan.as_dict()["path_name"]}
-                    if not args.no_cub and cub_comparable([c]):
-                        cs, cn, _, _ = time_group(torch, A, [c], [x], n, 5, stream, exact=False,
-                                                  cub=CubCalls(torch, [c]))
-                        row["cub_us_per_call"] = round(cs * 1e6 / cn, 3)
-                    if name == "narrow":
-                        # the narrow-row target: no slower than a thread-per-row kernel
-                        tpr = {}
-                        aligned = c.cols * W.ELEM_SIZE[c.dtype] % 16 == 0
-                        for label, vec in (("scalar_loads", False), ("vector_loads", True)):
-                            if vec and not aligned:
-                                continue
-                            ts, tn, _, _ = time_group(torch, A, [c], [x], n, 5, stream, exact=False,
-                                                      cub=ThreadPerRowCalls(A, [c], vec))
-                            tpr[label] = round(ts * 1e6 / tn, 3)
-                        row["thread_per_row_us_per_call"] = tpr
-                    table.append(row)
-            del ginputs
-        result["configs"] = table
-
     if not args.no_cpu_baseline and (world == 1 or rank == 0):
         us, ncalls, cores, el = oracle_time(cases, inputs, args.cpu_budget)
         result["cpu_baseline"] = {"value": round(us, 3), "unit": "us/call", "cores": cores, "kind": "oracle",
                                   "sample": f"{ncalls} oracle calls cycling over the {len(cases)} cases of the "
                                             f"step on host cores ({el:.1f} s)"}
+
+    if not args.no_configs and (world == 1 or rank == 0):
+        result["configs"], compact = config_table(torch, A, args, stream, peak)
+        # printed last, so that the per-config figures of the reduction
+        # configs survive a reader that keeps only the end of the line
+        result["configs_compact"] = compact
 
     if world == 1 or rank == 0:
         print(json.dumps(result), flush=True)

@@ -133,6 +133,14 @@ typedef struct {
  * compares the current batch, so its loads stay in flight while it compares;
  * twice the registers for loaded data, so at most 256 threads per CTA. */
 #define ARGR_PLAN_PIPELINE 32
+/* Plan flag (ROWS, SPLIT and CLUSTER paths): before its dependency wait, each
+ * CTA asks the L2 cache to fetch the part of x it reads first (bulk L2
+ * prefetches of 16-byte aligned pieces). A prefetch changes no value (L2 is
+ * where the GPU keeps memory coherent, so a line written by the previous
+ * grid is read as written), so results are the same; when the CTA starts
+ * while the previous grid in the stream is still running (ARGR_PLAN_PDL),
+ * the read of x from HBM overlaps that grid instead of following it. */
+#define ARGR_PLAN_PREFETCH 64
 
 /* A launch plan. Produced by argreduce_plan(); tests may edit it to force a
  * path and pass it to argreduce_with_plan(), which re-validates it. */
@@ -176,7 +184,10 @@ size_t argreduce_scratch_bytes(int64_t rows, int64_t cols, argr_dtype dtype, arg
 argr_status argreduce_scratch_init(void* scratch, size_t scratch_bytes, argr_stream stream);
 
 /*
- * Row-wise ArgMax (op = ARGR_MAX) or ArgMin (ARGR_MIN) of x[rows, cols].
+ * Row-wise ArgMax (op = ARGR_MAX) or ArgMin (ARGR_MIN) of x[rows, cols]
+ * (onnxruntime #32092, Approach: one int64 index per row of the last axis,
+ * chosen by a planner among thread-per-row, block-per-row and multi-block
+ * kernels; Semantics: the sequential first-occurrence scan, bit for bit).
  *
  *   x         device pointer to rows*cols elements of `dtype`, row-major and
  *             contiguous (row r starts at element r*cols). Any address that is
@@ -301,6 +312,10 @@ argr_status argreduce_cum_with_plan(const argr_plan* plan, const void* x, argr_d
 size_t argreduce_plan_scratch_bytes(const argr_plan* plan, int64_t rows);
 
 /*
+ * Failure reporting for the bounded device-side waits (onnxruntime #32092,
+ * Testing: forced dispatch paths must neither hang nor silently corrupt; the
+ * scan's waits follow Paddle issue #79670, "Possible fixes", whose two-pass
+ * scan hands chunk totals from one CTA to the next).
  * Synchronise `stream` and read the library's device error words (set by a
  * kernel whose bounded wait expired: for a bulk copy, after which the kernel
  * skips the rest of its work, or for another CTA's chunk record in the split
@@ -331,13 +346,20 @@ argr_status argreduce_read_error(void* scratch, argr_stream stream);
  *
  *   - The first call on each device (with that device current) finds the
  *     array's device address and zeroes it, synchronously. Make that first
- *     call before capturing any stream on the device.
- *   - Every call reuses the same array: two calls that can overlap on the GPU
- *     (other streams, other host threads) race on it and give wrong results;
- *     serialise them. Each call clears the counters it uses before its kernel.
+ *     call before capturing any stream on the device. The address is kept
+ *     for the device's primary context: after cudaDeviceReset(), or with a
+ *     context other than the primary one current, it is stale, so do not
+ *     call this entry point there.
+ *   - Every call reuses the same array, which keeps what the last call left:
+ *     two calls that can overlap on the GPU (other streams, other host
+ *     threads) race on it and give wrong results; serialise them. No call
+ *     clears it: each row's arrival counter is bumped with a wrapping
+ *     increment that leaves it at zero when the row's last CTA arrives, and
+ *     every partial is written before it is read.
  *   - A problem whose plan needs more than the array holds returns
  *     ARGR_ESCRATCH before anything is queued (on a GB300 every shape fits).
- *   - Other errors as for argreduce().
+ *   - Other errors as for argreduce(), checked before anything is queued:
+ *     ARGR_EUNSUPPORTED for the integer types, ARGR_EINVAL for the rest.
  */
 argr_status argreduce_noalloc(const void* x, argr_dtype dtype, int64_t rows, int64_t cols, argr_op op,
                               int64_t* out_idx, void* out_val, argr_stream stream);

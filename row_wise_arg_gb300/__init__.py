@@ -76,7 +76,12 @@ def _stream_ptr(stream, device_index: int) -> int:
 class Scratch:
     """Device scratch for one stream, grown on demand and prepared with
     argreduce_scratch_init() whenever it is (re)allocated. Two calls that can
-    run concurrently on the GPU must use different Scratch objects."""
+    run concurrently on the GPU must use different Scratch objects.
+
+    A buffer, once handed to a call, stays allocated for the lifetime of the
+    Scratch even after a larger one replaces it: a CUDA graph captured with
+    the smaller buffer still holds its address, so it must not go back to
+    torch's allocator while the graph may be replayed."""
 
     def __init__(self, device=None, nbytes: int = 0):
         torch = _torch()
@@ -84,6 +89,7 @@ class Scratch:
                                    torch.device(device).index or 0)
         self.buf = None
         self.nbytes = 0
+        self.retired = []  # buffers replaced by larger ones, kept alive (see above)
         if nbytes:
             self.ensure(nbytes, torch.cuda.current_stream(self.device).cuda_stream)
 
@@ -91,11 +97,19 @@ class Scratch:
         if nbytes <= self.nbytes:
             return
         torch = _torch()
-        n = max(nbytes, 4096)
-        self.buf = torch.empty(n, dtype=torch.uint8, device=self.device)
-        st = argreduce_scratch_init(self.buf.data_ptr(), n, stream_ptr)
+        if torch.cuda.is_current_stream_capturing():
+            # the preparing memset would be recorded into the graph instead of
+            # running now, leaving the new buffer unprepared for eager calls
+            raise RuntimeError("argreduce scratch must grow before a CUDA graph capture: make one call of the "
+                               "largest problem (or pass a Scratch of enough bytes) before capturing")
+        n = max(nbytes, 4096, 2 * self.nbytes)  # geometric growth: few buffers are ever retired
+        buf = torch.empty(n, dtype=torch.uint8, device=self.device)
+        st = argreduce_scratch_init(buf.data_ptr(), n, stream_ptr)
         if st != ARGR_OK:
             raise ArgreduceError(st, "argreduce_scratch_init")
+        if self.buf is not None:
+            self.retired.append(self.buf)
+        self.buf = buf
         self.nbytes = n
 
     @property

@@ -1,6 +1,8 @@
 // Timing comparison only: cub::DeviceReduce::ArgMax / ArgMin on one row
-// [1, n], called as a library (onnxruntime PR #32092, Results: CUB's
-// device-wide ArgMax is the other reference point for a single wide row).
+// [1, n], called as a library (onnxruntime PR #32092, Profile: after the
+// profile of [1, 202048] the PR compares its kernel with
+// cub::DeviceReduce::ArgMax on the same GPU and shape, the other reference
+// point for a single wide row).
 // Built into its own libcubcompare.so, which the benchmark and one GPU test
 // load; nothing in libargreduce.so uses it.
 //

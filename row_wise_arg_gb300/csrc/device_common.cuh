@@ -170,6 +170,35 @@ __device__ __forceinline__ void visit(Cand<Tag>& c, typename Tag::raw x, int j) 
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// L2 prefetch (ARGR_PLAN_PREFETCH). A kernel may issue it before its
+// dependency wait: a prefetch moves lines of HBM into L2, which is where this
+// GPU keeps global memory coherent, so it changes no value a later load sees
+// (a line the previous grid writes is read as written). When the CTA is
+// resident while the previous grid still runs, its input streams from HBM
+// into L2 during that grid instead of after it.
+constexpr uintptr_t kPrefetchMinPiece = 4096;         // bytes per bulk prefetch, at least
+constexpr uintptr_t kPrefetchMaxBytes = 128 * 1024;   // bytes one CTA prefetches, at most
+
+// One bulk prefetch of n bytes at p; p 16-byte aligned, n a positive multiple of 16.
+__device__ __forceinline__ void prefetch_l2_bulk(uintptr_t p, unsigned n) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(n) : "memory");
+}
+
+// Prefetch the bytes [lo, hi) of global memory, shrunk to 16-byte boundaries
+// and to the first kPrefetchMaxBytes: pieces of at least kPrefetchMinPiece
+// bytes, one per warp of the CTA, each issued by the warp's lane 0.
+__device__ __forceinline__ void prefetch_l2_range(const void* lo, const void* hi) {
+    const uintptr_t a = (reinterpret_cast<uintptr_t>(lo) + 15) & ~static_cast<uintptr_t>(15);
+    uintptr_t b = reinterpret_cast<uintptr_t>(hi) & ~static_cast<uintptr_t>(15);
+    if ((threadIdx.x & 31) != 0 || b <= a) return;
+    if (b - a > kPrefetchMaxBytes) b = a + kPrefetchMaxBytes;
+    const uintptr_t nw = (blockDim.x + 31) >> 5;
+    uintptr_t piece = ((b - a + nw - 1) / nw + 15) & ~static_cast<uintptr_t>(15);
+    if (piece < kPrefetchMinPiece) piece = kPrefetchMinPiece;
+    const uintptr_t s = a + (threadIdx.x >> 5) * piece;  // one piece per warp covers [a, b)
+    if (s < b) prefetch_l2_bulk(s, static_cast<unsigned>(b - s < piece ? b - s : piece));
+}
+
 // Merge of two candidates: better key wins; equal keys keep the lower index
 // (the higher index for the last-occurrence ops).
 template <class Tag, int OP>

@@ -42,16 +42,27 @@ namespace argr {
 template <class Tag, int OP, int G, bool VEC, int U, bool PIPE>
 __global__ void __launch_bounds__(PIPE ? kPipeMaxBlock : 1024)
 rows_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int64_t* __restrict__ out_idx,
-            typename Tag::raw* __restrict__ out_val) {
+            typename Tag::raw* __restrict__ out_val, bool prefetch) {
     using R = typename Tag::raw;
     constexpr int E = 16 / sizeof(R);
-    grid_dependency_wait();
-    allow_dependents();
     const int lg = threadIdx.x & (G - 1);
     const int lane = threadIdx.x & 31;
     const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
     const int groups_per_block = blockDim.x / G;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * groups_per_block;
+    if (prefetch) {
+        // the rows of this CTA's first step, before waiting for the previous grid
+        allow_dependents();
+        const int64_t r0 = static_cast<int64_t>(blockIdx.x) * groups_per_block;
+        if (r0 < rows) {
+            const int64_t r1 = rows - r0 > groups_per_block ? r0 + groups_per_block : rows;
+            prefetch_l2_range(x + r0 * cols, x + r1 * cols);
+        }
+        grid_dependency_wait();
+    } else {
+        grid_dependency_wait();
+        allow_dependents();
+    }
 
     for (int64_t r = static_cast<int64_t>(blockIdx.x) * groups_per_block + threadIdx.x / G; r < rows;
          r += stride) {
@@ -149,20 +160,44 @@ rows_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int
 // the body; CTA 0 also owns the head and CTA nb-1 the tail. Each thread visits
 // its elements in increasing index order (head, body, tail).
 // ---------------------------------------------------------------------------
+struct ShareBounds {
+    int head;  // elements before the first 16-byte boundary of the row
+    int nvec;  // 16-byte vectors of the body
+    int vb;    // this CTA's body vectors: [vb, ve)
+    int ve;
+};
+
+template <typename R>
+__device__ __forceinline__ ShareBounds share_bounds(const R* row, int cols, int b, int nb) {
+    constexpr int E = 16 / sizeof(R);
+    ShareBounds s;
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
+    s.head = static_cast<int>(((16u - (addr & 15u)) & 15u) / sizeof(R));
+    if (s.head > cols) s.head = cols;
+    s.nvec = (cols - s.head) / E;
+    const int chunk = s.nvec / nb + (s.nvec % nb != 0);
+    s.vb = b * chunk < s.nvec ? b * chunk : s.nvec;
+    s.ve = s.nvec - s.vb > chunk ? s.vb + chunk : s.nvec;
+    return s;
+}
+
+// L2 prefetch of CTA b's body vectors of a row (ARGR_PLAN_PREFETCH).
+template <typename R>
+__device__ __forceinline__ void prefetch_share(const R* row, int cols, int b, int nb) {
+    const ShareBounds s = share_bounds(row, cols, b, nb);
+    const uint4* rv = reinterpret_cast<const uint4*>(row + s.head);
+    prefetch_l2_range(rv + s.vb, rv + s.ve);
+}
+
 template <class Tag, int OP, int U>
 __device__ __forceinline__ Cand<Tag> scan_share(const typename Tag::raw* __restrict__ row, int cols, int b, int nb,
                                                 typename Tag::raw x0) {
     using R = typename Tag::raw;
     constexpr int E = 16 / sizeof(R);
-    const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
-    int head = static_cast<int>(((16u - (addr & 15u)) & 15u) / sizeof(R));
-    if (head > cols) head = cols;
-    const int nvec = (cols - head) / E;
+    const ShareBounds sb = share_bounds(row, cols, b, nb);
+    const int head = sb.head, nvec = sb.nvec, vb = sb.vb, ve = sb.ve;
     const int tail0 = head + nvec * E;
     const uint4* rv = reinterpret_cast<const uint4*>(row + head);
-    const int chunk = nvec / nb + (nvec % nb != 0);
-    const int vb = b * chunk < nvec ? b * chunk : nvec;
-    const int ve = nvec - vb > chunk ? vb + chunk : nvec;
 
     Cand<Tag> c = make_cand<Tag, OP>(x0, 0);
     const int t = threadIdx.x;
@@ -241,14 +276,20 @@ __device__ __forceinline__ uint4 ld_relaxed_gpu(const uint4* p) {
 template <class Tag, int OP, int U>
 __global__ void __launch_bounds__(1024)
 split_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int64_t* __restrict__ out_idx,
-             typename Tag::raw* __restrict__ out_val, unsigned char* __restrict__ scratch) {
+             typename Tag::raw* __restrict__ out_val, unsigned char* __restrict__ scratch, bool prefetch) {
     using R = typename Tag::raw;
     __shared__ Cand<Tag> smem[32];
     const int nb = gridDim.x;
     const int b = blockIdx.x;
     const int lane = threadIdx.x & 31;
-    grid_dependency_wait();
-    allow_dependents();
+    if (prefetch) {
+        allow_dependents();
+        if (blockIdx.y < rows) prefetch_share(x + static_cast<int64_t>(blockIdx.y) * cols, cols, b, nb);
+        grid_dependency_wait();
+    } else {
+        grid_dependency_wait();
+        allow_dependents();
+    }
     for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
         const R* row = x + r * static_cast<int64_t>(cols);
         const R x0 = ld_scalar(row);
@@ -316,7 +357,7 @@ __device__ __forceinline__ void cluster_started_wait() {
 template <class Tag, int OP, int U>
 __global__ void __launch_bounds__(1024)
 cluster_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int64_t* __restrict__ out_idx,
-               typename Tag::raw* __restrict__ out_val) {
+               typename Tag::raw* __restrict__ out_val, bool prefetch) {
     using R = typename Tag::raw;
     __shared__ Cand<Tag> smem[32];
     __shared__ __align__(16) uint4 slots[2][16];  // written by every CTA of the cluster into CTA 0
@@ -325,8 +366,14 @@ cluster_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, 
     int parity = 0;
     bool started = false;
     cluster_started_arrive();
-    grid_dependency_wait();
-    allow_dependents();
+    if (prefetch) {
+        allow_dependents();
+        if (blockIdx.y < rows) prefetch_share(x + static_cast<int64_t>(blockIdx.y) * cols, cols, b, nb);
+        grid_dependency_wait();
+    } else {
+        grid_dependency_wait();
+        allow_dependents();
+    }
     for (int64_t r = blockIdx.y; r < rows; r += gridDim.y, parity ^= 1) {
         const R* row = x + r * static_cast<int64_t>(cols);
         const R x0 = ld_scalar(row);
@@ -987,16 +1034,17 @@ cudaError_t launch_rows_gu(const argr_plan& p, const Problem& pr) {
     const dim3 grid(static_cast<unsigned>(p.grid_rows));
     const R* x = static_cast<const R*>(pr.x);
     R* ov = static_cast<R*>(pr.out_val);
+    const bool pf = (p.flags & ARGR_PLAN_PREFETCH) != 0;
     if constexpr (G >= 16) {
         if (p.flags & ARGR_PLAN_PIPELINE)  // check_plan admits it only with vec and G >= 16
             return launch_ex(rows_kernel<Tag, OP, G, true, U, true>, grid, dim3(p.block), 1, p, pr.stream, x,
-                             pr.rows, pr.cols, pr.out_idx, ov);
+                             pr.rows, pr.cols, pr.out_idx, ov, pf);
     }
     if (p.vec)
         return launch_ex(rows_kernel<Tag, OP, G, true, U, false>, grid, dim3(p.block), 1, p, pr.stream, x, pr.rows,
-                         pr.cols, pr.out_idx, ov);
+                         pr.cols, pr.out_idx, ov, pf);
     return launch_ex(rows_kernel<Tag, OP, G, false, U, false>, grid, dim3(p.block), 1, p, pr.stream, x, pr.rows,
-                     pr.cols, pr.out_idx, ov);
+                     pr.cols, pr.out_idx, ov, pf);
 }
 
 template <class Tag, int OP, int G>
@@ -1034,7 +1082,7 @@ cudaError_t launch_split_u(const argr_plan& p, const Problem& pr) {
     const dim3 grid(static_cast<unsigned>(p.blocks_per_row), static_cast<unsigned>(p.grid_rows));
     return launch_ex(split_kernel<Tag, OP, U>, grid, dim3(p.block), 1, p, pr.stream, static_cast<const R*>(pr.x),
                      pr.rows, pr.cols, pr.out_idx, static_cast<R*>(pr.out_val),
-                     static_cast<unsigned char*>(pr.scratch));
+                     static_cast<unsigned char*>(pr.scratch), (p.flags & ARGR_PLAN_PREFETCH) != 0);
 }
 
 template <class Tag, int OP>
@@ -1075,7 +1123,7 @@ cudaError_t launch_cluster_u(const argr_plan& p, const Problem& pr) {
     if (e != cudaSuccess) return e;
     if (!ok) return cudaErrorInvalidClusterSize;  // reported as ARGR_EUNSUPPORTED
     return launch_ex(kern, grid, dim3(p.block), p.cluster, p, pr.stream, static_cast<const R*>(pr.x), pr.rows,
-                     pr.cols, pr.out_idx, static_cast<R*>(pr.out_val));
+                     pr.cols, pr.out_idx, static_cast<R*>(pr.out_val), (p.flags & ARGR_PLAN_PREFETCH) != 0);
 }
 
 // Dynamic shared memory the bulk cluster kernel needs: the largest share of a

@@ -6,7 +6,13 @@
 // loads it. Host code cannot use the array's name as a device address (on the
 // host the name refers to a host-side shadow), so the first call on each
 // device looks up the real device address with cudaGetSymbolAddress() and
-// zeroes the array once; later calls reuse the cached address.
+// zeroes the array once; later calls reuse the cached address. The address
+// belongs to the device's primary context: after cudaDeviceReset(), or with
+// another context current, it is no longer valid (documented limit).
+//
+// No call clears anything: the split kernel bumps each row's arrival counter
+// with a wrapping increment, so the last CTA of a row leaves it at zero, and
+// the partials are written before they are read in every launch.
 #include <algorithm>
 #include <cstdint>
 #include <mutex>
@@ -52,16 +58,20 @@ argr_status scratch_for_current_device(void** out) {
     return ARGR_OK;
 }
 
-bool valid_args(const void* x, int dtype, int64_t rows, int64_t cols, int op, const int64_t* out_idx,
-                const void* out_val) {
+// The same checks as argreduce(): the integer types are argreduce_cum()'s
+// only (ARGR_EUNSUPPORTED), anything else malformed is ARGR_EINVAL.
+argr_status check_noalloc_args(const void* x, int dtype, int64_t rows, int64_t cols, int op, const int64_t* out_idx,
+                               const void* out_val) {
+    if (dtype == ARGR_I32 || dtype == ARGR_I64) return ARGR_EUNSUPPORTED;
+    if (dtype != ARGR_F32 && dtype != ARGR_F16 && dtype != ARGR_BF16 && dtype != ARGR_F64) return ARGR_EINVAL;
     const int es = elem_size(dtype);
-    if (es == 0 || op < ARGR_MAX || op > ARGR_MIN_LAST) return false;
-    if (rows < 0 || cols < 1 || cols > INT32_MAX || rows > INT64_MAX / cols / es) return false;
-    if (rows == 0) return true;
-    if (!x || !out_idx) return false;
-    if (reinterpret_cast<uintptr_t>(x) % es || reinterpret_cast<uintptr_t>(out_idx) % 8) return false;
-    if (out_val && reinterpret_cast<uintptr_t>(out_val) % es) return false;
-    return true;
+    if (op < ARGR_MAX || op > ARGR_MIN_LAST) return ARGR_EINVAL;
+    if (rows < 0 || cols < 1 || cols > INT32_MAX || rows > INT64_MAX / cols / es) return ARGR_EINVAL;
+    if (rows == 0) return ARGR_OK;
+    if (!x || !out_idx) return ARGR_EINVAL;
+    if (reinterpret_cast<uintptr_t>(x) % es || reinterpret_cast<uintptr_t>(out_idx) % 8) return ARGR_EINVAL;
+    if (out_val && reinterpret_cast<uintptr_t>(out_val) % es) return ARGR_EINVAL;
+    return ARGR_OK;
 }
 
 }  // namespace
@@ -71,8 +81,8 @@ using namespace argr;
 
 extern "C" argr_status argreduce_noalloc(const void* x, argr_dtype dtype, int64_t rows, int64_t cols, argr_op op,
                                          int64_t* out_idx, void* out_val, argr_stream stream) {
-    if (!valid_args(x, dtype, rows, cols, op, out_idx, out_val)) return ARGR_EINVAL;
-    if (rows == 0) return ARGR_OK;
+    const argr_status bad = check_noalloc_args(x, dtype, rows, cols, op, out_idx, out_val);
+    if (bad != ARGR_OK || rows == 0) return bad;
     argr_caps caps;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -110,15 +120,6 @@ extern "C" argr_status argreduce_noalloc(const void* x, argr_dtype dtype, int64_
     argr_status s = scratch_for_current_device(&scratch);
     if (s != ARGR_OK) return s;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (p.blocks_per_row > 1) {
-        // The array keeps whatever the previous call left; the arrival
-        // counters this call uses must start at zero.
-        if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + kCounterOffset, 0, 4 * static_cast<size_t>(rows),
-                            st) != cudaSuccess) {
-            cudaGetLastError();
-            return ARGR_ECUDA;
-        }
-    }
     Problem pr;
     pr.x = x;
     pr.dtype = dtype;

@@ -106,6 +106,8 @@ def forced_plan(path: str, **kw):
         p.grid_rows = kw["grid_rows"]
     else:
         raise ValueError(path)
+    if kw.get("prefetch"):
+        p.flags |= _lib.ARGR_PLAN_PREFETCH
     return p
 
 

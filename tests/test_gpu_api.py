@@ -196,6 +196,58 @@ def test_graph_capture_replay(path):
         assert (out.cpu().numpy() == exp[k % 4]).all(), f"replay {k}"
 
 
+def test_default_scratch_graph_after_growth():
+    """A graph captured with the stream's default scratch stays valid after a
+    larger call on the same stream grows that scratch: the old buffer is kept
+    alive, so 100 replays (new inputs each time) all match the oracle."""
+    rows, cols, dtype = 4, 120001, "f32"
+    stream = torch.cuda.Stream()
+    xs = [W.fuzz_rows(dtype, rows, cols, seed=700 + k, p_special=0.001) for k in range(4)]
+    exp = [oracle.argreduce(x, dtype, "max")[0] for x in xs]
+    xd = torch.empty((rows, cols), dtype=torch.float32, device="cuda")
+    out = torch.empty(rows, dtype=torch.int64, device="cuda")
+    plan = forced_plan("split", bpr=20, grid_rows=rows)  # a split plan: uses scratch
+    with torch.cuda.stream(stream):
+        xd.copy_(torch.from_numpy(xs[0]))
+        A.argreduce_with_plan(plan, xd, "max", out_idx=out, stream=stream)  # default scratch, warm-up
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            A.argreduce_with_plan(plan, xd, "max", out_idx=out, stream=stream)
+        # a larger problem on the same stream grows the default scratch
+        big_rows = 1500
+        big = W.fuzz_rows(dtype, big_rows, 40000, seed=77, p_special=0.001)
+        bigd = torch.from_numpy(big).cuda()
+        big_plan = forced_plan("split", bpr=12, grid_rows=big_rows)
+        assert big_plan.grid_rows * big_plan.blocks_per_row * 16 > 4 * plan.grid_rows * plan.blocks_per_row * 16
+        bi, _ = A.argreduce_with_plan(big_plan, bigd, "max", stream=stream)
+        # had the first buffer gone back to the allocator, one of these would
+        # likely take its place and fill its counters with junk
+        junk = [torch.full((16384,), 0x7F, dtype=torch.uint8, device="cuda") for _ in range(64)]
+        stream.synchronize()
+    assert (bi.cpu().numpy() == oracle.argreduce(big, dtype, "max")[0]).all()
+    host = [torch.from_numpy(x) for x in xs]
+    for k in range(100):
+        xd.copy_(host[k % 4])
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert (out.cpu().numpy() == exp[k % 4]).all(), f"replay {k}"
+    del junk
+
+
+def test_scratch_growth_refused_inside_capture():
+    """Growing a Scratch inside a capture would record its preparing memset
+    into the graph; the binding refuses with a clear error instead."""
+    s = A.Scratch()
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with pytest.raises(RuntimeError, match="before a CUDA graph capture"):
+            with torch.cuda.graph(g, stream=stream):
+                s.ensure(1 << 16, stream.cuda_stream)
+
+
 def test_streams_independent():
     """Two streams with their own scratch run concurrently and both match."""
     a = W.fuzz_rows("f32", 16, 300000, seed=3, p_special=0.001)

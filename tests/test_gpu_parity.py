@@ -126,6 +126,33 @@ def test_cluster_path(dtype, cluster):
 
 
 @pytest.mark.parametrize("dtype", W.DTYPES)
+def test_prefetch_paths(dtype):
+    """ARGR_PLAN_PREFETCH (L2 prefetch of each CTA's first share before the
+    dependency wait) on the rows, split and cluster paths, with aligned and
+    unaligned bases, ragged tails, row loops and shares wider than what one
+    CTA prefetches."""
+    es = W.ELEM_SIZE[dtype]
+    caps = A.argreduce_device_caps(torch.cuda.current_device())
+    for cols in (1, 9, 257, 4099, 20011, 300001):
+        rows = 2 if cols > 100000 else 5 if cols > 4000 else 37
+        x = W.fuzz_rows(dtype, rows, cols, seed=cols * 3 + es)
+        for op in W.ALL_OPS:
+            for off in (0, 1):
+                check(x, dtype, op, offset=off, plan=forced_plan("rows", group=32, vec=0, grid=3, prefetch=True))
+                check(x, dtype, op, offset=off, plan=forced_plan("split", bpr=1, grid_rows=2, prefetch=True))
+                check(x, dtype, op, offset=off, plan=forced_plan("split", bpr=7, grid_rows=rows, prefetch=True))
+                if caps.max_cluster >= 16:
+                    check(x, dtype, op, offset=off, plan=forced_plan("cluster", cluster=16, grid_rows=2,
+                                                                     block=512, unroll=8, prefetch=True))
+            if (cols * es) % 16 == 0:
+                for g in (4, 32):
+                    check(x, dtype, op, plan=forced_plan("rows", group=g, vec=1, grid=5, prefetch=True))
+                check(x, dtype, op, plan=forced_plan("rows", group=32, vec=1, grid=2, unroll=8, pipeline=True,
+                                                     prefetch=True))
+                check(x, dtype, op, plan=forced_plan("cluster", cluster=4, grid_rows=rows, prefetch=True))
+
+
+@pytest.mark.parametrize("dtype", W.DTYPES)
 @pytest.mark.parametrize("group", [1, 4, 32])
 def test_stream_path(dtype, group):
     """Per-warp bulk-copy streaming: rows that fit a stage (whole rows, G

@@ -750,6 +750,34 @@ def test_plan_check_without_a_gpu():
     assert chk(cp, rows=1, cols=202048) == L.ARGR_EINVAL
 
 
+def test_prefetch_flag_rules():
+    """ARGR_PLAN_PREFETCH: set by the planner exactly for inputs of at most
+    32 MiB, admitted on the rows, split and cluster paths only (not with bulk
+    copies, not on the streaming or non-last-axis paths)."""
+    from row_wise_arg_gb300 import _lib as L
+    PF = L.ARGR_PLAN_PREFETCH
+    for dt, es in (("f32", 4), ("bf16", 2), ("f64", 8)):
+        for rows, cols in CONFIG_SHAPES + [(1, 1), (5, 7), (2048, 4096), (2049, 4096), (8, 1 << 20), (9, 1 << 20)]:
+            p = A.argreduce_plan(rows, cols, dt, "max", GB300)
+            assert bool(p.flags & PF) == (rows * cols * es <= 32 << 20), (rows, cols, dt)
+            assert A.argreduce_plan_check(p, rows, cols, dt, GB300) == L.ARGR_OK
+    chk = lambda p, rows=4, cols=1 << 16: A.argreduce_plan_check(p, rows, cols, "f32", GB300, True)
+    cp = L.argr_plan()
+    cp.path, cp.block, cp.unroll, cp.cluster, cp.blocks_per_row, cp.grid_rows = L.ARGR_PATH_CLUSTER, 256, 4, 4, 4, 4
+    cp.flags = L.ARGR_PLAN_PDL | PF
+    assert chk(cp) == L.ARGR_OK
+    cp.flags |= L.ARGR_PLAN_BULK
+    assert chk(cp) == L.ARGR_EINVAL                      # bulk copies already fetch the share
+    st = L.argr_plan()
+    st.path, st.block, st.group, st.stages, st.stage_bytes, st.grid_rows = L.ARGR_PATH_STREAM, 128, 32, 2, 8192, 8
+    st.vec, st.flags = 1, L.ARGR_PLAN_PDL
+    assert chk(st) == L.ARGR_OK
+    st.flags |= PF
+    assert chk(st) == L.ARGR_EINVAL                      # not a prefetching path
+    ax = A.argreduce_axis_plan(64, 512, 256, "bf16", "max", GB300)
+    assert not ax.flags & PF
+
+
 def test_bench_thread_per_row_plans_are_valid():
     """The thread-per-row plans bench.py times beside the narrow configs pass the
     library's own plan checks (scalar loads always, vector loads on aligned rows)."""
