@@ -490,25 +490,34 @@ def time_group(torch, A, cases, inputs, steps, warmup, stream, dist=None, device
 
 
 def isolated_time(torch, A, c, x, stream, calls: int = 200) -> float:
-    """Latency of one call on its own: one call per CUDA graph (input copies
-    rotated so every call reads HBM), CUDA events around each replay, the
-    host waiting for each before the next; the median in microseconds. Each
-    figure includes the graph launch's own device-side cost."""
+    """Latency of one call on its own, as a sampler pays it: a sleep kernel
+    first holds the stream, so that the host has queued the event, the call
+    and the closing event before the GPU reaches them; the median of the
+    closing-minus-opening event time over `calls` calls, each on its own
+    L2-cold input copy, in microseconds. Unlike the step, no earlier call
+    overlaps its launch or its first loads."""
     copies = max(1, min(64, copies_for([c])))
-    dev = [to_dev(torch, x, c.dtype).reshape(-1)]
-    gs = GraphSet(torch, A, [c], dev, copies, 1, stream)
+    d0 = to_dev(torch, x, c.dtype).reshape(-1)
+    xs = [d0] + [d0.clone() for _ in range(copies - 1)]
+    out = torch.empty(max(n_outputs(c), 1), dtype=torch.int64, device="cuda")
+    vals = torch.empty_like(d0) if is_scan(c) else None
+    scratch = A.Scratch()
+    need = (A.argreduce_cum_scratch_bytes(c.rows, c.cols, c.dtype, c.op) if is_scan(c) else
+            A.argreduce_scratch_bytes(c.rows, c.cols, c.dtype, c.op))
+    scratch.ensure(max(need, 4096), stream.cuda_stream)
     ts = []
     with torch.cuda.stream(stream):
         for k in range(calls + 5):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(100000)  # ~50 us: the host queues what follows meanwhile
             e0.record(stream)
-            gs.graphs[k % len(gs.graphs)].replay()
+            call(A, c, xs[k % copies], out, scratch, stream, vals)
             e1.record(stream)
             e1.synchronize()
             if k >= 5:
                 ts.append(e0.elapsed_time(e1) * 1e3)
-    del gs, dev
+    del xs, d0
     return statistics.median(ts)
 
 
@@ -716,15 +725,15 @@ def config_table(torch, A, args, stream, peak):
                 table.append(row)
                 if c is c0 and 1 <= g <= 5:
                     short = c.name.split("_", 1)[1].replace("_unique", "")
-                    item = f"{short} {row['us_per_call']:.2f} {row['frac']:.3f} {path[:2]} iso{row['isolated_us']:.2f}"
+                    item = f"{short} {row['us_per_call']:.2f} {row['frac']:.3f} {path[:2]} i{row['isolated_us']:.2f}"
                     if "cpu_us_per_call" in row:
-                        item += f" cpu{row['cpu_us_per_call']:.0f}/{row['cpu_cores']}"
+                        item += f" c{row['cpu_us_per_call']:.0f}/{row['cpu_cores']}"
                     if "ncu_frac" in row:
-                        item += f" ncu{row['ncu_frac']:.3f}"
+                        item += f" n{row['ncu_frac']:.3f}"
                     compact.append(item)
         del ginputs
-    legend = ("case: us/call (graphs of ~16 calls, L2-cold inputs), frac of measured HBM peak, path, "
-              "isolated single-call us, oracle us/cores, ncu DRAM frac")
+    legend = ("case, us/call (graphs of ~16 calls, L2-cold inputs), frac of measured HBM peak, path, "
+              "i: isolated single-call us, c: oracle us/host cores, n: ncu DRAM GB/s frac of peak")
     return table, {"legend": legend, "rows": compact}
 
 

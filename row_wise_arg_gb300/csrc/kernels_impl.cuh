@@ -411,6 +411,113 @@ cluster_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, 
 }
 
 // ---------------------------------------------------------------------------
+// One cluster per row, each CTA with exactly one row (gridDim.y >= rows):
+// the push merge. Instead of a CTA merge and a cluster barrier, every warp
+// merges its lanes and pushes its 16-byte candidate into CTA 0's shared
+// memory with st.async, which also counts the bytes on an mbarrier of CTA 0.
+// A CTA other than 0 exits as soon as its warps have pushed (st.async takes
+// its data from registers, so nothing of the exiting CTA is read later); CTA
+// 0 stays until its barrier has counted every candidate of the cluster
+// (a bounded wait) and merges them. No release fence, no cluster barrier
+// after the start, and the SMs of a row's other CTAs are free for the next
+// grid while CTA 0 merges.
+// ---------------------------------------------------------------------------
+constexpr int kPushMaxSlots = 16 * 32;  // CTAs of a cluster x warps of a CTA
+
+__device__ __forceinline__ unsigned cluster_addr(unsigned local_smem, unsigned rank) {
+    unsigned remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_smem), "r"(rank));
+    return remote;
+}
+
+// Store 16 bytes into shared memory of a CTA of the cluster and count them on
+// that CTA's mbarrier (both addresses from cluster_addr()).
+__device__ __forceinline__ void st_async_v4(unsigned remote, const uint4& v, unsigned remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     remote),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+                 : "memory");
+}
+
+// try_wait with acquire at cluster scope: the candidates were written by
+// other CTAs of the cluster.
+__device__ __forceinline__ bool mbar_try_wait_cluster(unsigned bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+template <class Tag, int OP, int U>
+__global__ void __launch_bounds__(1024)
+cluster_push_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int64_t* __restrict__ out_idx,
+                    typename Tag::raw* __restrict__ out_val, bool prefetch) {
+    using R = typename Tag::raw;
+    __shared__ __align__(16) uint4 slots[kPushMaxSlots];  // CTA 0: candidate of warp w of CTA b at b * nwarps + w
+    __shared__ __align__(8) unsigned long long bar;
+    const int nb = gridDim.x;  // the cluster spans the grid's x dimension
+    const int b = blockIdx.x;  // == rank in the cluster
+    const int t = threadIdx.x;
+    const int lane = t & 31;
+    const int warp = t >> 5;
+    const int nwarps = (blockDim.x + 31) >> 5;
+    const unsigned bar_local = smem_u32(&bar);
+    if (b == 0 && t == 0) {
+        // one phase: the arrival below plus every candidate's bytes
+        mbar_init(bar_local, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_arrive_expect_tx(bar_local, static_cast<unsigned>(nb * nwarps) * 16u);
+    }
+    cluster_started_arrive();  // after the barrier's initialisation (released by the fence above)
+    const int64_t r = blockIdx.y;
+    if (prefetch) {
+        allow_dependents();
+        if (r < rows) prefetch_share(x + r * static_cast<int64_t>(cols), cols, b, nb);
+        grid_dependency_wait();
+    } else {
+        grid_dependency_wait();
+        allow_dependents();
+    }
+    if (r >= rows) {  // a whole cluster without a row (forced plans only): nothing is pushed
+        cluster_started_wait();
+        return;
+    }
+    const R* row = x + r * static_cast<int64_t>(cols);
+    const R x0 = ld_scalar(row);
+    const Cand<Tag> seed = make_cand<Tag, OP>(x0, 0);
+    Cand<Tag> c = scan_share<Tag, OP, U>(row, cols, b, nb, x0);
+    c = group_merge<Tag, OP, 32>(c, 0xffffffffu);  // the warp's candidate, in every lane
+    cluster_started_wait();  // every CTA of the cluster runs: CTA 0's barrier is initialised
+    if (lane == 0)
+        st_async_v4(cluster_addr(smem_u32(&slots[b * nwarps + warp]), 0), pack_cand<Tag>(c),
+                    cluster_addr(bar_local, 0));
+    if (b != 0 || warp != 0) return;
+    // CTA 0, warp 0: wait (bounded) until every candidate has landed, then merge.
+    bool ok = mbar_try_wait_cluster(bar_local, 0);
+    if (!ok) {
+        const unsigned long long t0 = global_timer_ns();
+        while (!(ok = mbar_try_wait_cluster(bar_local, 0)) && global_timer_ns() - t0 <= kWaitLimitNs) {
+        }
+    }
+    if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) record_device_error(kErrWaitExpired);
+        return;
+    }
+    Cand<Tag> m = seed;
+    for (int k = lane; k < nb * nwarps; k += 32) m = merge<Tag, OP>(m, unpack_cand<Tag, OP>(slots[k]));
+    m = group_merge<Tag, OP, 32>(m, 0xffffffffu);
+    if (lane == 0) {
+        out_idx[r] = m.i;
+        if (out_val) out_val[r] = cand_value<Tag>(m, row);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // One cluster per row, with every CTA's share fetched by bulk copies.
 //
 // Same decomposition and merge as cluster_kernel, but CTA b's part of the
@@ -1107,11 +1214,10 @@ cudaError_t launch_split_t(const argr_plan& p, const Problem& pr) {
     }
 }
 
-template <class Tag, int OP, int U>
-cudaError_t launch_cluster_u(const argr_plan& p, const Problem& pr) {
-    using R = typename Tag::raw;
-    auto kern = cluster_kernel<Tag, OP, U>;
-    static KernelLaunchCache cache;
+// Before launching a cluster kernel: enable cluster sizes above 8 for it and
+// check that the device can co-schedule the plan's cluster shape.
+template <class K>
+cudaError_t prepare_cluster_launch(K kern, KernelLaunchCache& cache, const argr_plan& p) {
     if (p.cluster > 8) {
         // Cluster sizes above the portable 8 must be enabled per kernel.
         cudaError_t e = allow_big_cluster(kern, cache);
@@ -1122,8 +1228,31 @@ cudaError_t launch_cluster_u(const argr_plan& p, const Problem& pr) {
     cudaError_t e = cluster_fits(kern, grid, p.block, p.cluster, 0, cache, &ok);
     if (e != cudaSuccess) return e;
     if (!ok) return cudaErrorInvalidClusterSize;  // reported as ARGR_EUNSUPPORTED
+    return cudaSuccess;
+}
+
+template <class Tag, int OP, int U>
+cudaError_t launch_cluster_u(const argr_plan& p, const Problem& pr) {
+    using R = typename Tag::raw;
+    const bool pf = (p.flags & ARGR_PLAN_PREFETCH) != 0;
+    if (p.grid_rows >= pr.rows) {
+        // one row per CTA: the push merge
+        auto kern = cluster_push_kernel<Tag, OP, U>;
+        static KernelLaunchCache push_cache;
+        cudaError_t e = prepare_cluster_launch(kern, push_cache, p);
+        if (e != cudaSuccess) return e;
+        const dim3 grid(static_cast<unsigned>(p.cluster), static_cast<unsigned>(p.grid_rows));
+        return launch_ex(kern, grid, dim3(p.block), p.cluster, p, pr.stream, static_cast<const R*>(pr.x), pr.rows,
+                         pr.cols, pr.out_idx, static_cast<R*>(pr.out_val), pf);
+    }
+    // rows loop over the row slots: the barrier merge
+    auto kern = cluster_kernel<Tag, OP, U>;
+    static KernelLaunchCache cache;
+    cudaError_t e = prepare_cluster_launch(kern, cache, p);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(static_cast<unsigned>(p.cluster), static_cast<unsigned>(p.grid_rows));
     return launch_ex(kern, grid, dim3(p.block), p.cluster, p, pr.stream, static_cast<const R*>(pr.x), pr.rows,
-                     pr.cols, pr.out_idx, static_cast<R*>(pr.out_val), (p.flags & ARGR_PLAN_PREFETCH) != 0);
+                     pr.cols, pr.out_idx, static_cast<R*>(pr.out_val), pf);
 }
 
 // Dynamic shared memory the bulk cluster kernel needs: the largest share of a

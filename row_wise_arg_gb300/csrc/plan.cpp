@@ -10,8 +10,9 @@
 //    medium width use one warp per row and wider rows one CTA per row;
 //  * a few wide rows get one thread-block cluster each (up to 16 CTAs, at most
 //    about two CTAs per SM in total), merged through distributed shared memory
-//    with no global round trip, as long as a CTA's share stays small enough
-//    (kClusterMaxCtaBytes) for the cluster's SMs to stream it quickly;
+//    with no global round trip (each warp pushes its candidate into CTA 0),
+//    as long as a CTA's share stays small enough (kClusterMaxCtaBytes) for the
+//    cluster's SMs to stream it quickly;
 //  * otherwise (very wide rows) a row is split over several CTAs of the whole
 //    device, about one wave in total (more CTAs than one wave was measured
 //    slower on the pages' H200, and the merge cost grows with the CTA count),
@@ -176,13 +177,10 @@ argr_status make_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_
         const int64_t per_cta = row_bytes / c;
         if (c <= caps.max_cluster && rows * c <= 2 * static_cast<int64_t>(caps.sm_count) &&
             per_cta <= kClusterMaxCtaBytes) {
-            // A single row with 48 KB or more per CTA: 1024 threads with fewer
-            // loads each ([1,262144] f32 3.28 -> 3.18 us); with more rows in
-            // flight 512 threads stay faster.
-            const int block = (rows == 1 && per_cta >= 49152) ? 1024
-                              : per_cta >= 16384                ? 512
-                              : per_cta >= 4096                 ? 256
-                                                                : 128;
+            // 512 threads from 16 KB per CTA (with the push merge a single row
+            // too: [1,202048] f32 2.78 us with 1024 threads and 4 loads each,
+            // 2.65 us with 512 threads and 8), 256 from 4 KB, else 128.
+            const int block = per_cta >= 16384 ? 512 : per_cta >= 4096 ? 256 : 128;
             int unroll = 1;
             while (unroll < 8 && static_cast<int64_t>(unroll) * block * 16 < per_cta) unroll <<= 1;
             out->path = ARGR_PATH_CLUSTER;

@@ -108,6 +108,9 @@ def test_split_path(dtype, bpr):
 @pytest.mark.parametrize("dtype", W.DTYPES)
 @pytest.mark.parametrize("cluster", [2, 4, 8, 16])
 def test_cluster_path(dtype, cluster):
+    """One row per CTA (row slots >= rows): every warp pushes its candidate
+    into CTA 0 (st.async on an mbarrier); fewer row slots than rows: CTAs loop
+    over rows and merge through a cluster barrier."""
     caps = A.argreduce_device_caps(torch.cuda.current_device())
     if caps.max_cluster < cluster:
         pytest.skip("cluster size not supported")
@@ -119,6 +122,9 @@ def test_cluster_path(dtype, cluster):
             check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=2, unroll=1, pdl=False),
                   offset=1)
             check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=rows, block=512, unroll=8))
+            # more row slots than rows: clusters without a row push nothing
+            check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=rows + 3, block=96, unroll=2),
+                  offset=3)
             if cols * W.ELEM_SIZE[dtype] // 16 <= cluster * 8192:  # share fits the 128 KiB bulk buffer
                 check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=rows, bulk=True))
                 check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=2, bulk=True, block=128),

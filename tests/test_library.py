@@ -126,8 +126,9 @@ def test_plan_paths_for_configs():
         assert d["flags"] & _lib.ARGR_PLAN_PDL
         if rows == 1:  # one batch of loads covers a CTA's share
             assert d["unroll"] * d["block"] * 16 * d["cluster"] >= cols * 4
-    # one row with >= 48 KB per CTA: 1024 threads; more rows or smaller shares: 512 or fewer
-    assert path(1, 202048)["block"] == 1024 and path(1, 262144)["block"] == 1024
+    # 16 KB or more per CTA: 512 threads (one row too, with 8 loads each); smaller shares: fewer
+    assert path(1, 202048)["block"] == 512 and path(1, 262144)["block"] == 512
+    assert path(1, 202048)["unroll"] == 8 and path(1, 32000)["block"] == 256
     assert path(1, 202048, "bf16")["block"] == 512 and path(8, 202048)["block"] == 512
     d = path(1, 10_000_000)  # too wide for one cluster: split over the device
     assert d["path_name"] == "split" and d["blocks_per_row"] > 152
