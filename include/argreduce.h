@@ -70,7 +70,12 @@ typedef enum {
     ARGR_PATH_SPLIT = 2,   /* `blocks_per_row` CTAs per row; >1 merges through scratch,
                               the last CTA to arrive for a row reduces the partials */
     ARGR_PATH_CLUSTER = 3, /* one thread-block cluster of `cluster` CTAs per row, merged
-                              through distributed shared memory; no scratch */
+                              through distributed shared memory; no scratch. With a row
+                              slot per row (grid_rows == rows) and at most 512 threads
+                              per CTA every warp pushes its
+                              candidate into CTA 0 (st.async on an mbarrier, a bounded
+                              wait in CTA 0); with fewer slots CTAs loop over rows and
+                              merge through a cluster barrier */
     ARGR_PATH_AXIS = 5,    /* non-last axis (argreduce_axis): a warp is `group` column lanes (each
                               V consecutive inner positions, `vec`: V-element vectors) by 32/group
                               lanes along R; the CTA's block/32 warps split R, and a cluster of
@@ -107,10 +112,14 @@ typedef struct {
  * memory by bulk (TMA) copies issued all at once, instead of by loads from
  * every thread. The share must be at most 128 KiB. */
 #define ARGR_PLAN_BULK 2
-/* Plan flag for tests of failure handling (STREAM, CUM_SPLIT and CUM_STREAM
- * paths only). STREAM: one bulk copy's barrier is made to expect more bytes
- * than arrive, so the kernel's bounded wait (2 ms under this flag) expires;
- * the kernel records the expiry, skips its work and returns. CUM_SPLIT and
+/* Plan flag for tests of failure handling (STREAM, CLUSTER with a row slot
+ * per row, CUM_SPLIT and CUM_STREAM paths only). STREAM: one bulk copy's
+ * barrier is made to expect more bytes than arrive, so the kernel's bounded
+ * wait (2 ms under this flag) expires; the kernel records the expiry, skips
+ * its work and returns. CLUSTER (push merge only: grid_rows == rows, at
+ * most 512 threads): CTA 0's barrier expects 16 bytes more than
+ * the cluster's candidates, so its wait expires and it returns without
+ * writing the row. CUM_SPLIT and
  * CUM_STREAM: the first chunk (tile) of each row never publishes its record,
  * so every wait for it expires after 2 ms. Either way argreduce_read_error()
  * then reports ARGR_ETIMEOUT and outputs are undefined. Never set in the

@@ -75,8 +75,10 @@ def _stream_ptr(stream, device_index: int) -> int:
 
 class Scratch:
     """Device scratch for one stream, grown on demand and prepared with
-    argreduce_scratch_init() whenever it is (re)allocated. Two calls that can
-    run concurrently on the GPU must use different Scratch objects.
+    argreduce_scratch_init() whenever it is (re)allocated; the preparation has
+    completed when the constructor or ensure() returns, so the buffer may be
+    used on any stream. Two calls that can run concurrently on the GPU must
+    use different Scratch objects.
 
     A buffer, once handed to a call, stays allocated for the lifetime of the
     Scratch even after a larger one replaces it: a CUDA graph captured with
@@ -107,6 +109,10 @@ class Scratch:
         st = argreduce_scratch_init(buf.data_ptr(), n, stream_ptr)
         if st != ARGR_OK:
             raise ArgreduceError(st, "argreduce_scratch_init")
+        # The buffer may be used next on another stream (torch's streams do not
+        # wait for each other): let the preparing memset finish first. Growth
+        # is rare (geometric) and never happens inside a capture.
+        torch.cuda.synchronize(self.device)
         if self.buf is not None:
             self.retired.append(self.buf)
         self.buf = buf

@@ -51,12 +51,16 @@ rows_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int
     const int groups_per_block = blockDim.x / G;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * groups_per_block;
     if (prefetch) {
-        // the rows of this CTA's first step, before waiting for the previous grid
+        // the rows of this CTA's grid-stride steps, up to kPrefetchMaxBytes,
+        // before waiting for the previous grid
         allow_dependents();
-        const int64_t r0 = static_cast<int64_t>(blockIdx.x) * groups_per_block;
-        if (r0 < rows) {
+        const int64_t row_bytes = static_cast<int64_t>(cols) * static_cast<int64_t>(sizeof(R));
+        int64_t budget = static_cast<int64_t>(kPrefetchMaxBytes);
+        for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * groups_per_block; r0 < rows && budget > 0;
+             r0 += stride) {
             const int64_t r1 = rows - r0 > groups_per_block ? r0 + groups_per_block : rows;
             prefetch_l2_range(x + r0 * cols, x + r1 * cols);
+            budget -= (r1 - r0) * row_bytes;
         }
         grid_dependency_wait();
     } else {
@@ -453,10 +457,16 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(unsigned bar, unsigned par
     return ok != 0;
 }
 
-template <class Tag, int OP, int U>
-__global__ void __launch_bounds__(1024)
-cluster_push_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int64_t* __restrict__ out_idx,
-                    typename Tag::raw* __restrict__ out_val, bool prefetch) {
+constexpr int kPushMaxBlock = 512;  // threads per CTA of the push merge kernel
+
+// At most 512 threads and at least two CTAs per SM (64 registers a thread).
+// PF (ARGR_PLAN_PREFETCH) and VAL (out_val given) are template parameters and
+// every CTA has a row (gridDim.y == rows): each runtime test of these, kept
+// live through the scan, measured 0.12-0.26 us slower per call.
+template <class Tag, int OP, int U, bool PF, bool VAL>
+__global__ void __launch_bounds__(kPushMaxBlock, 2)
+cluster_push_kernel(const typename Tag::raw* __restrict__ x, int cols, int64_t* __restrict__ out_idx,
+                    typename Tag::raw* __restrict__ out_val, int flags) {
     using R = typename Tag::raw;
     __shared__ __align__(16) uint4 slots[kPushMaxSlots];  // CTA 0: candidate of warp w of CTA b at b * nwarps + w
     __shared__ __align__(8) unsigned long long bar;
@@ -468,26 +478,25 @@ cluster_push_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int c
     const int nwarps = (blockDim.x + 31) >> 5;
     const unsigned bar_local = smem_u32(&bar);
     if (b == 0 && t == 0) {
-        // one phase: the arrival below plus every candidate's bytes
+        // One phase: the arrival below plus every candidate's bytes. Test hook
+        // (ARGR_PLAN_TEST_EXPIRE): 16 bytes more than the cluster pushes, so
+        // CTA 0's wait (2 ms under the flag) expires.
         mbar_init(bar_local, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        mbar_arrive_expect_tx(bar_local, static_cast<unsigned>(nb * nwarps) * 16u);
+        mbar_arrive_expect_tx(bar_local, static_cast<unsigned>(nb * nwarps) * 16u +
+                                             ((flags & ARGR_PLAN_TEST_EXPIRE) ? 16u : 0u));
     }
     cluster_started_arrive();  // after the barrier's initialisation (released by the fence above)
     const int64_t r = blockIdx.y;
-    if (prefetch) {
+    const R* row = x + r * static_cast<int64_t>(cols);
+    if constexpr (PF) {
         allow_dependents();
-        if (r < rows) prefetch_share(x + r * static_cast<int64_t>(cols), cols, b, nb);
+        prefetch_share(row, cols, b, nb);
         grid_dependency_wait();
     } else {
         grid_dependency_wait();
         allow_dependents();
     }
-    if (r >= rows) {  // a whole cluster without a row (forced plans only): nothing is pushed
-        cluster_started_wait();
-        return;
-    }
-    const R* row = x + r * static_cast<int64_t>(cols);
     const R x0 = ld_scalar(row);
     const Cand<Tag> seed = make_cand<Tag, OP>(x0, 0);
     Cand<Tag> c = scan_share<Tag, OP, U>(row, cols, b, nb, x0);
@@ -497,11 +506,15 @@ cluster_push_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int c
         st_async_v4(cluster_addr(smem_u32(&slots[b * nwarps + warp]), 0), pack_cand<Tag>(c),
                     cluster_addr(bar_local, 0));
     if (b != 0 || warp != 0) return;
-    // CTA 0, warp 0: wait (bounded) until every candidate has landed, then merge.
+    // CTA 0, warp 0: wait (bounded) until every candidate has landed, then
+    // merge. Every push of the cluster lands whether or not the wait expires
+    // (the CTAs of a cluster run together), so CTA 0 never leaves with a
+    // store into it still in flight.
+    const unsigned long long limit_ns = (flags & ARGR_PLAN_TEST_EXPIRE) ? 2ull * 1000 * 1000 : kWaitLimitNs;
     bool ok = mbar_try_wait_cluster(bar_local, 0);
     if (!ok) {
         const unsigned long long t0 = global_timer_ns();
-        while (!(ok = mbar_try_wait_cluster(bar_local, 0)) && global_timer_ns() - t0 <= kWaitLimitNs) {
+        while (!(ok = mbar_try_wait_cluster(bar_local, 0)) && global_timer_ns() - t0 <= limit_ns) {
         }
     }
     if (!__all_sync(0xffffffffu, ok)) {
@@ -513,7 +526,7 @@ cluster_push_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int c
     m = group_merge<Tag, OP, 32>(m, 0xffffffffu);
     if (lane == 0) {
         out_idx[r] = m.i;
-        if (out_val) out_val[r] = cand_value<Tag>(m, row);
+        if constexpr (VAL) out_val[r] = cand_value<Tag>(m, row);
     }
 }
 
@@ -1231,21 +1244,30 @@ cudaError_t prepare_cluster_launch(K kern, KernelLaunchCache& cache, const argr_
     return cudaSuccess;
 }
 
+template <class Tag, int OP, int U, bool PF, bool VAL>
+cudaError_t launch_push(const argr_plan& p, const Problem& pr) {
+    using R = typename Tag::raw;
+    auto kern = cluster_push_kernel<Tag, OP, U, PF, VAL>;
+    static KernelLaunchCache cache;
+    cudaError_t e = prepare_cluster_launch(kern, cache, p);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(static_cast<unsigned>(p.cluster), static_cast<unsigned>(p.grid_rows));
+    return launch_ex(kern, grid, dim3(p.block), p.cluster, p, pr.stream, static_cast<const R*>(pr.x), pr.cols,
+                     pr.out_idx, static_cast<R*>(pr.out_val), static_cast<int>(p.flags));
+}
+
 template <class Tag, int OP, int U>
 cudaError_t launch_cluster_u(const argr_plan& p, const Problem& pr) {
     using R = typename Tag::raw;
     const bool pf = (p.flags & ARGR_PLAN_PREFETCH) != 0;
-    if (p.grid_rows >= pr.rows) {
+    if (p.grid_rows == pr.rows && p.block <= kPushMaxBlock) {
         // one row per CTA: the push merge
-        auto kern = cluster_push_kernel<Tag, OP, U>;
-        static KernelLaunchCache push_cache;
-        cudaError_t e = prepare_cluster_launch(kern, push_cache, p);
-        if (e != cudaSuccess) return e;
-        const dim3 grid(static_cast<unsigned>(p.cluster), static_cast<unsigned>(p.grid_rows));
-        return launch_ex(kern, grid, dim3(p.block), p.cluster, p, pr.stream, static_cast<const R*>(pr.x), pr.rows,
-                         pr.cols, pr.out_idx, static_cast<R*>(pr.out_val), pf);
+        if (pr.out_val)
+            return pf ? launch_push<Tag, OP, U, true, true>(p, pr) : launch_push<Tag, OP, U, false, true>(p, pr);
+        return pf ? launch_push<Tag, OP, U, true, false>(p, pr) : launch_push<Tag, OP, U, false, false>(p, pr);
     }
-    // rows loop over the row slots: the barrier merge
+    // rows looping over fewer row slots, spare row slots, or CTAs of more than
+    // 512 threads: the barrier merge
     auto kern = cluster_kernel<Tag, OP, U>;
     static KernelLaunchCache cache;
     cudaError_t e = prepare_cluster_launch(kern, cache, p);

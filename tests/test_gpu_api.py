@@ -196,6 +196,28 @@ def test_graph_capture_replay(path):
         assert (out.cpu().numpy() == exp[k % 4]).all(), f"replay {k}"
 
 
+def test_push_merge_wait_expires_and_is_reported():
+    """The push merge's CTA 0 waits (bounded) for the cluster's candidates.
+    Under the test flag its barrier expects 16 bytes more than arrive: the
+    wait runs out after 2 ms, the kernel returns, the host reads
+    ARGR_ETIMEOUT, and the next call is exact."""
+    x = W.fuzz_rows("f32", 3, 50000, seed=5, p_special=0.001)
+    xd, _keep = to_device(x, "f32")
+    s = torch.cuda.current_stream().cuda_stream
+    assert A.argreduce_read_error(0, s) == _lib.ARGR_OK
+    plan = forced_plan("cluster", cluster=4, grid_rows=3)
+    plan.flags |= _lib.ARGR_PLAN_TEST_EXPIRE
+    A.argreduce_with_plan(plan, xd, "max")
+    assert A.argreduce_read_error(0, s) == _lib.ARGR_ETIMEOUT
+    assert A.argreduce_read_error(0, s) == _lib.ARGR_OK  # cleared
+    idx, _ = run(x, "f32", "max", plan=forced_plan("cluster", cluster=4, grid_rows=3))
+    assert (idx == oracle.argreduce(x, "f32", "max")[0]).all()
+    bad = forced_plan("cluster", cluster=4, grid_rows=2)  # rows loop: no push wait to expire
+    bad.flags |= _lib.ARGR_PLAN_TEST_EXPIRE
+    with pytest.raises(A.ArgreduceError):
+        A.argreduce_with_plan(bad, xd, "max")
+
+
 def test_default_scratch_graph_after_growth():
     """A graph captured with the stream's default scratch stays valid after a
     larger call on the same stream grows that scratch: the old buffer is kept

@@ -441,3 +441,23 @@ def test_cum_stream_long_rows_graphs_and_scratch():
     bad.blocks_per_row += 1  # not the row's tile count
     assert _lib.argreduce_cum_raw(xd.data_ptr(), "f32", 2, 400001, "max", out_i.data_ptr(), 0, sc.ptr, sc.nbytes, 0,
                                   bad) == _lib.ARGR_EINVAL
+
+
+def test_scratch_prepared_before_use_on_another_stream():
+    """A Scratch made (and zeroed) on torch's current stream and used at once
+    on a different stream: torch's streams do not wait for each other, so the
+    binding lets the preparing memset finish before it hands the buffer out.
+    A split scan (tickets, a done counter, records) and a split reduction
+    both depend on that; every call is exact and no wait expires."""
+    x = np.random.Generator(np.random.PCG64(44)).integers(-500, 500, size=(1, 1 << 21)).astype(np.int64)
+    xd = torch.from_numpy(x).cuda()
+    eidx, _ = oracle.cumreduce(x, "i64", "max", want_val=False)
+    plan = A.argreduce_cum_plan(1, 1 << 21, "i64", "max")
+    assert plan.path == _lib.ARGR_PATH_CUM_SPLIT
+    for k in range(3):
+        sc = A.Scratch(nbytes=2 << 20)
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            idx, _ = A.argreduce_cum(xd, "max", scratch=sc, stream=s, with_values=False)
+        assert A.argreduce_read_error(sc.ptr, s.cuda_stream) == _lib.ARGR_OK
+        assert (idx.cpu().numpy() == eidx).all(), k

@@ -122,7 +122,7 @@ def test_cluster_path(dtype, cluster):
             check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=2, unroll=1, pdl=False),
                   offset=1)
             check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=rows, block=512, unroll=8))
-            # more row slots than rows: clusters without a row push nothing
+            # more row slots than rows: the barrier merge with idle clusters
             check(x, dtype, op, plan=forced_plan("cluster", cluster=cluster, grid_rows=rows + 3, block=96, unroll=2),
                   offset=3)
             if cols * W.ELEM_SIZE[dtype] // 16 <= cluster * 8192:  # share fits the 128 KiB bulk buffer

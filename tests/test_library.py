@@ -749,6 +749,13 @@ def test_plan_check_without_a_gpu():
     assert A.argreduce_plan_check(cp, 1, 202048, "f32", A.make_caps(152, max_cluster=8)) == L.ARGR_EUNSUPPORTED
     cp.cluster = cp.blocks_per_row = 17
     assert chk(cp, rows=1, cols=202048) == L.ARGR_EINVAL
+    # the test hook of the push merge's bounded wait: a row slot per row, no bulk copies
+    cp.cluster = cp.blocks_per_row = 16
+    cp.flags = L.ARGR_PLAN_PDL | L.ARGR_PLAN_TEST_EXPIRE
+    assert chk(cp, rows=1, cols=202048) == L.ARGR_OK
+    assert chk(cp, rows=2, cols=202048) == L.ARGR_EINVAL     # rows loop: barrier merge, no such wait
+    cp.flags |= L.ARGR_PLAN_BULK
+    assert chk(cp, rows=1, cols=202048) == L.ARGR_EINVAL
 
 
 def test_prefetch_flag_rules():
