@@ -58,7 +58,7 @@ WORKLOADS = {
                      "[256,65536] f32"),
 }
 DTYPE_LABEL = {"f32": "f32", "f16": "f16", "bf16": "bf16", "f64": "f64", "i32": "i32", "i64": "i64"}
-KERNEL_OF_PATH = {"rows": "rows_kernel", "split": "split_kernel", "cluster": "cluster_kernel", "axis": "axis_kernel",
+KERNEL_OF_PATH = {"rows": "rows_kernel", "split": "split_kernel", "cluster": "cluster_push_kernel", "axis": "axis_kernel",
                   "stream": "stream_kernel", "cum": "cum_kernel", "cum_split": "cum_split_kernel", "none": "none"}
 
 
@@ -216,15 +216,20 @@ def config_group_cases(groups=range(1, 6)):
     return [c for g in groups for c in W.config_cases(g) if c.variant != "dup"]
 
 
-def ncu_cases(torch, A):
+def ncu_cases(torch, A, only: str = None, reps: int = 1):
     """One planner call per reduction config case, in table order, each on
     its own freshly allocated input (for one ncu capture of every case: the
-    i-th captured launch is the i-th case printed)."""
+    i-th captured launch is the i-th case printed). `only`: just the cases
+    whose name contains it, each called `reps` times (for a full capture of
+    one launch, skipping the first)."""
     for c in config_group_cases():
+        if only is not None and only not in c.name:
+            continue
         x = W.make(c)
         d = to_dev(torch, x, c.dtype).view(c.rows, c.cols)
         out = torch.empty(c.rows, dtype=torch.int64, device="cuda")
-        A.argreduce(d, c.op, dtype=c.dtype, out_idx=out)
+        for _ in range(reps):
+            A.argreduce(d, c.op, dtype=c.dtype, out_idx=out)
         torch.cuda.synchronize()
         print(c.name, flush=True)
         del d, out
@@ -777,6 +782,8 @@ def main():
     ap.add_argument("--no-cub", action="store_true", help="skip the cub::DeviceReduce timing comparison")
     ap.add_argument("--ncu-cases", action="store_true",
                     help="no timing: one planner call per reduction config case, for an ncu capture")
+    ap.add_argument("--ncu-case", metavar="NAME",
+                    help="no timing: three planner calls of each reduction config case whose name contains NAME")
     ap.add_argument("--ncu-summarize", metavar="CSV",
                     help="no GPU: print profiles/traffic_configs.txt lines from an ncu CSV of --ncu-cases")
     args = ap.parse_args()
@@ -785,12 +792,15 @@ def main():
     if args.ncu_summarize:
         summarize_ncu(args.ncu_summarize)
         return 0
-    if args.ncu_cases:
+    if args.ncu_cases or args.ncu_case:
         import torch
         from row_wise_arg_gb300.build import build
         build()
         import row_wise_arg_gb300 as A
-        ncu_cases(torch, A)
+        if args.ncu_case:
+            ncu_cases(torch, A, only=args.ncu_case, reps=3)
+        else:
+            ncu_cases(torch, A)
         return 0
 
     rank, world, local, dist = dist_setup(args.gpus)
