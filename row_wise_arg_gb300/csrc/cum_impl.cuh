@@ -209,25 +209,64 @@ __device__ __forceinline__ KI<CT> block_first_best(KI<CT> a, KI<CT>* warp_tot) {
     return a;
 }
 
+// L2 residency for the split scan's second read of its chunk: phase A loads
+// the chunk with an evict-last policy, and every scan writes its outputs as
+// streaming stores (st.global.cs: evict-first), so that the outputs, twice to
+// three times the input's bytes, do not push the chunk out of L2 before
+// phase B reads it again.
+__device__ __forceinline__ unsigned long long l2_evict_last_policy() {
+    unsigned long long pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+template <typename R>
+__device__ __forceinline__ R ld_keep(const R* p, unsigned long long pol) {
+    R r;
+    if constexpr (sizeof(R) == 8) {
+        unsigned long long v;
+        asm volatile("ld.global.nc.L2::cache_hint.b64 %0, [%1], %2;" : "=l"(v) : "l"(p), "l"(pol));
+        __builtin_memcpy(&r, &v, 8);
+    } else if constexpr (sizeof(R) == 4) {
+        unsigned v;
+        asm volatile("ld.global.nc.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(pol));
+        __builtin_memcpy(&r, &v, 4);
+    } else {
+        unsigned short v;
+        asm volatile("ld.global.nc.L2::cache_hint.b16 %0, [%1], %2;" : "=h"(v) : "l"(p), "l"(pol));
+        __builtin_memcpy(&r, &v, 2);
+    }
+    return r;
+}
+
+// An element load: with KEEP, under the evict-last policy.
+template <bool KEEP, typename R>
+__device__ __forceinline__ R ld_elem(const R* p, unsigned long long pol) {
+    if constexpr (KEEP) return ld_keep(p, pol);
+    else return ld_scalar(p);
+}
+
 // The first tile of row[cb, ce) into registers, in the layout the scan uses
 // (thread t holds elements cb + t + q * NT); phase A reduces it and phase B
 // scans it without loading it again.
-template <class CT, int ITEMS>
+template <class CT, int ITEMS, bool KEEP = false>
 __device__ __forceinline__ void load_first_tile(const typename CT::raw* row, int cb, int ce,
                                                 typename CT::raw (&v)[ITEMS]) {
     const int nt = blockDim.x;
     const int n = ce - cb < nt * ITEMS ? ce - cb : nt * ITEMS;
+    const unsigned long long pol = KEEP ? l2_evict_last_policy() : 0ull;
 #pragma unroll
     for (int q = 0; q < ITEMS; ++q)
-        if (static_cast<int>(threadIdx.x) + q * nt < n) v[q] = ld_scalar(row + cb + threadIdx.x + q * nt);
+        if (static_cast<int>(threadIdx.x) + q * nt < n) v[q] = ld_elem<KEEP>(row + cb + threadIdx.x + q * nt, pol);
 }
 
 // Phase A: the aggregate of row[cb, ce) (its first best element): the first
 // tile from v, the rest with kCumLoadsA independent loads in flight per
 // thread. Valid in warp 0.
-template <class CT, int OP, int ITEMS>
+template <class CT, int OP, int ITEMS, bool KEEP = false>
 __device__ __forceinline__ KI<CT> chunk_aggregate(const typename CT::raw* row, int cb, int ce,
                                                   const typename CT::raw (&v)[ITEMS], KI<CT>* warp_tot) {
+    const unsigned long long pol = KEEP ? l2_evict_last_policy() : 0ull;
     using R = typename CT::raw;
     using K = typename CT::key;
     const int nt = blockDim.x;
@@ -249,7 +288,7 @@ __device__ __forceinline__ KI<CT> chunk_aggregate(const typename CT::raw* row, i
         R w[kCumLoadsA];
 #pragma unroll
         for (int u = 0; u < kCumLoadsA; ++u)
-            if (j0 + u * nt < ce) w[u] = ld_scalar(row + j0 + u * nt);
+            if (j0 + u * nt < ce) w[u] = ld_elem<KEEP>(row + j0 + u * nt, pol);
 #pragma unroll
         for (int u = 0; u < kCumLoadsA; ++u) {
             if (j0 + u * nt < ce) {
@@ -337,17 +376,19 @@ __device__ __forceinline__ void scan_tile(const typename CT::raw* row, int base,
     const KI<CT> tot = *s_total;
     __syncthreads();
     // Coalesced stores. An index before this tile can only be the carry's.
+    // Streaming (evict-first) stores: the outputs are not read again here.
     int64_t* oi = oi_row + base;
 #pragma unroll
     for (int q = 0; q < ITEMS; ++q)
-        if (FULL || t + q * nt < n) oi[t + q * nt] = tidx[t + q * nt];
+        if (FULL || t + q * nt < n)
+            __stcs(reinterpret_cast<long long*>(oi + t + q * nt), static_cast<long long>(tidx[t + q * nt]));
     if (ov_row) {
         typename CT::raw* ov = ov_row + base;
 #pragma unroll
         for (int q = 0; q < ITEMS; ++q) {
             if (FULL || t + q * nt < n) {
                 const int i = tidx[t + q * nt];
-                ov[t + q * nt] = i >= base ? tin[i - base] : carry_v;
+                __stcs(ov + t + q * nt, i >= base ? tin[i - base] : carry_v);
             }
         }
     }
@@ -707,8 +748,8 @@ cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols,
         stash = stash_fill<CT>(row, cb, ce, cum_smem, &stash_bar, limit_ns, err);
         a = stash_aggregate<CT, OP>(stash, cb, ce, warp_tot);
     } else {
-        load_first_tile<CT, ITEMS>(row, cb, ce, v);
-        a = chunk_aggregate<CT, OP, ITEMS>(row, cb, ce, v, warp_tot);
+        load_first_tile<CT, ITEMS, true>(row, cb, ce, v);
+        a = chunk_aggregate<CT, OP, ITEMS, true>(row, cb, ce, v, warp_tot);
     }
     KI<CT> seed;
     seed.k = CT::template seed_key<OP>(x0);

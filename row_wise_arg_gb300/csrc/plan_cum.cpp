@@ -89,8 +89,13 @@ argr_status make_cum_plan(int64_t rows, int64_t cols, int dtype, int op, const a
     // kCumSplitElems elements in total, from half an SM's worth up to two
     // 512-thread CTAs per SM for one row, or as many 128-thread CTAs as the
     // records allow for several rows.
-    const int64_t max_ctas = rows == 1 ? 2 * sms : kCumMaxChunks;
-    const int max_block = rows == 1 ? 512 : 128;
+    // One row of 64 MiB or more: four 256-thread chunks per SM, two waves, so
+    // that the chunks in flight fit L2 and phase B's second read of a chunk
+    // mostly hits it ([1,2^24] int64 107.4 -> 102.5 us, [1,2^25] f32 142.1 ->
+    // 137.9 us against two 512-thread chunks per SM).
+    const bool big_row = rows == 1 && cols * static_cast<int64_t>(elem_size(dtype)) >= (int64_t(64) << 20);
+    const int64_t max_ctas = big_row ? 4 * sms : rows == 1 ? 2 * sms : kCumMaxChunks;
+    const int max_block = big_row ? 256 : rows == 1 ? 512 : 128;
     // One row of at most 64K elements: a quarter of the SMs, in 256-thread
     // CTAs instead of half of them in 128-thread CTAs ([1,65536] int64
     // 8.68 -> 8.63 us, f64 9.04 -> 8.87 us; one run, median of three).

@@ -511,14 +511,18 @@ def test_cum_plans_and_validation():
             assert d["scratch_bytes"] == (256 if total <= 1024 else 1 << 20) + 8 * total
         elif d["path_name"] == "cum_split":
             # long rows, fewer than the SMs: 76..304 CTAs (38 for one row of <= 64K
-            # elements), records of one launch <= 1024
+            # elements, 608 of 256 threads for one row of 64 MiB or more), records of
+            # one launch <= 1024
             chunks = d["blocks_per_row"]
             assert rows < 152 and chunks >= 2 and rows * chunks <= 1024 and cols > 32768
-            assert rows * chunks <= (2 * 152 + 1 if rows == 1 else 1024)
+            big = rows == 1 and cols * es >= 64 << 20
+            assert rows * chunks <= (4 * 152 if big else 2 * 152 + 1 if rows == 1 else 1024)
+            if big:
+                assert d["block"] == 256
             floor = 38 if rows == 1 and cols <= 65536 else 76
             assert rows * chunks >= floor or cols // chunks < 1024 or chunks == 1024 // rows
             assert cols // chunks >= 512
-            cap = 512 if rows == 1 else 128
+            cap = 256 if big else 512 if rows == 1 else 128
             assert d["block"] in (64, 128, 256, 512) and d["block"] <= cap
             assert d["block"] * 7 >= -(-cols // chunks) or d["block"] == cap
             assert d["scratch_bytes"] == 256 + 8 * rows * chunks and d["cluster"] == 1
@@ -538,7 +542,7 @@ def test_cum_plans_and_validation():
                 assert d["block"] <= 128 and (d["block"] == 32 or d["block"] * 7 <= cols)
     assert seen == {("cum_split", False), ("cum", True), ("cum", False)}
     big = A.argreduce_cum_plan(1, 16777216, "i64", "max", GB300).as_dict()
-    assert big["blocks_per_row"] == 304 and big["flags"] & 8 == 0  # the stash is a forced-plan option
+    assert big["blocks_per_row"] == 608 and big["flags"] & 8 == 0  # the stash is a forced-plan option
     d = A.argreduce_cum_plan(1, 65536, "i64", "max", GB300).as_dict()  # the pages' 65536-element int64 row
     assert d["blocks_per_row"] == 38 and d["block"] == 256
     assert A.argreduce_cum_plan(1, 131072, "i64", "max", GB300).as_dict()["blocks_per_row"] == 76
