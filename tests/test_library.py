@@ -514,9 +514,10 @@ def test_cum_plans_and_validation():
             # elements, 608 of 256 threads for one row of 64 MiB or more), records of
             # one launch <= 1024
             chunks = d["blocks_per_row"]
-            assert rows < 152 and chunks >= 2 and rows * chunks <= 1024 and cols > 32768
+            many = rows > 1 and rows * cols >= 1 << 24  # several long rows: up to 8 x 152 chunks
+            assert rows < 152 and chunks >= 2 and rows * chunks <= (8 * 152 if many else 1024) and cols > 32768
             big = rows == 1 and cols * es >= 64 << 20
-            assert rows * chunks <= (4 * 152 if big else 2 * 152 + 1 if rows == 1 else 1024)
+            assert rows * chunks <= (4 * 152 if big else 2 * 152 + 1 if rows == 1 else 8 * 152 if many else 1024)
             if big:
                 assert d["block"] == 256
             floor = 38 if rows == 1 and cols <= 65536 else 76
@@ -525,7 +526,8 @@ def test_cum_plans_and_validation():
             cap = 256 if big else 512 if rows == 1 else 128
             assert d["block"] in (64, 128, 256, 512) and d["block"] <= cap
             assert d["block"] * 7 >= -(-cols // chunks) or d["block"] == cap
-            assert d["scratch_bytes"] == 256 + 8 * rows * chunks and d["cluster"] == 1
+            total = rows * chunks
+            assert d["scratch_bytes"] == (256 if total <= 1024 else 1 << 20) + 8 * total and d["cluster"] == 1
             assert d["grid_rows"] == rows and cols > 32768 and (es == 8 or cols > 65536 or rows * 16 > 304)
         elif d["cluster"] > 1:
             # short rows, fewer than the SMs: one cluster per row
