@@ -179,7 +179,12 @@ __device__ __forceinline__ KI<CT> shfl_xor_ki(const KI<CT>& p, int d) {
 }
 
 constexpr int kCumMaxCluster = 16;
-constexpr int kCumLoadsA = 4;  // independent loads in flight per thread in phase A
+constexpr int kCumLoadsA = 4;  // independent loads in flight per thread in phase A (stashed chunks)
+// 16-byte loads in flight per thread in the 16-byte phase A: 8 for 8-byte
+// elements, 4 for smaller ones (their wider per-vector key loop would spill).
+template <typename R>
+constexpr int kCumLoadsVec = sizeof(R) == 8 ? 8 : 4;
+constexpr int kCumVecTiles = 4;  // chunks of at least this many tiles use the 16-byte phase A
 
 // Total order for merging aggregates of disjoint ranges: the higher key, then
 // the lower index. Commutative, so the order in which partial aggregates meet
@@ -237,6 +242,23 @@ __device__ __forceinline__ R ld_keep(const R* p, unsigned long long pol) {
         __builtin_memcpy(&r, &v, 2);
     }
     return r;
+}
+
+// A 16-byte load under the evict-last policy.
+__device__ __forceinline__ uint4 ld_keep16(const void* p, unsigned long long pol) {
+    uint4 r;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p), "l"(pol));
+    return r;
+}
+
+// Element k of a 16-byte vector of raw elements.
+template <typename R>
+__device__ __forceinline__ R vec_item(const uint4& v, int k) {
+    R e;
+    __builtin_memcpy(&e, reinterpret_cast<const char*>(&v) + k * sizeof(R), sizeof(R));
+    return e;
 }
 
 // An element load: with KEEP, under the evict-last policy.
@@ -328,6 +350,32 @@ __device__ __forceinline__ void scan_tile(const typename CT::raw* row, int base,
         for (int q = 0; q < ITEMS; ++q)
             if (t + q * nt < nn) v[q] = ld_scalar(row + nbase + t + q * nt);
     }
+    // A tile with no element better than the carry (ties keep the carry's
+    // earlier index): every output of the tile is the carry and the carry
+    // stays; no scan is needed. One barrier decides it for the CTA, before
+    // the prefixes below take their registers. Elements of 8 bytes skip the
+    // test: the extra branch makes the 64-register kernels spill there.
+    bool better = sizeof(typename CT::raw) > 4;
+#pragma unroll
+    for (int q = 0; q < ITEMS; ++q) {
+        const int j = t * ITEMS + q;
+        if (sizeof(typename CT::raw) <= 4 && (FULL || j < n)) better |= CT::template elem_key<OP>(tin[j]) > carry.k;
+    }
+    if (sizeof(typename CT::raw) <= 4 && !__syncthreads_or(better)) {
+        const long long ci = carry.i;
+        long long* oi = reinterpret_cast<long long*>(oi_row + base);
+#pragma unroll
+        for (int q = 0; q < ITEMS; ++q)
+            if (FULL || t + q * nt < n) __stcs(oi + t + q * nt, ci);
+        if (ov_row) {
+            typename CT::raw* ov = ov_row + base;
+#pragma unroll
+            for (int q = 0; q < ITEMS; ++q)
+                if (FULL || t + q * nt < n) __stcs(ov + t + q * nt, carry_v);
+        }
+        __syncthreads();  // the tile buffers are reused by the next tile
+        return;
+    }
     // thread-local inclusive prefixes of ITEMS consecutive elements
     KI<CT> p[ITEMS];
     KI<CT> run = ki_identity<CT>();
@@ -397,6 +445,100 @@ __device__ __forceinline__ void scan_tile(const typename CT::raw* row, int base,
         carry_v = tin[tot.i - base];
     }
     __syncthreads();  // the tile buffers are reused by the next tile
+}
+
+// Phase A with 16-byte loads: the first best element of row[cb, ce) (best
+// key, then lowest index), U vector loads in flight per thread under the
+// evict-last policy (the chunk stays in L2 for a phase B that needs it); the
+// part before the first 16-byte boundary and the part after the last one
+// element by element. Every thread visits its elements in increasing index
+// order (head, vectors, tail), so the strict comparison keeps its first best;
+// the CTA merge breaks ties toward the lower index. Valid in warp 0.
+template <class CT, int OP, int U>
+__device__ __forceinline__ KI<CT> chunk_aggregate_vec(const typename CT::raw* row, int cb, int ce,
+                                                      KI<CT>* warp_tot) {
+    using R = typename CT::raw;
+    using K = typename CT::key;
+    constexpr int E = 16 / sizeof(R);
+    const int nt = blockDim.x;
+    const int t = threadIdx.x;
+    const int n = ce - cb;
+    const R* base = row + cb;
+    int head = static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(base) & 15u)) & 15u) / sizeof(R));
+    if (head > n) head = n;
+    const int nv = (n - head) / E;
+    const int tail0 = head + nv * E;
+    const uint4* vb = reinterpret_cast<const uint4*>(base + head);
+    const unsigned long long pol = l2_evict_last_policy();
+    KI<CT> a = ki_identity<CT>();
+    if (t < head) {
+        const K k = CT::template elem_key<OP>(ld_keep(base + t, pol));
+        if (k > a.k) {
+            a.k = k;
+            a.i = cb + t;
+        }
+    }
+    for (int v0 = t; v0 < nv; v0 += U * nt) {
+        uint4 buf[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (v0 + u * nt < nv) buf[u] = ld_keep16(vb + v0 + u * nt, pol);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (v0 + u * nt < nv) {
+                const int j0 = cb + head + (v0 + u * nt) * E;
+#pragma unroll
+                for (int k = 0; k < E; ++k) {
+                    const K key = CT::template elem_key<OP>(vec_item<R>(buf[u], k));
+                    if (key > a.k) {
+                        a.k = key;
+                        a.i = j0 + k;
+                    }
+                }
+            }
+        }
+    }
+    if (t < n - tail0) {
+        const K k = CT::template elem_key<OP>(ld_keep(base + tail0 + t, pol));
+        if (k > a.k) {
+            a.k = k;
+            a.i = cb + tail0 + t;
+        }
+    }
+    return block_first_best(a, warp_tot);
+}
+
+// p[0, n) = val, as streaming stores: 16-byte stores between the first and
+// the last 16-byte boundary, single elements before and after.
+template <typename T>
+__device__ __forceinline__ void fill_const(T* __restrict__ p, int n, T val) {
+    constexpr int E = 16 / sizeof(T);
+    const int nt = blockDim.x;
+    const int t = threadIdx.x;
+    int head = static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(p) & 15u)) & 15u) / sizeof(T));
+    if (head > n) head = n;
+    const int nv = (n - head) / E;
+    const int tail0 = head + nv * E;
+    if (t < head) __stcs(p + t, val);
+    uint4 pat;
+#pragma unroll
+    for (int k = 0; k < E; ++k) __builtin_memcpy(reinterpret_cast<char*>(&pat) + k * sizeof(T), &val, sizeof(T));
+    uint4* pv = reinterpret_cast<uint4*>(p + head);
+    for (int v = t; v < nv; v += nt) __stcs(pv + v, pat);
+    if (t < n - tail0) __stcs(p + tail0 + t, val);
+}
+
+// Phase B of a dominated chunk: when the carry-in is at least as good as the
+// chunk's best element (its phase-A aggregate; ties keep the carry, whose
+// index is earlier), every prefix of the row that ends in the chunk has the
+// carry as its result, so phase B writes (carry_i, carry_v) to every output
+// of row[cb, ce) and neither reads nor scans the chunk again. In a long row
+// only the chunks that hold a new best of the row so far are not dominated.
+template <class CT>
+__device__ __forceinline__ void fill_chunk(int cb, int ce, int carry_i, typename CT::raw carry_v,
+                                           int64_t* __restrict__ oi_row, typename CT::raw* __restrict__ ov_row) {
+    fill_const<long long>(reinterpret_cast<long long*>(oi_row + cb), ce - cb, static_cast<long long>(carry_i));
+    if (ov_row) fill_const<typename CT::raw>(ov_row + cb, ce - cb, carry_v);
 }
 
 // Phase B: scan row[cb, ce) tile by tile (NT threads x ITEMS consecutive
@@ -532,6 +674,7 @@ cum_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols, int64
     __shared__ KI<CT> warp_tot[32];
     __shared__ KI<CT> s_total;
     __shared__ __align__(16) uint4 agg_slots[2][kCumMaxCluster];  // aggregates pushed by earlier CTAs
+    __shared__ bool s_dominated;
     const int t = threadIdx.x;
     const int C = CLUSTER ? static_cast<int>(gridDim.x) : 1;
     const int b = CLUSTER ? static_cast<int>(blockIdx.x) : 0;
@@ -580,6 +723,14 @@ cum_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols, int64
                     carry.i = static_cast<int>(pk.z);
                     carry_v = ld_scalar(row + carry.i);  // the winner's raw bits (an L2 hit)
                 }
+            }
+            if (t == 0) s_dominated = !(a.k > carry.k);  // a is valid in warp 0
+            __syncthreads();
+            if (s_dominated) {
+                fill_chunk<CT>(cb, ce, carry.i, carry_v, out_idx + r * static_cast<int64_t>(cols),
+                               out_val ? out_val + r * static_cast<int64_t>(cols) : nullptr);
+                __syncthreads();  // s_dominated is rewritten for the next row
+                continue;
             }
         }
         scan_chunk<CT, OP, ITEMS>(row, cb, ce, carry, carry_v, v, out_idx + r * static_cast<int64_t>(cols),
@@ -701,7 +852,7 @@ __device__ __forceinline__ bool decode_record(unsigned long long w, const typena
 // the work per CTA does not grow with the chunk count; merging an inclusive
 // prefix with aggregates it already covers is harmless (first_best is
 // idempotent). Records: [aggregate, inclusive] per chunk.
-template <class CT, int OP, int ITEMS, bool STASH, bool LOOKBACK>
+template <class CT, int OP, int ITEMS, bool STASH, bool LOOKBACK, bool VEC>
 __global__ void __launch_bounds__(1024)
 cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols, int chunks,
                  int64_t* __restrict__ out_idx, typename CT::raw* __restrict__ out_val,
@@ -713,6 +864,7 @@ cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols,
     __shared__ KI<CT> warp_tot[32];
     __shared__ KI<CT> s_total;
     __shared__ unsigned s_flag;
+    __shared__ bool s_dominated;
     __shared__ int s_near;
     __shared__ __align__(8) unsigned long long stash_bar;
     const int t = threadIdx.x;
@@ -747,6 +899,8 @@ cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols,
     if constexpr (STASH) {
         stash = stash_fill<CT>(row, cb, ce, cum_smem, &stash_bar, limit_ns, err);
         a = stash_aggregate<CT, OP>(stash, cb, ce, warp_tot);
+    } else if constexpr (VEC) {
+        a = chunk_aggregate_vec<CT, OP, kCumLoadsVec<R>>(row, cb, ce, warp_tot);
     } else {
         load_first_tile<CT, ITEMS, true>(row, cb, ce, v);
         a = chunk_aggregate<CT, OP, ITEMS, true>(row, cb, ce, v, warp_tot);
@@ -837,6 +991,7 @@ cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols,
         acc = first_best(seed, acc);
         if (t == 0) {
             s_total = acc;
+            s_dominated = !(a.k > acc.k);  // the carry-in is at least as good as the chunk's best
             // LOOKBACK: the inclusive prefix of this chunk, for the chunks after it.
             if (LOOKBACK && c > 0) st_release_gpu_u64(row_records + 2 * c + 1, make_record(first_best(acc, a)));
             // Every record this CTA needs has been read (the barrier above);
@@ -851,11 +1006,15 @@ cum_split_kernel(const typename CT::raw* __restrict__ x, int64_t rows, int cols,
     const R carry_v = carry.i == 0 ? x0 : ld_scalar(row + carry.i);
     int64_t* const oi_row = out_idx + r * static_cast<int64_t>(cols);
     R* const ov_row = out_val ? out_val + r * static_cast<int64_t>(cols) : nullptr;
-    if constexpr (STASH)
+    if (s_dominated) {
+        fill_chunk<CT>(cb, ce, carry.i, carry_v, oi_row, ov_row);
+    } else if constexpr (STASH) {
         scan_stash<CT, OP, ITEMS>(row, stash, cb, ce, carry, carry_v, oi_row, ov_row,
                                   reinterpret_cast<int*>(cum_smem + kCumStashBytes + 16), warp_tot, &s_total);
-    else
+    } else {
+        if constexpr (VEC) load_first_tile<CT, ITEMS>(row, cb, ce, v);  // from L2: phase A kept the chunk there
         scan_chunk<CT, OP, ITEMS>(row, cb, ce, carry, carry_v, v, oi_row, ov_row, cum_smem, warp_tot, &s_total);
+    }
     // The CTA that counted last clears the records of the whole launch.
     if (t == 0) {
         s_flag = done_old == total - 1 ? 1u : 0u;
@@ -1089,10 +1248,10 @@ constexpr int kCumItems = 7;
 
 inline size_t cum_smem_bytes(int block, int es) { return static_cast<size_t>(block) * kCumItems * (es + 4); }
 
-template <class CT, int OP, bool STASH, bool LOOKBACK>
+template <class CT, int OP, bool STASH, bool LOOKBACK, bool VEC>
 cudaError_t launch_cum_split_s(const argr_plan& p, const Problem& pr) {
     using R = typename CT::raw;
-    auto kern = cum_split_kernel<CT, OP, kCumItems, STASH, LOOKBACK>;
+    auto kern = cum_split_kernel<CT, OP, kCumItems, STASH, LOOKBACK, VEC>;
     // Stash: the chunk (16 bytes of slack for its alignment) and the tile indices.
     const size_t smem = STASH ? kCumStashBytes + 16 + static_cast<size_t>(p.block) * kCumItems * 4
                               : cum_smem_bytes(p.block, sizeof(R));
@@ -1105,11 +1264,19 @@ cudaError_t launch_cum_split_s(const argr_plan& p, const Problem& pr) {
                           static_cast<unsigned char*>(pr.scratch), (p.flags & ARGR_PLAN_TEST_EXPIRE) ? 1 : 0);
 }
 
+// Chunks of kCumVecTiles tiles or more take the 16-byte phase A (phase B, if
+// needed, reloads its first tile from L2); shorter chunks keep their first
+// tile in registers from phase A to phase B. Either variant is correct for any
+// chunk length; the choice is only one of speed.
 template <class CT, int OP>
 cudaError_t launch_cum_split(const argr_plan& p, const Problem& pr) {
-    if (p.flags & ARGR_PLAN_STASH) return launch_cum_split_s<CT, OP, true, false>(p, pr);
-    if (p.flags & ARGR_PLAN_LOOKBACK) return launch_cum_split_s<CT, OP, false, true>(p, pr);
-    return launch_cum_split_s<CT, OP, false, false>(p, pr);
+    if (p.flags & ARGR_PLAN_STASH) return launch_cum_split_s<CT, OP, true, false, false>(p, pr);
+    const bool vec = pr.cols / p.blocks_per_row >= static_cast<int64_t>(kCumVecTiles) * p.block * kCumItems;
+    if (p.flags & ARGR_PLAN_LOOKBACK)
+        return vec ? launch_cum_split_s<CT, OP, false, true, true>(p, pr)
+                   : launch_cum_split_s<CT, OP, false, true, false>(p, pr);
+    return vec ? launch_cum_split_s<CT, OP, false, false, true>(p, pr)
+               : launch_cum_split_s<CT, OP, false, false, false>(p, pr);
 }
 
 template <class CT, int OP>

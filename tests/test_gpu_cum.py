@@ -461,3 +461,49 @@ def test_scratch_prepared_before_use_on_another_stream():
             idx, _ = A.argreduce_cum(xd, "max", scratch=sc, stream=s, with_values=False)
         assert A.argreduce_read_error(sc.ptr, s.cuda_stream) == _lib.ARGR_OK
         assert (idx.cpu().numpy() == eidx).all(), k
+
+
+def structured_rows(dtype, rows, cols, kind, seed):
+    """Rows whose chunks are all dominated by their carry-in (decreasing,
+    constant, an early maximum), none (increasing), or some (steps with ties
+    at and around chunk boundaries)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    j = np.arange(cols, dtype=np.float64)
+    if kind == "increasing":
+        v = j / 8.0
+    elif kind == "decreasing":
+        v = -j / 8.0
+    elif kind == "constant":
+        v = np.zeros(cols)
+    elif kind == "early_max":
+        v = rng.integers(-50, 50, size=cols).astype(np.float64)
+        v[3] = 1000.0
+    else:  # steps: a new maximum every ~cols/13 elements, repeated ties in between
+        v = np.floor(j / max(1, cols // 13)) + (rng.random(cols) < 0.5) * 0.0
+    v = np.broadcast_to(v, (rows, cols)) + np.arange(rows)[:, None] * 0.0
+    if dtype in ("i32", "i64"):
+        return np.ascontiguousarray(np.clip(np.round(v * 8), -2**30, 2**30)).astype(VIEW[dtype])
+    if dtype == "f16":
+        v = np.clip(v, -60000, 60000)
+    return np.ascontiguousarray(W.encode(v, dtype))
+
+
+@pytest.mark.parametrize("dtype", CUM_DTYPES)
+def test_cum_dominated_chunks(dtype):
+    """Phase B writes the carry-in without reading a chunk again when the
+    carry is at least as good as the chunk's best element, and scans it
+    otherwise: rows where every chunk, no chunk, or some chunks are dominated,
+    for the split scan (all its variants) and the cluster scan."""
+    for kind in ("increasing", "decreasing", "constant", "early_max", "steps"):
+        for rows, cols in ((1, 40000), (3, 20011)):
+            x = structured_rows(dtype, rows, cols, kind, seed=cols + len(kind))
+            for op in ("max", "min"):
+                check_cum(x, dtype, op)
+                for chunks, block in ((2, 64), (13, 128), (40, 256)):
+                    check_cum(x, dtype, op, plan=split_plan(chunks, block, rows))
+                    check_cum(x, dtype, op, plan=split_plan(chunks, block, rows, flags=1 | LOOKBACK))
+                stash_chunks = 3 if -(-cols // 3) * W.ELEM_SIZE[dtype] <= 80 * 1024 else 6
+                check_cum(x, dtype, op, plan=split_plan(stash_chunks, 128, rows, flags=1 | STASH))
+                for cluster in (2, 7, 16):
+                    check_cum(x, dtype, op, plan=cum_plan(cluster, 128, grid=rows))
+                check_cum(x, dtype, op, plan=cum_plan(4, 64, grid=rows + 2))  # spare row slots
