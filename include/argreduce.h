@@ -142,8 +142,8 @@ typedef struct {
  * compares the current batch, so its loads stay in flight while it compares;
  * twice the registers for loaded data, so at most 256 threads per CTA. */
 #define ARGR_PLAN_PIPELINE 32
-/* Plan flag (ROWS, SPLIT and CLUSTER paths): before its dependency wait, each
- * CTA asks the L2 cache to fetch the part of x it reads first (bulk L2
+/* Plan flag (ROWS, SPLIT, CLUSTER and STREAM paths): before its dependency
+ * wait, each CTA asks the L2 cache to fetch the part of x it reads first (bulk L2
  * prefetches of 16-byte aligned pieces). A prefetch changes no value (L2 is
  * where the GPU keeps memory coherent, so a line written by the previous
  * grid is read as written), so results are the same; when the CTA starts

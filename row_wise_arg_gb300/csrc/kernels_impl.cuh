@@ -909,9 +909,6 @@ stream_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, i
     constexpr int E = 16 / sizeof(R);
     extern __shared__ __align__(128) unsigned char stream_smem[];
     __shared__ __align__(8) unsigned long long bars[kMaxStreamWarps * kMaxStreamStages];
-    grid_dependency_wait();
-    allow_dependents();
-
     const int lane = threadIdx.x & 31;
     const int w = threadIdx.x >> 5;
     const int W = blockDim.x >> 5;
@@ -919,6 +916,18 @@ stream_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, i
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * W + w;
     const int64_t r0 = rows * gw / nw;
     const int64_t r1 = rows * (gw + 1) / nw;
+    if (flags & ARGR_PLAN_PREFETCH) {
+        // the CTA's rows (contiguous: its warps' ranges follow one another),
+        // up to kPrefetchMaxBytes, before waiting for the previous grid
+        allow_dependents();
+        const int64_t c0 = rows * (static_cast<int64_t>(blockIdx.x) * W) / nw;
+        const int64_t c1 = rows * (static_cast<int64_t>(blockIdx.x + 1) * W) / nw;
+        prefetch_l2_range(x + c0 * cols, x + c1 * cols);
+        grid_dependency_wait();
+    } else {
+        grid_dependency_wait();
+        allow_dependents();
+    }
     const int64_t row_bytes = static_cast<int64_t>(cols) * static_cast<int64_t>(sizeof(R));
     // Rows that fit a stage travel whole (rows_per_piece > 0); wider rows in pieces.
     const int rows_per_piece = row_bytes <= stage_bytes ? static_cast<int>(stage_bytes / row_bytes) : 0;

@@ -340,7 +340,8 @@ argr_status check_plan(const argr_plan& p, int64_t rows, int64_t cols, int dtype
         return ARGR_EINVAL;
     if ((p.flags & ARGR_PLAN_BULK) && p.path != ARGR_PATH_CLUSTER) return ARGR_EINVAL;
     if ((p.flags & ARGR_PLAN_PREFETCH) &&
-        ((p.path != ARGR_PATH_ROWS && p.path != ARGR_PATH_SPLIT && p.path != ARGR_PATH_CLUSTER) ||
+        ((p.path != ARGR_PATH_ROWS && p.path != ARGR_PATH_SPLIT && p.path != ARGR_PATH_CLUSTER &&
+          p.path != ARGR_PATH_STREAM) ||
          (p.flags & ARGR_PLAN_BULK)))
         return ARGR_EINVAL;
     if ((p.flags & ARGR_PLAN_PIPELINE) &&

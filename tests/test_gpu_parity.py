@@ -134,9 +134,9 @@ def test_cluster_path(dtype, cluster):
 @pytest.mark.parametrize("dtype", W.DTYPES)
 def test_prefetch_paths(dtype):
     """ARGR_PLAN_PREFETCH (L2 prefetch of each CTA's first share before the
-    dependency wait) on the rows, split and cluster paths, with aligned and
-    unaligned bases, ragged tails, row loops and shares wider than what one
-    CTA prefetches."""
+    dependency wait) on the rows, split, cluster and streaming paths, with
+    aligned and unaligned bases, ragged tails, row loops and shares wider than
+    what one CTA prefetches."""
     es = W.ELEM_SIZE[dtype]
     caps = A.argreduce_device_caps(torch.cuda.current_device())
     for cols in (1, 9, 257, 4099, 20011, 300001):
@@ -156,6 +156,8 @@ def test_prefetch_paths(dtype):
                 check(x, dtype, op, plan=forced_plan("rows", group=32, vec=1, grid=2, unroll=8, pipeline=True,
                                                      prefetch=True))
                 check(x, dtype, op, plan=forced_plan("cluster", cluster=4, grid_rows=rows, prefetch=True))
+                check(x, dtype, op, plan=forced_plan("stream", group=32, stages=2, stage_bytes=8192, grid=3,
+                                                     block=128, prefetch=True))
 
 
 @pytest.mark.parametrize("dtype", W.DTYPES)

@@ -766,8 +766,8 @@ def test_plan_check_without_a_gpu():
 
 def test_prefetch_flag_rules():
     """ARGR_PLAN_PREFETCH: set by the planner exactly for inputs of at most
-    32 MiB, admitted on the rows, split and cluster paths only (not with bulk
-    copies, not on the streaming or non-last-axis paths)."""
+    32 MiB, admitted on the rows, split, cluster and streaming paths only (not
+    with the cluster's bulk copies, not on the non-last-axis path)."""
     from row_wise_arg_gb300 import _lib as L
     PF = L.ARGR_PLAN_PREFETCH
     for dt, es in (("f32", 4), ("bf16", 2), ("f64", 8)):
@@ -787,7 +787,9 @@ def test_prefetch_flag_rules():
     st.vec, st.flags = 1, L.ARGR_PLAN_PDL
     assert chk(st) == L.ARGR_OK
     st.flags |= PF
-    assert chk(st) == L.ARGR_EINVAL                      # not a prefetching path
+    assert chk(st) == L.ARGR_OK                          # its CTA's rows, before the wait
+    st.flags |= L.ARGR_PLAN_BULK
+    assert chk(st) == L.ARGR_EINVAL                      # bulk flag: cluster plans only
     ax = A.argreduce_axis_plan(64, 512, 256, "bf16", "max", GB300)
     assert not ax.flags & PF
 
