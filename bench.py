@@ -221,15 +221,20 @@ def ncu_cases(torch, A, only: str = None, reps: int = 1):
     its own freshly allocated input (for one ncu capture of every case: the
     i-th captured launch is the i-th case printed). `only`: just the cases
     whose name contains it, each called `reps` times (for a full capture of
-    one launch, skipping the first)."""
-    for c in config_group_cases():
+    one launch, skipping the first); with `only`, the non-last-axis cases are
+    searched too."""
+    cases = config_group_cases() + (W.config_cases(WORKLOADS["axis"][0]) if only is not None else [])
+    for c in cases:
         if only is not None and only not in c.name:
             continue
         x = W.make(c)
-        d = to_dev(torch, x, c.dtype).view(c.rows, c.cols)
-        out = torch.empty(c.rows, dtype=torch.int64, device="cuda")
+        d = to_dev(torch, x, c.dtype)
+        out = torch.empty(c.rows * c.inner, dtype=torch.int64, device="cuda")
         for _ in range(reps):
-            A.argreduce(d, c.op, dtype=c.dtype, out_idx=out)
+            if c.inner > 1:
+                A.argreduce_axis(d.view(c.rows, c.cols, c.inner), 1, c.op, dtype=c.dtype, out_idx=out)
+            else:
+                A.argreduce(d.view(c.rows, c.cols), c.op, dtype=c.dtype, out_idx=out)
         torch.cuda.synchronize()
         print(c.name, flush=True)
         del d, out
@@ -783,7 +788,7 @@ def main():
     ap.add_argument("--ncu-cases", action="store_true",
                     help="no timing: one planner call per reduction config case, for an ncu capture")
     ap.add_argument("--ncu-case", metavar="NAME",
-                    help="no timing: three planner calls of each reduction config case whose name contains NAME")
+                    help="no timing: three planner calls of each reduction config case (or non-last-axis case) whose name contains NAME")
     ap.add_argument("--ncu-summarize", metavar="CSV",
                     help="no GPU: print profiles/traffic_configs.txt lines from an ncu CSV of --ncu-cases")
     args = ap.parse_args()
