@@ -150,6 +150,12 @@ typedef struct {
  * while the previous grid in the stream is still running (ARGR_PLAN_PDL),
  * the read of x from HBM overlaps that grid instead of following it. */
 #define ARGR_PLAN_PREFETCH 64
+/* Plan flag (ROWS path, with ARGR_PLAN_PREFETCH): each CTA prefetches at most
+ * 16 KiB (the head of its rows) instead of 128 KiB. For inputs above 32 MiB,
+ * where two calls' inputs no longer share L2: only the first bytes each CTA
+ * reads come early, covering the gap between the previous grid's last loads
+ * and this grid's first, without evicting what the previous grid still needs. */
+#define ARGR_PLAN_PREFETCH_HEAD 128
 
 /* A launch plan. Produced by argreduce_plan(); tests may edit it to force a
  * path and pass it to argreduce_with_plan(), which re-validates it. */

@@ -26,6 +26,7 @@ ARGR_PLAN_STASH = 8
 ARGR_PLAN_LOOKBACK = 16
 ARGR_PLAN_PIPELINE = 32
 ARGR_PLAN_PREFETCH = 64
+ARGR_PLAN_PREFETCH_HEAD = 128
 
 DTYPE_CODES = {"f32": ARGR_F32, "f16": ARGR_F16, "bf16": ARGR_BF16, "f64": ARGR_F64, "i32": ARGR_I32,
                "i64": ARGR_I64}

@@ -178,6 +178,7 @@ __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontro
 // into L2 during that grid instead of after it.
 constexpr uintptr_t kPrefetchMinPiece = 4096;         // bytes per bulk prefetch, at least
 constexpr uintptr_t kPrefetchMaxBytes = 128 * 1024;   // bytes one CTA prefetches, at most
+constexpr uintptr_t kPrefetchHeadBytes = 16 * 1024;   // the same under ARGR_PLAN_PREFETCH_HEAD
 
 // One bulk prefetch of n bytes at p; p 16-byte aligned, n a positive multiple of 16.
 __device__ __forceinline__ void prefetch_l2_bulk(uintptr_t p, unsigned n) {
@@ -185,13 +186,14 @@ __device__ __forceinline__ void prefetch_l2_bulk(uintptr_t p, unsigned n) {
 }
 
 // Prefetch the bytes [lo, hi) of global memory, shrunk to 16-byte boundaries
-// and to the first kPrefetchMaxBytes: pieces of at least kPrefetchMinPiece
-// bytes, one per warp of the CTA, each issued by the warp's lane 0.
-__device__ __forceinline__ void prefetch_l2_range(const void* lo, const void* hi) {
+// and to the first max_bytes: pieces of at least kPrefetchMinPiece bytes, one
+// per warp of the CTA, each issued by the warp's lane 0.
+__device__ __forceinline__ void prefetch_l2_range(const void* lo, const void* hi,
+                                                  uintptr_t max_bytes = kPrefetchMaxBytes) {
     const uintptr_t a = (reinterpret_cast<uintptr_t>(lo) + 15) & ~static_cast<uintptr_t>(15);
     uintptr_t b = reinterpret_cast<uintptr_t>(hi) & ~static_cast<uintptr_t>(15);
     if ((threadIdx.x & 31) != 0 || b <= a) return;
-    if (b - a > kPrefetchMaxBytes) b = a + kPrefetchMaxBytes;
+    if (b - a > max_bytes) b = a + max_bytes;
     const uintptr_t nw = (blockDim.x + 31) >> 5;
     uintptr_t piece = ((b - a + nw - 1) / nw + 15) & ~static_cast<uintptr_t>(15);
     if (piece < kPrefetchMinPiece) piece = kPrefetchMinPiece;

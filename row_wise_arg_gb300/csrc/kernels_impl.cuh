@@ -42,7 +42,7 @@ namespace argr {
 template <class Tag, int OP, int G, bool VEC, int U, bool PIPE>
 __global__ void __launch_bounds__(PIPE ? kPipeMaxBlock : 1024)
 rows_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int64_t* __restrict__ out_idx,
-            typename Tag::raw* __restrict__ out_val, bool prefetch) {
+            typename Tag::raw* __restrict__ out_val, unsigned prefetch_bytes) {
     using R = typename Tag::raw;
     constexpr int E = 16 / sizeof(R);
     const int lg = threadIdx.x & (G - 1);
@@ -50,16 +50,16 @@ rows_kernel(const typename Tag::raw* __restrict__ x, int64_t rows, int cols, int
     const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
     const int groups_per_block = blockDim.x / G;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * groups_per_block;
-    if (prefetch) {
-        // the rows of this CTA's grid-stride steps, up to kPrefetchMaxBytes,
+    if (prefetch_bytes) {
+        // the rows of this CTA's grid-stride steps, up to prefetch_bytes,
         // before waiting for the previous grid
         allow_dependents();
         const int64_t row_bytes = static_cast<int64_t>(cols) * static_cast<int64_t>(sizeof(R));
-        int64_t budget = static_cast<int64_t>(kPrefetchMaxBytes);
+        int64_t budget = static_cast<int64_t>(prefetch_bytes);
         for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * groups_per_block; r0 < rows && budget > 0;
              r0 += stride) {
             const int64_t r1 = rows - r0 > groups_per_block ? r0 + groups_per_block : rows;
-            prefetch_l2_range(x + r0 * cols, x + r1 * cols);
+            prefetch_l2_range(x + r0 * cols, x + r1 * cols, static_cast<uintptr_t>(budget));
             budget -= (r1 - r0) * row_bytes;
         }
         grid_dependency_wait();
@@ -1163,7 +1163,10 @@ cudaError_t launch_rows_gu(const argr_plan& p, const Problem& pr) {
     const dim3 grid(static_cast<unsigned>(p.grid_rows));
     const R* x = static_cast<const R*>(pr.x);
     R* ov = static_cast<R*>(pr.out_val);
-    const bool pf = (p.flags & ARGR_PLAN_PREFETCH) != 0;
+    // bytes each CTA prefetches before its dependency wait (0: none)
+    const unsigned pf = !(p.flags & ARGR_PLAN_PREFETCH)    ? 0u
+                        : (p.flags & ARGR_PLAN_PREFETCH_HEAD) ? static_cast<unsigned>(kPrefetchHeadBytes)
+                                                              : static_cast<unsigned>(kPrefetchMaxBytes);
     if constexpr (G >= 16) {
         if (p.flags & ARGR_PLAN_PIPELINE)  // check_plan admits it only with vec and G >= 16
             return launch_ex(rows_kernel<Tag, OP, G, true, U, true>, grid, dim3(p.block), 1, p, pr.stream, x,

@@ -48,7 +48,8 @@ constexpr int64_t kMinSplitShare = 32768;    // a row is shared by several CTAs 
 // still there when it reads it. Measured on GB300 (graphs of 16 calls, L2-cold
 // inputs): [32,202048] bf16 5.22 -> 4.72 us, [8,202048] f32 4.14 -> 3.80 us,
 // [1,202048] f32 3.31 -> 3.11 us, [4096,128] f32 2.08 -> 1.93 us; above it,
-// [4096,4096] f32 (67 MB) 11.6 -> 14.2 us.
+// [4096,4096] f32 (67 MB) 11.6 -> 14.2 us, so larger inputs on the rows path
+// prefetch only the head of each CTA's rows (ARGR_PLAN_PREFETCH_HEAD).
 constexpr int64_t kPrefetchMaxInput = 32 * 1024 * 1024;
 
 int64_t ceil_div(int64_t a, int64_t b) { return a / b + (a % b != 0); }
@@ -111,7 +112,8 @@ argr_status make_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_
     out->block = kBlock;
     out->cluster = 0;
     out->flags = ARGR_PLAN_PDL;
-    if (rows <= kPrefetchMaxInput / row_bytes) out->flags |= ARGR_PLAN_PREFETCH;
+    const bool big = rows > kPrefetchMaxInput / row_bytes;
+    if (!big) out->flags |= ARGR_PLAN_PREFETCH;
 
     if (row_bytes <= kNarrowRowBytes) {
         // One batch of kRowsUnroll loads per lane covers the row.
@@ -163,6 +165,11 @@ argr_status make_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_
             }
             out->grid_rows = std::min(ceil_div(rows, out->block / g), kRowsWaves * ctas_per_wave(caps, out->block));
             out->blocks_per_row = 1;
+            // Inputs above 32 MiB: only the head of each CTA's rows (16 KiB)
+            // before the dependency wait ([4096,4096] f64 23.4 -> 22.0 us, f32
+            // 11.6 -> 11.3 us, [65536,1024] f32 38.1 -> 37.5 us; the full 128 KiB
+            // evicts lines the previous call still reads: f32 11.6 -> 14.2 us).
+            if (big) out->flags |= ARGR_PLAN_PREFETCH | ARGR_PLAN_PREFETCH_HEAD;
         } else {
             // One CTA per row: small CTAs with 8 loads in flight per thread,
             // more rows in flight per SM ([1024,16384] f32 14.1 -> 12.6 us).
@@ -336,7 +343,10 @@ argr_status check_plan(const argr_plan& p, int64_t rows, int64_t cols, int dtype
     if (!valid_dtype(dtype) || rows < 0 || cols < 1 || cols > INT_MAX) return ARGR_EINVAL;
     if (rows == 0) return ARGR_OK;
     if (p.block < 32 || p.block > 1024 || p.block % 32 != 0) return ARGR_EINVAL;
-    if (p.flags & ~(ARGR_PLAN_PDL | ARGR_PLAN_BULK | ARGR_PLAN_TEST_EXPIRE | ARGR_PLAN_PIPELINE | ARGR_PLAN_PREFETCH))
+    if (p.flags & ~(ARGR_PLAN_PDL | ARGR_PLAN_BULK | ARGR_PLAN_TEST_EXPIRE | ARGR_PLAN_PIPELINE | ARGR_PLAN_PREFETCH |
+                    ARGR_PLAN_PREFETCH_HEAD))
+        return ARGR_EINVAL;
+    if ((p.flags & ARGR_PLAN_PREFETCH_HEAD) && (p.path != ARGR_PATH_ROWS || !(p.flags & ARGR_PLAN_PREFETCH)))
         return ARGR_EINVAL;
     if ((p.flags & ARGR_PLAN_BULK) && p.path != ARGR_PATH_CLUSTER) return ARGR_EINVAL;
     if ((p.flags & ARGR_PLAN_PREFETCH) &&

@@ -108,6 +108,8 @@ def forced_plan(path: str, **kw):
         raise ValueError(path)
     if kw.get("prefetch"):
         p.flags |= _lib.ARGR_PLAN_PREFETCH
+    if kw.get("prefetch_head"):
+        p.flags |= _lib.ARGR_PLAN_PREFETCH | _lib.ARGR_PLAN_PREFETCH_HEAD
     return p
 
 

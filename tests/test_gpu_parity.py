@@ -134,9 +134,9 @@ def test_cluster_path(dtype, cluster):
 @pytest.mark.parametrize("dtype", W.DTYPES)
 def test_prefetch_paths(dtype):
     """ARGR_PLAN_PREFETCH (L2 prefetch of each CTA's first share before the
-    dependency wait) on the rows, split, cluster and streaming paths, with
-    aligned and unaligned bases, ragged tails, row loops and shares wider than
-    what one CTA prefetches."""
+    dependency wait) on the rows, split, cluster and streaming paths, and its
+    16 KiB head variant on the rows path, with aligned and unaligned bases,
+    ragged tails, row loops and shares wider than what one CTA prefetches."""
     es = W.ELEM_SIZE[dtype]
     caps = A.argreduce_device_caps(torch.cuda.current_device())
     for cols in (1, 9, 257, 4099, 20011, 300001):
@@ -145,6 +145,7 @@ def test_prefetch_paths(dtype):
         for op in W.ALL_OPS:
             for off in (0, 1):
                 check(x, dtype, op, offset=off, plan=forced_plan("rows", group=32, vec=0, grid=3, prefetch=True))
+                check(x, dtype, op, offset=off, plan=forced_plan("rows", group=32, vec=0, grid=3, prefetch_head=True))
                 check(x, dtype, op, offset=off, plan=forced_plan("split", bpr=1, grid_rows=2, prefetch=True))
                 check(x, dtype, op, offset=off, plan=forced_plan("split", bpr=7, grid_rows=rows, prefetch=True))
                 if caps.max_cluster >= 16:
@@ -153,6 +154,7 @@ def test_prefetch_paths(dtype):
             if (cols * es) % 16 == 0:
                 for g in (4, 32):
                     check(x, dtype, op, plan=forced_plan("rows", group=g, vec=1, grid=5, prefetch=True))
+                    check(x, dtype, op, plan=forced_plan("rows", group=g, vec=1, grid=5, prefetch_head=True))
                 check(x, dtype, op, plan=forced_plan("rows", group=32, vec=1, grid=2, unroll=8, pipeline=True,
                                                      prefetch=True))
                 check(x, dtype, op, plan=forced_plan("cluster", cluster=4, grid_rows=rows, prefetch=True))

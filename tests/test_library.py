@@ -765,16 +765,24 @@ def test_plan_check_without_a_gpu():
 
 
 def test_prefetch_flag_rules():
-    """ARGR_PLAN_PREFETCH: set by the planner exactly for inputs of at most
-    32 MiB, admitted on the rows, split, cluster and streaming paths only (not
-    with the cluster's bulk copies, not on the non-last-axis path)."""
+    """ARGR_PLAN_PREFETCH: set by the planner for inputs of at most 32 MiB,
+    and with ARGR_PLAN_PREFETCH_HEAD (16 KiB a CTA) for larger inputs on the
+    rows path; admitted on the rows, split, cluster and streaming paths only
+    (not with the cluster's bulk copies, not on the non-last-axis path), the
+    head variant on the rows path only."""
     from row_wise_arg_gb300 import _lib as L
-    PF = L.ARGR_PLAN_PREFETCH
+    PF, HEAD = L.ARGR_PLAN_PREFETCH, L.ARGR_PLAN_PREFETCH_HEAD
     for dt, es in (("f32", 4), ("bf16", 2), ("f64", 8)):
-        for rows, cols in CONFIG_SHAPES + [(1, 1), (5, 7), (2048, 4096), (2049, 4096), (8, 1 << 20), (9, 1 << 20)]:
+        for rows, cols in CONFIG_SHAPES + [(1, 1), (5, 7), (2048, 4096), (2049, 4096), (8, 1 << 20), (9, 1 << 20),
+                                           (1024, 16384), (1 << 20, 64)]:
             p = A.argreduce_plan(rows, cols, dt, "max", GB300)
-            assert bool(p.flags & PF) == (rows * cols * es <= 32 << 20), (rows, cols, dt)
+            small = rows * cols * es <= 32 << 20
+            head = not small and p.path == L.ARGR_PATH_ROWS and cols * es > 1024
+            assert bool(p.flags & PF) == (small or head), (rows, cols, dt)
+            assert bool(p.flags & HEAD) == head, (rows, cols, dt)
             assert A.argreduce_plan_check(p, rows, cols, dt, GB300) == L.ARGR_OK
+    for rows, cols, dt in ((4096, 4096, "f32"), (4096, 4096, "f64"), (65536, 1024, "f32"), (65536, 1024, "f64")):
+        assert A.argreduce_plan(rows, cols, dt, "max", GB300).flags & HEAD, (rows, cols, dt)
     chk = lambda p, rows=4, cols=1 << 16: A.argreduce_plan_check(p, rows, cols, "f32", GB300, True)
     cp = L.argr_plan()
     cp.path, cp.block, cp.unroll, cp.cluster, cp.blocks_per_row, cp.grid_rows = L.ARGR_PATH_CLUSTER, 256, 4, 4, 4, 4
@@ -790,6 +798,12 @@ def test_prefetch_flag_rules():
     assert chk(st) == L.ARGR_OK                          # its CTA's rows, before the wait
     st.flags |= L.ARGR_PLAN_BULK
     assert chk(st) == L.ARGR_EINVAL                      # bulk flag: cluster plans only
+    rp = A.argreduce_plan(4096, 4096, "f32", "max", GB300)
+    assert chk(rp, rows=4096, cols=4096) == L.ARGR_OK
+    rp.flags &= ~PF
+    assert chk(rp, rows=4096, cols=4096) == L.ARGR_EINVAL  # the head variant of a prefetch
+    cp.grid_rows, cp.flags = 4, L.ARGR_PLAN_PDL | PF | HEAD
+    assert chk(cp) == L.ARGR_EINVAL                      # rows path only
     ax = A.argreduce_axis_plan(64, 512, 256, "bf16", "max", GB300)
     assert not ax.flags & PF
 
