@@ -734,16 +734,17 @@ def config_table(torch, A, args, stream, peak):
                     row["thread_per_row_us_per_call"] = tpr
                 table.append(row)
                 if c is c0 and 1 <= g <= 5:
+                    # short enough that the last 1500 characters of the line hold every row
                     short = c.name.split("_", 1)[1].replace("_unique", "")
-                    item = f"{short} {row['us_per_call']:.2f} {row['frac']:.3f} {path[:2]} i{row['isolated_us']:.2f}"
+                    frac = f"{row['frac']:.3f}".removeprefix("0")
+                    item = f"{short} {row['us_per_call']:.2f} {frac} {path[:2]} i{row['isolated_us']:.1f}"
                     if "cpu_us_per_call" in row:
                         item += f" c{row['cpu_us_per_call']:.0f}/{row['cpu_cores']}"
                     if "ncu_frac" in row:
-                        item += f" n{row['ncu_frac']:.3f}"
+                        item += " n" + f"{row['ncu_frac']:.3f}".removeprefix("0")
                     compact.append(item)
         del ginputs
-    legend = ("case, us/call (graphs of ~16 calls, L2-cold inputs), frac of measured HBM peak, path, "
-              "i: isolated single-call us, c: oracle us/host cores, n: ncu DRAM GB/s frac of peak")
+    legend = ("case us/call frac-of-HBM-peak path, i: isolated us, c: oracle us/host cores, n: ncu frac")
     return table, {"legend": legend, "rows": compact}
 
 
