@@ -34,6 +34,7 @@ constexpr int64_t kWarpRowBytes = 32768;   // many rows up to this width: a warp
 constexpr int kManyRowsBlock = 128;        // CTA size on the many-rows path
 constexpr int kManyRowsUnroll = 8;         // 16-byte loads in flight per lane on the many-rows path
 constexpr int kBlock = 256;                // threads per CTA on every path
+constexpr int kNarrowVecBlock = 128;       // narrow rows with vector loads
 constexpr int kRowsUnroll = 4;             // loads in flight per lane on the rows path
 constexpr int kSplitUnroll = 4;            // vector loads in flight per thread on the split path
 constexpr int64_t kRowsWaves = 8;          // rows path: grid of at most this many waves (grid-stride beyond)
@@ -123,13 +124,20 @@ argr_status make_plan(int64_t rows, int64_t cols, int dtype, int op, const argr_
         out->group = g;
         out->vec = aligned ? 1 : 0;
         out->unroll = kRowsUnroll;
-        const int64_t rows_per_cta = kBlock / g;
+        // Vector rows that would give fewer 256-thread CTAs than SMs:
+        // 128-thread CTAs, so that the rows spread over twice the SMs
+        // ([4096,8] f32 1.61 -> 1.40 us, [16384,32] 2.07 -> 2.02, [1000,64]
+        // 1.67 -> 1.63). With more rows 256 stays ([30000,100] f32 3.84
+        // against 4.03 us with 128; [65536,64] and [131072,16] the same).
+        out->block = (aligned && ceil_div(rows, kBlock / g) < caps.sm_count) ? kNarrowVecBlock : kBlock;
+        const int64_t rows_per_cta = out->block / g;
         // With the prefetch, at most half the device's threads: the next
         // call's CTAs then find room while this one runs and fetch their rows
-        // meanwhile ([65536,64] f32 4.67 -> 3.97 us with 608 CTAs instead of
-        // 1024); without it, up to kRowsWaves waves.
-        const int64_t max_grid = (out->flags & ARGR_PLAN_PREFETCH) ? std::max<int64_t>(1, ctas_per_wave(caps, kBlock) / 2)
-                                                                    : kRowsWaves * ctas_per_wave(caps, kBlock);
+        // meanwhile ([65536,64] f32 4.67 -> 3.97 us with 608 CTAs of 256
+        // instead of 1024); without it, up to kRowsWaves waves.
+        const int64_t wave_ctas = ctas_per_wave(caps, out->block);
+        const int64_t max_grid = (out->flags & ARGR_PLAN_PREFETCH) ? std::max<int64_t>(1, wave_ctas / 2)
+                                                                    : kRowsWaves * wave_ctas;
         out->grid_rows = std::min(ceil_div(rows, rows_per_cta), max_grid);
         out->blocks_per_row = 1;
         out->scratch_bytes = 0;

@@ -136,6 +136,11 @@ def test_plan_paths_for_configs():
     for cols in (8, 64, 128):
         d = path(65536 if cols == 64 else 4096, cols)
         assert d["path_name"] == "rows" and d["vec"] == 1 and d["group"] <= 8
+    # narrow vector rows: 128-thread CTAs when 256-thread ones would not reach every SM
+    assert path(4096, 8)["block"] == 128 and path(4096, 8)["grid_rows"] == 32
+    assert path(4096, 128)["block"] == 128 and path(16384, 32)["block"] == 128
+    assert path(65536, 64)["block"] == 256 and path(65536, 64)["grid_rows"] == 608
+    assert path(30000, 100)["block"] == 256 and path(4096, 9)["block"] == 256  # many CTAs; scalar rows
     # medium rows: warp per row from 4 KB of binary32; pipelined loads from
     # 16 KB (binary32) / 32 KB (binary64) rows, 8 deep while the rows fit
     # 16 warps per SM, else 4 deep
