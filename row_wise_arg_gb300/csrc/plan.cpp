@@ -35,6 +35,7 @@ constexpr int kManyRowsBlock = 128;        // CTA size on the many-rows path
 constexpr int kManyRowsUnroll = 8;         // 16-byte loads in flight per lane on the many-rows path
 constexpr int kBlock = 256;                // threads per CTA on every path
 constexpr int kNarrowVecBlock = 128;       // narrow rows with vector loads
+constexpr int64_t kAxisWarpsPerSmNarrow = 32;  // non-last axis, narrow column segments: warps per SM
 constexpr int kRowsUnroll = 4;             // loads in flight per lane on the rows path
 constexpr int kSplitUnroll = 4;            // vector loads in flight per thread on the split path
 constexpr int64_t kRowsWaves = 8;          // rows path: grid of at most this many waves (grid-stride beyond)
@@ -301,8 +302,13 @@ argr_status make_axis_plan(int64_t outer, int64_t reduce, int64_t inner, int dty
     const int64_t rg = 32 / cg;
     const int64_t ctas = slots * tiles;
     // Warps along R: enough for ~16 warps per SM over the grid, each R lane
-    // keeping at least 16 steps.
-    int64_t y = ceil_div(16 * sms, ctas);
+    // keeping at least 16 steps. Column segments narrower than a 128-byte
+    // line on a grid of at least a CTA per SM wait on their loads: there ~32
+    // ([64,512,256] bf16 8.35 -> 8.02 us, [16,2048,384] f64 27.8 -> 25.9 us;
+    // 512-byte segments were slower with 32, [1,1000,100000] f32 65.8 -> 77.0,
+    // and so was a grid below one CTA per SM, [1,100000,1000] f32 71.0 -> 72.5).
+    const bool narrow_segments = cg * v * es < 128 && ctas >= sms;
+    int64_t y = ceil_div((narrow_segments ? kAxisWarpsPerSmNarrow : 16) * sms, ctas);
     y = std::max<int64_t>(1, std::min<int64_t>({y, 32, reduce / (rg * 16)}));
     int64_t c = 1;
     if (ctas * y < 4 * sms && outer <= kMaxGridY && caps.max_cluster >= 2) {

@@ -491,6 +491,11 @@ def test_axis_plans():
         assert d["group"] in (1, 2, 4, 8, 16, 32)
         tiles = -(-inner // (d["group"] * v))
         assert (d["grid_rows"] * tiles * d["cluster"]) >= min(2 * 152, d["grid_rows"] * tiles)
+    # warps along R: ~32 a SM for column segments below a line on a grid of a CTA per SM or more, else ~16
+    blocks = {shape: A.argreduce_axis_plan(*shape, "max", caps).as_dict()["block"]
+              for shape in [(64, 512, 256, "bf16"), (16, 2048, 384, "f64"), (1, 1000, 100000, "f32"),
+                            (1, 100000, 1000, "f32"), (128, 4096, 8, "f32")]}
+    assert list(blocks.values()) == [128, 224, 128, 640, 512], blocks
     with pytest.raises(A.ArgreduceError):
         A.argreduce_axis_plan(1, 0, 5, "f32", "max", caps)
     assert _lib.argreduce_axis_raw(0x10000, "f32", 0, 10, 5, "max", 0x10000, 0, 0, 0, 0) == _lib.ARGR_OK
