@@ -547,9 +547,11 @@ def test_cum_plans_and_validation():
             assert d["grid_rows"] == rows and d["scratch_bytes"] == 0
             assert d["blocks_per_row"] == d["cluster"]
         else:
-            # one CTA per row: as many rows as SMs, or rows too short to split
-            assert d["path_name"] == "cum" and d["scratch_bytes"] == 0 and 32 <= d["block"] <= 256
+            # one CTA per row: as many rows as SMs, or rows too short to split; 512
+            # threads with fewer than two CTAs a SM and rows of two such tiles
+            assert d["path_name"] == "cum" and d["scratch_bytes"] == 0 and 32 <= d["block"] <= 512
             assert rows >= 152 or cols < 4 * 7 * d["block"]
+            assert (d["block"] == 512) == (152 <= rows < 304 and cols >= 2 * 512 * 7), (rows, cols)
             if rows >= 4 * 152:
                 assert d["block"] <= 128 and (d["block"] == 32 or d["block"] * 7 <= cols)
     assert seen == {("cum_split", False), ("cum", True), ("cum", False)}
