@@ -508,7 +508,7 @@ def test_cum_plans_and_validation():
                            (4, 16384, "i32"), (1, 65536, "f32"), (256, 256, "bf16"), (1, 3, "f64"),
                            (1, 16777216, "i64"), (64, 65536, "f32"), (600, 100000, "f16"), (1, 16384, "i64"),
                            (200, 30000, "f32"), (4096, 4096, "f32"), (65536, 256, "f32"), (256, 65536, "f32"),
-                           (16, 1 << 20, "f64")]:
+                           (16, 1 << 20, "f64"), (128, 131072, "f64"), (100, 131072, "f32")]:
         d = A.argreduce_cum_plan(rows, cols, dt, "max", GB300).as_dict()
         seen.add((d["path_name"], d["cluster"] > 1))
         es = {"f32": 4, "f16": 2, "bf16": 2, "f64": 8, "i32": 4, "i64": 8}[dt]
@@ -548,10 +548,12 @@ def test_cum_plans_and_validation():
             assert d["blocks_per_row"] == d["cluster"]
         else:
             # one CTA per row: as many rows as SMs, or rows too short to split; 512
-            # threads with fewer than two CTAs a SM and rows of two such tiles
-            assert d["path_name"] == "cum" and d["scratch_bytes"] == 0 and 32 <= d["block"] <= 512
-            assert rows >= 152 or cols < 4 * 7 * d["block"]
+            # threads with fewer than two CTAs a SM and rows of two such tiles, 1024
+            # from three quarters of a row per SM and rows of two such tiles
+            assert d["path_name"] == "cum" and d["scratch_bytes"] == 0 and 32 <= d["block"] <= 1024
+            assert rows >= 152 or cols < 4 * 7 * d["block"] or (d["block"] == 1024 and rows >= 114)
             assert (d["block"] == 512) == (152 <= rows < 304 and cols >= 2 * 512 * 7), (rows, cols)
+            assert (d["block"] == 1024) == (114 <= rows < 152 and cols >= 2 * 1024 * 7), (rows, cols)
             if rows >= 4 * 152:
                 assert d["block"] <= 128 and (d["block"] == 32 or d["block"] * 7 <= cols)
     assert seen == {("cum_split", False), ("cum", True), ("cum", False)}
