@@ -76,8 +76,9 @@ argr_status make_cum_plan(int64_t rows, int64_t cols, int dtype, int op, const a
     }
     if (rows >= 3 * sms / 4 && rows < sms && cols >= 2 * 1024 * kCumItems) {
         // Almost a row per SM: one 1024-thread CTA per row instead of the
-        // split scan ([128,131072] f32 56.7 -> 49.1 us, [128,262144] 110.2 ->
-        // 90.5 us; with 64 rows the split stays much faster, 29.2 against 45.8).
+        // split scan ([128,131072] f32 56.6 -> 49.0 us, f64 91.7 -> 83.0,
+        // [140,65536] i32 32.1 -> 27.5; with 64 rows the split stays much
+        // faster, [64,131072] f32 29.2 against 45.8 us).
         out->block = 1024;
         return ARGR_OK;
     }
