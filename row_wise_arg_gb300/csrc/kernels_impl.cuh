@@ -1,7 +1,7 @@
 // argreduce kernels, templated on element tag, op and geometry. Each
 // kernels_<dtype>.cu instantiates them for one element type.
 //
-// Three paths (onnxruntime #32092 Approach, #31694 Description):
+// Paths (onnxruntime #32092 Approach, #31694 Description):
 //  * rows_kernel    - G lanes per row (G = 1: one thread per row, G = 32: one
 //                     warp per row), many rows per CTA, rows 16-byte aligned
 //                     (VEC) or not (scalar loads). For narrow and medium rows.
@@ -11,14 +11,21 @@
 //                     counter; the CTA that arrives last merges the partials.
 //                     The counter is bumped with a wrapping increment, so it
 //                     is back at zero after every row and needs no memset.
-//  * cluster_kernel - one thread-block cluster per row: CTAs push their
-//                     candidates into CTA 0's shared memory (distributed shared
-//                     memory) and meet at a cluster barrier. No scratch.
+//  * cluster_push_kernel - one thread-block cluster per row, a row slot per
+//                     row: every warp pushes its candidate into CTA 0's shared
+//                     memory (st.async on an mbarrier) and all CTAs but CTA 0
+//                     leave at once; CTA 0 waits (bounded) and merges. No scratch.
+//  * cluster_kernel - the same with fewer row slots than rows (CTAs loop over
+//                     rows) or CTAs of more than 512 threads: CTAs store their
+//                     candidates into CTA 0 and meet at a cluster barrier.
+//  * cluster_bulk_kernel - a cluster per row with each CTA's share copied into
+//                     shared memory by bulk (TMA) copies (forced plans).
 //  * stream_kernel  - every warp owns a contiguous range of rows and streams
 //                     them through its own shared-memory stages with bulk
 //                     (TMA) copies, several in flight; rows that fit a stage
 //                     are scanned G lanes per row, wider rows piece by piece
 //                     by the whole warp. Rows must start on 16-byte boundaries.
+//  * axis_kernel    - reduction over a non-last axis, x[outer][R][inner] over R.
 //
 // Index arithmetic: within a row every position is an int in [0, cols) with
 // cols <= INT32_MAX. Loops are written with differences (remaining = end -
