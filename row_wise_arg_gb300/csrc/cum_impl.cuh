@@ -19,6 +19,11 @@
 // ITEMS elements; tiles loaded and stored through shared memory so that
 // global accesses are coalesced, ITEMS odd so that a thread's run of
 // consecutive elements spreads over the banks), carrying the running prefix.
+// A chunk whose carry-in is at least as good as its aggregate is only filled
+// with the carry (no second read), and within a scanned chunk a tile with no
+// element better than the carry is filled the same way (elements of up to 4
+// bytes). Split-scan chunks of four tiles or more read phase A with 16-byte
+// loads; shorter ones keep their first tile in registers for phase B.
 #pragma once
 
 #include "device_common.cuh"
